@@ -1,0 +1,210 @@
+"""Plain CPU float64 oracle of the latent-MoE layer tail.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+timing leg of ``bench.py`` may import this package.  It shares no code with the CUDA
+path; the two meet only through the seeded inputs.
+
+What it computes, step by step (sources are the four pages on the Kimi K3 latent MoE:
+vLLM "Fuse BF16 shared experts into latent MegaMoE tail" (Summary), DeepGEMM PR 416
+"Fuse and publish Kimi K3's BF16 shared expert" (Summary), the tokenspeed recipe
+"Kimi-K3 DEP16 with sharded shared experts" (Communication and validation) and tokenspeed
+PR 1062 "MNNVL CuTe-DSL finalize tail" (commit notes and Summary)):
+
+1. Route: per token, the k largest router logits (ties: lower expert index first), weights
+   = softmax over the selected k logits (so they sum to 1).
+2. Quantise the latent input z per token per 128 columns to e4m3 with an fp32 scale
+   amax/448 (scale 1 for an all-zero group), quotient and scale in fp32, round to nearest
+   even, saturating.
+3. Routed experts in the 3584-wide latent space: h = deq(zq) deq(W13_e)^T, gate = first I
+   rows of W13_e, up = next I; a = silu(gate) * up; a is quantised per 128 like step 2
+   (from float32(a)); y = deq(aq) deq(W2_e)^T.
+4. Combine ("finalize"): r = sum_j w_j y_j (top-k weighted sum).
+5. RMSNorm of r (eps, weight gamma), then the 3584 -> 7168 up-projection.
+6. Shared expert on the 7168-wide hidden state: gate/up -> SwiGLU -> down.
+7. out = up-projection + shared output (the oracle rounds nothing here; the tail emits
+   bf16).
+
+Every product and sum runs in float64 on exactly dequantised weights.
+"""
+from __future__ import annotations
+
+from typing import Dict, Iterable, Optional
+
+import numpy as np
+
+from .codecs import e2m1_decode, e4m3_decode, e4m3_encode, unpack_e2m1
+
+__all__ = ["route", "permutation", "quant_per128", "silu", "dequant_fp8_blocks",
+           "dequant_nvfp4", "rmsnorm", "swiglu_mlp", "tail", "to_f64"]
+
+
+def to_f64(t) -> np.ndarray:
+    """torch tensor (any float dtype) or array -> float64 numpy array (exact)."""
+    if hasattr(t, "detach"):
+        import torch
+        return t.detach().to(torch.float64).numpy()
+    return np.asarray(t, dtype=np.float64)
+
+
+def _rows_f64(t, rows) -> np.ndarray:
+    if hasattr(t, "detach"):
+        import torch
+        return to_f64(t[torch.as_tensor(rows, dtype=torch.long)])
+    return np.asarray(t, dtype=np.float64)[rows]
+
+
+def _np(t) -> np.ndarray:
+    return t.detach().numpy() if hasattr(t, "detach") else np.asarray(t)
+
+
+# ---------------------------------------------------------------- step 1: route
+
+def route(logits, k: int):
+    """Top-k of each row (descending logit, ties to the lower index) and the softmax of
+    the selected logits.  Returns (ids int32 [M,k], w float64 [M,k])."""
+    lg = np.asarray(_np(logits), dtype=np.float32).astype(np.float64)
+    order = np.argsort(-lg, axis=1, kind="stable")
+    ids = order[:, :k]
+    sel = np.take_along_axis(lg, ids, axis=1)
+    ex = np.exp(sel - sel[:, :1])
+    w = ex / ex.sum(axis=1, keepdims=True)
+    return ids.astype(np.int32), w
+
+
+def permutation(ids, E: int):
+    """Stable grouping of the (token, choice) pairs by expert.
+
+    Pair i = t*k + j.  p runs over pairs sorted by expert, pairs of one expert in
+    ascending i (hence ascending token).  Returns cnt[E], off[E+1], gidx[M*k] (token of
+    pair p), slot[M*k] (= i of pair p), pos[M,k] (p of pair (t, j))."""
+    ids = np.asarray(ids)
+    M, k = ids.shape
+    flat = ids.reshape(-1).astype(np.int64)
+    order = np.argsort(flat, kind="stable")
+    cnt = np.bincount(flat, minlength=E).astype(np.int32)
+    off = np.zeros(E + 1, dtype=np.int32)
+    off[1:] = np.cumsum(cnt)
+    slot = order.astype(np.int32)
+    gidx = (order // k).astype(np.int32)
+    pos = np.empty(M * k, dtype=np.int32)
+    pos[order] = np.arange(M * k, dtype=np.int32)
+    return cnt, off, gidx, slot, pos.reshape(M, k)
+
+
+# ---------------------------------------------------------------- step 2: act quant
+
+def quant_per128(v32):
+    """Per row, per 128 columns: s = fp32(amax)/448 (1 if amax == 0); q = e4m3(v/s) with
+    the quotient in fp32.  Returns (codes uint8 [n,C], scales float32 [n,C/128])."""
+    v = np.asarray(v32, dtype=np.float32)
+    n, C = v.shape
+    g = v.reshape(n, C // 128, 128)
+    amax = np.abs(g).max(axis=-1)
+    s = np.where(amax == 0, np.float32(1.0), amax / np.float32(448.0)).astype(np.float32)
+    quot = (g / s[..., None]).astype(np.float32)
+    q = e4m3_encode(quot).reshape(n, C)
+    return q, s
+
+
+def dequant_act(q, s) -> np.ndarray:
+    q = np.asarray(q)
+    n, C = q.shape
+    return (e4m3_decode(q).reshape(n, C // 128, 128)
+            * np.asarray(s, dtype=np.float64)[..., None]).reshape(n, C)
+
+
+# ---------------------------------------------------------------- weights
+
+def dequant_fp8_blocks(q, s) -> np.ndarray:
+    """e4m3 codes [R,C] with fp32 scales [R/128,C/128] -> float64 [R,C]."""
+    q = _np(q)
+    R, C = q.shape
+    v = e4m3_decode(q).reshape(R // 128, 128, C // 128, 128)
+    return (v * np.asarray(_np(s), dtype=np.float64)[:, None, :, None]).reshape(R, C)
+
+
+def dequant_nvfp4(packed, sb, g) -> np.ndarray:
+    """packed e2m1 [R,C/2], e4m3 block scales [R,C/16], fp32 matrix scale -> float64."""
+    codes = unpack_e2m1(_np(packed))
+    R, C = codes.shape
+    vals = e2m1_decode(codes).reshape(R, C // 16, 16)
+    scale = e4m3_decode(_np(sb)) * float(g)
+    return (vals * scale[..., None]).reshape(R, C)
+
+
+# ---------------------------------------------------------------- math pieces
+
+def silu(v):
+    with np.errstate(over="ignore"):
+        return v / (1.0 + np.exp(-v))
+
+
+def rmsnorm(r, gamma, eps: float):
+    """r / sqrt(mean(r^2) + eps) * gamma, per row."""
+    r = np.asarray(r, dtype=np.float64)
+    return r / np.sqrt(np.mean(r * r, axis=-1, keepdims=True) + eps) * gamma
+
+
+def swiglu_mlp(x, w13, w2):
+    """SwiGLU MLP: gate = first half of w13's rows, up = second half."""
+    inter = w13.shape[0] // 2
+    h = x @ w13.T
+    return (silu(h[:, :inter]) * h[:, inter:]) @ w2.T
+
+
+# ---------------------------------------------------------------- the tail
+
+def _expert_weights(w: Dict, fmt: str, e: int):
+    if fmt == "fp8":
+        return (dequant_fp8_blocks(w["w13_q"][e], w["w13_s"][e]),
+                dequant_fp8_blocks(w["w2_q"][e], w["w2_s"][e]))
+    return (dequant_nvfp4(w["w13_q"][e], w["w13_sb"][e], float(w["w13_g"][e])),
+            dequant_nvfp4(w["w2_q"][e], w["w2_sb"][e], float(w["w2_g"][e])))
+
+
+def tail(act: Dict, w: Dict, cfg, tokens: Optional[Iterable[int]] = None) -> Dict:
+    """Run the whole tail.  ``tokens`` limits the per-token work to a subset (each token's
+    output depends on that token alone); routing and the permutation always cover every
+    token.  Returns every intermediate, indexed by the selected tokens' order."""
+    k, E, I = cfg.topk, cfg.E, cfg.I
+    logits = act["logits"]
+    M = logits.shape[0]
+    ids, wts = route(logits, k)
+    cnt, off, gidx, slot, pos = permutation(ids, E)
+    tok = np.arange(M) if tokens is None else np.asarray(list(tokens), dtype=np.int64)
+    n = len(tok)
+
+    z = _rows_f64(act["z"], tok)
+    zq, zs = quant_per128(z.astype(np.float32))
+    zdq = dequant_act(zq, zs)
+
+    # Routed experts, one expert at a time (bounded memory).
+    r = np.zeros((n, cfg.L))
+    aq = np.zeros((n, k, I), dtype=np.uint8)
+    as_ = np.zeros((n, k, I // 128), dtype=np.float32)
+    sel_ids = ids[tok]
+    for e in np.unique(sel_ids):
+        rows, js = np.nonzero(sel_ids == e)
+        w13, w2 = _expert_weights(w, cfg.routed_fmt, int(e))
+        h = zdq[rows] @ w13.T
+        a = silu(h[:, :I]) * h[:, I:]
+        q, s = quant_per128(a.astype(np.float32))
+        aq[rows, js], as_[rows, js] = q, s
+        y = dequant_act(q, s) @ w2.T
+        np.add.at(r, rows, wts[tok][rows, js][:, None] * y)
+
+    gamma = to_f64(w["gamma"])
+    nrm = rmsnorm(r, gamma, cfg.eps)
+    up = nrm @ to_f64(w["w_up"]).T
+
+    x = _rows_f64(act["x"], tok)
+    ws13 = to_f64(w["ws13"])
+    hs = x @ ws13.T
+    a_s = silu(hs[:, :cfg.Is]) * hs[:, cfg.Is:]
+    s_out = a_s @ to_f64(w["ws2"]).T
+
+    return {
+        "tokens": tok, "ids": ids, "w": wts, "cnt": cnt, "off": off, "gidx": gidx,
+        "slot": slot, "pos": pos, "zq": zq, "zs": zs, "aq": aq, "as": as_, "r": r,
+        "n": nrm, "up": up, "a_s": a_s, "s": s_out, "out": up + s_out,
+    }

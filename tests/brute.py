@@ -1,0 +1,105 @@
+"""Pure-Python scalar re-derivation of the latent-MoE tail for tiny shapes.
+
+It pins the numpy oracle by a different route: format values come from a table built
+with ``math.ldexp`` on the bit fields, e4m3 rounding is a nearest-value search over the
+whole code table, float32 steps are emulated by ``struct`` round trips (exact for one
++,-,*,/ of float32 operands: double rounding through float64 is innocuous for those),
+top-k is ``sorted`` and every product is an explicit loop.
+"""
+from __future__ import annotations
+
+import math
+import struct
+
+
+def f32(v: float) -> float:
+    return struct.unpack("f", struct.pack("f", v))[0]
+
+
+def _e4m3_table():
+    vals = {}
+    for c in range(256):
+        s = -1.0 if c & 0x80 else 1.0
+        e, m = (c >> 3) & 0xF, c & 7
+        if e == 0xF and m == 7:
+            continue
+        vals[c] = s * (math.ldexp(m, -9) if e == 0 else math.ldexp(8 + m, e - 10))
+    return vals
+
+
+E4M3 = _e4m3_table()
+E4M3_POS = sorted((v, c) for c, v in E4M3.items() if c < 0x80)
+
+
+def e4m3_value(c: int) -> float:
+    return E4M3[c]
+
+
+def e4m3_round(v: float) -> int:
+    """Nearest finite e4m3 code, ties to the code with an even mantissa; saturating."""
+    sign = 0x80 if math.copysign(1.0, v) < 0 else 0
+    a = abs(v)
+    best = None
+    for val, c in E4M3_POS:
+        d = abs(val - a)
+        key = (d, c & 1)
+        if best is None or key < best[0]:
+            best = (key, c)
+    return best[1] | sign
+
+
+def e2m1_value(c: int) -> float:
+    s = -1.0 if c & 8 else 1.0
+    e, m = (c >> 1) & 3, c & 1
+    return s * (0.5 * m if e == 0 else math.ldexp(2 + m, e - 2))
+
+
+def quant_group(vals):
+    """One 128-wide group of float32 values -> (codes, scale)."""
+    amax = max(abs(v) for v in vals)
+    s = 1.0 if amax == 0 else f32(amax / 448.0)
+    return [e4m3_round(f32(v / s)) for v in vals], s
+
+
+def silu(v: float) -> float:
+    return v / (1.0 + math.exp(-v))
+
+
+def matvec(w, x):
+    return [sum(wr[i] * x[i] for i in range(len(x))) for wr in w]
+
+
+def tail_token(logits, z, x, k, experts, gamma, eps, ws13, ws2, w_up):
+    """Output vector of one token.  ``experts[e] = (w13 rows, w2 rows)`` dequantised."""
+    order = sorted(range(len(logits)), key=lambda e: (-logits[e], e))[:k]
+    mx = logits[order[0]]
+    ex = [math.exp(logits[e] - mx) for e in order]
+    tot = sum(ex)
+    wts = [v / tot for v in ex]
+    zd = []
+    for g0 in range(0, len(z), 128):
+        q, s = quant_group([f32(v) for v in z[g0:g0 + 128]])
+        zd += [e4m3_value(c) * s for c in q]
+    L = len(z)
+    r = [0.0] * L
+    for e, wj in zip(order, wts):
+        w13, w2 = experts[e]
+        inter = len(w13) // 2
+        h = matvec(w13, zd)
+        a = [silu(h[i]) * h[inter + i] for i in range(inter)]
+        ad = []
+        for g0 in range(0, inter, 128):
+            q, s = quant_group([f32(v) for v in a[g0:g0 + 128]])
+            ad += [e4m3_value(c) * s for c in q]
+        y = matvec(w2, ad)
+        for c in range(L):
+            r[c] += wj * y[c]
+    ms = sum(v * v for v in r) / L
+    inv = 1.0 / math.sqrt(ms + eps)
+    n = [r[c] * inv * gamma[c] for c in range(L)]
+    up = matvec(w_up, n)
+    hs = matvec(ws13, x)
+    inter_s = len(ws13) // 2
+    a_s = [silu(hs[i]) * hs[inter_s + i] for i in range(inter_s)]
+    s_out = matvec(ws2, a_s)
+    return [up[i] + s_out[i] for i in range(len(up))], order, wts
