@@ -1,0 +1,184 @@
+/*
+ * klt.h -- C ABI of the GB300 latent-MoE layer tail library (libklt.so).
+ *
+ * The tail (Kimi K3 latent MoE, as described in the vLLM pull request "Fuse BF16 shared
+ * experts into latent MegaMoE tail", Summary, and DeepGEMM PR 416 "Fuse and publish Kimi
+ * K3's BF16 shared expert", Summary) computes, for every token t:
+ *
+ *   ids, w   = top-k of logits[t] and the softmax of the selected logits   (routing)
+ *   zq, zs   = e4m3 quantisation of z[t] per 128 columns, fp32 scale amax/448
+ *   r[t]     = sum_j w_j * SwiGLU-expert_{ids_j}(zq)       (routed experts, latent width L)
+ *   n[t]     = RMSNorm(r[t]) * gamma                       (fp32 statistics)
+ *   out[t]   = bf16( n[t] W_up^T + SwiGLU-shared(x[t]) )   (3584 -> 7168 up-projection
+ *                                                           plus the BF16 shared expert,
+ *                                                           summed in fp32, rounded once)
+ *
+ * Routed expert e: h = zq W13_e^T with gate = rows [0, I), up = rows [I, 2I);
+ * a = silu(gate) * up quantised per 128 like z; y = aq W2_e^T.  Shared expert:
+ * hs = x Ws13^T (gate rows [0, Is), up rows [Is, 2 Is)); s = (silu(g) * u) Ws2^T.
+ *
+ * Conventions for every entry point:
+ *  - every function returns a klt status code (KLT_OK == 0);
+ *  - pointers named "device" must be CUDA device pointers on the current device and
+ *    16-byte aligned; the library never frees caller memory;
+ *  - arguments are checked on the host before anything is launched; a failed check
+ *    launches nothing and changes no state;
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).
+ */
+#ifndef KLT_H_
+#define KLT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------------ status codes */
+enum klt_status_code {
+  KLT_OK = 0,
+  KLT_ERR_INVALID_ARG = 1,     /* null pointer, M < 0, M > max_tokens, bad eps, ...     */
+  KLT_ERR_UNSUPPORTED = 2,     /* a width not a multiple of 128, topk > E, E > 256,
+                                  routed format unknown, device is not sm_103          */
+  KLT_ERR_ALIGN = 3,           /* a pointer is not 16-byte aligned                     */
+  KLT_ERR_CUDA = 4,            /* a CUDA runtime call or launch failed                 */
+  KLT_ERR_DEVICE_TIMEOUT = 5,  /* a bounded on-device wait ran out (sticky)            */
+  KLT_ERR_OOM = 6              /* device allocation failed in klt_create               */
+};
+
+/* Routed expert weight formats. */
+enum klt_routed_format {
+  KLT_FMT_FP8_B128 = 0,  /* e4m3 codes, one fp32 scale per 128 x 128 block            */
+  KLT_FMT_NVFP4 = 1      /* e2m1 codes (two per byte, even K in the low nibble), one
+                            e4m3 scale per 16 K-elements, one fp32 scale per matrix    */
+};
+
+/* klt_create flags. */
+enum klt_flags {
+  KLT_FLAG_NO_PDL = 1u << 0  /* launch the kernels with plain stream ordering instead of
+                                programmatic dependent launch                          */
+};
+
+/* Layer shape.  H, L, I, Is must be multiples of 128; 1 <= topk <= min(E, 32);
+ * 1 <= E <= 256; 1 <= max_tokens and max_tokens * topk <= 2^20; eps > 0. */
+typedef struct klt_dims {
+  int32_t H;           /* hidden width (7168): shared-expert input and tail output   */
+  int32_t L;           /* latent width (3584): routed-expert input and output         */
+  int32_t E;           /* routed experts                                              */
+  int32_t topk;        /* experts per token                                           */
+  int32_t I;           /* routed expert intermediate width                            */
+  int32_t Is;          /* shared expert intermediate width                            */
+  int32_t routed_fmt;  /* enum klt_routed_format                                      */
+  float eps;           /* RMSNorm epsilon                                             */
+  int32_t max_tokens;  /* largest M klt_forward accepts; sizes the workspace          */
+} klt_dims;
+
+/* Layer weights, all device pointers, row-major.  klt_create copies them into memory the
+ * handle owns (re-laid out for the kernels); the caller's buffers are not referenced after
+ * klt_create returns.
+ *   FP8 routed:   w13 e4m3 [E, 2I, L]; w13_scale f32 [E, 2I/128, L/128];
+ *                 w2  e4m3 [E, L, I];  w2_scale  f32 [E, L/128, I/128];
+ *                 w13_global, w2_global unused (may be NULL).
+ *   NVFP4 routed: w13 packed e2m1 [E, 2I, L/2]; w13_scale e4m3 [E, 2I, L/16];
+ *                 w13_global f32 [E]; w2 packed [E, L, I/2]; w2_scale e4m3 [E, L, I/16];
+ *                 w2_global f32 [E].
+ *   Shared/dense: ws13 bf16 [2 Is, H] (gate rows first); ws2 bf16 [H, Is];
+ *                 w_up bf16 [H, L]; gamma bf16 [L]. */
+typedef struct klt_weights {
+  const void* w13;
+  const void* w13_scale;
+  const float* w13_global;
+  const void* w2;
+  const void* w2_scale;
+  const float* w2_global;
+  const void* ws13;
+  const void* ws2;
+  const void* w_up;
+  const void* gamma;
+} klt_weights;
+
+/* Optional routing outputs of klt_forward (every pointer may be NULL; device memory,
+ * caller owned).  Pair i = t * topk + j.  Pairs are grouped by expert, pairs of one expert
+ * in ascending i; p indexes that order.
+ *   ids int32 [M, topk] (descending logit, ties to the lower expert index);
+ *   weights f32 [M, topk] (softmax over the selected logits);
+ *   cnt int32 [E]; off int32 [E + 1] (exclusive prefix of cnt);
+ *   gidx int32 [M * topk] (token of pair p); slot int32 [M * topk] (i of pair p);
+ *   pos int32 [M, topk] (p of pair (t, j)). */
+typedef struct klt_routing {
+  int32_t* ids;
+  float* weights;
+  int32_t* cnt;
+  int32_t* off;
+  int32_t* gidx;
+  int32_t* slot;
+  int32_t* pos;
+} klt_routing;
+
+/* Optional stage outputs for testing and profiling (every pointer may be NULL; device
+ * memory, caller owned; copied on `stream` after the stage that writes them).
+ *   zq e4m3 [M, L], zs f32 [M, L/128]: quantised latent input;
+ *   aq e4m3 [M * topk, I], as f32 [M * topk, I/128]: quantised routed SwiGLU output,
+ *     rows in pair order p;
+ *   r f32 [M, L]: routed combine; n bf16 [M, L]: RMSNorm output (gamma applied);
+ *   a_s bf16 [M, Is]: shared-expert SwiGLU output;
+ *   events: up to 8 cudaEvent_t handles, events[i] recorded after launch i (NULL skips);
+ *   stall_after_kblocks: test hook, 0 = off; when > 0 the tile producer of the first
+ *     GEMM stops feeding data after that many k-blocks, so its consumers' bounded waits
+ *     run out and klt_status reports KLT_ERR_DEVICE_TIMEOUT;
+ *   timeout_ms: bound of every on-device wait for this call (0 = the default, 1000 ms). */
+typedef struct klt_debug {
+  uint8_t* zq;
+  float* zs;
+  uint8_t* aq;
+  float* as;
+  float* r;
+  void* n;
+  void* a_s;
+  void* events[8];
+  int32_t stall_after_kblocks;
+  int32_t timeout_ms;
+} klt_debug;
+
+typedef struct klt_handle klt_handle;
+
+/* Create a tail for one layer on the current device.  Synchronous.  Copies and re-lays out
+ * the weights, allocates the workspace for `d->max_tokens` tokens and encodes the TMA
+ * descriptors.  Errors: KLT_ERR_INVALID_ARG (null d/w/out or a null weight pointer),
+ * KLT_ERR_UNSUPPORTED (shape rules above; device is not compute capability 10.3),
+ * KLT_ERR_ALIGN, KLT_ERR_OOM, KLT_ERR_CUDA.  On error *out is left NULL. */
+int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_handle** out);
+
+/* Run the tail for M tokens, asynchronously on `stream`.
+ *   x      device bf16 [M, H]  hidden state (shared-expert input);
+ *   z      device bf16 [M, L]  latent state (routed-expert input);
+ *   logits device f32  [M, E]  router logits (finite values);
+ *   out    device bf16 [M, H]  result.
+ * M == 0 launches nothing and returns KLT_OK.  The handle's workspace is reused by every
+ * call, so calls on one handle must be ordered on one stream (or synchronised).
+ * Errors: KLT_ERR_INVALID_ARG (null handle or pointer, M < 0, M > max_tokens),
+ * KLT_ERR_ALIGN, KLT_ERR_CUDA (a launch failed).  Device-side faults of bounded waits are
+ * reported later by klt_status. */
+int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits, int32_t M,
+                void* out, klt_routing* routing_out, klt_debug* dbg, void* stream);
+
+/* Sticky device status of the handle: KLT_OK or KLT_ERR_DEVICE_TIMEOUT.  Reads device
+ * memory synchronously, so call it after the forward's stream has been synchronised.  A
+ * handle that reported a device error must be destroyed. */
+int klt_status(klt_handle* h);
+
+/* Free everything the handle owns (synchronises the device first).  NULL is a no-op. */
+int klt_destroy(klt_handle* h);
+
+/* Static description of a status code. */
+const char* klt_strerror(int code);
+
+/* Number of kernels one klt_forward launches for the given M and handle (0 for M == 0). */
+int klt_launch_count(const klt_handle* h, int32_t M);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KLT_H_ */

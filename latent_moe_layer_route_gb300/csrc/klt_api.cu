@@ -1,0 +1,509 @@
+// Host side of the latent-MoE tail C ABI: argument checks, owned weight copies, the
+// workspace, TMA descriptor encoding and the per-forward launch chain
+//
+//   route_quant -> perm_hist -> perm_scatter -> GEMM(shared L1 + routed L1)
+//   -> GEMM(routed L2 + combine) -> norm -> GEMM(up-projection + shared L2 -> out)
+//
+// all on the caller's stream, chained with programmatic dependent launch.  The shared
+// expert's down-projection is fused into the output GEMM as extra K blocks
+// ([n | a_s] . [W_up | Ws2]^T), so the shared output is added to the up-projection in
+// the fp32 accumulator and the result is rounded to bf16 once.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "../../include/klt.h"
+#include "klt_internal.h"
+
+using namespace klt;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// Row-major [rows, cols] matrix of `esize`-byte elements; box = box_cols x box_rows with
+// box_cols * esize == 128 (one 128-byte swizzle row); out-of-range elements read as zero.
+bool encode_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize,
+               uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * static_cast<uint64_t>(esize)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int kNumBN = 2;
+constexpr int kBN[kNumBN] = {16, 128};
+constexpr int kMaxSplitUnits = 3 * 160;  // split-K tiles*splits bound per task
+
+}  // namespace
+
+struct klt_handle {
+  klt_dims d;
+  uint32_t flags;
+  int device;
+  int num_sms;
+  // owned weights
+  uint8_t *w13, *w2;
+  float *w13_s, *w2_s;
+  __nv_bfloat16 *ws13, *ws2, *w_up, *gamma;
+  // workspace
+  int32_t *ids, *cnt, *off, *tile_off, *gidx, *slot, *pos, *hist;
+  float *wts, *zs, *zsT, *asT, *r, *ws;
+  uint8_t *zq, *zq_perm, *aq;
+  __nv_bfloat16 *n, *a_s;
+  int *split_cnt, *sched, *err;
+  int cap, max_hist_blocks;
+  // descriptors per BN variant (token-side maps depend on the box height)
+  CUtensorMap tm_w13, tm_w2, tm_ws13, tm_ws2, tm_wup;
+  CUtensorMap tm_zqp[kNumBN], tm_aq[kNumBN], tm_n[kNumBN], tm_as[kNumBN];
+  void* allocs[48];
+  int nallocs;
+};
+
+namespace {
+
+cudaError_t halloc(klt_handle* h, void** p, size_t bytes) {
+  cudaError_t e = cudaMalloc(p, bytes < 256 ? 256 : bytes);
+  if (e != cudaSuccess) return e;
+  h->allocs[h->nallocs++] = *p;
+  return cudaMemset(*p, 0, bytes < 256 ? 256 : bytes);
+}
+
+void free_all(klt_handle* h) {
+  for (int i = 0; i < h->nallocs; ++i) cudaFree(h->allocs[i]);
+  h->nallocs = 0;
+}
+
+int check_dims(const klt_dims* d) {
+  if (!(d->eps > 0.f) || d->eps > 1.f || d->max_tokens < 1 || d->E < 1 || d->topk < 1)
+    return KLT_ERR_INVALID_ARG;
+  if (d->H <= 0 || d->L <= 0 || d->I <= 0 || d->Is <= 0) return KLT_ERR_INVALID_ARG;
+  if (d->H % 128 || d->L % 128 || d->I % 128 || d->Is % 128) return KLT_ERR_UNSUPPORTED;
+  if (d->E > MAX_E || d->topk > d->E || d->topk > MAX_TOPK) return KLT_ERR_UNSUPPORTED;
+  if (d->routed_fmt != KLT_FMT_FP8_B128 && d->routed_fmt != KLT_FMT_NVFP4)
+    return KLT_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(d->max_tokens) * d->topk > (1 << 20)) return KLT_ERR_UNSUPPORTED;
+  return KLT_OK;
+}
+
+int bn_index(int M) { return M <= 32 ? 0 : 1; }
+
+// k splits for a non-routed task so that a launch has enough units to fill the GPU,
+// keeping split-K partial traffic small next to the weight bytes.
+void plan_split(GemmTask& T, int ntiles, int target_units, int bn) {
+  const int tiles = ntiles * T.ftiles;
+  int ks = 1;
+  if (tiles < target_units) {
+    ks = (target_units + tiles - 1) / tiles;
+    const int min_kb = std::max(4, bn / 8);
+    ks = std::min(ks, std::max(1, T.kb_total / min_kb));
+    while (ks > 1 && tiles * ks > kMaxSplitUnits) --ks;
+  }
+  T.kb_per_split = (T.kb_total + ks - 1) / ks;
+  T.ksplit = (T.kb_total + T.kb_per_split - 1) / T.kb_per_split;
+  T.ntiles = ntiles;
+  T.units = ntiles * T.ftiles * T.ksplit;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* klt_strerror(int code) {
+  switch (code) {
+    case KLT_OK: return "ok";
+    case KLT_ERR_INVALID_ARG: return "invalid argument";
+    case KLT_ERR_UNSUPPORTED: return "unsupported shape, format or device";
+    case KLT_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case KLT_ERR_CUDA: return "CUDA call failed";
+    case KLT_ERR_DEVICE_TIMEOUT: return "bounded device wait expired";
+    case KLT_ERR_OOM: return "device allocation failed";
+    default: return "unknown status";
+  }
+}
+
+int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_handle** out) {
+  if (!out) return KLT_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!d || !w) return KLT_ERR_INVALID_ARG;
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (d->routed_fmt == KLT_FMT_NVFP4) return KLT_ERR_UNSUPPORTED;  // not in this build yet
+  const void* ptrs[] = {w->w13, w->w13_scale, w->w2, w->w2_scale, w->ws13, w->ws2,
+                        w->w_up, w->gamma};
+  for (const void* p : ptrs)
+    if (!p) return KLT_ERR_INVALID_ARG;
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return KLT_ERR_ALIGN;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KLT_ERR_CUDA;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return KLT_ERR_CUDA;
+  if (prop.major != 10 || prop.minor != 3) return KLT_ERR_UNSUPPORTED;
+  if (!get_encode()) return KLT_ERR_CUDA;
+
+  klt_handle* h = new (std::nothrow) klt_handle();
+  if (!h) return KLT_ERR_OOM;
+  std::memset(h, 0, sizeof(*h));
+  h->d = *d;
+  h->flags = flags;
+  h->device = dev;
+  h->num_sms = prop.multiProcessorCount;
+  const int64_t E = d->E, H = d->H, L = d->L, I = d->I, Is = d->Is, k = d->topk;
+  const int64_t Mx = d->max_tokens;
+  h->cap = static_cast<int>(Mx * k);
+  h->max_hist_blocks = (h->cap + PERM_BLOCK - 1) / PERM_BLOCK;
+  const int64_t cap = h->cap;
+
+#define KLT_ALLOC(ptr, bytes)                                                   \
+  do {                                                                          \
+    if (halloc(h, reinterpret_cast<void**>(&(ptr)), (bytes)) != cudaSuccess) {  \
+      free_all(h);                                                              \
+      delete h;                                                                 \
+      return KLT_ERR_OOM;                                                       \
+    }                                                                           \
+  } while (0)
+  KLT_ALLOC(h->w13, E * 2 * I * L);
+  KLT_ALLOC(h->w13_s, E * (2 * I / 128) * (L / 128) * 4);
+  KLT_ALLOC(h->w2, E * L * I);
+  KLT_ALLOC(h->w2_s, E * (L / 128) * (I / 128) * 4);
+  KLT_ALLOC(h->ws13, 2 * Is * H * 2);
+  KLT_ALLOC(h->ws2, H * Is * 2);
+  KLT_ALLOC(h->w_up, H * L * 2);
+  KLT_ALLOC(h->gamma, L * 2);
+  KLT_ALLOC(h->ids, cap * 4);
+  KLT_ALLOC(h->wts, cap * 4);
+  KLT_ALLOC(h->pos, cap * 4);
+  KLT_ALLOC(h->gidx, cap * 4);
+  KLT_ALLOC(h->slot, cap * 4);
+  KLT_ALLOC(h->hist, static_cast<int64_t>(h->max_hist_blocks) * E * 4);
+  KLT_ALLOC(h->cnt, E * 4);
+  KLT_ALLOC(h->off, (E + 1) * 4);
+  KLT_ALLOC(h->tile_off, (E + 1) * 4);
+  KLT_ALLOC(h->zq, Mx * L);
+  KLT_ALLOC(h->zs, Mx * (L / 128) * 4);
+  KLT_ALLOC(h->zq_perm, cap * L);
+  KLT_ALLOC(h->zsT, (L / 128) * cap * 4);
+  KLT_ALLOC(h->aq, cap * I);
+  KLT_ALLOC(h->asT, (I / 128) * cap * 4);
+  KLT_ALLOC(h->r, Mx * L * 4);
+  KLT_ALLOC(h->n, Mx * L * 2);
+  KLT_ALLOC(h->a_s, Mx * Is * 2);
+  KLT_ALLOC(h->ws, 2LL * kMaxSplitUnits * 2 * 128 * 128 * 4);
+  KLT_ALLOC(h->split_cnt, 2LL * kMaxSplitUnits * 4);
+  KLT_ALLOC(h->sched, 64 * 4);
+  KLT_ALLOC(h->err, 256);
+#undef KLT_ALLOC
+
+  bool ok = true;
+  ok &= cudaMemcpy(h->w13, w->w13, E * 2 * I * L, cudaMemcpyDeviceToDevice) == cudaSuccess;
+  ok &= cudaMemcpy(h->w13_s, w->w13_scale, E * (2 * I / 128) * (L / 128) * 4,
+                   cudaMemcpyDeviceToDevice) == cudaSuccess;
+  ok &= cudaMemcpy(h->w2, w->w2, E * L * I, cudaMemcpyDeviceToDevice) == cudaSuccess;
+  ok &= cudaMemcpy(h->w2_s, w->w2_scale, E * (L / 128) * (I / 128) * 4,
+                   cudaMemcpyDeviceToDevice) == cudaSuccess;
+  ok &= cudaMemcpy(h->ws13, w->ws13, 2 * Is * H * 2, cudaMemcpyDeviceToDevice) == cudaSuccess;
+  ok &= cudaMemcpy(h->ws2, w->ws2, H * Is * 2, cudaMemcpyDeviceToDevice) == cudaSuccess;
+  ok &= cudaMemcpy(h->w_up, w->w_up, H * L * 2, cudaMemcpyDeviceToDevice) == cudaSuccess;
+  ok &= cudaMemcpy(h->gamma, w->gamma, L * 2, cudaMemcpyDeviceToDevice) == cudaSuccess;
+
+  const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  ok &= encode_2d(&h->tm_w13, h->w13, U8, 1, E * 2 * I, L, 128);
+  ok &= encode_2d(&h->tm_w2, h->w2, U8, 1, E * L, I, 128);
+  ok &= encode_2d(&h->tm_ws13, h->ws13, BF, 2, 2 * Is, H, 128);
+  ok &= encode_2d(&h->tm_ws2, h->ws2, BF, 2, H, Is, 128);
+  ok &= encode_2d(&h->tm_wup, h->w_up, BF, 2, H, L, 128);
+  for (int b = 0; b < kNumBN; ++b) {
+    ok &= encode_2d(&h->tm_zqp[b], h->zq_perm, U8, 1, cap, L, kBN[b]);
+    ok &= encode_2d(&h->tm_aq[b], h->aq, U8, 1, cap, I, kBN[b]);
+    ok &= encode_2d(&h->tm_n[b], h->n, BF, 2, Mx, L, kBN[b]);
+    ok &= encode_2d(&h->tm_as[b], h->a_s, BF, 2, Mx, Is, kBN[b]);
+  }
+  if (!ok || cudaDeviceSynchronize() != cudaSuccess) {
+    free_all(h);
+    delete h;
+    return KLT_ERR_CUDA;
+  }
+  *out = h;
+  return KLT_OK;
+}
+
+int klt_launch_count(const klt_handle* h, int32_t M) {
+  if (!h || M <= 0) return 0;
+  return 7;
+}
+
+int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits, int32_t M,
+                void* out, klt_routing* ro, klt_debug* dbg, void* stream) {
+  if (!h) return KLT_ERR_INVALID_ARG;
+  if (M < 0 || M > h->d.max_tokens) return KLT_ERR_INVALID_ARG;
+  if (M == 0) return KLT_OK;
+  if (!x || !z || !logits || !out) return KLT_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(z) || !aligned16(logits) || !aligned16(out))
+    return KLT_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool pdl = !(h->flags & KLT_FLAG_NO_PDL);
+  const klt_dims& d = h->d;
+  const int E = d.E, k = d.topk, L = d.L, I = d.I, Is = d.Is, H = d.H;
+  const int bi = bn_index(M);
+  const int BN = kBN[bi];
+  const int Mk = M * k;
+  const int nblocks = (Mk + PERM_BLOCK - 1) / PERM_BLOCK;
+  const long long timeout_cycles =
+      static_cast<long long>(dbg && dbg->timeout_ms > 0 ? dbg->timeout_ms : 1000) * 2000000LL;
+  int launch = 0;
+  auto mark = [&]() {
+    if (dbg && launch < 8 && dbg->events[launch])
+      cudaEventRecord(static_cast<cudaEvent_t>(dbg->events[launch]), s);
+    ++launch;
+  };
+#define KLT_LAUNCH(expr)                      \
+  do {                                        \
+    if ((expr) != cudaSuccess) return KLT_ERR_CUDA; \
+    mark();                                   \
+  } while (0)
+
+  // ---- K0: routing + latent quantisation + zero r + zero tile counters
+  RouteParams rp;
+  rp.logits = logits;
+  rp.z = static_cast<const __nv_bfloat16*>(z);
+  rp.ids = h->ids;
+  rp.wts = h->wts;
+  rp.zq = h->zq;
+  rp.zs = h->zs;
+  rp.r = h->r;
+  rp.sched = h->sched;
+  rp.nsched = 8;
+  rp.M = M;
+  rp.E = E;
+  rp.k = k;
+  rp.L = L;
+  KLT_LAUNCH(launch_route(rp, s, pdl));
+
+  // ---- K1: permutation
+  PermParams pp;
+  pp.ids = h->ids;
+  pp.hist = h->hist;
+  pp.cnt = h->cnt;
+  pp.off = h->off;
+  pp.tile_off = h->tile_off;
+  pp.gidx = h->gidx;
+  pp.slot = h->slot;
+  pp.pos = h->pos;
+  pp.zq = h->zq;
+  pp.zs = h->zs;
+  pp.zq_perm = h->zq_perm;
+  pp.zsT = h->zsT;
+  pp.M = M;
+  pp.E = E;
+  pp.k = k;
+  pp.L = L;
+  pp.cap = h->cap;
+  pp.bn = BN;
+  pp.nblocks = nblocks;
+  KLT_LAUNCH(launch_perm_hist(pp, s, pdl));
+  KLT_LAUNCH(launch_perm_scatter(pp, s, pdl));
+
+  // ---- common GEMM parameters
+  GemmParams gp;
+  std::memset(&gp, 0, sizeof(gp));
+  gp.M = M;
+  gp.E = E;
+  gp.L = L;
+  gp.I = I;
+  gp.Is = Is;
+  gp.H = H;
+  gp.cap = h->cap;
+  gp.tile_off = h->tile_off;
+  gp.off = h->off;
+  gp.gidx = h->gidx;
+  gp.slot = h->slot;
+  gp.wts = h->wts;
+  gp.zsT = h->zsT;
+  gp.w13_s = h->w13_s;
+  gp.w2_s = h->w2_s;
+  gp.aq = h->aq;
+  gp.asT = h->asT;
+  gp.r = h->r;
+  gp.a_s = h->a_s;
+  gp.out = static_cast<__nv_bfloat16*>(out);
+  gp.ws = h->ws;
+  gp.cnt = h->split_cnt;
+  gp.err = h->err;
+  gp.timeout = timeout_cycles;
+  const int ntiles = (M + BN - 1) / BN;
+  const int grid = h->num_sms;
+  const size_t ws_task = static_cast<size_t>(kMaxSplitUnits) * 2 * 128 * 128;
+
+  // ---- GEMM 1: shared L1 (bf16, split-K) + routed L1 (fp8, SwiGLU + act quant)
+  {
+    GemmParams g1 = gp;
+    g1.ntasks = 2;
+    g1.sched = h->sched + 0;
+    g1.stall_after = dbg ? dbg->stall_after_kblocks : 0;
+    GemmTask& S = g1.task[0];
+    S.kind = TASK_SHARED_L1;
+    S.routed = 0;
+    S.ftiles = Is / 128;
+    S.kb_total = H / 64;
+    S.kb_split0 = S.kb_total;
+    S.a_up_off = Is;
+    S.ws_tile_base = 0;
+    // split so that a shared unit streams about as many bytes as a routed L1 unit
+    plan_split(S, ntiles,
+               std::min(ntiles * S.ftiles * std::max(1, (S.kb_total * 128) / L),
+                        2 * h->num_sms),
+               BN);
+    if (!encode_2d(&S.tmB[0], x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, H, BN))
+      return KLT_ERR_CUDA;
+    S.tmA[0] = h->tm_ws13;
+    S.tmA[1] = h->tm_ws13;
+    S.tmB[1] = S.tmB[0];
+    GemmTask& R = g1.task[1];
+    R.kind = TASK_ROUTED_L1;
+    R.routed = 1;
+    R.ftiles = I / 128;
+    R.kb_total = L / 128;
+    R.kb_split0 = R.kb_total;
+    R.ksplit = 1;
+    R.kb_per_split = R.kb_total;
+    R.a_up_off = I;
+    R.a_rows_expert = 2 * I;
+    R.tmA[0] = h->tm_w13;
+    R.tmA[1] = h->tm_w13;
+    R.tmB[0] = h->tm_zqp[bi];
+    R.tmB[1] = h->tm_zqp[bi];
+    KLT_LAUNCH(launch_gemm(g1, BN, grid, s, pdl));
+  }
+  // ---- GEMM 2: routed L2 with the top-k weighted scatter-combine into r
+  {
+    GemmParams g2 = gp;
+    g2.ntasks = 1;
+    g2.sched = h->sched + 1;
+    GemmTask& R = g2.task[0];
+    R.kind = TASK_ROUTED_L2;
+    R.routed = 1;
+    R.ftiles = L / 128;
+    R.kb_total = I / 128;
+    R.kb_split0 = R.kb_total;
+    R.ksplit = 1;
+    R.kb_per_split = R.kb_total;
+    R.a_rows_expert = L;
+    R.tmA[0] = h->tm_w2;
+    R.tmA[1] = h->tm_w2;
+    R.tmB[0] = h->tm_aq[bi];
+    R.tmB[1] = h->tm_aq[bi];
+    KLT_LAUNCH(launch_gemm(g2, BN, grid, s, pdl));
+  }
+  // ---- RMSNorm of the combine
+  NormParams np;
+  np.r = h->r;
+  np.gamma = h->gamma;
+  np.n = h->n;
+  np.M = M;
+  np.L = L;
+  np.eps = d.eps;
+  KLT_LAUNCH(launch_norm(np, s, pdl));
+  // ---- GEMM 3: out = bf16([n | a_s] . [W_up | Ws2]^T)
+  {
+    GemmParams g3 = gp;
+    g3.ntasks = 1;
+    g3.sched = h->sched + 2;
+    g3.ws = h->ws + ws_task;
+    g3.cnt = h->split_cnt + kMaxSplitUnits;
+    GemmTask& O = g3.task[0];
+    O.kind = TASK_OUT;
+    O.routed = 0;
+    O.ftiles = H / 128;
+    O.kb_total = L / 64 + Is / 64;
+    O.kb_split0 = L / 64;
+    O.ws_tile_base = 0;
+    plan_split(O, ntiles, 2 * h->num_sms, BN);
+    O.tmA[0] = h->tm_wup;
+    O.tmA[1] = h->tm_ws2;
+    O.tmB[0] = h->tm_n[bi];
+    O.tmB[1] = h->tm_as[bi];
+    KLT_LAUNCH(launch_gemm(g3, BN, grid, s, pdl));
+  }
+#undef KLT_LAUNCH
+
+  // ---- optional copies of routing results and stage outputs
+  auto cp = [&](void* dst, const void* src, size_t bytes) -> bool {
+    return !dst || cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s) == cudaSuccess;
+  };
+  bool ok = true;
+  if (ro) {
+    ok &= cp(ro->ids, h->ids, static_cast<size_t>(Mk) * 4);
+    ok &= cp(ro->weights, h->wts, static_cast<size_t>(Mk) * 4);
+    ok &= cp(ro->cnt, h->cnt, static_cast<size_t>(E) * 4);
+    ok &= cp(ro->off, h->off, static_cast<size_t>(E + 1) * 4);
+    ok &= cp(ro->gidx, h->gidx, static_cast<size_t>(Mk) * 4);
+    ok &= cp(ro->slot, h->slot, static_cast<size_t>(Mk) * 4);
+    ok &= cp(ro->pos, h->pos, static_cast<size_t>(Mk) * 4);
+  }
+  if (dbg) {
+    ok &= cp(dbg->zq, h->zq, static_cast<size_t>(M) * L);
+    ok &= cp(dbg->zs, h->zs, static_cast<size_t>(M) * (L / 128) * 4);
+    ok &= cp(dbg->r, h->r, static_cast<size_t>(M) * L * 4);
+    ok &= cp(dbg->n, h->n, static_cast<size_t>(M) * L * 2);
+    ok &= cp(dbg->a_s, h->a_s, static_cast<size_t>(M) * Is * 2);
+    ok &= cp(dbg->aq, h->aq, static_cast<size_t>(Mk) * I);
+    if (dbg->as) {  // stored transposed [I/128, cap] on the device
+      const int G = I / 128;
+      for (int g = 0; g < G; ++g)
+        ok &= cudaMemcpy2DAsync(dbg->as + g, G * sizeof(float),
+                                h->asT + static_cast<size_t>(g) * h->cap, sizeof(float),
+                                sizeof(float), Mk, cudaMemcpyDeviceToDevice,
+                                s) == cudaSuccess;
+    }
+  }
+  return ok ? KLT_OK : KLT_ERR_CUDA;
+}
+
+int klt_status(klt_handle* h) {
+  if (!h) return KLT_ERR_INVALID_ARG;
+  int e = 0;
+  if (cudaMemcpy(&e, h->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return KLT_ERR_CUDA;
+  return e ? KLT_ERR_DEVICE_TIMEOUT : KLT_OK;
+}
+
+int klt_destroy(klt_handle* h) {
+  if (!h) return KLT_OK;
+  cudaDeviceSynchronize();
+  free_all(h);
+  delete h;
+  return KLT_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,555 @@
+// Persistent tile engine of the latent-MoE tail on sm_103a (tcgen05 + TMEM + TMA).
+//
+// One kernel serves every GEMM of the tail.  A launch carries up to two tasks; its
+// persistent CTAs pull work units (one 128-row output tile x one token tile x one K
+// range) from a device counter, so routed expert tiles and shared-expert tiles of one
+// launch interleave on the SMs the way the MegaMoE scheduler co-schedules routed and
+// shared L1/L2 work (DeepGEMM PR 416, Implementation).
+//
+// Orientation: the weight matrix is the MMA "A" operand (128 output features per tile,
+// one TMEM lane each) and the tokens are the "B" operand (BN columns), so a decode batch
+// of a few tokens still fills the 128-row MMA and the kernel streams weights.
+//
+// Roles per CTA (1 CTA per SM):
+//   warp 0      TMA producer: decodes units, publishes them to a ring, streams A/B tiles
+//               (128-byte swizzled K-major, 128 bytes of K per stage) into STAGES buffers;
+//   warp 1      MMA issuer (one thread): tcgen05.mma into TMEM accumulator slots;
+//   warps 2..   epilogue: TMEM -> registers, then the task's fused epilogue.
+//
+// FP8 routed tasks use per-128-K promotion: every 128-wide K block is accumulated by the
+// tensor core into its own TMEM slot and the epilogue adds it into fp32 registers scaled
+// by (weight block scale x token group scale), because the scales are general fp32 and
+// no hardware block-scaled MMA takes them.  BF16 tasks accumulate the whole K range in
+// TMEM.  Every wait is bounded; an expired wait raises the CTA abort flag and the sticky
+// device error, and the CTA drains its own copies and MMAs before freeing TMEM.
+#include "klt_device.cuh"
+#include "klt_internal.h"
+
+namespace klt {
+
+namespace {
+
+template <int BN>
+struct Cfg {
+  static constexpr int EPI_WARPS = BN >= 64 ? 8 : 4;
+  static constexpr int THREADS = (2 + EPI_WARPS) * 32;
+  static constexpr int EPI_THREADS = EPI_WARPS * 32;
+  static constexpr int A_BYTES = 128 * 128;
+  static constexpr int B_BYTES = BN * 128;
+  static constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES;
+  static constexpr int STAGES = BN == 16 ? 6 : (BN == 128 ? 4 : 5);
+  static constexpr int SLOT_COLS = 2 * BN;
+  static constexpr int TMEM_COLS = BN <= 64 ? 256 : 512;
+  static constexpr int NACC = TMEM_COLS / SLOT_COLS;
+  static constexpr int US = 8;
+  static constexpr int COLS = BN / (EPI_WARPS / 4);
+  static_assert(COLS % 16 == 0, "epilogue works in 16-column chunks");
+  static_assert(NACC >= 2, "need two accumulator slots");
+};
+
+struct UnitInfo {
+  int task;   // -1: no more work
+  int e;      // routed expert
+  int row0;   // first token row of the B tile
+  int rows;   // valid token rows (D columns)
+  int ftile;  // 128-row output tile
+  int arow0;  // first A-map row of the (gate) tile
+  int kb0, kb1;
+  int tile_id;  // split-K tile (non-routed)
+  int split;
+};
+
+template <int BN>
+struct Smem {
+  using C = Cfg<BN>;
+  uint8_t* stages;
+  uint64_t *full, *empty, *tfull, *tempty, *ufull, *uempty, *drain;
+  UnitInfo* ring;
+  uint32_t* tmem_holder;
+  int* abort_flag;
+  int* last_flag;
+  float* red;  // [EPI_WARPS][COLS]
+
+  static constexpr int BAR_BYTES = 8 * (2 * C::STAGES + 2 * C::NACC + 2 * C::US + 1);
+  static constexpr int bytes() {
+    return C::STAGES * C::STAGE_BYTES + BAR_BYTES + C::US * (int)sizeof(UnitInfo) + 64 +
+           C::EPI_WARPS * C::COLS * 4 + 1024 /* alignment slack */;
+  }
+  __device__ explicit Smem(uint8_t* raw) {
+    uint8_t* base = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    stages = base;
+    uint64_t* b = reinterpret_cast<uint64_t*>(base + C::STAGES * C::STAGE_BYTES);
+    full = b;
+    empty = full + C::STAGES;
+    tfull = empty + C::STAGES;
+    tempty = tfull + C::NACC;
+    ufull = tempty + C::NACC;
+    uempty = ufull + C::US;
+    drain = uempty + C::US;
+    ring = reinterpret_cast<UnitInfo*>(drain + 1);
+    tmem_holder = reinterpret_cast<uint32_t*>(ring + C::US);
+    abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
+    last_flag = abort_flag + 1;
+    red = reinterpret_cast<float*>(tmem_holder + 16);
+  }
+};
+
+__device__ __forceinline__ bool is_pair(int kind) {
+  return kind == TASK_SHARED_L1 || kind == TASK_ROUTED_L1;
+}
+__device__ __forceinline__ bool is_promote(int kind) {
+  return kind == TASK_ROUTED_L1 || kind == TASK_ROUTED_L2;
+}
+
+template <int BN>
+__device__ UnitInfo decode_unit(const GemmParams& p, int u) {
+  UnitInfo info;
+  info.task = -1;
+  for (int ti = 0; ti < p.ntasks; ++ti) {
+    const GemmTask& T = p.task[ti];
+    if (T.routed) {
+      const int ntiles = p.tile_off[p.E];
+      const int units = ntiles * T.ftiles;
+      if (u < units) {
+        const int t = u / T.ftiles;
+        const int ft = u - t * T.ftiles;
+        int lo = 0, hi = p.E - 1;  // largest e with tile_off[e] <= t
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (p.tile_off[mid] <= t) lo = mid; else hi = mid - 1;
+        }
+        const int e = lo;
+        info.task = ti;
+        info.e = e;
+        info.row0 = p.off[e] + (t - p.tile_off[e]) * BN;
+        info.rows = min(BN, p.off[e + 1] - info.row0);
+        info.ftile = ft;
+        info.arow0 = e * T.a_rows_expert + ft * 128;
+        info.kb0 = 0;
+        info.kb1 = T.kb_total;
+        info.tile_id = 0;
+        info.split = 0;
+        return info;
+      }
+      u -= units;
+    } else {
+      if (u < T.units) {
+        const int per_n = T.ftiles * T.ksplit;
+        const int nt = u / per_n;
+        const int rem = u - nt * per_n;
+        const int ft = rem / T.ksplit;
+        const int sp = rem - ft * T.ksplit;
+        info.task = ti;
+        info.e = 0;
+        info.row0 = nt * BN;
+        info.rows = min(BN, p.M - info.row0);
+        info.ftile = ft;
+        info.arow0 = ft * 128;
+        info.kb0 = sp * T.kb_per_split;
+        info.kb1 = min(T.kb_total, info.kb0 + T.kb_per_split);
+        info.tile_id = T.ws_tile_base + nt * T.ftiles + ft;
+        info.split = sp;
+        return info;
+      }
+      u -= T.units;
+    }
+  }
+  return info;
+}
+
+// ------------------------------------------------------------------ producer (1 thread)
+template <int BN>
+__device__ void run_producer(const GemmParams& p, Smem<BN>& sm) {
+  using C = Cfg<BN>;
+  const uint64_t pol_w = policy_evict_first();
+  const uint64_t pol_t = policy_evict_last();
+  int stage = 0, us = 0;
+  uint32_t phase = 0, uphase = 0;
+  long long issued = 0;
+  int dummy_abort = 0;
+  bool stalled = false;
+  for (;;) {
+    const int u = atomicAdd(p.sched, 1);
+    const UnitInfo info = decode_unit<BN>(p, u);
+    if (!mbar_wait(&sm.uempty[us], uphase ^ 1, sm.abort_flag, p.err, p.timeout)) break;
+    sm.ring[us] = info;
+    mbar_arrive(&sm.ufull[us]);
+    if (++us == C::US) { us = 0; uphase ^= 1; }
+    if (info.task < 0) break;
+    const GemmTask& T = p.task[info.task];
+    const bool pair = is_pair(T.kind);
+    const int elems_per_kb = is_promote(T.kind) ? 128 : 64;
+    const uint32_t bytes = (pair ? 2 : 1) * C::A_BYTES + C::B_BYTES;
+    for (int kb = info.kb0; kb < info.kb1; ++kb) {
+      if (p.stall_after > 0 && issued >= p.stall_after) { stalled = true; break; }
+      if (!mbar_wait(&sm.empty[stage], phase ^ 1, sm.abort_flag, p.err, p.timeout)) {
+        stalled = true;
+        break;
+      }
+      const int m = kb < T.kb_split0 ? 0 : 1;
+      const int inner = (m ? kb - T.kb_split0 : kb) * elems_per_kb;
+      uint8_t* st = sm.stages + stage * C::STAGE_BYTES;
+      mbar_arrive_expect_tx(&sm.full[stage], bytes);
+      tma_load_2d(st, &T.tmA[m], &sm.full[stage], inner, info.arow0, pol_w);
+      if (pair)
+        tma_load_2d(st + C::A_BYTES, &T.tmA[m], &sm.full[stage], inner,
+                    info.arow0 + T.a_up_off, pol_w);
+      tma_load_2d(st + 2 * C::A_BYTES, &T.tmB[m], &sm.full[stage], inner, info.row0, pol_t);
+      ++issued;
+      if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+    }
+    if (stalled) break;
+  }
+  // Drain: wait (bounded, ignoring the abort flag) for this thread's last copies, so no
+  // TMA write into shared memory outlives the CTA.
+  const long long first = issued > C::STAGES ? issued - C::STAGES : 0;
+  for (long long i = first; i < issued; ++i) {
+    const int s = static_cast<int>(i % C::STAGES);
+    const uint32_t par = static_cast<uint32_t>((i / C::STAGES) & 1);
+    mbar_wait(&sm.full[s], par, &dummy_abort, p.err, p.timeout);
+  }
+}
+
+// ------------------------------------------------------------------ MMA issuer (1 thread)
+template <int BN>
+__device__ void run_mma(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_base) {
+  using C = Cfg<BN>;
+  int stage = 0, us = 0, acc = 0;
+  uint32_t phase = 0, uphase = 0, aphase = 0;
+  bool ok = true;
+  const uint32_t idesc_bf16 = idesc_make(1, 128, BN);
+  const uint32_t idesc_fp8 = idesc_make(0, 128, BN);
+  while (ok) {
+    if (!mbar_wait(&sm.ufull[us], uphase, sm.abort_flag, p.err, p.timeout)) break;
+    const UnitInfo info = sm.ring[us];
+    mbar_arrive(&sm.uempty[us]);
+    if (++us == C::US) { us = 0; uphase ^= 1; }
+    if (info.task < 0) break;
+    const int kind = p.task[info.task].kind;
+    const bool pair = is_pair(kind);
+    const bool promote = is_promote(kind);
+    const uint32_t idesc = promote ? idesc_fp8 : idesc_bf16;
+    if (!promote) {
+      if (!mbar_wait(&sm.tempty[acc], aphase ^ 1, sm.abort_flag, p.err, p.timeout)) break;
+      tc_fence_after();
+    }
+    for (int kb = info.kb0; kb < info.kb1; ++kb) {
+      if (promote) {
+        if (!mbar_wait(&sm.tempty[acc], aphase ^ 1, sm.abort_flag, p.err, p.timeout)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      if (!mbar_wait(&sm.full[stage], phase, sm.abort_flag, p.err, p.timeout)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d = tmem_base + static_cast<uint32_t>(acc * C::SLOT_COLS);
+      const uint32_t sa = smem_u32(sm.stages + stage * C::STAGE_BYTES);
+      const uint64_t da = sdesc_sw128(sa);
+      const uint64_t du = sdesc_sw128(sa + C::A_BYTES);
+      const uint64_t db = sdesc_sw128(sa + 2 * C::A_BYTES);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint32_t accum = promote ? (kk > 0) : (kb > info.kb0 || kk > 0);
+        if (promote) {
+          mma_fp8(d, da + 2 * kk, db + 2 * kk, idesc, accum);
+          if (pair) mma_fp8(d + BN, du + 2 * kk, db + 2 * kk, idesc, accum);
+        } else {
+          mma_bf16(d, da + 2 * kk, db + 2 * kk, idesc, accum);
+          if (pair) mma_bf16(d + BN, du + 2 * kk, db + 2 * kk, idesc, accum);
+        }
+      }
+      tc_commit(&sm.empty[stage]);
+      if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+      if (promote) {
+        tc_commit(&sm.tfull[acc]);
+        if (++acc == C::NACC) { acc = 0; aphase ^= 1; }
+      }
+    }
+    if (!ok) break;
+    if (!promote) {
+      tc_commit(&sm.tfull[acc]);
+      if (++acc == C::NACC) { acc = 0; aphase ^= 1; }
+    }
+  }
+  // Drain: all MMAs issued by this thread complete before TMEM is released.
+  int dummy_abort = 0;
+  tc_commit(sm.drain);
+  mbar_wait(sm.drain, 0, &dummy_abort, p.err, p.timeout);
+}
+
+// ------------------------------------------------------------------ epilogue
+template <int BN>
+__device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_base) {
+  using C = Cfg<BN>;
+  constexpr int COLS = C::COLS;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ew = warp - 2;
+  const int quad = warp & 3;            // TMEM lane quadrant this warp may access
+  const int half = ew >> 2;             // column group of this warp
+  const int row = quad * 32 + lane;     // output feature within the tile
+  const int c0 = half * COLS;
+  const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+  int us = 0, acc = 0;
+  uint32_t uphase = 0, aphase = 0;
+  const int G_L = p.L / 128, G_I = p.I / 128;
+
+  for (;;) {
+    if (!mbar_wait(&sm.ufull[us], uphase, sm.abort_flag, p.err, p.timeout)) return;
+    const UnitInfo info = sm.ring[us];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.uempty[us]);
+    if (++us == C::US) { us = 0; uphase ^= 1; }
+    if (info.task < 0) return;
+    const GemmTask& T = p.task[info.task];
+    const int kind = T.kind;
+    const bool pair = is_pair(kind);
+
+    float g[COLS], u[COLS];
+#pragma unroll
+    for (int j = 0; j < COLS; ++j) { g[j] = 0.f; u[j] = 0.f; }
+
+    if (is_promote(kind)) {
+      const float* tok_scale = kind == TASK_ROUTED_L1 ? p.zsT : p.asT;
+      for (int kb = info.kb0; kb < info.kb1; ++kb) {
+        float sw_g, sw_u = 0.f;
+        if (kind == TASK_ROUTED_L1) {
+          const size_t rb = static_cast<size_t>(info.e) * (2 * G_I);
+          sw_g = __ldg(p.w13_s + (rb + info.ftile) * G_L + kb);
+          sw_u = __ldg(p.w13_s + (rb + G_I + info.ftile) * G_L + kb);
+        } else {
+          sw_g = __ldg(p.w2_s + (static_cast<size_t>(info.e) * G_L + info.ftile) * G_I + kb);
+        }
+        const float* ts = tok_scale + static_cast<size_t>(kb) * p.cap + info.row0 + c0;
+        if (!mbar_wait(&sm.tfull[acc], aphase, sm.abort_flag, p.err, p.timeout)) return;
+        tc_fence_after();
+        const uint32_t tb = tmem_base + lane_base + static_cast<uint32_t>(acc * C::SLOT_COLS);
+#pragma unroll
+        for (int ch = 0; ch < COLS / 16; ++ch) {
+          float pg[16], pu[16];
+          if (pair)
+            tmem_ld16x2(tb + c0 + ch * 16, tb + BN + c0 + ch * 16, pg, pu);
+          else
+            tmem_ld16(tb + c0 + ch * 16, pg);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int j = ch * 16 + i;
+            const float sa = (c0 + j < info.rows) ? __ldg(ts + j) : 0.f;
+            g[j] = fmaf(pg[i], sw_g * sa, g[j]);
+            if (pair) u[j] = fmaf(pu[i], sw_u * sa, u[j]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.tempty[acc]);
+        if (++acc == C::NACC) { acc = 0; aphase ^= 1; }
+      }
+    } else {
+      if (!mbar_wait(&sm.tfull[acc], aphase, sm.abort_flag, p.err, p.timeout)) return;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + lane_base + static_cast<uint32_t>(acc * C::SLOT_COLS);
+#pragma unroll
+      for (int ch = 0; ch < COLS / 16; ++ch) {
+        if (pair)
+          tmem_ld16x2(tb + c0 + ch * 16, tb + BN + c0 + ch * 16, g + ch * 16, u + ch * 16);
+        else
+          tmem_ld16(tb + c0 + ch * 16, g + ch * 16);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.tempty[acc]);
+      if (++acc == C::NACC) { acc = 0; aphase ^= 1; }
+    }
+
+    // ---- split-K: publish the partial; the last arriving split reduces in split order
+    if (!T.routed && T.ksplit > 1) {
+      const int parts = pair ? 2 : 1;
+      const size_t tile_floats = static_cast<size_t>(parts) * BN * 128;
+      float* mine = p.ws + (static_cast<size_t>(info.tile_id) * T.ksplit + info.split) *
+                               tile_floats;
+#pragma unroll
+      for (int j = 0; j < COLS; ++j) {
+        __stcg(mine + static_cast<size_t>(c0 + j) * 128 + row, g[j]);
+        if (pair) __stcg(mine + static_cast<size_t>(BN + c0 + j) * 128 + row, u[j]);
+      }
+      __threadfence();
+      named_bar_sync(1, C::EPI_THREADS);
+      if (ew == 0 && lane == 0) {
+        const int old = atomicAdd(p.cnt + info.tile_id, 1);
+        const int last = old == T.ksplit - 1;
+        if (last) p.cnt[info.tile_id] = 0;
+        *sm.last_flag = last;
+      }
+      named_bar_sync(1, C::EPI_THREADS);
+      if (!*sm.last_flag) continue;
+      __threadfence();
+      const float* all = p.ws + static_cast<size_t>(info.tile_id) * T.ksplit * tile_floats;
+#pragma unroll
+      for (int j = 0; j < COLS; ++j) { g[j] = 0.f; u[j] = 0.f; }
+      for (int s = 0; s < T.ksplit; ++s) {
+        const float* ps = all + static_cast<size_t>(s) * tile_floats;
+#pragma unroll
+        for (int j = 0; j < COLS; ++j) {
+          g[j] += __ldcg(ps + static_cast<size_t>(c0 + j) * 128 + row);
+          if (pair) u[j] += __ldcg(ps + static_cast<size_t>(BN + c0 + j) * 128 + row);
+        }
+      }
+    }
+
+    // ---- fused epilogues
+    if (kind == TASK_SHARED_L1) {
+      __nv_bfloat16* dst = p.a_s + static_cast<size_t>(info.ftile) * 128 + row;
+#pragma unroll
+      for (int j = 0; j < COLS; ++j) {
+        if (c0 + j < info.rows)
+          dst[static_cast<size_t>(info.row0 + c0 + j) * p.Is] =
+              __float2bfloat16_rn(silu_f(g[j]) * u[j]);
+      }
+    } else if (kind == TASK_OUT) {
+      __nv_bfloat16* dst = p.out + static_cast<size_t>(info.ftile) * 128 + row;
+#pragma unroll
+      for (int j = 0; j < COLS; ++j) {
+        if (c0 + j < info.rows)
+          dst[static_cast<size_t>(info.row0 + c0 + j) * p.H] = __float2bfloat16_rn(g[j]);
+      }
+    } else if (kind == TASK_ROUTED_L2) {
+      const int col = info.ftile * 128 + row;
+#pragma unroll
+      for (int j = 0; j < COLS; ++j) {
+        if (c0 + j < info.rows) {
+          const int pp = info.row0 + c0 + j;
+          const int tok = __ldg(p.gidx + pp);
+          const float wv = __ldg(p.wts + __ldg(p.slot + pp));
+          atomicAdd(p.r + static_cast<size_t>(tok) * p.L + col, wv * g[j]);
+        }
+      }
+    } else {  // TASK_ROUTED_L1: SwiGLU, then e4m3 per 128 features of each token
+      float* red = sm.red + ew * COLS;
+#pragma unroll
+      for (int j = 0; j < COLS; ++j) {
+        g[j] = silu_f(g[j]) * u[j];
+        float a = fabsf(g[j]);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+        if (lane == 0) red[j] = a;
+      }
+      named_bar_sync(2 + half, 128);
+      const float* r0 = sm.red + (half * 4) * COLS;
+      uint8_t* dst = p.aq + static_cast<size_t>(info.ftile) * 128 + row;
+#pragma unroll
+      for (int j = 0; j < COLS; ++j) {
+        const float amax = fmaxf(fmaxf(r0[j], r0[COLS + j]), fmaxf(r0[2 * COLS + j],
+                                                                   r0[3 * COLS + j]));
+        const float s = amax == 0.f ? 1.0f : amax / 448.0f;
+        if (c0 + j < info.rows) {
+          const size_t pp = static_cast<size_t>(info.row0 + c0 + j);
+          dst[pp * p.I] = f32_to_e4m3(g[j] / s);
+          if (quad == 0 && lane == 0) p.asT[static_cast<size_t>(info.ftile) * p.cap + pp] = s;
+        }
+      }
+      named_bar_sync(2 + half, 128);
+    }
+  }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
+    gemm_kernel(const __grid_constant__ GemmParams p) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  Smem<BN> sm(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    for (int a = 0; a < C::NACC; ++a) {
+      mbar_init(&sm.tfull[a], 1);
+      mbar_init(&sm.tempty[a], C::EPI_WARPS);
+    }
+    for (int u = 0; u < C::US; ++u) {
+      mbar_init(&sm.ufull[u], 1);
+      mbar_init(&sm.uempty[u], 1 + C::EPI_WARPS);
+    }
+    mbar_init(sm.drain, 1);
+    *sm.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int t = 0; t < p.ntasks; ++t) {
+      tma_prefetch_desc(&p.task[t].tmA[0]);
+      tma_prefetch_desc(&p.task[t].tmA[1]);
+      tma_prefetch_desc(&p.task[t].tmB[0]);
+      tma_prefetch_desc(&p.task[t].tmB[1]);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(sm.tmem_holder, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *sm.tmem_holder;
+
+  // Everything above touches only this CTA's resources; inputs written by the previous
+  // kernel in the stream are read only after this point.
+  pdl_wait();
+  pdl_trigger();
+
+  if (warp == 0) {
+    if (lane == 0) run_producer<BN>(p, sm);
+  } else if (warp == 1) {
+    if (lane == 0) run_mma<BN>(p, sm, tmem_base);
+  } else {
+    run_epilogue<BN>(p, sm, tmem_base);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+template <int BN>
+cudaError_t launch_bn(const GemmParams& p, int grid, cudaStream_t s, bool pdl) {
+  using C = Cfg<BN>;
+  const int smem = Smem<BN>::bytes();
+  cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<BN>, p);
+}
+
+}  // namespace
+
+int gemm_smem_bytes(int bn) {
+  return bn == 16 ? Smem<16>::bytes() : Smem<128>::bytes();
+}
+
+cudaError_t launch_gemm(const GemmParams& p, int bn, int grid, cudaStream_t s, bool pdl) {
+  if (bn == 16) return launch_bn<16>(p, grid, s, pdl);
+  if (bn == 128) return launch_bn<128>(p, grid, s, pdl);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace klt

@@ -1,0 +1,117 @@
+// Host/device shared definitions of the latent-MoE tail library: kernel parameter blocks
+// and the launchers each kernel file exports to the host API.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace klt {
+
+// ------------------------------------------------------------------ routing kernels
+struct RouteParams {
+  const float* logits;     // [M, E]
+  const __nv_bfloat16* z;  // [M, L]
+  int32_t* ids;            // [M, k]
+  float* wts;              // [M, k]
+  uint8_t* zq;             // [M, L]
+  float* zs;               // [M, L/128]
+  float* r;                // [M, L] zeroed here (the routed combine accumulates into it)
+  int* sched;              // per-launch tile counters, zeroed here
+  int nsched;
+  int M, E, k, L;
+};
+
+struct PermParams {
+  const int32_t* ids;  // [M*k]
+  int* hist;           // [nblocks, E] per-block expert counts
+  int32_t* cnt;        // [E]
+  int32_t* off;        // [E+1]
+  int32_t* tile_off;   // [E+1] prefix of ceil(cnt/BN)
+  int32_t* gidx;       // [cap]
+  int32_t* slot;       // [cap]
+  int32_t* pos;        // [M*k]
+  const uint8_t* zq;   // [M, L]
+  const float* zs;     // [M, L/128]
+  uint8_t* zq_perm;    // [cap, L]
+  float* zsT;          // [L/128, cap]
+  int M, E, k, L, cap, bn, nblocks;
+};
+
+struct NormParams {
+  const float* r;              // [M, L]
+  const __nv_bfloat16* gamma;  // [L]
+  __nv_bfloat16* n;            // [M, L]
+  int M, L;
+  float eps;
+};
+
+// ------------------------------------------------------------------ tile GEMM engine
+enum TaskKind : int {
+  TASK_NONE = 0,
+  TASK_SHARED_L1 = 1,  // bf16 x . Ws13^T, gate/up pair -> SwiGLU -> a_s (bf16)
+  TASK_ROUTED_L1 = 2,  // fp8 zq_perm . W13_e^T, pair, per-128-K promotion -> SwiGLU ->
+                       // per-128 e4m3 quantisation -> aq, asT
+  TASK_ROUTED_L2 = 3,  // fp8 aq . W2_e^T, promotion -> r[gidx] += w * y (fp32 atomics)
+  TASK_OUT = 4         // bf16 [n | a_s] . [W_up | Ws2]^T -> out (bf16, one rounding)
+};
+
+struct GemmTask {
+  CUtensorMap tmA[2];  // weight operand maps (128-row boxes); [1] used past kb_split0
+  CUtensorMap tmB[2];  // token operand maps (BN-row boxes)
+  int kind;
+  int routed;          // units come from the device tile list (tile_off/off)
+  int ftiles;          // 128-row output tiles (gate/up pairs for L1 kinds)
+  int kb_total;        // k-blocks of 128 bytes per row
+  int kb_split0;       // k-blocks served by map pair 0
+  int ksplit;          // k splits (non-routed only); >1 => partials + last-arriver reduce
+  int kb_per_split;
+  int a_up_off;        // rows from a gate tile to its up tile in tmA (pair kinds)
+  int a_rows_expert;   // routed: rows per expert in tmA
+  int ntiles;          // non-routed: token tiles
+  int units;           // non-routed: ntiles * ftiles * ksplit
+  int ws_tile_base;    // first split-K workspace tile / counter of this task
+};
+
+struct GemmParams {
+  GemmTask task[2];
+  int ntasks;
+  int M;                       // tokens of this forward
+  int E, L, I, Is, H, cap;     // cap = max_tokens * topk (rows of the permuted buffers)
+  const int32_t* tile_off;     // [E+1]
+  const int32_t* off;          // [E+1]
+  const int32_t* gidx;         // [cap]
+  const int32_t* slot;         // [cap]
+  const float* wts;            // [M*k] routing weights by pair i
+  const float* zsT;            // [L/128, cap]
+  const float* w13_s;          // [E, 2I/128, L/128]
+  const float* w2_s;           // [E, L/128, I/128]
+  uint8_t* aq;                 // [cap, I]
+  float* asT;                  // [I/128, cap]
+  float* r;                    // [M, L]
+  __nv_bfloat16* a_s;          // [max_tokens, Is]
+  __nv_bfloat16* out;          // [M, H]
+  float* ws;                   // split-K partials
+  int* cnt;                    // split-K arrival counters (zero between uses)
+  int* sched;                  // this launch's dynamic tile counter (zeroed by routing)
+  int* err;                    // sticky device error word
+  long long timeout;           // SM cycles per bounded wait
+  int stall_after;             // test hook (0 = off)
+};
+
+// Launchers (return cudaError_t of the launch).
+cudaError_t launch_route(const RouteParams& p, cudaStream_t s, bool pdl);
+cudaError_t launch_perm_hist(const PermParams& p, cudaStream_t s, bool pdl);
+cudaError_t launch_perm_scatter(const PermParams& p, cudaStream_t s, bool pdl);
+cudaError_t launch_norm(const NormParams& p, cudaStream_t s, bool pdl);
+// bn in {16, 128}; grid = persistent CTAs.
+cudaError_t launch_gemm(const GemmParams& p, int bn, int grid, cudaStream_t s, bool pdl);
+int gemm_smem_bytes(int bn);
+
+constexpr int PERM_BLOCK = 1024;  // pairs per permutation block
+constexpr int ROUTE_WARPS = 4;    // tokens per routing block
+constexpr int MAX_TOPK = 32;
+constexpr int MAX_E = 256;
+
+}  // namespace klt

@@ -1,0 +1,276 @@
+// Routing, latent activation quantisation, expert permutation and the RMSNorm step of the
+// latent-MoE tail (sm_103a).
+//
+//  route_quant_kernel  top-k + softmax over the selected logits per token, e4m3 per-128
+//                      quantisation of z, zeroing of the fp32 combine buffer r.
+//  perm_hist_kernel    per-block expert histogram of the (token, choice) pairs.
+//  perm_scatter_kernel stable counting-sort scatter: cnt/off/tile_off, gidx/slot/pos,
+//                      and the gather of each pair's quantised latent row into expert
+//                      order (the routed L1 GEMM reads it with plain TMA tiles).
+//  norm_kernel         RMSNorm of the routed combine with fp32 statistics on the fp32
+//                      sum (tokenspeed PR 1062 commit notes: fp32-internal norm), gamma
+//                      applied, rounded once to bf16 as the up-projection operand.
+#include "klt_device.cuh"
+#include "klt_internal.h"
+
+namespace klt {
+
+namespace {
+
+__device__ __forceinline__ uint32_t ordered_key(float v) {
+  uint32_t u = __float_as_uint(v);
+  if ((u & 0x7FFFFFFFu) == 0) u = 0;  // -0 and +0 compare equal
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// One warp per token.
+__global__ void __launch_bounds__(32 * ROUTE_WARPS)
+    route_quant_kernel(const RouteParams p) {
+  pdl_wait();
+  pdl_trigger();
+  const int lane = lane_id();
+  const int t = blockIdx.x * ROUTE_WARPS + (threadIdx.x >> 5);
+  if (blockIdx.x == 0 && threadIdx.x < p.nsched) p.sched[threadIdx.x] = 0;
+  if (t >= p.M) return;
+
+  // ---- top-k selection: key = (ordered logit, inverted index) so larger key wins and
+  // equal logits go to the lower expert index.
+  const float* lg = p.logits + static_cast<size_t>(t) * p.E;
+  constexpr int PER_LANE = MAX_E / 32;
+  uint32_t keys[PER_LANE];
+#pragma unroll
+  for (int i = 0; i < PER_LANE; ++i) {
+    const int e = lane + 32 * i;
+    keys[i] = e < p.E ? ordered_key(__ldg(lg + e)) : 0u;
+  }
+  uint32_t taken = 0;  // bit i: entry i of this lane already selected
+  int my_idx = 0;
+  float my_val = 0.f;
+  for (int j = 0; j < p.k; ++j) {
+    unsigned long long best = 0ull;
+#pragma unroll
+    for (int i = 0; i < PER_LANE; ++i) {
+      const int e = lane + 32 * i;
+      if (e < p.E && !(taken >> i & 1u)) {
+        const unsigned long long kk =
+            (static_cast<unsigned long long>(keys[i]) << 32) | (0xFFFFFFFFu - e);
+        best = kk > best ? kk : best;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+      best = other > best ? other : best;
+    }
+    const int e = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best & 0xFFFFFFFFull));
+    if ((e & 31) == lane) taken |= 1u << (e >> 5);
+    if (lane == j) {
+      my_idx = e;
+      my_val = __ldg(lg + e);
+    }
+  }
+  const float vmax = __shfl_sync(0xFFFFFFFFu, my_val, 0);
+  const float ex = lane < p.k ? expf(my_val - vmax) : 0.f;
+  float sum = ex;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+  if (lane < p.k) {
+    p.ids[static_cast<size_t>(t) * p.k + lane] = my_idx;
+    p.wts[static_cast<size_t>(t) * p.k + lane] = ex / sum;
+  }
+
+  // ---- per-128-column e4m3 quantisation of z (4 columns per lane per group)
+  const int G = p.L / 128;
+  const __nv_bfloat16* zr = p.z + static_cast<size_t>(t) * p.L;
+  for (int g = 0; g < G; ++g) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(zr + g * 128 + lane * 4);
+    const __nv_bfloat162 b01 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+    const __nv_bfloat162 b23 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+    const float v0 = __low2float(b01), v1 = __high2float(b01);
+    const float v2 = __low2float(b23), v3 = __high2float(b23);
+    float amax = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const float s = amax == 0.f ? 1.0f : amax / 448.0f;
+    const uint32_t q = static_cast<uint32_t>(f32_to_e4m3(v0 / s)) |
+                       (static_cast<uint32_t>(f32_to_e4m3(v1 / s)) << 8) |
+                       (static_cast<uint32_t>(f32_to_e4m3(v2 / s)) << 16) |
+                       (static_cast<uint32_t>(f32_to_e4m3(v3 / s)) << 24);
+    *reinterpret_cast<uint32_t*>(p.zq + static_cast<size_t>(t) * p.L + g * 128 + lane * 4) = q;
+    if (lane == 0) p.zs[static_cast<size_t>(t) * G + g] = s;
+  }
+
+  // ---- zero this token's row of the combine buffer
+  float4* rr = reinterpret_cast<float4*>(p.r + static_cast<size_t>(t) * p.L);
+  for (int c = lane; c < p.L / 4; c += 32) rr[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+__global__ void __launch_bounds__(PERM_BLOCK) perm_hist_kernel(const PermParams p) {
+  __shared__ int hist[MAX_E];
+  pdl_wait();
+  pdl_trigger();
+  for (int e = threadIdx.x; e < p.E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int i = blockIdx.x * PERM_BLOCK + threadIdx.x;
+  if (i < p.M * p.k) atomicAdd(&hist[p.ids[i]], 1);
+  __syncthreads();
+  for (int e = threadIdx.x; e < p.E; e += blockDim.x)
+    p.hist[blockIdx.x * p.E + e] = hist[e];
+}
+
+__global__ void __launch_bounds__(PERM_BLOCK) perm_scatter_kernel(const PermParams p) {
+  __shared__ int warp_cnt[PERM_BLOCK / 32][MAX_E];
+  __shared__ int base[MAX_E];
+  __shared__ int total[MAX_E];
+  __shared__ int tiles[MAX_E];
+  __shared__ int ppos[PERM_BLOCK];
+  pdl_wait();
+  pdl_trigger();
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int Mk = p.M * p.k;
+  for (int c = tid; c < (PERM_BLOCK / 32) * MAX_E; c += PERM_BLOCK)
+    (&warp_cnt[0][0])[c] = 0;
+  // expert totals and the count of this expert's pairs in earlier blocks
+  if (tid < p.E) {
+    int tot = 0, pre = 0;
+    for (int b = 0; b < p.nblocks; ++b) {
+      const int h = p.hist[b * p.E + tid];
+      tot += h;
+      if (b < static_cast<int>(blockIdx.x)) pre += h;
+    }
+    total[tid] = tot;
+    base[tid] = pre;
+    tiles[tid] = (tot + p.bn - 1) / p.bn;
+  }
+  __syncthreads();
+  if (tid == 0) {  // exclusive scans over experts (E <= 256)
+    int acc = 0, tacc = 0;
+    for (int e = 0; e < p.E; ++e) {
+      const int c = total[e], tc = tiles[e];
+      total[e] = acc;  // now the expert offset
+      tiles[e] = tacc;
+      acc += c;
+      tacc += tc;
+      if (blockIdx.x == 0) {
+        p.cnt[e] = c;
+        p.off[e] = total[e];
+        p.tile_off[e] = tiles[e];
+      }
+    }
+    if (blockIdx.x == 0) {
+      p.off[p.E] = acc;
+      p.tile_off[p.E] = tacc;
+    }
+  }
+  __syncthreads();
+  if (tid < p.E) base[tid] += total[tid];
+
+  // rank inside the warp among pairs of the same expert (lower lane = lower pair index)
+  const int i = blockIdx.x * PERM_BLOCK + tid;
+  const int e = i < Mk ? p.ids[i] : -1 - lane;  // inactive lanes get unique keys
+  const unsigned same = __match_any_sync(0xFFFFFFFFu, e);
+  const int rank = __popc(same & ((1u << lane) - 1u));
+  if (e >= 0 && rank == 0) warp_cnt[w][e] = __popc(same);
+  __syncthreads();
+  if (tid < p.E) {  // exclusive scan over warps, per expert
+    int acc = 0;
+    for (int ww = 0; ww < PERM_BLOCK / 32; ++ww) {
+      const int c = warp_cnt[ww][tid];
+      warp_cnt[ww][tid] = acc;
+      acc += c;
+    }
+  }
+  __syncthreads();
+  if (e >= 0) {
+    const int pp = base[e] + warp_cnt[w][e] + rank;
+    p.gidx[pp] = i / p.k;
+    p.slot[pp] = i;
+    p.pos[i] = pp;
+    ppos[tid] = pp;
+  }
+  __syncthreads();
+
+  // gather each pair's quantised latent row (and its scales, transposed) into pair order
+  const int G = p.L / 128;
+  const int row16 = p.L / 16;
+  for (int q = 0; q < 32; ++q) {
+    const int ii = blockIdx.x * PERM_BLOCK + w * 32 + q;
+    if (ii >= Mk) break;
+    const int t = ii / p.k;
+    const int pp = ppos[w * 32 + q];
+    const uint4* src = reinterpret_cast<const uint4*>(p.zq + static_cast<size_t>(t) * p.L);
+    uint4* dst = reinterpret_cast<uint4*>(p.zq_perm + static_cast<size_t>(pp) * p.L);
+    for (int c = lane; c < row16; c += 32) dst[c] = src[c];
+    for (int g = lane; g < G; g += 32)
+      p.zsT[static_cast<size_t>(g) * p.cap + pp] = p.zs[static_cast<size_t>(t) * G + g];
+  }
+}
+
+__global__ void __launch_bounds__(128) norm_kernel(const NormParams p) {
+  __shared__ float red[4];
+  pdl_wait();
+  pdl_trigger();
+  const int t = blockIdx.x;
+  const float4* rr = reinterpret_cast<const float4*>(p.r + static_cast<size_t>(t) * p.L);
+  float ss = 0.f;
+  for (int c = threadIdx.x; c < p.L / 4; c += 128) {
+    const float4 v = rr[c];
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  const float tot = red[0] + red[1] + red[2] + red[3];
+  const float inv = rsqrtf(tot / static_cast<float>(p.L) + p.eps);
+  const uint2* gg = reinterpret_cast<const uint2*>(p.gamma);
+  uint2* nn = reinterpret_cast<uint2*>(p.n + static_cast<size_t>(t) * p.L);
+  for (int c = threadIdx.x; c < p.L / 4; c += 128) {
+    const float4 v = rr[c];
+    const uint2 graw = gg[c];
+    const __nv_bfloat162 g01 = *reinterpret_cast<const __nv_bfloat162*>(&graw.x);
+    const __nv_bfloat162 g23 = *reinterpret_cast<const __nv_bfloat162*>(&graw.y);
+    const __nv_bfloat162 o01 = __floats2bfloat162_rn(v.x * inv * __low2float(g01),
+                                                     v.y * inv * __high2float(g01));
+    const __nv_bfloat162 o23 = __floats2bfloat162_rn(v.z * inv * __low2float(g23),
+                                                     v.w * inv * __high2float(g23));
+    uint2 o;
+    o.x = *reinterpret_cast<const uint32_t*>(&o01);
+    o.y = *reinterpret_cast<const uint32_t*>(&o23);
+    nn[c] = o;
+  }
+}
+
+template <typename Kern, typename Param>
+cudaError_t launch_simple(Kern k, dim3 grid, dim3 block, const Param& prm, cudaStream_t s,
+                          bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k, prm);
+}
+
+}  // namespace
+
+cudaError_t launch_route(const RouteParams& p, cudaStream_t s, bool pdl) {
+  const int blocks = (p.M + ROUTE_WARPS - 1) / ROUTE_WARPS;
+  return launch_simple(route_quant_kernel, dim3(blocks), dim3(32 * ROUTE_WARPS), p, s, pdl);
+}
+cudaError_t launch_perm_hist(const PermParams& p, cudaStream_t s, bool pdl) {
+  return launch_simple(perm_hist_kernel, dim3(p.nblocks), dim3(PERM_BLOCK), p, s, pdl);
+}
+cudaError_t launch_perm_scatter(const PermParams& p, cudaStream_t s, bool pdl) {
+  return launch_simple(perm_scatter_kernel, dim3(p.nblocks), dim3(PERM_BLOCK), p, s, pdl);
+}
+cudaError_t launch_norm(const NormParams& p, cudaStream_t s, bool pdl) {
+  return launch_simple(norm_kernel, dim3(p.M), dim3(128), p, s, pdl);
+}
+
+}  // namespace klt

@@ -1,0 +1,176 @@
+"""CUDA path vs the float64 oracle, through the C ABI, on seeded synthetic inputs.
+
+Index and permutation outputs and the latent quantisation must match bit for bit; float
+stages must meet the tail's bar (relative Frobenius error <= 5e-3 and per element
+|err| <= 0.03*rms(ref) + 0.01*|ref|)."""
+import numpy as np
+import pytest
+import torch
+
+from latent_moe_layer_route_gb300 import binding as B
+from latent_moe_layer_route_gb300 import build, configs, inputs
+from oracle import model as T
+import parity_util as PU
+
+pytestmark = pytest.mark.gpu
+
+_CACHE = {}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    B.load_library()
+    yield
+    _CACHE.clear()
+
+
+def weights_for(cfg):
+    key = (cfg.E, cfg.topk, cfg.I, cfg.H, cfg.L, cfg.Is, cfg.routed_fmt, cfg.seed)
+    if key not in _CACHE:
+        _CACHE.clear()
+        w = inputs.make_weights(cfg)
+        _CACHE[key] = (w, PU.to_cuda(w))
+    return _CACHE[key]
+
+
+def run_case(cfg, M=None, act=None, tokens=None, max_tokens=None, tail=None):
+    w_cpu, w_gpu = weights_for(cfg)
+    if act is None:
+        act = inputs.make_activations(cfg, M)
+    M = act["x"].shape[0]
+    own = tail is None
+    if own:
+        tail = B.LatentMoETail(cfg, w_gpu, max_tokens=max_tokens or M)
+    run = PU.Run(tail, PU.to_cuda(act), cfg)
+    assert tail.status() == B.KLT_OK
+    o = T.tail(act, w_cpu, cfg, tokens=tokens)
+    PU.check_routing(run, o, cfg)
+    rf = PU.check_stages(run, o, cfg)
+    if own:
+        tail.close()
+    return run, o, rf
+
+
+# ------------------------------------------------------------------ small shapes
+
+@pytest.mark.parametrize("M", [1, 6, 17, 40])
+def test_small_shapes(M):
+    run_case(configs.SMALL, M=M)
+
+
+def test_small_all_experts_selected():
+    run_case(configs.SMALL.with_(E=4, topk=4, seed=21), M=9)
+
+
+def test_small_wider_k_tail_shapes():
+    # several 128-tiles in every dimension and a ragged token count
+    run_case(configs.SMALL.with_(H=512, L=384, I=256, Is=384, E=8, topk=3, seed=22), M=29)
+
+
+def test_one_hot_routing_sends_every_token_to_one_expert():
+    cfg = configs.SMALL.with_(E=8, topk=2, seed=23)
+    act = inputs.make_activations(cfg, 33)
+    act["logits"][:, 5] += 50.0
+    run, o, _ = run_case(cfg, act=act)
+    assert o["cnt"][5] == 33
+
+
+def test_zero_latent_leaves_shared_expert_only():
+    cfg = configs.SMALL.with_(seed=24)
+    act = inputs.make_activations(cfg, 8)
+    act["z"] = torch.zeros_like(act["z"])
+    run, o, _ = run_case(cfg, act=act)
+    assert float(run.r.abs().max()) == 0.0
+
+
+def test_zero_hidden_leaves_routed_branch_only():
+    cfg = configs.SMALL.with_(seed=25)
+    act = inputs.make_activations(cfg, 8)
+    act["x"] = torch.zeros_like(act["x"])
+    run, o, _ = run_case(cfg, act=act)
+    assert float(run.a_s.float().abs().max()) == 0.0
+
+
+def test_repeated_calls_and_smaller_m_reuse_the_workspace():
+    cfg = configs.SMALL.with_(seed=26)
+    w_cpu, w_gpu = weights_for(cfg)
+    tail = B.LatentMoETail(cfg, w_gpu, max_tokens=64)
+    try:
+        for M in (64, 5, 64, 33):
+            act = inputs.make_activations(cfg, M)
+            run = PU.Run(tail, PU.to_cuda(act), cfg)
+            o = T.tail(act, w_cpu, cfg)
+            PU.check_routing(run, o, cfg)
+            PU.check_stages(run, o, cfg)
+        assert tail.status() == B.KLT_OK
+    finally:
+        tail.close()
+
+
+def test_m_zero_is_a_noop_and_bad_m_is_rejected():
+    cfg = configs.SMALL
+    _, w_gpu = weights_for(cfg)
+    tail = B.LatentMoETail(cfg, w_gpu, max_tokens=8)
+    try:
+        x = torch.zeros((8, cfg.H), dtype=torch.bfloat16, device="cuda")
+        z = torch.zeros((8, cfg.L), dtype=torch.bfloat16, device="cuda")
+        lg = torch.zeros((8, cfg.E), dtype=torch.float32, device="cuda")
+        out = torch.full((8, cfg.H), 3.0, dtype=torch.bfloat16, device="cuda")
+        s = torch.cuda.current_stream().cuda_stream
+        assert B.klt_forward(tail.handle, x, z, lg, 0, out, stream=s) == B.KLT_OK
+        torch.cuda.synchronize()
+        assert bool((out == 3.0).all())
+        assert B.klt_forward(tail.handle, x, z, lg, 9, out, stream=s) == B.KLT_ERR_INVALID_ARG
+        assert B.klt_forward(tail.handle, x, z, lg, -1, out, stream=s) == \
+            B.KLT_ERR_INVALID_ARG
+        lib = B.load_library()
+        assert lib.klt_forward(tail.handle, x.data_ptr() + 2, z.data_ptr(), lg.data_ptr(), 4,
+                               out.data_ptr(), None, None, s) == B.KLT_ERR_ALIGN
+        assert lib.klt_forward(tail.handle, None, z.data_ptr(), lg.data_ptr(), 4,
+                               out.data_ptr(), None, None, s) == B.KLT_ERR_INVALID_ARG
+        assert tail.launch_count(4) == 7 and tail.launch_count(0) == 0
+    finally:
+        tail.close()
+
+
+def test_bounded_wait_expires_into_status_without_faulting():
+    cfg = configs.SMALL.with_(seed=27)
+    w_cpu, w_gpu = weights_for(cfg)
+    tail = B.LatentMoETail(cfg, w_gpu, max_tokens=16)
+    try:
+        act = PU.to_cuda(inputs.make_activations(cfg, 16))
+        PU.Run(tail, act, cfg, stall_after=1, timeout_ms=20)
+        assert tail.status() == B.KLT_ERR_DEVICE_TIMEOUT
+        # the context is still usable: a fresh handle runs correctly
+        run_case(cfg, M=16)
+    finally:
+        tail.close()
+
+
+# ------------------------------------------------------------------ the named workloads
+
+def test_tiny_m4():
+    _, _, rf = run_case(configs.TINY_M4)
+    print("tiny rel_fro", rf)
+
+
+def test_decode_m16():
+    _, _, rf = run_case(configs.DECODE_M16)
+    print("decode m16 rel_fro", rf)
+
+
+def test_decode_m128():
+    _, _, rf = run_case(configs.DECODE_M128)
+    print("decode m128 rel_fro", rf)
+
+
+@pytest.mark.slow
+def test_prefill_m4096_sampled_tokens():
+    cfg = configs.PREFILL_M4096
+    rng = np.random.default_rng(0)
+    tok = np.sort(rng.choice(cfg.M, 48, replace=False))
+    tok[0], tok[-1] = 0, cfg.M - 1
+    run_case(cfg, tokens=tok)
