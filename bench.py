@@ -1,0 +1,351 @@
+"""Benchmark of the latent-MoE layer tail on GB300.
+
+One step = one klt_forward (routing, permutation, routed FP8 experts, combine, RMSNorm,
+up-projection + BF16 shared expert) over one batch of synthetic tokens.  Prints one JSON
+line.  Default workload: decode batch of 16 tokens, E=64, top-8, routed intermediate
+1024 (FP8 128x128 block scales), shared intermediate 2048, H=7168, L=3584.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+Multi-GPU (under torchrun): the tail has no exchange step, so every rank runs an
+independent replica on its own tokens (weak scaling); time = max over ranks.
+`--impl reference` times the CPU float64 oracle (the only other implementation) on a
+bounded token sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-tail tokens/sec & µs/layer at M=16..8192; % of HBM or tensor roofline"
+HBM_NOMINAL_GBS = 8000.0
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), float(pk["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[2:6]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def algorithmic_bytes(cfg, cnt: np.ndarray, M: int):
+    """Bytes each launch must move at least once (weights of touched experts, token
+    inputs, stage outputs), per the tail's data flow."""
+    H, L, I, Is, k, E = cfg.H, cfg.L, cfg.I, cfg.Is, cfg.topk, cfg.E
+    touched = int((cnt > 0).sum())
+    Mk = M * k
+    wb = 1.0 if cfg.routed_fmt == "fp8" else 0.5 + 1.0 / 16
+    w13 = touched * 2 * I * L * wb
+    w2 = touched * L * I * wb
+    g1 = 2 * Is * H * 2 + M * H * 2 + w13 + Mk * L + Mk * I + M * Is * 2
+    g2 = w2 + Mk * I + M * L * 4
+    norm = M * L * 4 + M * L * 2
+    g3 = H * L * 2 + H * Is * 2 + M * L * 2 + M * Is * 2 + M * H * 2
+    route = M * E * 4 + M * L * 2 + M * L + M * L * 4
+    perm = Mk * L * 2
+    total = g1 + g2 + norm + g3 + route + perm
+    return {"gemm_l1": g1, "gemm_l2": g2, "norm": norm, "gemm_out": g3, "route": route,
+            "perm": perm, "total": total, "touched_experts": touched}
+
+
+def flops(cfg, M: int):
+    H, L, I, Is, k = cfg.H, cfg.L, cfg.I, cfg.Is, cfg.topk
+    routed = 2.0 * M * k * (2 * I * L + L * I)
+    dense = 2.0 * M * (2 * Is * H + H * Is + H * L)
+    return routed, dense
+
+
+def run_reference(cfg, args, ws, rank):
+    """The CPU float64 oracle as it stands, on a bounded token sample per step."""
+    if rank != 0:
+        return
+    from latent_moe_layer_route_gb300 import inputs
+    from oracle import model as oracle_model
+    act, w = inputs.make_inputs(cfg)
+    sample = min(cfg.M, 2)
+    tok = np.arange(sample)
+    for _ in range(args.warmup):
+        oracle_model.tail(act, w, cfg, tokens=tok)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_model.tail(act, w, cfg, tokens=tok)
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0))
+    value = sample * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "M": cfg.M, "sample_tokens": sample},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"first {sample} of {cfg.M} tokens per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(cfg, act, w):
+    from oracle import model as oracle_model
+    cores = len(os.sched_getaffinity(0))
+    tok = np.arange(cfg.M)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        oracle_model.tail(act, w, cfg, tokens=tok)
+        n += 1
+        if time.perf_counter() - t0 > 10.0 or n >= 5:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": cfg.M * n / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} full step(s) of all {cfg.M} tokens, {dt:.1f} s"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode_m16_e64_k8_fp8")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from latent_moe_layer_route_gb300 import configs
+    cfg = configs.BY_NAME[args.workload]
+    ws, rank, local = _dist()
+
+    if args.impl == "reference":
+        run_reference(cfg, args, ws, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+    from latent_moe_layer_route_gb300 import binding as B
+    from latent_moe_layer_route_gb300 import build, inputs
+
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl")
+    build.build()
+    B.load_library()
+    M = cfg.M
+    act_cpu, w_cpu = inputs.make_inputs(cfg)
+    w = {k: v.cuda() for k, v in w_cpu.items()}
+    act = {k: v.cuda() for k, v in act_cpu.items()}
+    tail = B.LatentMoETail(cfg, w)
+    del w
+    out = torch.empty((M, cfg.H), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    cnt = torch.zeros(cfg.E, dtype=torch.int32, device="cuda")
+    ro = B.KltRouting(None, None, cnt.data_ptr(), None, None, None, None)
+    tail.forward(act["x"], act["z"], act["logits"], out=out, routing=ro)
+    torch.cuda.synchronize()
+    assert tail.status() == B.KLT_OK
+    nl = tail.launch_count(M)
+
+    def step():
+        tail.forward(act["x"], act["z"], act["logits"], out=out)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+
+    # ---- timed region: device time of each step, L2 flushed between steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with Clocks(local) as clk:
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+    if ws > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    value = ws * M * args.steps / (ms / 1e3)
+    assert tail.status() == B.KLT_OK
+
+    # ---- per-launch breakdown (events between launches; separate loop)
+    nev = nl + 1
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    for row in evs:  # torch creates the CUDA event on first record
+        for ev in row:
+            ev.record(stream)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        dbg = B.KltDebug()
+        evs[i][0].record(stream)
+        for j in range(nl):
+            dbg.events[j] = evs[i][j + 1].cuda_event
+        tail.forward(act["x"], act["z"], act["logits"], out=out, debug=dbg)
+    torch.cuda.synchronize()
+    per = np.zeros(nl)
+    for i in range(args.steps):
+        for j in range(nl):
+            per[j] += evs[i][j].elapsed_time(evs[i][j + 1])
+    per /= args.steps
+    names = ["route", "perm_hist", "perm_scatter", "gemm_l1", "gemm_l2", "norm", "gemm_out"]
+    per_launch_us = {n: round(float(v) * 1e3, 2) for n, v in zip(names, per)}
+
+    # ---- end to end through the public API with host buffers
+    xh = act_cpu["x"].pin_memory()
+    zh = act_cpu["z"].pin_memory()
+    lh = act_cpu["logits"].pin_memory()
+    oh = torch.empty((M, cfg.H), dtype=torch.bfloat16).pin_memory()
+    xd, zd, ld = torch.empty_like(act["x"]), torch.empty_like(act["z"]), torch.empty_like(
+        act["logits"])
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        e0[i].record(stream)
+        xd.copy_(xh, non_blocking=True)
+        zd.copy_(zh, non_blocking=True)
+        ld.copy_(lh, non_blocking=True)
+        tail.forward(xd, zd, ld, out=out)
+        oh.copy_(out, non_blocking=True)
+        e1[i].record(stream)
+    torch.cuda.synchronize()
+    ems = sum(a.elapsed_time(b) for a, b in zip(e0, e1))
+    if ws > 1:
+        t = torch.tensor([ems], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ems = float(t.item())
+    e2e = ws * M * args.steps / (ems / 1e3)
+    h2d = xh.numel() * 2 + zh.numel() * 2 + lh.numel() * 4
+    d2h = oh.numel() * 2
+
+    # ---- roofline of the dominant launch
+    cnt_h = cnt.cpu().numpy()
+    ab = algorithmic_bytes(cfg, cnt_h, M)
+    hbm, bf16_tf, peak_src = _peaks()
+    dom = max(("gemm_l1", "gemm_l2", "gemm_out"), key=lambda n: per_launch_us[n])
+    dom_bytes = ab[dom]
+    achieved = dom_bytes / (per_launch_us[dom] * 1e-6) / 1e9
+    routed_f, dense_f = flops(cfg, M)
+    roof_time_us = max(ab["total"] / (HBM_NOMINAL_GBS * 1e9),
+                       routed_f / (2 * bf16_tf * 1e12) + dense_f / (bf16_tf * 1e12)) * 1e6
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "us_per_layer": ms_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp8e4m3+bf16 (fp32 accumulate)",
+        "data": "synthetic (seeded numpy draws, random-init weights)",
+        "config": {"workload": cfg.name, "M": M, "H": cfg.H, "L": cfg.L, "E": cfg.E,
+                   "topk": cfg.topk, "I": cfg.I, "Is": cfg.Is, "routed_fmt": cfg.routed_fmt,
+                   "l2": "flushed (512 MB write) before every timed step",
+                   "parallelism": f"replicas x{ws}"},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
+                     "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                     "peak_source": peak_src, "traffic": None,
+                     "algorithmic_bytes": int(dom_bytes)},
+        "step_roofline": {"algorithmic_bytes": int(ab["total"]),
+                          "touched_experts": ab["touched_experts"],
+                          "roofline_us_at_8TBps": round(roof_time_us, 2),
+                          "frac_of_roofline": round(roof_time_us / (ms_step * 1e3), 4),
+                          "achieved_GBps": round(ab["total"] / (ms_step * 1e-3) / 1e9, 1)},
+        "per_launch_us": per_launch_us,
+        "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": nl * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, act_cpu, w_cpu)
+    tail.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

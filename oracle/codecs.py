@@ -13,9 +13,8 @@ import numpy as np
 E4M3_MAX = 448.0
 
 
-def e4m3_decode(codes) -> np.ndarray:
-    """uint8 codes -> float64 values (NaN for the two NaN codes)."""
-    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+def _e4m3_value(c: np.ndarray) -> np.ndarray:
+    """Value of each code from its bit fields."""
     sign = np.where(c & 0x80, -1.0, 1.0)
     e = (c >> 3) & 0xF
     m = (c & 0x7).astype(np.float64)
@@ -23,6 +22,15 @@ def e4m3_decode(codes) -> np.ndarray:
     nrm = (1.0 + m / 8.0) * np.exp2((e - 7).astype(np.float64))
     v = np.where(e == 0, sub, nrm) * sign
     return np.where((c & 0x7F) == 0x7F, np.nan, v)
+
+
+_E4M3_TABLE = _e4m3_value(np.arange(256, dtype=np.int64))
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """uint8 codes -> float64 values (NaN for the two NaN codes); the 256 values come from
+    the bit-field formula above and large arrays are decoded by table lookup."""
+    return _E4M3_TABLE[np.asarray(codes, dtype=np.uint8)]
 
 
 def e4m3_encode(v) -> np.ndarray:
@@ -47,14 +55,22 @@ def e4m3_encode(v) -> np.ndarray:
     return (code | sign).astype(np.uint8)
 
 
-def e2m1_decode(codes) -> np.ndarray:
-    """4-bit e2m1 codes (one per array element, 0..15) -> float64."""
-    c = np.asarray(codes).astype(np.int64) & 0xF
+def _e2m1_value(c: np.ndarray) -> np.ndarray:
+    """Value of each 4-bit code from its bit fields."""
     sign = np.where(c & 0x8, -1.0, 1.0)
     e = (c >> 1) & 0x3
     m = (c & 0x1).astype(np.float64)
     v = np.where(e == 0, m * 0.5, (1.0 + m / 2.0) * np.exp2((e - 1).astype(np.float64)))
     return v * sign
+
+
+_E2M1_TABLE = _e2m1_value(np.arange(16, dtype=np.int64))
+
+
+def e2m1_decode(codes) -> np.ndarray:
+    """4-bit e2m1 codes (one per array element, 0..15) -> float64, by table lookup of the
+    16 values given by the bit-field formula above."""
+    return _E2M1_TABLE[np.asarray(codes).astype(np.int64) & 0xF]
 
 
 def unpack_e2m1(packed) -> np.ndarray:
