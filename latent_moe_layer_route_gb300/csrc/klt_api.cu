@@ -1,7 +1,7 @@
 // Host side of the latent-MoE tail C ABI: argument checks, owned weight copies, the
 // workspace, TMA descriptor encoding and the per-forward launch chain
 //
-//   route_quant -> perm_hist -> perm_scatter -> GEMM(shared L1 + routed L1)
+//   route_quant -> [perm_hist] -> perm_scatter -> perm_gather -> GEMM(shared L1 + routed L1)
 //   -> GEMM(routed L2 + combine) -> norm -> GEMM(up-projection + shared L2 -> out)
 //
 // all on the caller's stream, chained with programmatic dependent launch.  The shared
@@ -108,6 +108,7 @@ int check_dims(const klt_dims* d) {
   if (d->H <= 0 || d->L <= 0 || d->I <= 0 || d->Is <= 0) return KLT_ERR_INVALID_ARG;
   if (d->H % 128 || d->L % 128 || d->I % 128 || d->Is % 128) return KLT_ERR_UNSUPPORTED;
   if (d->E > MAX_E || d->topk > d->E || d->topk > MAX_TOPK) return KLT_ERR_UNSUPPORTED;
+  if (d->L > 128 * MAX_KB || d->I > 128 * MAX_KB) return KLT_ERR_UNSUPPORTED;
   if (d->routed_fmt != KLT_FMT_FP8_B128 && d->routed_fmt != KLT_FMT_NVFP4)
     return KLT_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(d->max_tokens) * d->topk > (1 << 20)) return KLT_ERR_UNSUPPORTED;
@@ -260,7 +261,8 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
 
 int klt_launch_count(const klt_handle* h, int32_t M) {
   if (!h || M <= 0) return 0;
-  return 7;
+  const int nblocks = (M * h->d.topk + PERM_BLOCK - 1) / PERM_BLOCK;
+  return 7 + (nblocks > 1 ? 1 : 0);
 }
 
 int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits, int32_t M,
@@ -331,8 +333,9 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
   pp.cap = h->cap;
   pp.bn = BN;
   pp.nblocks = nblocks;
-  KLT_LAUNCH(launch_perm_hist(pp, s, pdl));
+  if (nblocks > 1) KLT_LAUNCH(launch_perm_hist(pp, s, pdl));
   KLT_LAUNCH(launch_perm_scatter(pp, s, pdl));
+  KLT_LAUNCH(launch_perm_gather(pp, s, pdl));
 
   // ---- common GEMM parameters
   GemmParams gp;

@@ -37,12 +37,14 @@ struct Cfg {
   static constexpr int A_BYTES = 128 * 128;
   static constexpr int B_BYTES = BN * 128;
   static constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES;
-  static constexpr int STAGES = BN == 16 ? 6 : (BN == 128 ? 4 : 5);
+  static constexpr int STAGES = BN == 16 ? 6 : (BN == 128 ? 3 : 5);
   static constexpr int SLOT_COLS = 2 * BN;
   static constexpr int TMEM_COLS = BN <= 64 ? 256 : 512;
   static constexpr int NACC = TMEM_COLS / SLOT_COLS;
   static constexpr int US = 8;
   static constexpr int COLS = BN / (EPI_WARPS / 4);
+  // per-unit scale staging: token group scales [MAX_KB][BN] + weight scales [MAX_KB][2]
+  static constexpr int SC_FLOATS = MAX_KB * BN + 2 * MAX_KB;
   static_assert(COLS % 16 == 0, "epilogue works in 16-column chunks");
   static_assert(NACC >= 2, "need two accumulator slots");
 };
@@ -69,11 +71,12 @@ struct Smem {
   int* abort_flag;
   int* last_flag;
   float* red;  // [EPI_WARPS][COLS]
+  float* sc;   // [2][SC_FLOATS]
 
   static constexpr int BAR_BYTES = 8 * (2 * C::STAGES + 2 * C::NACC + 2 * C::US + 1);
   static constexpr int bytes() {
     return C::STAGES * C::STAGE_BYTES + BAR_BYTES + C::US * (int)sizeof(UnitInfo) + 64 +
-           C::EPI_WARPS * C::COLS * 4 + 1024 /* alignment slack */;
+           C::EPI_WARPS * C::COLS * 4 + 2 * C::SC_FLOATS * 4 + 1024 /* alignment slack */;
   }
   __device__ explicit Smem(uint8_t* raw) {
     uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -92,6 +95,7 @@ struct Smem {
     abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
     last_flag = abort_flag + 1;
     red = reinterpret_cast<float*>(tmem_holder + 16);
+    sc = red + C::EPI_WARPS * C::COLS;
   }
 };
 
@@ -169,9 +173,11 @@ __device__ void run_producer(const GemmParams& p, Smem<BN>& sm) {
   long long issued = 0;
   int dummy_abort = 0;
   bool stalled = false;
+  int u = atomicAdd(p.sched, 1);
   for (;;) {
-    const int u = atomicAdd(p.sched, 1);
     const UnitInfo info = decode_unit<BN>(p, u);
+    // claim the next unit now so the counter round trip overlaps this unit's copies
+    if (info.task >= 0) u = atomicAdd(p.sched, 1);
     if (!mbar_wait(&sm.uempty[us], uphase ^ 1, sm.abort_flag, p.err, p.timeout)) break;
     sm.ring[us] = info;
     mbar_arrive(&sm.ufull[us]);
@@ -294,7 +300,7 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
   const int row = quad * 32 + lane;     // output feature within the tile
   const int c0 = half * COLS;
   const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-  int us = 0, acc = 0;
+  int us = 0, acc = 0, sc_buf = 0;
   uint32_t uphase = 0, aphase = 0;
   const int G_L = p.L / 128, G_I = p.I / 128;
 
@@ -314,17 +320,39 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
     for (int j = 0; j < COLS; ++j) { g[j] = 0.f; u[j] = 0.f; }
 
     if (is_promote(kind)) {
+      // Stage this unit's scales in shared memory once: token group scales [kb][column]
+      // and the weight block scale(s) per kb.  Double-buffered by unit parity; the barrier
+      // also guarantees every epilogue thread has finished the previous unit.
       const float* tok_scale = kind == TASK_ROUTED_L1 ? p.zsT : p.asT;
-      for (int kb = info.kb0; kb < info.kb1; ++kb) {
-        float sw_g, sw_u = 0.f;
+      float* sb = sm.sc + sc_buf * C::SC_FLOATS;
+      sc_buf ^= 1;
+      const int nkb = info.kb1 - info.kb0;
+      const int etid = threadIdx.x - 64;
+      for (int i = etid; i < nkb * BN; i += C::EPI_THREADS) {
+        const int kbi = i / BN, j = i - kbi * BN;
+        sb[i] = j < info.rows
+                    ? __ldg(tok_scale + static_cast<size_t>(info.kb0 + kbi) * p.cap +
+                            info.row0 + j)
+                    : 0.f;
+      }
+      for (int kbi = etid; kbi < nkb; kbi += C::EPI_THREADS) {
+        const int kb = info.kb0 + kbi;
+        float a, b = 0.f;
         if (kind == TASK_ROUTED_L1) {
           const size_t rb = static_cast<size_t>(info.e) * (2 * G_I);
-          sw_g = __ldg(p.w13_s + (rb + info.ftile) * G_L + kb);
-          sw_u = __ldg(p.w13_s + (rb + G_I + info.ftile) * G_L + kb);
+          a = __ldg(p.w13_s + (rb + info.ftile) * G_L + kb);
+          b = __ldg(p.w13_s + (rb + G_I + info.ftile) * G_L + kb);
         } else {
-          sw_g = __ldg(p.w2_s + (static_cast<size_t>(info.e) * G_L + info.ftile) * G_I + kb);
+          a = __ldg(p.w2_s + (static_cast<size_t>(info.e) * G_L + info.ftile) * G_I + kb);
         }
-        const float* ts = tok_scale + static_cast<size_t>(kb) * p.cap + info.row0 + c0;
+        sb[MAX_KB * BN + 2 * kbi] = a;
+        sb[MAX_KB * BN + 2 * kbi + 1] = b;
+      }
+      named_bar_sync(1, C::EPI_THREADS);
+      for (int kbi = 0; kbi < nkb; ++kbi) {
+        const float sw_g = sb[MAX_KB * BN + 2 * kbi];
+        const float sw_u = sb[MAX_KB * BN + 2 * kbi + 1];
+        const float* ts = sb + kbi * BN + c0;
         if (!mbar_wait(&sm.tfull[acc], aphase, sm.abort_flag, p.err, p.timeout)) return;
         tc_fence_after();
         const uint32_t tb = tmem_base + lane_base + static_cast<uint32_t>(acc * C::SLOT_COLS);
@@ -338,7 +366,7 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int j = ch * 16 + i;
-            const float sa = (c0 + j < info.rows) ? __ldg(ts + j) : 0.f;
+            const float sa = ts[j];
             g[j] = fmaf(pg[i], sw_g * sa, g[j]);
             if (pair) u[j] = fmaf(pu[i], sw_u * sa, u[j]);
           }
@@ -541,6 +569,9 @@ cudaError_t launch_bn(const GemmParams& p, int grid, cudaStream_t s, bool pdl) {
 }
 
 }  // namespace
+
+static_assert(Smem<16>::bytes() <= 227 * 1024, "shared memory budget");
+static_assert(Smem<128>::bytes() <= 227 * 1024, "shared memory budget");
 
 int gemm_smem_bytes(int bn) {
   return bn == 16 ? Smem<16>::bytes() : Smem<128>::bytes();

@@ -104,14 +104,16 @@ struct GemmParams {
 cudaError_t launch_route(const RouteParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_perm_hist(const PermParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_perm_scatter(const PermParams& p, cudaStream_t s, bool pdl);
+cudaError_t launch_perm_gather(const PermParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_norm(const NormParams& p, cudaStream_t s, bool pdl);
 // bn in {16, 128}; grid = persistent CTAs.
 cudaError_t launch_gemm(const GemmParams& p, int bn, int grid, cudaStream_t s, bool pdl);
 int gemm_smem_bytes(int bn);
 
 constexpr int PERM_BLOCK = 1024;  // pairs per permutation block
-constexpr int ROUTE_WARPS = 4;    // tokens per routing block
+constexpr int ROUTE_WARPS = 8;    // warps per routing block
 constexpr int MAX_TOPK = 32;
 constexpr int MAX_E = 256;
+constexpr int MAX_KB = 32;       // routed K blocks of 128 per unit (L, I <= 4096)
 
 }  // namespace klt

@@ -4,9 +4,9 @@
 //  route_quant_kernel  top-k + softmax over the selected logits per token, e4m3 per-128
 //                      quantisation of z, zeroing of the fp32 combine buffer r.
 //  perm_hist_kernel    per-block expert histogram of the (token, choice) pairs.
-//  perm_scatter_kernel stable counting-sort scatter: cnt/off/tile_off, gidx/slot/pos,
-//                      and the gather of each pair's quantised latent row into expert
-//                      order (the routed L1 GEMM reads it with plain TMA tiles).
+//  perm_scatter_kernel stable counting-sort scatter: cnt/off/tile_off, gidx/slot/pos.
+//  perm_gather_kernel  gather of each pair's quantised latent row into expert order (the
+//                      routed L1 GEMM reads it with plain TMA tiles).
 //  norm_kernel         RMSNorm of the routed combine with fp32 statistics on the fp32
 //                      sum (tokenspeed PR 1062 commit notes: fp32-internal norm), gamma
 //                      applied, rounded once to bf16 as the up-projection operand.
@@ -23,86 +23,91 @@ __device__ __forceinline__ uint32_t ordered_key(float v) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// One warp per token.
+// Warp w handles token t = w / (G + 1): part 0 routes the token, part g + 1 quantises
+// its 128-column group g of z and zeroes the matching 128 floats of the combine buffer.
 __global__ void __launch_bounds__(32 * ROUTE_WARPS)
     route_quant_kernel(const RouteParams p) {
   pdl_wait();
   pdl_trigger();
   const int lane = lane_id();
-  const int t = blockIdx.x * ROUTE_WARPS + (threadIdx.x >> 5);
   if (blockIdx.x == 0 && threadIdx.x < p.nsched) p.sched[threadIdx.x] = 0;
+  const int G = p.L / 128;
+  const long long w = static_cast<long long>(blockIdx.x) * ROUTE_WARPS + (threadIdx.x >> 5);
+  const int t = static_cast<int>(w / (G + 1));
+  const int part = static_cast<int>(w - static_cast<long long>(t) * (G + 1));
   if (t >= p.M) return;
 
-  // ---- top-k selection: key = (ordered logit, inverted index) so larger key wins and
-  // equal logits go to the lower expert index.
-  const float* lg = p.logits + static_cast<size_t>(t) * p.E;
-  constexpr int PER_LANE = MAX_E / 32;
-  uint32_t keys[PER_LANE];
-#pragma unroll
-  for (int i = 0; i < PER_LANE; ++i) {
-    const int e = lane + 32 * i;
-    keys[i] = e < p.E ? ordered_key(__ldg(lg + e)) : 0u;
-  }
-  uint32_t taken = 0;  // bit i: entry i of this lane already selected
-  int my_idx = 0;
-  float my_val = 0.f;
-  for (int j = 0; j < p.k; ++j) {
-    unsigned long long best = 0ull;
+  if (part == 0) {
+    // ---- top-k selection: key = (ordered logit, inverted index) so larger key wins and
+    // equal logits go to the lower expert index.
+    const float* lg = p.logits + static_cast<size_t>(t) * p.E;
+    constexpr int PER_LANE = MAX_E / 32;
+    uint32_t keys[PER_LANE];
 #pragma unroll
     for (int i = 0; i < PER_LANE; ++i) {
       const int e = lane + 32 * i;
-      if (e < p.E && !(taken >> i & 1u)) {
-        const unsigned long long kk =
-            (static_cast<unsigned long long>(keys[i]) << 32) | (0xFFFFFFFFu - e);
-        best = kk > best ? kk : best;
+      keys[i] = e < p.E ? ordered_key(__ldg(lg + e)) : 0u;
+    }
+    uint32_t taken = 0;  // bit i: entry i of this lane already selected
+    int my_idx = 0;
+    float my_val = 0.f;
+    for (int j = 0; j < p.k; ++j) {
+      unsigned long long best = 0ull;
+#pragma unroll
+      for (int i = 0; i < PER_LANE; ++i) {
+        const int e = lane + 32 * i;
+        if (e < p.E && !(taken >> i & 1u)) {
+          const unsigned long long kk =
+              (static_cast<unsigned long long>(keys[i]) << 32) | (0xFFFFFFFFu - e);
+          best = kk > best ? kk : best;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+        best = other > best ? other : best;
+      }
+      const int e =
+          static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best & 0xFFFFFFFFull));
+      if ((e & 31) == lane) taken |= 1u << (e >> 5);
+      if (lane == j) {
+        my_idx = e;
+        my_val = __ldg(lg + e);
       }
     }
+    const float vmax = __shfl_sync(0xFFFFFFFFu, my_val, 0);
+    const float ex = lane < p.k ? expf(my_val - vmax) : 0.f;
+    float sum = ex;
 #pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-      best = other > best ? other : best;
+    for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+    if (lane < p.k) {
+      p.ids[static_cast<size_t>(t) * p.k + lane] = my_idx;
+      p.wts[static_cast<size_t>(t) * p.k + lane] = ex / sum;
     }
-    const int e = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best & 0xFFFFFFFFull));
-    if ((e & 31) == lane) taken |= 1u << (e >> 5);
-    if (lane == j) {
-      my_idx = e;
-      my_val = __ldg(lg + e);
-    }
-  }
-  const float vmax = __shfl_sync(0xFFFFFFFFu, my_val, 0);
-  const float ex = lane < p.k ? expf(my_val - vmax) : 0.f;
-  float sum = ex;
-#pragma unroll
-  for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-  if (lane < p.k) {
-    p.ids[static_cast<size_t>(t) * p.k + lane] = my_idx;
-    p.wts[static_cast<size_t>(t) * p.k + lane] = ex / sum;
+    return;
   }
 
-  // ---- per-128-column e4m3 quantisation of z (4 columns per lane per group)
-  const int G = p.L / 128;
-  const __nv_bfloat16* zr = p.z + static_cast<size_t>(t) * p.L;
-  for (int g = 0; g < G; ++g) {
-    const uint2 raw = *reinterpret_cast<const uint2*>(zr + g * 128 + lane * 4);
-    const __nv_bfloat162 b01 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-    const __nv_bfloat162 b23 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-    const float v0 = __low2float(b01), v1 = __high2float(b01);
-    const float v2 = __low2float(b23), v3 = __high2float(b23);
-    float amax = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
+  // ---- e4m3 quantisation of one 128-column group (4 columns per lane)
+  const int g = part - 1;
+  const __nv_bfloat16* zr = p.z + static_cast<size_t>(t) * p.L + g * 128;
+  const uint2 raw = *reinterpret_cast<const uint2*>(zr + lane * 4);
+  const __nv_bfloat162 b01 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+  const __nv_bfloat162 b23 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+  const float v0 = __low2float(b01), v1 = __high2float(b01);
+  const float v2 = __low2float(b23), v3 = __high2float(b23);
+  float amax = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
 #pragma unroll
-    for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-    const float s = amax == 0.f ? 1.0f : amax / 448.0f;
-    const uint32_t q = static_cast<uint32_t>(f32_to_e4m3(v0 / s)) |
-                       (static_cast<uint32_t>(f32_to_e4m3(v1 / s)) << 8) |
-                       (static_cast<uint32_t>(f32_to_e4m3(v2 / s)) << 16) |
-                       (static_cast<uint32_t>(f32_to_e4m3(v3 / s)) << 24);
-    *reinterpret_cast<uint32_t*>(p.zq + static_cast<size_t>(t) * p.L + g * 128 + lane * 4) = q;
-    if (lane == 0) p.zs[static_cast<size_t>(t) * G + g] = s;
-  }
-
-  // ---- zero this token's row of the combine buffer
-  float4* rr = reinterpret_cast<float4*>(p.r + static_cast<size_t>(t) * p.L);
-  for (int c = lane; c < p.L / 4; c += 32) rr[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+  const float s = amax == 0.f ? 1.0f : amax / 448.0f;
+  const uint32_t q = static_cast<uint32_t>(f32_to_e4m3(v0 / s)) |
+                     (static_cast<uint32_t>(f32_to_e4m3(v1 / s)) << 8) |
+                     (static_cast<uint32_t>(f32_to_e4m3(v2 / s)) << 16) |
+                     (static_cast<uint32_t>(f32_to_e4m3(v3 / s)) << 24);
+  *reinterpret_cast<uint32_t*>(p.zq + static_cast<size_t>(t) * p.L + g * 128 + lane * 4) = q;
+  if (lane == 0) p.zs[static_cast<size_t>(t) * G + g] = s;
+  // ---- zero the matching 128 floats of the combine buffer
+  reinterpret_cast<float4*>(p.r + static_cast<size_t>(t) * p.L + g * 128)[lane] =
+      make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 __global__ void __launch_bounds__(PERM_BLOCK) perm_hist_kernel(const PermParams p) {
@@ -123,15 +128,24 @@ __global__ void __launch_bounds__(PERM_BLOCK) perm_scatter_kernel(const PermPara
   __shared__ int base[MAX_E];
   __shared__ int total[MAX_E];
   __shared__ int tiles[MAX_E];
-  __shared__ int ppos[PERM_BLOCK];
   pdl_wait();
   pdl_trigger();
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int Mk = p.M * p.k;
   for (int c = tid; c < (PERM_BLOCK / 32) * MAX_E; c += PERM_BLOCK)
     (&warp_cnt[0][0])[c] = 0;
-  // expert totals and the count of this expert's pairs in earlier blocks
-  if (tid < p.E) {
+  // expert totals and the count of this expert's pairs in earlier blocks (a single block
+  // counts its own pairs and needs no histogram pass)
+  if (p.nblocks == 1) {
+    if (tid < p.E) total[tid] = 0;
+    __syncthreads();
+    if (tid < Mk) atomicAdd(&total[p.ids[tid]], 1);
+    __syncthreads();
+    if (tid < p.E) {
+      base[tid] = 0;
+      tiles[tid] = (total[tid] + p.bn - 1) / p.bn;
+    }
+  } else if (tid < p.E) {
     int tot = 0, pre = 0;
     for (int b = 0; b < p.nblocks; ++b) {
       const int h = p.hist[b * p.E + tid];
@@ -186,23 +200,31 @@ __global__ void __launch_bounds__(PERM_BLOCK) perm_scatter_kernel(const PermPara
     p.gidx[pp] = i / p.k;
     p.slot[pp] = i;
     p.pos[i] = pp;
-    ppos[tid] = pp;
   }
-  __syncthreads();
+}
 
-  // gather each pair's quantised latent row (and its scales, transposed) into pair order
+// Gather of each pair's quantised latent row (and its scales, transposed to [group, pair])
+// into pair order, so the routed L1 GEMM streams an expert's token rows as plain tiles.
+// One thread per 16-byte chunk.
+__global__ void __launch_bounds__(256) perm_gather_kernel(const PermParams p) {
+  pdl_wait();
+  pdl_trigger();
   const int G = p.L / 128;
   const int row16 = p.L / 16;
-  for (int q = 0; q < 32; ++q) {
-    const int ii = blockIdx.x * PERM_BLOCK + w * 32 + q;
-    if (ii >= Mk) break;
-    const int t = ii / p.k;
-    const int pp = ppos[w * 32 + q];
-    const uint4* src = reinterpret_cast<const uint4*>(p.zq + static_cast<size_t>(t) * p.L);
-    uint4* dst = reinterpret_cast<uint4*>(p.zq_perm + static_cast<size_t>(pp) * p.L);
-    for (int c = lane; c < row16; c += 32) dst[c] = src[c];
-    for (int g = lane; g < G; g += 32)
-      p.zsT[static_cast<size_t>(g) * p.cap + pp] = p.zs[static_cast<size_t>(t) * G + g];
+  const long long Mk = static_cast<long long>(p.M) * p.k;
+  const long long c = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
+  if (c < Mk * row16) {
+    const int pp = static_cast<int>(c / row16);
+    const int ch = static_cast<int>(c - static_cast<long long>(pp) * row16);
+    const int t = __ldg(p.gidx + pp);
+    reinterpret_cast<uint4*>(p.zq_perm + static_cast<size_t>(pp) * p.L)[ch] =
+        reinterpret_cast<const uint4*>(p.zq + static_cast<size_t>(t) * p.L)[ch];
+  }
+  if (c < Mk * G) {
+    const int pp = static_cast<int>(c / G);
+    const int g = static_cast<int>(c - static_cast<long long>(pp) * G);
+    p.zsT[static_cast<size_t>(g) * p.cap + pp] =
+        p.zs[static_cast<size_t>(__ldg(p.gidx + pp)) * G + g];
   }
 }
 
@@ -260,7 +282,8 @@ cudaError_t launch_simple(Kern k, dim3 grid, dim3 block, const Param& prm, cudaS
 }  // namespace
 
 cudaError_t launch_route(const RouteParams& p, cudaStream_t s, bool pdl) {
-  const int blocks = (p.M + ROUTE_WARPS - 1) / ROUTE_WARPS;
+  const long long warps = static_cast<long long>(p.M) * (p.L / 128 + 1);
+  const int blocks = static_cast<int>((warps + ROUTE_WARPS - 1) / ROUTE_WARPS);
   return launch_simple(route_quant_kernel, dim3(blocks), dim3(32 * ROUTE_WARPS), p, s, pdl);
 }
 cudaError_t launch_perm_hist(const PermParams& p, cudaStream_t s, bool pdl) {
@@ -268,6 +291,11 @@ cudaError_t launch_perm_hist(const PermParams& p, cudaStream_t s, bool pdl) {
 }
 cudaError_t launch_perm_scatter(const PermParams& p, cudaStream_t s, bool pdl) {
   return launch_simple(perm_scatter_kernel, dim3(p.nblocks), dim3(PERM_BLOCK), p, s, pdl);
+}
+cudaError_t launch_perm_gather(const PermParams& p, cudaStream_t s, bool pdl) {
+  const long long chunks = static_cast<long long>(p.M) * p.k * (p.L / 16);
+  return launch_simple(perm_gather_kernel, dim3(static_cast<unsigned>((chunks + 255) / 256)),
+                       dim3(256), p, s, pdl);
 }
 cudaError_t launch_norm(const NormParams& p, cudaStream_t s, bool pdl) {
   return launch_simple(norm_kernel, dim3(p.M), dim3(128), p, s, pdl);
