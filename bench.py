@@ -270,7 +270,8 @@ def main():
         for j in range(nl):
             per[j] += evs[i][j].elapsed_time(evs[i][j + 1])
     per /= args.steps
-    names = ["route", "perm_hist", "perm_scatter", "gemm_l1", "gemm_l2", "norm", "gemm_out"]
+    names = (["route"] + (["perm_hist"] if nl == 8 else []) +
+             ["perm_scatter", "perm_gather", "gemm_l1", "gemm_l2", "norm", "gemm_out"])
     per_launch_us = {n: round(float(v) * 1e3, 2) for n, v in zip(names, per)}
 
     # ---- end to end through the public API with host buffers

@@ -76,7 +76,7 @@ struct klt_handle {
   __nv_bfloat16 *ws13, *ws2, *w_up, *gamma;
   // workspace
   int32_t *ids, *cnt, *off, *tile_off, *gidx, *slot, *pos, *hist;
-  float *wts, *zs, *zsT, *asT, *r, *ws;
+  float *wts, *wperm, *zs, *zsT, *asT, *r, *ws;
   uint8_t *zq, *zq_perm, *aq;
   __nv_bfloat16 *n, *a_s;
   int *split_cnt, *sched, *err;
@@ -203,6 +203,7 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
   KLT_ALLOC(h->gamma, L * 2);
   KLT_ALLOC(h->ids, cap * 4);
   KLT_ALLOC(h->wts, cap * 4);
+  KLT_ALLOC(h->wperm, cap * 4);
   KLT_ALLOC(h->pos, cap * 4);
   KLT_ALLOC(h->gidx, cap * 4);
   KLT_ALLOC(h->slot, cap * 4);
@@ -225,25 +226,28 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
   KLT_ALLOC(h->err, 256);
 #undef KLT_ALLOC
 
+  // Weights are copied tile-major (one contiguous 16 KB block per 128 rows x 128 bytes of
+  // K), so every TMA box of a weight operand is a single contiguous DRAM stream.
   bool ok = true;
-  ok &= cudaMemcpy(h->w13, w->w13, E * 2 * I * L, cudaMemcpyDeviceToDevice) == cudaSuccess;
+  ok &= launch_tile_relayout(w->w13, h->w13, E * 2 * I, L, 0) == cudaSuccess;
+  ok &= launch_tile_relayout(w->w2, h->w2, E * L, I, 0) == cudaSuccess;
+  ok &= launch_tile_relayout(w->ws13, h->ws13, 2 * Is, H * 2, 0) == cudaSuccess;
+  ok &= launch_tile_relayout(w->ws2, h->ws2, H, Is * 2, 0) == cudaSuccess;
+  ok &= launch_tile_relayout(w->w_up, h->w_up, H, L * 2, 0) == cudaSuccess;
   ok &= cudaMemcpy(h->w13_s, w->w13_scale, E * (2 * I / 128) * (L / 128) * 4,
                    cudaMemcpyDeviceToDevice) == cudaSuccess;
-  ok &= cudaMemcpy(h->w2, w->w2, E * L * I, cudaMemcpyDeviceToDevice) == cudaSuccess;
   ok &= cudaMemcpy(h->w2_s, w->w2_scale, E * (L / 128) * (I / 128) * 4,
                    cudaMemcpyDeviceToDevice) == cudaSuccess;
-  ok &= cudaMemcpy(h->ws13, w->ws13, 2 * Is * H * 2, cudaMemcpyDeviceToDevice) == cudaSuccess;
-  ok &= cudaMemcpy(h->ws2, w->ws2, H * Is * 2, cudaMemcpyDeviceToDevice) == cudaSuccess;
-  ok &= cudaMemcpy(h->w_up, w->w_up, H * L * 2, cudaMemcpyDeviceToDevice) == cudaSuccess;
   ok &= cudaMemcpy(h->gamma, w->gamma, L * 2, cudaMemcpyDeviceToDevice) == cudaSuccess;
 
   const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  ok &= encode_2d(&h->tm_w13, h->w13, U8, 1, E * 2 * I, L, 128);
-  ok &= encode_2d(&h->tm_w2, h->w2, U8, 1, E * L, I, 128);
-  ok &= encode_2d(&h->tm_ws13, h->ws13, BF, 2, 2 * Is, H, 128);
-  ok &= encode_2d(&h->tm_ws2, h->ws2, BF, 2, H, Is, 128);
-  ok &= encode_2d(&h->tm_wup, h->w_up, BF, 2, H, L, 128);
+  // tile-major weight maps: [tiles * 128 rows, 128 bytes]
+  ok &= encode_2d(&h->tm_w13, h->w13, U8, 1, E * 2 * I * (L / 128), 128, 128);
+  ok &= encode_2d(&h->tm_w2, h->w2, U8, 1, E * L * (I / 128), 128, 128);
+  ok &= encode_2d(&h->tm_ws13, h->ws13, BF, 2, 2 * Is * (H / 64), 64, 128);
+  ok &= encode_2d(&h->tm_ws2, h->ws2, BF, 2, H * (Is / 64), 64, 128);
+  ok &= encode_2d(&h->tm_wup, h->w_up, BF, 2, H * (L / 64), 64, 128);
   for (int b = 0; b < kNumBN; ++b) {
     ok &= encode_2d(&h->tm_zqp[b], h->zq_perm, U8, 1, cap, L, kBN[b]);
     ok &= encode_2d(&h->tm_aq[b], h->aq, U8, 1, cap, I, kBN[b]);
@@ -326,6 +330,8 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
   pp.zs = h->zs;
   pp.zq_perm = h->zq_perm;
   pp.zsT = h->zsT;
+  pp.wts = h->wts;
+  pp.wperm = h->wperm;
   pp.M = M;
   pp.E = E;
   pp.k = k;
@@ -350,8 +356,7 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
   gp.tile_off = h->tile_off;
   gp.off = h->off;
   gp.gidx = h->gidx;
-  gp.slot = h->slot;
-  gp.wts = h->wts;
+  gp.wperm = h->wperm;
   gp.zsT = h->zsT;
   gp.w13_s = h->w13_s;
   gp.w2_s = h->w2_s;
@@ -380,7 +385,8 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
     S.ftiles = Is / 128;
     S.kb_total = H / 64;
     S.kb_split0 = S.kb_total;
-    S.a_up_off = Is;
+    S.a_rb_up = Is / 128;
+    S.a_kb[0] = S.a_kb[1] = H / 64;
     S.ws_tile_base = 0;
     // split so that a shared unit streams about as many bytes as a routed L1 unit
     plan_split(S, ntiles,
@@ -400,8 +406,9 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
     R.kb_split0 = R.kb_total;
     R.ksplit = 1;
     R.kb_per_split = R.kb_total;
-    R.a_up_off = I;
-    R.a_rows_expert = 2 * I;
+    R.a_rb_up = I / 128;
+    R.a_rb_expert = 2 * I / 128;
+    R.a_kb[0] = R.a_kb[1] = L / 128;
     R.tmA[0] = h->tm_w13;
     R.tmA[1] = h->tm_w13;
     R.tmB[0] = h->tm_zqp[bi];
@@ -421,7 +428,8 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
     R.kb_split0 = R.kb_total;
     R.ksplit = 1;
     R.kb_per_split = R.kb_total;
-    R.a_rows_expert = L;
+    R.a_rb_expert = L / 128;
+    R.a_kb[0] = R.a_kb[1] = I / 128;
     R.tmA[0] = h->tm_w2;
     R.tmA[1] = h->tm_w2;
     R.tmB[0] = h->tm_aq[bi];
@@ -451,6 +459,8 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
     O.kb_total = L / 64 + Is / 64;
     O.kb_split0 = L / 64;
     O.ws_tile_base = 0;
+    O.a_kb[0] = L / 64;
+    O.a_kb[1] = Is / 64;
     plan_split(O, ntiles, 2 * h->num_sms, BN);
     O.tmA[0] = h->tm_wup;
     O.tmA[1] = h->tm_ws2;

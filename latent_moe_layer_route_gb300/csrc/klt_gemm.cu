@@ -55,7 +55,7 @@ struct UnitInfo {
   int row0;   // first token row of the B tile
   int rows;   // valid token rows (D columns)
   int ftile;  // 128-row output tile
-  int arow0;  // first A-map row of the (gate) tile
+  int arb;    // 128-row block of the (gate) weight tile
   int kb0, kb1;
   int tile_id;  // split-K tile (non-routed)
   int split;
@@ -107,13 +107,14 @@ __device__ __forceinline__ bool is_promote(int kind) {
 }
 
 template <int BN>
-__device__ UnitInfo decode_unit(const GemmParams& p, int u) {
+__device__ UnitInfo decode_unit(const GemmParams& p, const int* s_tile_off, const int* s_off,
+                                int u) {
   UnitInfo info;
   info.task = -1;
   for (int ti = 0; ti < p.ntasks; ++ti) {
     const GemmTask& T = p.task[ti];
     if (T.routed) {
-      const int ntiles = p.tile_off[p.E];
+      const int ntiles = s_tile_off[p.E];
       const int units = ntiles * T.ftiles;
       if (u < units) {
         const int t = u / T.ftiles;
@@ -121,15 +122,15 @@ __device__ UnitInfo decode_unit(const GemmParams& p, int u) {
         int lo = 0, hi = p.E - 1;  // largest e with tile_off[e] <= t
         while (lo < hi) {
           const int mid = (lo + hi + 1) >> 1;
-          if (p.tile_off[mid] <= t) lo = mid; else hi = mid - 1;
+          if (s_tile_off[mid] <= t) lo = mid; else hi = mid - 1;
         }
         const int e = lo;
         info.task = ti;
         info.e = e;
-        info.row0 = p.off[e] + (t - p.tile_off[e]) * BN;
-        info.rows = min(BN, p.off[e + 1] - info.row0);
+        info.row0 = s_off[e] + (t - s_tile_off[e]) * BN;
+        info.rows = min(BN, s_off[e + 1] - info.row0);
         info.ftile = ft;
-        info.arow0 = e * T.a_rows_expert + ft * 128;
+        info.arb = e * T.a_rb_expert + ft;
         info.kb0 = 0;
         info.kb1 = T.kb_total;
         info.tile_id = 0;
@@ -149,7 +150,7 @@ __device__ UnitInfo decode_unit(const GemmParams& p, int u) {
         info.row0 = nt * BN;
         info.rows = min(BN, p.M - info.row0);
         info.ftile = ft;
-        info.arow0 = ft * 128;
+        info.arb = ft;
         info.kb0 = sp * T.kb_per_split;
         info.kb1 = min(T.kb_total, info.kb0 + T.kb_per_split);
         info.tile_id = T.ws_tile_base + nt * T.ftiles + ft;
@@ -164,7 +165,8 @@ __device__ UnitInfo decode_unit(const GemmParams& p, int u) {
 
 // ------------------------------------------------------------------ producer (1 thread)
 template <int BN>
-__device__ void run_producer(const GemmParams& p, Smem<BN>& sm) {
+__device__ void run_producer(const GemmParams& p, Smem<BN>& sm, const int* s_tile_off,
+                             const int* s_off) {
   using C = Cfg<BN>;
   const uint64_t pol_w = policy_evict_first();
   const uint64_t pol_t = policy_evict_last();
@@ -175,7 +177,7 @@ __device__ void run_producer(const GemmParams& p, Smem<BN>& sm) {
   bool stalled = false;
   int u = atomicAdd(p.sched, 1);
   for (;;) {
-    const UnitInfo info = decode_unit<BN>(p, u);
+    const UnitInfo info = decode_unit<BN>(p, s_tile_off, s_off, u);
     // claim the next unit now so the counter round trip overlaps this unit's copies
     if (info.task >= 0) u = atomicAdd(p.sched, 1);
     if (!mbar_wait(&sm.uempty[us], uphase ^ 1, sm.abort_flag, p.err, p.timeout)) break;
@@ -194,13 +196,16 @@ __device__ void run_producer(const GemmParams& p, Smem<BN>& sm) {
         break;
       }
       const int m = kb < T.kb_split0 ? 0 : 1;
-      const int inner = (m ? kb - T.kb_split0 : kb) * elems_per_kb;
+      const int kk = m ? kb - T.kb_split0 : kb;
+      const int inner = kk * elems_per_kb;
       uint8_t* st = sm.stages + stage * C::STAGE_BYTES;
       mbar_arrive_expect_tx(&sm.full[stage], bytes);
-      tma_load_2d(st, &T.tmA[m], &sm.full[stage], inner, info.arow0, pol_w);
+      // weights are stored tile-major: one contiguous 16 KB block per (row block, kb)
+      tma_load_2d(st, &T.tmA[m], &sm.full[stage], 0, (info.arb * T.a_kb[m] + kk) * 128,
+                  pol_w);
       if (pair)
-        tma_load_2d(st + C::A_BYTES, &T.tmA[m], &sm.full[stage], inner,
-                    info.arow0 + T.a_up_off, pol_w);
+        tma_load_2d(st + C::A_BYTES, &T.tmA[m], &sm.full[stage], 0,
+                    ((info.arb + T.a_rb_up) * T.a_kb[m] + kk) * 128, pol_w);
       tma_load_2d(st + 2 * C::A_BYTES, &T.tmB[m], &sm.full[stage], inner, info.row0, pol_t);
       ++issued;
       if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
@@ -451,7 +456,7 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
         if (c0 + j < info.rows) {
           const int pp = info.row0 + c0 + j;
           const int tok = __ldg(p.gidx + pp);
-          const float wv = __ldg(p.wts + __ldg(p.slot + pp));
+          const float wv = __ldg(p.wperm + pp);
           atomicAdd(p.r + static_cast<size_t>(tok) * p.L + col, wv * g[j]);
         }
       }
@@ -532,7 +537,14 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
   pdl_trigger();
 
   if (warp == 0) {
-    if (lane == 0) run_producer<BN>(p, sm);
+    // routing tile offsets for the producer's unit decode, read once per CTA
+    __shared__ int s_tile_off[MAX_E + 1], s_off[MAX_E + 1];
+    for (int i = lane; i <= p.E; i += 32) {
+      s_tile_off[i] = p.tile_off[i];
+      s_off[i] = p.off[i];
+    }
+    __syncwarp();
+    if (lane == 0) run_producer<BN>(p, sm, s_tile_off, s_off);
   } else if (warp == 1) {
     if (lane == 0) run_mma<BN>(p, sm, tmem_base);
   } else {

@@ -36,6 +36,8 @@ struct PermParams {
   const float* zs;     // [M, L/128]
   uint8_t* zq_perm;    // [cap, L]
   float* zsT;          // [L/128, cap]
+  const float* wts;    // [M*k] routing weights by pair i
+  float* wperm;        // [cap] routing weight of pair p
   int M, E, k, L, cap, bn, nblocks;
 };
 
@@ -67,8 +69,9 @@ struct GemmTask {
   int kb_split0;       // k-blocks served by map pair 0
   int ksplit;          // k splits (non-routed only); >1 => partials + last-arriver reduce
   int kb_per_split;
-  int a_up_off;        // rows from a gate tile to its up tile in tmA (pair kinds)
-  int a_rows_expert;   // routed: rows per expert in tmA
+  int a_rb_up;         // 128-row blocks from a gate tile to its up tile (pair kinds)
+  int a_rb_expert;     // routed: 128-row blocks per expert
+  int a_kb[2];         // k-blocks per 128-row block in tmA[0], tmA[1] (tile-major weights)
   int ntiles;          // non-routed: token tiles
   int units;           // non-routed: ntiles * ftiles * ksplit
   int ws_tile_base;    // first split-K workspace tile / counter of this task
@@ -82,8 +85,7 @@ struct GemmParams {
   const int32_t* tile_off;     // [E+1]
   const int32_t* off;          // [E+1]
   const int32_t* gidx;         // [cap]
-  const int32_t* slot;         // [cap]
-  const float* wts;            // [M*k] routing weights by pair i
+  const float* wperm;          // [cap] routing weight of pair p
   const float* zsT;            // [L/128, cap]
   const float* w13_s;          // [E, 2I/128, L/128]
   const float* w2_s;           // [E, L/128, I/128]
@@ -106,6 +108,10 @@ cudaError_t launch_perm_hist(const PermParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_perm_scatter(const PermParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_perm_gather(const PermParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_norm(const NormParams& p, cudaStream_t s, bool pdl);
+// Row-major [rows, row_bytes] -> 128-row x 128-byte tiles, tile (rb, kb) at
+// ((rb * row_bytes/128) + kb) * 16384 bytes (rows % 128 == 0, row_bytes % 128 == 0).
+cudaError_t launch_tile_relayout(const void* src, void* dst, long long rows, long long row_bytes,
+                                 cudaStream_t s);
 // bn in {16, 128}; grid = persistent CTAs.
 cudaError_t launch_gemm(const GemmParams& p, int bn, int grid, cudaStream_t s, bool pdl);
 int gemm_smem_bytes(int bn);

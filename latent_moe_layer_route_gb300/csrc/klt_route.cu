@@ -200,6 +200,7 @@ __global__ void __launch_bounds__(PERM_BLOCK) perm_scatter_kernel(const PermPara
     p.gidx[pp] = i / p.k;
     p.slot[pp] = i;
     p.pos[i] = pp;
+    p.wperm[pp] = p.wts[i];
   }
 }
 
@@ -263,6 +264,18 @@ __global__ void __launch_bounds__(128) norm_kernel(const NormParams p) {
   }
 }
 
+__global__ void __launch_bounds__(256)
+    tile_relayout_kernel(const uint8_t* src, uint8_t* dst, long long rows, long long row_bytes) {
+  const long long c16 = row_bytes / 16;
+  const long long q = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
+  if (q >= rows * c16) return;
+  const long long row = q / c16, col = q - row * c16;
+  const long long rb = row >> 7, r = row & 127, kb = col >> 3, ch = col & 7;
+  const long long dst_off = (((rb * (row_bytes / 128)) + kb) * 128 + r) * 128 + ch * 16;
+  *reinterpret_cast<uint4*>(dst + dst_off) =
+      *reinterpret_cast<const uint4*>(src + row * row_bytes + col * 16);
+}
+
 template <typename Kern, typename Param>
 cudaError_t launch_simple(Kern k, dim3 grid, dim3 block, const Param& prm, cudaStream_t s,
                           bool pdl) {
@@ -299,6 +312,14 @@ cudaError_t launch_perm_gather(const PermParams& p, cudaStream_t s, bool pdl) {
 }
 cudaError_t launch_norm(const NormParams& p, cudaStream_t s, bool pdl) {
   return launch_simple(norm_kernel, dim3(p.M), dim3(128), p, s, pdl);
+}
+
+cudaError_t launch_tile_relayout(const void* src, void* dst, long long rows, long long row_bytes,
+                                 cudaStream_t s) {
+  const long long chunks = rows * (row_bytes / 16);
+  tile_relayout_kernel<<<static_cast<unsigned>((chunks + 255) / 256), 256, 0, s>>>(
+      static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst), rows, row_bytes);
+  return cudaGetLastError();
 }
 
 }  // namespace klt
