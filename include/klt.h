@@ -127,7 +127,12 @@ typedef struct klt_routing {
  *   stall_after_kblocks: test hook, 0 = off; when > 0 the tile producer of the first
  *     GEMM stops feeding data after that many k-blocks, so its consumers' bounded waits
  *     run out and klt_status reports KLT_ERR_DEVICE_TIMEOUT;
- *   timeout_ms: bound of every on-device wait for this call (0 = the default, 1000 ms). */
+ *   timeout_ms: bound of every on-device wait for this call (0 = the default, 1000 ms);
+ *   trace: optional device int64 buffer of 3 * trace_entries * 3 * (SM count) entries; when
+ *     set, each GEMM launch g (0..2) records globaltimer stamps (ns) per CTA c and role r
+ *     (0 = weight tile copy issued, 1 = tile consumed by the MMA issuer, 2 = epilogue step
+ *     done) at trace[((g * SMs + c) * 3 + r) * trace_entries + i], first trace_entries
+ *     events each; unused entries are left untouched. */
 typedef struct klt_debug {
   uint8_t* zq;
   float* zs;
@@ -139,6 +144,8 @@ typedef struct klt_debug {
   void* events[8];
   int32_t stall_after_kblocks;
   int32_t timeout_ms;
+  int64_t* trace;
+  int32_t trace_entries;
 } klt_debug;
 
 typedef struct klt_handle klt_handle;

@@ -62,6 +62,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 constexpr int kNumBN = 2;
 constexpr int kBN[kNumBN] = {16, 128};
 constexpr int kMaxSplitUnits = 3 * 160;  // split-K tiles*splits bound per task
+constexpr int kMaxCounters = 8192;       // arrival counters per split task
 
 }  // namespace
 
@@ -221,7 +222,7 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
   KLT_ALLOC(h->n, Mx * L * 2);
   KLT_ALLOC(h->a_s, Mx * Is * 2);
   KLT_ALLOC(h->ws, 2LL * kMaxSplitUnits * 2 * 128 * 128 * 4);
-  KLT_ALLOC(h->split_cnt, 2LL * kMaxSplitUnits * 4);
+  KLT_ALLOC(h->split_cnt, 2LL * kMaxCounters * 4);
   KLT_ALLOC(h->sched, 64 * 4);
   KLT_ALLOC(h->err, 256);
 #undef KLT_ALLOC
@@ -369,6 +370,10 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
   gp.cnt = h->split_cnt;
   gp.err = h->err;
   gp.timeout = timeout_cycles;
+  gp.trace_n = dbg ? dbg->trace_entries : 0;
+  long long* trace = (dbg && dbg->trace && dbg->trace_entries > 0)
+                         ? reinterpret_cast<long long*>(dbg->trace) : nullptr;
+  const long long trace_launch = static_cast<long long>(h->num_sms) * 3 * gp.trace_n;
   const int ntiles = (M + BN - 1) / BN;
   const int grid = h->num_sms;
   const size_t ws_task = static_cast<size_t>(kMaxSplitUnits) * 2 * 128 * 128;
@@ -379,26 +384,9 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
     g1.ntasks = 2;
     g1.sched = h->sched + 0;
     g1.stall_after = dbg ? dbg->stall_after_kblocks : 0;
-    GemmTask& S = g1.task[0];
-    S.kind = TASK_SHARED_L1;
-    S.routed = 0;
-    S.ftiles = Is / 128;
-    S.kb_total = H / 64;
-    S.kb_split0 = S.kb_total;
-    S.a_rb_up = Is / 128;
-    S.a_kb[0] = S.a_kb[1] = H / 64;
-    S.ws_tile_base = 0;
-    // split so that a shared unit streams about as many bytes as a routed L1 unit
-    plan_split(S, ntiles,
-               std::min(ntiles * S.ftiles * std::max(1, (S.kb_total * 128) / L),
-                        2 * h->num_sms),
-               BN);
-    if (!encode_2d(&S.tmB[0], x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, H, BN))
-      return KLT_ERR_CUDA;
-    S.tmA[0] = h->tm_ws13;
-    S.tmA[1] = h->tm_ws13;
-    S.tmB[1] = S.tmB[0];
-    GemmTask& R = g1.task[1];
+    g1.trace = trace;
+    // Routed units first, then the shared expert in small k-splits that fill the tail.
+    GemmTask& R = g1.task[0];
     R.kind = TASK_ROUTED_L1;
     R.routed = 1;
     R.ftiles = I / 128;
@@ -413,6 +401,21 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
     R.tmA[1] = h->tm_w13;
     R.tmB[0] = h->tm_zqp[bi];
     R.tmB[1] = h->tm_zqp[bi];
+    GemmTask& S = g1.task[1];
+    S.kind = TASK_SHARED_L1;
+    S.routed = 0;
+    S.ftiles = Is / 128;
+    S.kb_total = H / 64;
+    S.kb_split0 = S.kb_total;
+    S.a_rb_up = Is / 128;
+    S.a_kb[0] = S.a_kb[1] = H / 64;
+    S.ws_tile_base = 0;
+    plan_split(S, ntiles, ntiles * S.ftiles * std::max(1, S.kb_total / 8), BN);
+    if (!encode_2d(&S.tmB[0], x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, H, BN))
+      return KLT_ERR_CUDA;
+    S.tmA[0] = h->tm_ws13;
+    S.tmA[1] = h->tm_ws13;
+    S.tmB[1] = S.tmB[0];
     KLT_LAUNCH(launch_gemm(g1, BN, grid, s, pdl));
   }
   // ---- GEMM 2: routed L2 with the top-k weighted scatter-combine into r
@@ -420,6 +423,7 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
     GemmParams g2 = gp;
     g2.ntasks = 1;
     g2.sched = h->sched + 1;
+    g2.trace = trace ? trace + trace_launch : nullptr;
     GemmTask& R = g2.task[0];
     R.kind = TASK_ROUTED_L2;
     R.routed = 1;
@@ -450,8 +454,9 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
     GemmParams g3 = gp;
     g3.ntasks = 1;
     g3.sched = h->sched + 2;
+    g3.trace = trace ? trace + 2 * trace_launch : nullptr;
     g3.ws = h->ws + ws_task;
-    g3.cnt = h->split_cnt + kMaxSplitUnits;
+    g3.cnt = h->split_cnt + kMaxCounters;
     GemmTask& O = g3.task[0];
     O.kind = TASK_OUT;
     O.routed = 0;
@@ -461,7 +466,16 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
     O.ws_tile_base = 0;
     O.a_kb[0] = L / 64;
     O.a_kb[1] = Is / 64;
-    plan_split(O, ntiles, 2 * h->num_sms, BN);
+    O.ksplit = 1;
+    O.kb_per_split = O.kb_total;
+    O.ntiles = ntiles;
+    O.units = ntiles * O.ftiles;
+    if (O.units < 4 * grid) {
+      // static stream-K: every CTA streams the same number of k-blocks
+      O.streamk = 1;
+      O.sk_grid = grid;
+      O.sk_total = static_cast<long long>(O.units) * O.kb_total;
+    }
     O.tmA[0] = h->tm_wup;
     O.tmA[1] = h->tm_ws2;
     O.tmB[0] = h->tm_n[bi];

@@ -207,6 +207,12 @@ KLT_DEV uint8_t f32_to_e4m3(float v) {
 
 KLT_DEV int lane_id() { return threadIdx.x & 31; }
 
+KLT_DEV long long global_ns() {
+  long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
 KLT_DEV void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

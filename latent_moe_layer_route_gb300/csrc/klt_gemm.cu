@@ -36,7 +36,10 @@ struct Cfg {
   static constexpr int EPI_THREADS = EPI_WARPS * 32;
   static constexpr int A_BYTES = 128 * 128;
   static constexpr int B_BYTES = BN * 128;
-  static constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES;
+  // Single-tile tasks carry two k-blocks per stage (A0/A1 + B0/B1) when the stage fits,
+  // so every stage keeps ~32 KB of weights in flight.
+  static constexpr bool DUAL = BN <= 32;
+  static constexpr int STAGE_BYTES = 2 * A_BYTES + (DUAL ? 2 : 1) * B_BYTES;
   static constexpr int STAGES = BN == 16 ? 6 : (BN == 128 ? 3 : 5);
   static constexpr int SLOT_COLS = 2 * BN;
   static constexpr int TMEM_COLS = BN <= 64 ? 256 : 512;
@@ -57,9 +60,27 @@ struct UnitInfo {
   int ftile;  // 128-row output tile
   int arb;    // 128-row block of the (gate) weight tile
   int kb0, kb1;
-  int tile_id;  // split-K tile (non-routed)
-  int split;
+  int tile_id;   // split-K / stream-K tile (non-routed)
+  int split;     // fixed split index
+  int ncontrib;  // units contributing to this tile (1: no partials)
+  int cfirst;    // stream-K: first contributing CTA
+  int wslot;     // stream-K: this unit's partial slot
 };
+
+// Stream-K helpers: CTA c owns k-blocks [b(c), b(c+1)) of the task's flattened
+// (tile, kb) sequence, b(c) = c * total / grid.
+__device__ __forceinline__ long long sk_begin(long long total, int grid, int c) {
+  return static_cast<long long>(c) * total / grid;
+}
+__device__ __forceinline__ int sk_owner(long long total, int grid, long long x) {
+  return static_cast<int>(((x + 1) * grid + total - 1) / total - 1);
+}
+// Partial slot of CTA c for tile t: 0 for its first tile, 1 for its last.
+__device__ __forceinline__ int sk_slot(long long total, int grid, int kb_per_tile, int c,
+                                       int t) {
+  const int first_tile = static_cast<int>(sk_begin(total, grid, c) / kb_per_tile);
+  return c * 2 + (t == first_tile ? 0 : 1);
+}
 
 template <int BN>
 struct Smem {
@@ -99,6 +120,12 @@ struct Smem {
   }
 };
 
+// Optional event trace: stamp i of role r for this CTA.
+__device__ __forceinline__ void trace_mark(const GemmParams& p, int role, int i) {
+  if (p.trace != nullptr && i < p.trace_n)
+    p.trace[(static_cast<long long>(blockIdx.x) * 3 + role) * p.trace_n + i] = global_ns();
+}
+
 __device__ __forceinline__ bool is_pair(int kind) {
   return kind == TASK_SHARED_L1 || kind == TASK_ROUTED_L1;
 }
@@ -135,6 +162,9 @@ __device__ UnitInfo decode_unit(const GemmParams& p, const int* s_tile_off, cons
         info.kb1 = T.kb_total;
         info.tile_id = 0;
         info.split = 0;
+        info.ncontrib = 1;
+        info.cfirst = 0;
+        info.wslot = 0;
         return info;
       }
       u -= units;
@@ -155,11 +185,44 @@ __device__ UnitInfo decode_unit(const GemmParams& p, const int* s_tile_off, cons
         info.kb1 = min(T.kb_total, info.kb0 + T.kb_per_split);
         info.tile_id = T.ws_tile_base + nt * T.ftiles + ft;
         info.split = sp;
+        info.ncontrib = T.ksplit;
+        info.cfirst = 0;
+        info.wslot = 0;
         return info;
       }
       u -= T.units;
     }
   }
+  return info;
+}
+
+// Next stream-K piece of this CTA (task 0); advances the cursor x.
+template <int BN>
+__device__ UnitInfo next_streamk_piece(const GemmParams& p, long long& x, long long end) {
+  UnitInfo info;
+  info.task = -1;
+  if (x >= end) return info;
+  const GemmTask& T = p.task[0];
+  const int K = T.kb_total;
+  const int t = static_cast<int>(x / K);
+  const int kb0 = static_cast<int>(x - static_cast<long long>(t) * K);
+  const int kb1 = static_cast<int>(min(static_cast<long long>(K), kb0 + (end - x)));
+  x += kb1 - kb0;
+  const int nt = t / T.ftiles, ft = t - nt * T.ftiles;
+  info.task = 0;
+  info.e = 0;
+  info.row0 = nt * BN;
+  info.rows = min(BN, p.M - info.row0);
+  info.ftile = ft;
+  info.arb = ft;
+  info.kb0 = kb0;
+  info.kb1 = kb1;
+  info.tile_id = T.ws_tile_base + t;
+  info.split = 0;
+  info.cfirst = sk_owner(T.sk_total, T.sk_grid, static_cast<long long>(t) * K);
+  info.ncontrib =
+      sk_owner(T.sk_total, T.sk_grid, static_cast<long long>(t + 1) * K - 1) - info.cfirst + 1;
+  info.wslot = sk_slot(T.sk_total, T.sk_grid, K, blockIdx.x, t);
   return info;
 }
 
@@ -175,11 +238,24 @@ __device__ void run_producer(const GemmParams& p, Smem<BN>& sm, const int* s_til
   long long issued = 0;
   int dummy_abort = 0;
   bool stalled = false;
-  int u = atomicAdd(p.sched, 1);
+  const bool streamk = p.task[0].streamk != 0;
+  long long sk_x = 0, sk_end = 0;
+  int u = 0;
+  if (streamk) {
+    sk_x = sk_begin(p.task[0].sk_total, p.task[0].sk_grid, blockIdx.x);
+    sk_end = sk_begin(p.task[0].sk_total, p.task[0].sk_grid, blockIdx.x + 1);
+  } else {
+    u = atomicAdd(p.sched, 1);
+  }
   for (;;) {
-    const UnitInfo info = decode_unit<BN>(p, s_tile_off, s_off, u);
-    // claim the next unit now so the counter round trip overlaps this unit's copies
-    if (info.task >= 0) u = atomicAdd(p.sched, 1);
+    UnitInfo info;
+    if (streamk) {
+      info = next_streamk_piece<BN>(p, sk_x, sk_end);
+    } else {
+      info = decode_unit<BN>(p, s_tile_off, s_off, u);
+      // claim the next unit now so the counter round trip overlaps this unit's copies
+      if (info.task >= 0) u = atomicAdd(p.sched, 1);
+    }
     if (!mbar_wait(&sm.uempty[us], uphase ^ 1, sm.abort_flag, p.err, p.timeout)) break;
     sm.ring[us] = info;
     mbar_arrive(&sm.ufull[us]);
@@ -188,25 +264,32 @@ __device__ void run_producer(const GemmParams& p, Smem<BN>& sm, const int* s_til
     const GemmTask& T = p.task[info.task];
     const bool pair = is_pair(T.kind);
     const int elems_per_kb = is_promote(T.kind) ? 128 : 64;
-    const uint32_t bytes = (pair ? 2 : 1) * C::A_BYTES + C::B_BYTES;
-    for (int kb = info.kb0; kb < info.kb1; ++kb) {
+    const int step = (pair || !C::DUAL) ? 1 : 2;
+    for (int kb = info.kb0; kb < info.kb1; kb += step) {
       if (p.stall_after > 0 && issued >= p.stall_after) { stalled = true; break; }
       if (!mbar_wait(&sm.empty[stage], phase ^ 1, sm.abort_flag, p.err, p.timeout)) {
         stalled = true;
         break;
       }
-      const int m = kb < T.kb_split0 ? 0 : 1;
-      const int kk = m ? kb - T.kb_split0 : kb;
-      const int inner = kk * elems_per_kb;
+      const int nsub = min(step, info.kb1 - kb);
       uint8_t* st = sm.stages + stage * C::STAGE_BYTES;
+      const uint32_t bytes = pair ? 2 * C::A_BYTES + C::B_BYTES
+                                  : static_cast<uint32_t>(nsub) * (C::A_BYTES + C::B_BYTES);
       mbar_arrive_expect_tx(&sm.full[stage], bytes);
-      // weights are stored tile-major: one contiguous 16 KB block per (row block, kb)
-      tma_load_2d(st, &T.tmA[m], &sm.full[stage], 0, (info.arb * T.a_kb[m] + kk) * 128,
-                  pol_w);
-      if (pair)
-        tma_load_2d(st + C::A_BYTES, &T.tmA[m], &sm.full[stage], 0,
-                    ((info.arb + T.a_rb_up) * T.a_kb[m] + kk) * 128, pol_w);
-      tma_load_2d(st + 2 * C::A_BYTES, &T.tmB[m], &sm.full[stage], inner, info.row0, pol_t);
+      for (int sub = 0; sub < nsub; ++sub) {
+        const int kbs = kb + sub;
+        const int m = kbs < T.kb_split0 ? 0 : 1;
+        const int kk = m ? kbs - T.kb_split0 : kbs;
+        // weights are stored tile-major: one contiguous 16 KB block per (row block, kb)
+        tma_load_2d(st + sub * C::A_BYTES, &T.tmA[m], &sm.full[stage], 0,
+                    (info.arb * T.a_kb[m] + kk) * 128, pol_w);
+        if (pair)
+          tma_load_2d(st + C::A_BYTES, &T.tmA[m], &sm.full[stage], 0,
+                      ((info.arb + T.a_rb_up) * T.a_kb[m] + kk) * 128, pol_w);
+        tma_load_2d(st + 2 * C::A_BYTES + sub * C::B_BYTES, &T.tmB[m], &sm.full[stage],
+                    kk * elems_per_kb, info.row0, pol_t);
+      }
+      trace_mark(p, 0, static_cast<int>(issued));
       ++issued;
       if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
     }
@@ -226,7 +309,7 @@ __device__ void run_producer(const GemmParams& p, Smem<BN>& sm, const int* s_til
 template <int BN>
 __device__ void run_mma(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_base) {
   using C = Cfg<BN>;
-  int stage = 0, us = 0, acc = 0;
+  int stage = 0, us = 0, acc = 0, consumed = 0;
   uint32_t phase = 0, uphase = 0, aphase = 0;
   bool ok = true;
   const uint32_t idesc_bf16 = idesc_make(1, 128, BN);
@@ -241,45 +324,50 @@ __device__ void run_mma(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_base) {
     const bool pair = is_pair(kind);
     const bool promote = is_promote(kind);
     const uint32_t idesc = promote ? idesc_fp8 : idesc_bf16;
+    const int step = (pair || !C::DUAL) ? 1 : 2;
     if (!promote) {
       if (!mbar_wait(&sm.tempty[acc], aphase ^ 1, sm.abort_flag, p.err, p.timeout)) break;
       tc_fence_after();
     }
-    for (int kb = info.kb0; kb < info.kb1; ++kb) {
-      if (promote) {
-        if (!mbar_wait(&sm.tempty[acc], aphase ^ 1, sm.abort_flag, p.err, p.timeout)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-      }
+    for (int kb = info.kb0; kb < info.kb1 && ok; kb += step) {
       if (!mbar_wait(&sm.full[stage], phase, sm.abort_flag, p.err, p.timeout)) {
         ok = false;
         break;
       }
+      trace_mark(p, 1, consumed++);
       tc_fence_after();
-      const uint32_t d = tmem_base + static_cast<uint32_t>(acc * C::SLOT_COLS);
+      const int nsub = min(step, info.kb1 - kb);
       const uint32_t sa = smem_u32(sm.stages + stage * C::STAGE_BYTES);
-      const uint64_t da = sdesc_sw128(sa);
-      const uint64_t du = sdesc_sw128(sa + C::A_BYTES);
-      const uint64_t db = sdesc_sw128(sa + 2 * C::A_BYTES);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint32_t accum = promote ? (kk > 0) : (kb > info.kb0 || kk > 0);
+      for (int sub = 0; sub < nsub; ++sub) {
         if (promote) {
-          mma_fp8(d, da + 2 * kk, db + 2 * kk, idesc, accum);
-          if (pair) mma_fp8(d + BN, du + 2 * kk, db + 2 * kk, idesc, accum);
-        } else {
-          mma_bf16(d, da + 2 * kk, db + 2 * kk, idesc, accum);
-          if (pair) mma_bf16(d + BN, du + 2 * kk, db + 2 * kk, idesc, accum);
+          if (!mbar_wait(&sm.tempty[acc], aphase ^ 1, sm.abort_flag, p.err, p.timeout)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * C::SLOT_COLS);
+        const uint64_t da = sdesc_sw128(sa + sub * C::A_BYTES);
+        const uint64_t du = sdesc_sw128(sa + C::A_BYTES);
+        const uint64_t db = sdesc_sw128(sa + 2 * C::A_BYTES + sub * C::B_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint32_t accum = promote ? (kk > 0) : (kb + sub > info.kb0 || kk > 0);
+          if (promote) {
+            mma_fp8(d, da + 2 * kk, db + 2 * kk, idesc, accum);
+            if (pair) mma_fp8(d + BN, du + 2 * kk, db + 2 * kk, idesc, accum);
+          } else {
+            mma_bf16(d, da + 2 * kk, db + 2 * kk, idesc, accum);
+            if (pair) mma_bf16(d + BN, du + 2 * kk, db + 2 * kk, idesc, accum);
+          }
+        }
+        if (promote) {
+          tc_commit(&sm.tfull[acc]);
+          if (++acc == C::NACC) { acc = 0; aphase ^= 1; }
         }
       }
       tc_commit(&sm.empty[stage]);
       if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
-      if (promote) {
-        tc_commit(&sm.tfull[acc]);
-        if (++acc == C::NACC) { acc = 0; aphase ^= 1; }
-      }
     }
     if (!ok) break;
     if (!promote) {
@@ -305,7 +393,7 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
   const int row = quad * 32 + lane;     // output feature within the tile
   const int c0 = half * COLS;
   const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-  int us = 0, acc = 0, sc_buf = 0;
+  int us = 0, acc = 0, sc_buf = 0, steps = 0;
   uint32_t uphase = 0, aphase = 0;
   const int G_L = p.L / 128, G_I = p.I / 128;
 
@@ -380,6 +468,7 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.tempty[acc]);
         if (++acc == C::NACC) { acc = 0; aphase ^= 1; }
+        if (ew == 0 && lane == 0) trace_mark(p, 2, steps++);
       }
     } else {
       if (!mbar_wait(&sm.tfull[acc], aphase, sm.abort_flag, p.err, p.timeout)) return;
@@ -396,14 +485,17 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.tempty[acc]);
       if (++acc == C::NACC) { acc = 0; aphase ^= 1; }
+      if (ew == 0 && lane == 0) trace_mark(p, 2, steps++);
     }
 
-    // ---- split-K: publish the partial; the last arriving split reduces in split order
-    if (!T.routed && T.ksplit > 1) {
+    // ---- split-K / stream-K: publish the partial; the last arriving contributor sums
+    // all contributors' partials in a fixed order (deterministic)
+    if (info.ncontrib > 1) {
       const int parts = pair ? 2 : 1;
       const size_t tile_floats = static_cast<size_t>(parts) * BN * 128;
-      float* mine = p.ws + (static_cast<size_t>(info.tile_id) * T.ksplit + info.split) *
-                               tile_floats;
+      const size_t own = T.streamk ? static_cast<size_t>(info.wslot)
+                                   : static_cast<size_t>(info.tile_id) * T.ksplit + info.split;
+      float* mine = p.ws + own * tile_floats;
 #pragma unroll
       for (int j = 0; j < COLS; ++j) {
         __stcg(mine + static_cast<size_t>(c0 + j) * 128 + row, g[j]);
@@ -413,18 +505,22 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
       named_bar_sync(1, C::EPI_THREADS);
       if (ew == 0 && lane == 0) {
         const int old = atomicAdd(p.cnt + info.tile_id, 1);
-        const int last = old == T.ksplit - 1;
+        const int last = old == info.ncontrib - 1;
         if (last) p.cnt[info.tile_id] = 0;
         *sm.last_flag = last;
       }
       named_bar_sync(1, C::EPI_THREADS);
       if (!*sm.last_flag) continue;
       __threadfence();
-      const float* all = p.ws + static_cast<size_t>(info.tile_id) * T.ksplit * tile_floats;
 #pragma unroll
       for (int j = 0; j < COLS; ++j) { g[j] = 0.f; u[j] = 0.f; }
-      for (int s = 0; s < T.ksplit; ++s) {
-        const float* ps = all + static_cast<size_t>(s) * tile_floats;
+      for (int s = 0; s < info.ncontrib; ++s) {
+        const size_t idx =
+            T.streamk ? static_cast<size_t>(sk_slot(T.sk_total, T.sk_grid, T.kb_total,
+                                                    info.cfirst + s,
+                                                    info.tile_id - T.ws_tile_base))
+                      : static_cast<size_t>(info.tile_id) * T.ksplit + s;
+        const float* ps = p.ws + idx * tile_floats;
 #pragma unroll
         for (int j = 0; j < COLS; ++j) {
           g[j] += __ldcg(ps + static_cast<size_t>(c0 + j) * 128 + row);
@@ -582,8 +678,9 @@ cudaError_t launch_bn(const GemmParams& p, int grid, cudaStream_t s, bool pdl) {
 
 }  // namespace
 
-static_assert(Smem<16>::bytes() <= 227 * 1024, "shared memory budget");
-static_assert(Smem<128>::bytes() <= 227 * 1024, "shared memory budget");
+// dynamic shared memory plus the producer's static offset tables
+static_assert(Smem<16>::bytes() + 2 * (MAX_E + 1) * 4 <= 227 * 1024, "shared memory budget");
+static_assert(Smem<128>::bytes() + 2 * (MAX_E + 1) * 4 <= 227 * 1024, "shared memory budget");
 
 int gemm_smem_bytes(int bn) {
   return bn == 16 ? Smem<16>::bytes() : Smem<128>::bytes();

@@ -75,6 +75,10 @@ struct GemmTask {
   int ntiles;          // non-routed: token tiles
   int units;           // non-routed: ntiles * ftiles * ksplit
   int ws_tile_base;    // first split-K workspace tile / counter of this task
+  int streamk;         // 1: static stream-K partition of ntiles*ftiles*kb_total k-blocks
+                       //    over sk_grid CTAs (non-routed, bf16, sole task of its launch)
+  int sk_grid;
+  long long sk_total;
 };
 
 struct GemmParams {
@@ -100,6 +104,8 @@ struct GemmParams {
   int* err;                    // sticky device error word
   long long timeout;           // SM cycles per bounded wait
   int stall_after;             // test hook (0 = off)
+  long long* trace;            // optional timestamp trace (this launch's region)
+  int trace_n;                 // entries per (CTA, role)
 };
 
 // Launchers (return cudaError_t of the launch).
