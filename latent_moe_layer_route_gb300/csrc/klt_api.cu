@@ -83,7 +83,6 @@ struct klt_handle {
   int *split_cnt, *sched, *err;
   int cap, max_hist_blocks;
   // descriptors per BN variant (token-side maps depend on the box height)
-  CUtensorMap tm_w13, tm_w2, tm_ws13, tm_ws2, tm_wup;
   CUtensorMap tm_zqp[kNumBN], tm_aq[kNumBN], tm_n[kNumBN], tm_as[kNumBN];
   void* allocs[48];
   int nallocs;
@@ -243,12 +242,6 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
 
   const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  // tile-major weight maps: [tiles * 128 rows, 128 bytes]
-  ok &= encode_2d(&h->tm_w13, h->w13, U8, 1, E * 2 * I * (L / 128), 128, 128);
-  ok &= encode_2d(&h->tm_w2, h->w2, U8, 1, E * L * (I / 128), 128, 128);
-  ok &= encode_2d(&h->tm_ws13, h->ws13, BF, 2, 2 * Is * (H / 64), 64, 128);
-  ok &= encode_2d(&h->tm_ws2, h->ws2, BF, 2, H * (Is / 64), 64, 128);
-  ok &= encode_2d(&h->tm_wup, h->w_up, BF, 2, H * (L / 64), 64, 128);
   for (int b = 0; b < kNumBN; ++b) {
     ok &= encode_2d(&h->tm_zqp[b], h->zq_perm, U8, 1, cap, L, kBN[b]);
     ok &= encode_2d(&h->tm_aq[b], h->aq, U8, 1, cap, I, kBN[b]);
@@ -397,8 +390,7 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
     R.a_rb_up = I / 128;
     R.a_rb_expert = 2 * I / 128;
     R.a_kb[0] = R.a_kb[1] = L / 128;
-    R.tmA[0] = h->tm_w13;
-    R.tmA[1] = h->tm_w13;
+    R.a_ptr[0] = R.a_ptr[1] = h->w13;
     R.tmB[0] = h->tm_zqp[bi];
     R.tmB[1] = h->tm_zqp[bi];
     GemmTask& S = g1.task[1];
@@ -413,8 +405,7 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
     plan_split(S, ntiles, ntiles * S.ftiles * std::max(1, S.kb_total / 8), BN);
     if (!encode_2d(&S.tmB[0], x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, H, BN))
       return KLT_ERR_CUDA;
-    S.tmA[0] = h->tm_ws13;
-    S.tmA[1] = h->tm_ws13;
+    S.a_ptr[0] = S.a_ptr[1] = reinterpret_cast<const uint8_t*>(h->ws13);
     S.tmB[1] = S.tmB[0];
     KLT_LAUNCH(launch_gemm(g1, BN, grid, s, pdl));
   }
@@ -434,8 +425,7 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
     R.kb_per_split = R.kb_total;
     R.a_rb_expert = L / 128;
     R.a_kb[0] = R.a_kb[1] = I / 128;
-    R.tmA[0] = h->tm_w2;
-    R.tmA[1] = h->tm_w2;
+    R.a_ptr[0] = R.a_ptr[1] = h->w2;
     R.tmB[0] = h->tm_aq[bi];
     R.tmB[1] = h->tm_aq[bi];
     KLT_LAUNCH(launch_gemm(g2, BN, grid, s, pdl));
@@ -471,13 +461,14 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
     O.ntiles = ntiles;
     O.units = ntiles * O.ftiles;
     if (O.units < 4 * grid) {
-      // static stream-K: every CTA streams the same number of k-blocks
+      // static stream-K: every CTA streams the same number of k-blocks (no more CTAs than
+      // k-blocks, so every CTA's range is non-empty)
       O.streamk = 1;
-      O.sk_grid = grid;
       O.sk_total = static_cast<long long>(O.units) * O.kb_total;
+      O.sk_grid = static_cast<int>(std::min<long long>(grid, O.sk_total));
     }
-    O.tmA[0] = h->tm_wup;
-    O.tmA[1] = h->tm_ws2;
+    O.a_ptr[0] = reinterpret_cast<const uint8_t*>(h->w_up);
+    O.a_ptr[1] = reinterpret_cast<const uint8_t*>(h->ws2);
     O.tmB[0] = h->tm_n[bi];
     O.tmB[1] = h->tm_as[bi];
     KLT_LAUNCH(launch_gemm(g3, BN, grid, s, pdl));

@@ -84,6 +84,16 @@ KLT_DEV void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "l"(policy)
       : "memory");
 }
+// 1-D bulk copy of `bytes` contiguous bytes (16-byte aligned, multiple of 16) into shared
+// memory, completing the transaction count on `bar`.
+KLT_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                       uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
 KLT_DEV uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

@@ -242,8 +242,10 @@ __device__ void run_producer(const GemmParams& p, Smem<BN>& sm, const int* s_til
   long long sk_x = 0, sk_end = 0;
   int u = 0;
   if (streamk) {
-    sk_x = sk_begin(p.task[0].sk_total, p.task[0].sk_grid, blockIdx.x);
-    sk_end = sk_begin(p.task[0].sk_total, p.task[0].sk_grid, blockIdx.x + 1);
+    if (static_cast<int>(blockIdx.x) < p.task[0].sk_grid) {
+      sk_x = sk_begin(p.task[0].sk_total, p.task[0].sk_grid, blockIdx.x);
+      sk_end = sk_begin(p.task[0].sk_total, p.task[0].sk_grid, blockIdx.x + 1);
+    }
   } else {
     u = atomicAdd(p.sched, 1);
   }
@@ -280,12 +282,16 @@ __device__ void run_producer(const GemmParams& p, Smem<BN>& sm, const int* s_til
         const int kbs = kb + sub;
         const int m = kbs < T.kb_split0 ? 0 : 1;
         const int kk = m ? kbs - T.kb_split0 : kbs;
-        // weights are stored tile-major: one contiguous 16 KB block per (row block, kb)
-        tma_load_2d(st + sub * C::A_BYTES, &T.tmA[m], &sm.full[stage], 0,
-                    (info.arb * T.a_kb[m] + kk) * 128, pol_w);
+        // weights are stored pre-swizzled tile-major: one contiguous 16 KB image per
+        // (row block, kb), copied as is
+        bulk_load(st + sub * C::A_BYTES,
+                  T.a_ptr[m] + (static_cast<size_t>(info.arb) * T.a_kb[m] + kk) * C::A_BYTES,
+                  C::A_BYTES, &sm.full[stage], pol_w);
         if (pair)
-          tma_load_2d(st + C::A_BYTES, &T.tmA[m], &sm.full[stage], 0,
-                      ((info.arb + T.a_rb_up) * T.a_kb[m] + kk) * 128, pol_w);
+          bulk_load(st + C::A_BYTES,
+                    T.a_ptr[m] + (static_cast<size_t>(info.arb + T.a_rb_up) * T.a_kb[m] + kk) *
+                                     C::A_BYTES,
+                    C::A_BYTES, &sm.full[stage], pol_w);
         tma_load_2d(st + 2 * C::A_BYTES + sub * C::B_BYTES, &T.tmB[m], &sm.full[stage],
                     kk * elems_per_kb, info.row0, pol_t);
       }
@@ -612,8 +618,6 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
   }
   if (warp == 0 && lane == 0) {
     for (int t = 0; t < p.ntasks; ++t) {
-      tma_prefetch_desc(&p.task[t].tmA[0]);
-      tma_prefetch_desc(&p.task[t].tmA[1]);
       tma_prefetch_desc(&p.task[t].tmB[0]);
       tma_prefetch_desc(&p.task[t].tmB[1]);
     }

@@ -60,8 +60,8 @@ enum TaskKind : int {
 };
 
 struct GemmTask {
-  CUtensorMap tmA[2];  // weight operand maps (128-row boxes); [1] used past kb_split0
-  CUtensorMap tmB[2];  // token operand maps (BN-row boxes)
+  CUtensorMap tmB[2];  // token operand maps (BN-row boxes); [1] used past kb_split0
+  const uint8_t* a_ptr[2];  // weight operands, pre-swizzled tile-major (16 KB per tile)
   int kind;
   int routed;          // units come from the device tile list (tile_off/off)
   int ftiles;          // 128-row output tiles (gate/up pairs for L1 kinds)
@@ -71,7 +71,7 @@ struct GemmTask {
   int kb_per_split;
   int a_rb_up;         // 128-row blocks from a gate tile to its up tile (pair kinds)
   int a_rb_expert;     // routed: 128-row blocks per expert
-  int a_kb[2];         // k-blocks per 128-row block in tmA[0], tmA[1] (tile-major weights)
+  int a_kb[2];         // k-blocks per 128-row block of a_ptr[0], a_ptr[1]
   int ntiles;          // non-routed: token tiles
   int units;           // non-routed: ntiles * ftiles * ksplit
   int ws_tile_base;    // first split-K workspace tile / counter of this task
@@ -115,7 +115,9 @@ cudaError_t launch_perm_scatter(const PermParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_perm_gather(const PermParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_norm(const NormParams& p, cudaStream_t s, bool pdl);
 // Row-major [rows, row_bytes] -> 128-row x 128-byte tiles, tile (rb, kb) at
-// ((rb * row_bytes/128) + kb) * 16384 bytes (rows % 128 == 0, row_bytes % 128 == 0).
+// ((rb * row_bytes/128) + kb) * 16384 bytes (rows % 128 == 0, row_bytes % 128 == 0), each
+// tile stored in the 128-byte-swizzled K-major image the tensor core reads from shared
+// memory: 16-byte chunk c of row r at r * 128 + (c ^ (r % 8)) * 16.
 cudaError_t launch_tile_relayout(const void* src, void* dst, long long rows, long long row_bytes,
                                  cudaStream_t s);
 // bn in {16, 128}; grid = persistent CTAs.

@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(256)
   if (q >= rows * c16) return;
   const long long row = q / c16, col = q - row * c16;
   const long long rb = row >> 7, r = row & 127, kb = col >> 3, ch = col & 7;
-  const long long dst_off = (((rb * (row_bytes / 128)) + kb) * 128 + r) * 128 + ch * 16;
+  const long long dst_off = (((rb * (row_bytes / 128)) + kb) * 128 + r) * 128 + ((ch ^ (r & 7)) * 16);
   *reinterpret_cast<uint4*>(dst + dst_off) =
       *reinterpret_cast<const uint4*>(src + row * row_bytes + col * 16);
 }
