@@ -167,6 +167,29 @@ KLT_DEV void mma_fp8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t i
       : "memory");
 }
 
+// The four MMAs of one 128-byte K block (K = 4 x 32 bytes) into one accumulator, issued
+// from a single asm block: the first accumulates iff `accumulate`, the rest always do.
+// `kind` is the tcgen05.mma kind string (kind::f16 or kind::f8f6f4).
+#define KLT_MMA4(KIND)                                                                    \
+  asm volatile(                                                                           \
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 q, 0, 0;\n\t"        \
+      "tcgen05.mma.cta_group::1." KIND " [%0], %1, %2, %3, p;\n\t"                         \
+      "tcgen05.mma.cta_group::1." KIND " [%0], %5, %6, %3, q;\n\t"                         \
+      "tcgen05.mma.cta_group::1." KIND " [%0], %7, %8, %3, q;\n\t"                         \
+      "tcgen05.mma.cta_group::1." KIND " [%0], %9, %10, %3, q;\n\t}" ::"r"(d),             \
+      "l"(da), "l"(db), "r"(idesc), "r"(accumulate), "l"(da + 2), "l"(db + 2), "l"(da + 4),  \
+      "l"(db + 4), "l"(da + 6), "l"(db + 6)                                                \
+      : "memory")
+KLT_DEV void mma4_bf16(uint32_t d, uint64_t da, uint64_t db, uint32_t idesc,
+                       uint32_t accumulate) {
+  KLT_MMA4("kind::f16");
+}
+KLT_DEV void mma4_fp8(uint32_t d, uint64_t da, uint64_t db, uint32_t idesc,
+                      uint32_t accumulate) {
+  KLT_MMA4("kind::f8f6f4");
+}
+#undef KLT_MMA4
+
 // Load 16 consecutive fp32 columns of this thread's TMEM lane and wait for them (the
 // wait is in the same asm statement so no use of the registers can move above it).
 KLT_DEV void tmem_ld16(uint32_t taddr, float* v) {

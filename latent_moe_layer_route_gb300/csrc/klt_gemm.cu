@@ -47,7 +47,8 @@ struct Cfg {
   static constexpr int US = 8;
   static constexpr int COLS = BN / (EPI_WARPS / 4);
   // per-unit scale staging: token group scales [MAX_KB][BN] + weight scales [MAX_KB][2]
-  static constexpr int SC_FLOATS = MAX_KB * BN + 2 * MAX_KB;
+  // plus, for the combine, the token index and routing weight of each column [2][BN]
+  static constexpr int SC_FLOATS = MAX_KB * BN + 2 * MAX_KB + 2 * BN;
   static_assert(COLS % 16 == 0, "epilogue works in 16-column chunks");
   static_assert(NACC >= 2, "need two accumulator slots");
 };
@@ -356,16 +357,13 @@ __device__ void run_mma(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_base) {
         const uint64_t da = sdesc_sw128(sa + sub * C::A_BYTES);
         const uint64_t du = sdesc_sw128(sa + C::A_BYTES);
         const uint64_t db = sdesc_sw128(sa + 2 * C::A_BYTES + sub * C::B_BYTES);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint32_t accum = promote ? (kk > 0) : (kb + sub > info.kb0 || kk > 0);
-          if (promote) {
-            mma_fp8(d, da + 2 * kk, db + 2 * kk, idesc, accum);
-            if (pair) mma_fp8(d + BN, du + 2 * kk, db + 2 * kk, idesc, accum);
-          } else {
-            mma_bf16(d, da + 2 * kk, db + 2 * kk, idesc, accum);
-            if (pair) mma_bf16(d + BN, du + 2 * kk, db + 2 * kk, idesc, accum);
-          }
+        const uint32_t accum = promote ? 0u : static_cast<uint32_t>(kb + sub > info.kb0);
+        if (promote) {
+          mma4_fp8(d, da, db, idesc, accum);
+          if (pair) mma4_fp8(d + BN, du, db, idesc, accum);
+        } else {
+          mma4_bf16(d, da, db, idesc, accum);
+          if (pair) mma4_bf16(d + BN, du, db, idesc, accum);
         }
         if (promote) {
           tc_commit(&sm.tfull[acc]);
@@ -417,13 +415,13 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
     float g[COLS], u[COLS];
 #pragma unroll
     for (int j = 0; j < COLS; ++j) { g[j] = 0.f; u[j] = 0.f; }
+    float* sb = sm.sc + sc_buf * C::SC_FLOATS;
 
     if (is_promote(kind)) {
       // Stage this unit's scales in shared memory once: token group scales [kb][column]
       // and the weight block scale(s) per kb.  Double-buffered by unit parity; the barrier
       // also guarantees every epilogue thread has finished the previous unit.
       const float* tok_scale = kind == TASK_ROUTED_L1 ? p.zsT : p.asT;
-      float* sb = sm.sc + sc_buf * C::SC_FLOATS;
       sc_buf ^= 1;
       const int nkb = info.kb1 - info.kb0;
       const int etid = threadIdx.x - 64;
@@ -446,6 +444,14 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
         }
         sb[MAX_KB * BN + 2 * kbi] = a;
         sb[MAX_KB * BN + 2 * kbi + 1] = b;
+      }
+      if (kind == TASK_ROUTED_L2) {  // combine targets of each column
+        for (int j = etid; j < BN; j += C::EPI_THREADS) {
+          const int pp = info.row0 + j;
+          sb[MAX_KB * BN + 2 * MAX_KB + j] =
+              __int_as_float(j < info.rows ? __ldg(p.gidx + pp) : 0);
+          sb[MAX_KB * BN + 2 * MAX_KB + BN + j] = j < info.rows ? __ldg(p.wperm + pp) : 0.f;
+        }
       }
       named_bar_sync(1, C::EPI_THREADS);
       for (int kbi = 0; kbi < nkb; ++kbi) {
@@ -556,9 +562,8 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
 #pragma unroll
       for (int j = 0; j < COLS; ++j) {
         if (c0 + j < info.rows) {
-          const int pp = info.row0 + c0 + j;
-          const int tok = __ldg(p.gidx + pp);
-          const float wv = __ldg(p.wperm + pp);
+          const int tok = __float_as_int(sb[MAX_KB * BN + 2 * MAX_KB + c0 + j]);
+          const float wv = sb[MAX_KB * BN + 2 * MAX_KB + BN + c0 + j];
           atomicAdd(p.r + static_cast<size_t>(tok) * p.L + col, wv * g[j]);
         }
       }
