@@ -44,7 +44,8 @@ enum klt_status_code {
   KLT_ERR_ALIGN = 3,           /* a pointer is not 16-byte aligned                     */
   KLT_ERR_CUDA = 4,            /* a CUDA runtime call or launch failed                 */
   KLT_ERR_DEVICE_TIMEOUT = 5,  /* a bounded on-device wait ran out (sticky)            */
-  KLT_ERR_OOM = 6              /* device allocation failed in klt_create               */
+  KLT_ERR_OOM = 6,             /* device allocation failed in klt_create               */
+  KLT_ERR_TOO_LARGE = 7        /* request exceeds the fixed scratch of klt_route_noalloc */
 };
 
 /* Routed expert weight formats. */
@@ -183,6 +184,27 @@ const char* klt_strerror(int code);
 
 /* Number of kernels one klt_forward launches for the given M and handle (0 for M == 0). */
 int klt_launch_count(const klt_handle* h, int32_t M);
+
+/* Largest M * topk klt_route_noalloc accepts (its fixed scratch size, about 320 KB). */
+#define KLT_NOALLOC_MAX_PAIRS 65536
+
+/* Routing and expert permutation without a handle and without any device allocation.
+ * The pages describe no such entry point; it exists for callers that cannot allocate
+ * device memory where they route (inside another framework's memory pool, serving loops
+ * that fix every allocation at start-up, runtimes without allocator access).
+ * Computes the same ids, weights, cnt, off, gidx, slot and pos as klt_forward's routing
+ * outputs (same layouts as klt_routing) for `logits` f32 [M, E], all pointers device
+ * memory, caller owned, 16-byte aligned, none NULL.  Internal buffers live in one
+ * fixed-size device array (KLT_NOALLOC_MAX_PAIRS pairs) that every GPU loading the library
+ * holds until exit; calls share it, so calls whose kernels overlap on the GPU race; order
+ * them on one stream.  The first call on a device resolves the array's device address;
+ * make that first call before any stream capture.  Asynchronous on `stream`.
+ * Errors: KLT_ERR_INVALID_ARG (M < 0, E or topk < 1, NULL pointer), KLT_ERR_UNSUPPORTED
+ * (E > 256, topk > E, topk > 32), KLT_ERR_TOO_LARGE (M * topk > KLT_NOALLOC_MAX_PAIRS),
+ * KLT_ERR_ALIGN, KLT_ERR_CUDA.  M == 0 launches nothing. */
+int klt_route_noalloc(const float* logits, int32_t M, int32_t E, int32_t topk, int32_t* ids,
+                      float* weights, int32_t* cnt, int32_t* off, int32_t* gidx,
+                      int32_t* slot, int32_t* pos, void* stream);
 
 #ifdef __cplusplus
 }

@@ -19,12 +19,14 @@ KLT_ERR_ALIGN = 3
 KLT_ERR_CUDA = 4
 KLT_ERR_DEVICE_TIMEOUT = 5
 KLT_ERR_OOM = 6
+KLT_ERR_TOO_LARGE = 7
+KLT_NOALLOC_MAX_PAIRS = 65536
 KLT_FMT_FP8_B128 = 0
 KLT_FMT_NVFP4 = 1
 KLT_FLAG_NO_PDL = 1
 
 EXPORTS = ("klt_create", "klt_forward", "klt_status", "klt_destroy", "klt_strerror",
-           "klt_launch_count")
+           "klt_launch_count", "klt_route_noalloc")
 
 
 class KltDims(ctypes.Structure):
@@ -87,6 +89,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.klt_strerror.restype = ctypes.c_char_p
     lib.klt_launch_count.argtypes = [ctypes.c_void_p, ctypes.c_int32]
     lib.klt_launch_count.restype = ctypes.c_int
+    lib.klt_route_noalloc.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                      ctypes.c_int32] + [ctypes.c_void_p] * 8
+    lib.klt_route_noalloc.restype = ctypes.c_int
     _LIB = lib
     return lib
 
@@ -144,6 +149,16 @@ def klt_destroy(h) -> int:
 
 def klt_launch_count(h, M: int) -> int:
     return load_library().klt_launch_count(h, M)
+
+
+def klt_route_noalloc(logits, topk: int, ids, weights, cnt, off, gidx, slot, pos,
+                      stream: Optional[int] = None) -> int:
+    """Routing + permutation with no device allocation (fixed internal scratch); tensors
+    are caller-owned CUDA tensors with the klt_routing layouts."""
+    M, E = logits.shape
+    return load_library().klt_route_noalloc(
+        _ptr(logits), M, E, topk, _ptr(ids), _ptr(weights), _ptr(cnt), _ptr(off), _ptr(gidx),
+        _ptr(slot), _ptr(pos), stream)
 
 
 class LatentMoETail:

@@ -147,6 +147,7 @@ const char* klt_strerror(int code) {
     case KLT_ERR_CUDA: return "CUDA call failed";
     case KLT_ERR_DEVICE_TIMEOUT: return "bounded device wait expired";
     case KLT_ERR_OOM: return "device allocation failed";
+    case KLT_ERR_TOO_LARGE: return "request exceeds the fixed scratch capacity";
     default: return "unknown status";
   }
 }
