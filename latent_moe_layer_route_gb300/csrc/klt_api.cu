@@ -79,7 +79,7 @@ struct klt_handle {
   int32_t *ids, *cnt, *off, *tile_off, *gidx, *slot, *pos, *hist;
   float *wts, *wperm, *zs, *zsT, *asT, *r, *ws;
   uint8_t *zq, *zq_perm, *aq;
-  __nv_bfloat16 *n, *a_s;
+  __nv_bfloat16 *n, *a_s, *zqb_perm, *aqb;
   int *split_cnt, *sched, *err;
   int cap, max_hist_blocks;
   // descriptors per BN variant (token-side maps depend on the box height)
@@ -158,7 +158,9 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
   if (!d || !w) return KLT_ERR_INVALID_ARG;
   int rc = check_dims(d);
   if (rc) return rc;
-  if (d->routed_fmt == KLT_FMT_NVFP4) return KLT_ERR_UNSUPPORTED;  // not in this build yet
+  const bool nvfp4 = d->routed_fmt == KLT_FMT_NVFP4;
+  if (nvfp4 && (!w->w13_global || !w->w2_global)) return KLT_ERR_INVALID_ARG;
+  if (nvfp4 && (!aligned16(w->w13_global) || !aligned16(w->w2_global))) return KLT_ERR_ALIGN;
   const void* ptrs[] = {w->w13, w->w13_scale, w->w2, w->w2_scale, w->ws13, w->ws2,
                         w->w_up, w->gamma};
   for (const void* p : ptrs)
@@ -194,9 +196,11 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
       return KLT_ERR_OOM;                                                       \
     }                                                                           \
   } while (0)
-  KLT_ALLOC(h->w13, E * 2 * I * L);
+  // NVFP4 weights are held as their exact bf16 values (2 bytes per weight)
+  const int64_t wbytes = nvfp4 ? 2 : 1;
+  KLT_ALLOC(h->w13, E * 2 * I * L * wbytes);
   KLT_ALLOC(h->w13_s, E * (2 * I / 128) * (L / 128) * 4);
-  KLT_ALLOC(h->w2, E * L * I);
+  KLT_ALLOC(h->w2, E * L * I * wbytes);
   KLT_ALLOC(h->w2_s, E * (L / 128) * (I / 128) * 4);
   KLT_ALLOC(h->ws13, 2 * Is * H * 2);
   KLT_ALLOC(h->ws2, H * Is * 2);
@@ -214,7 +218,11 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
   KLT_ALLOC(h->tile_off, (E + 1) * 4);
   KLT_ALLOC(h->zq, Mx * L);
   KLT_ALLOC(h->zs, Mx * (L / 128) * 4);
-  KLT_ALLOC(h->zq_perm, cap * L);
+  KLT_ALLOC(h->zq_perm, nvfp4 ? 16 : cap * L);
+  if (nvfp4) {
+    KLT_ALLOC(h->zqb_perm, cap * L * 2);
+    KLT_ALLOC(h->aqb, cap * I * 2);
+  }
   KLT_ALLOC(h->zsT, (L / 128) * cap * 4);
   KLT_ALLOC(h->aq, cap * I);
   KLT_ALLOC(h->asT, (I / 128) * cap * 4);
@@ -230,22 +238,44 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
   // Weights are copied tile-major (one contiguous 16 KB block per 128 rows x 128 bytes of
   // K), so every TMA box of a weight operand is a single contiguous DRAM stream.
   bool ok = true;
-  ok &= launch_tile_relayout(w->w13, h->w13, E * 2 * I, L, 0) == cudaSuccess;
-  ok &= launch_tile_relayout(w->w2, h->w2, E * L, I, 0) == cudaSuccess;
+  if (nvfp4) {
+    // exact bf16 values e2m1 * e4m3 block scale; the fp32 matrix scale becomes the
+    // promotion scale of every 128-wide K group
+    ok &= launch_nvfp4_expand(static_cast<const uint8_t*>(w->w13),
+                              static_cast<const uint8_t*>(w->w13_scale), h->w13, E * 2 * I, L,
+                              0) == cudaSuccess;
+    ok &= launch_nvfp4_expand(static_cast<const uint8_t*>(w->w2),
+                              static_cast<const uint8_t*>(w->w2_scale), h->w2, E * L, I,
+                              0) == cudaSuccess;
+    ok &= launch_fill_expert_scale(w->w13_global, h->w13_s, static_cast<int>(E),
+                                   (2 * I / 128) * (L / 128), 0) == cudaSuccess;
+    ok &= launch_fill_expert_scale(w->w2_global, h->w2_s, static_cast<int>(E),
+                                   (L / 128) * (I / 128), 0) == cudaSuccess;
+  } else {
+    ok &= launch_tile_relayout(w->w13, h->w13, E * 2 * I, L, 0) == cudaSuccess;
+    ok &= launch_tile_relayout(w->w2, h->w2, E * L, I, 0) == cudaSuccess;
+  }
   ok &= launch_tile_relayout(w->ws13, h->ws13, 2 * Is, H * 2, 0) == cudaSuccess;
   ok &= launch_tile_relayout(w->ws2, h->ws2, H, Is * 2, 0) == cudaSuccess;
   ok &= launch_tile_relayout(w->w_up, h->w_up, H, L * 2, 0) == cudaSuccess;
-  ok &= cudaMemcpy(h->w13_s, w->w13_scale, E * (2 * I / 128) * (L / 128) * 4,
-                   cudaMemcpyDeviceToDevice) == cudaSuccess;
-  ok &= cudaMemcpy(h->w2_s, w->w2_scale, E * (L / 128) * (I / 128) * 4,
-                   cudaMemcpyDeviceToDevice) == cudaSuccess;
+  if (!nvfp4) {
+    ok &= cudaMemcpy(h->w13_s, w->w13_scale, E * (2 * I / 128) * (L / 128) * 4,
+                     cudaMemcpyDeviceToDevice) == cudaSuccess;
+    ok &= cudaMemcpy(h->w2_s, w->w2_scale, E * (L / 128) * (I / 128) * 4,
+                     cudaMemcpyDeviceToDevice) == cudaSuccess;
+  }
   ok &= cudaMemcpy(h->gamma, w->gamma, L * 2, cudaMemcpyDeviceToDevice) == cudaSuccess;
 
   const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   for (int b = 0; b < kNumBN; ++b) {
-    ok &= encode_2d(&h->tm_zqp[b], h->zq_perm, U8, 1, cap, L, kBN[b]);
-    ok &= encode_2d(&h->tm_aq[b], h->aq, U8, 1, cap, I, kBN[b]);
+    if (nvfp4) {
+      ok &= encode_2d(&h->tm_zqp[b], h->zqb_perm, BF, 2, cap, L, kBN[b]);
+      ok &= encode_2d(&h->tm_aq[b], h->aqb, BF, 2, cap, I, kBN[b]);
+    } else {
+      ok &= encode_2d(&h->tm_zqp[b], h->zq_perm, U8, 1, cap, L, kBN[b]);
+      ok &= encode_2d(&h->tm_aq[b], h->aq, U8, 1, cap, I, kBN[b]);
+    }
     ok &= encode_2d(&h->tm_n[b], h->n, BF, 2, Mx, L, kBN[b]);
     ok &= encode_2d(&h->tm_as[b], h->a_s, BF, 2, Mx, Is, kBN[b]);
   }
@@ -278,6 +308,8 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
   const int E = d.E, k = d.topk, L = d.L, I = d.I, Is = d.Is, H = d.H;
   const int bi = bn_index(M);
   const int BN = kBN[bi];
+  const bool nvfp4 = d.routed_fmt == KLT_FMT_NVFP4;
+  const int rkb = nvfp4 ? 64 : 128;  // routed K elements per k-block
   const int Mk = M * k;
   const int nblocks = (Mk + PERM_BLOCK - 1) / PERM_BLOCK;
   const long long timeout_cycles =
@@ -324,6 +356,7 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
   pp.zq = h->zq;
   pp.zs = h->zs;
   pp.zq_perm = h->zq_perm;
+  pp.zqb_perm = nvfp4 ? h->zqb_perm : nullptr;
   pp.zsT = h->zsT;
   pp.wts = h->wts;
   pp.wperm = h->wperm;
@@ -356,6 +389,7 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
   gp.w13_s = h->w13_s;
   gp.w2_s = h->w2_s;
   gp.aq = h->aq;
+  gp.aqb = nvfp4 ? h->aqb : nullptr;
   gp.asT = h->asT;
   gp.r = h->r;
   gp.a_s = h->a_s;
@@ -382,15 +416,17 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
     // Routed units first, then the shared expert in small k-splits that fill the tail.
     GemmTask& R = g1.task[0];
     R.kind = TASK_ROUTED_L1;
+    R.fp8 = !nvfp4;
+    R.kpg = nvfp4 ? 2 : 1;
     R.routed = 1;
     R.ftiles = I / 128;
-    R.kb_total = L / 128;
+    R.kb_total = L / rkb;
     R.kb_split0 = R.kb_total;
     R.ksplit = 1;
     R.kb_per_split = R.kb_total;
     R.a_rb_up = I / 128;
     R.a_rb_expert = 2 * I / 128;
-    R.a_kb[0] = R.a_kb[1] = L / 128;
+    R.a_kb[0] = R.a_kb[1] = L / rkb;
     R.a_ptr[0] = R.a_ptr[1] = h->w13;
     R.tmB[0] = h->tm_zqp[bi];
     R.tmB[1] = h->tm_zqp[bi];
@@ -418,14 +454,16 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
     g2.trace = trace ? trace + trace_launch : nullptr;
     GemmTask& R = g2.task[0];
     R.kind = TASK_ROUTED_L2;
+    R.fp8 = !nvfp4;
+    R.kpg = nvfp4 ? 2 : 1;
     R.routed = 1;
     R.ftiles = L / 128;
-    R.kb_total = I / 128;
+    R.kb_total = I / rkb;
     R.kb_split0 = R.kb_total;
     R.ksplit = 1;
     R.kb_per_split = R.kb_total;
     R.a_rb_expert = L / 128;
-    R.a_kb[0] = R.a_kb[1] = I / 128;
+    R.a_kb[0] = R.a_kb[1] = I / rkb;
     R.a_ptr[0] = R.a_ptr[1] = h->w2;
     R.tmB[0] = h->tm_aq[bi];
     R.tmB[1] = h->tm_aq[bi];

@@ -233,6 +233,19 @@ KLT_DEV void tmem_ld16x2(uint32_t ta, uint32_t tb, float* va, float* vb) {
 // ------------------------------------------------------------------ misc
 KLT_DEV float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
+// e4m3 code -> fp32 (exact).
+KLT_DEV float e4m3_to_f32(uint8_t c) {
+  const __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(c), __NV_E4M3);
+  return __half2float(__half(h));
+}
+// e2m1 code (low 4 bits) -> fp32: values 0, 0.5, 1, 1.5, 2, 3, 4, 6 and their negatives.
+KLT_DEV float e2m1_to_f32(uint32_t c) {
+  const uint32_t e = (c >> 1) & 3u, m = c & 1u;
+  const float mag = e == 0 ? 0.5f * static_cast<float>(m)
+                           : __int_as_float(static_cast<int>((126u + e) << 23 | (m << 22)));
+  return (c & 8u) ? -mag : mag;
+}
+
 // fp32 -> e4m3 code, round to nearest even, saturating to +-448.
 KLT_DEV uint8_t f32_to_e4m3(float v) {
   return static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));

@@ -130,9 +130,6 @@ __device__ __forceinline__ void trace_mark(const GemmParams& p, int role, int i)
 __device__ __forceinline__ bool is_pair(int kind) {
   return kind == TASK_SHARED_L1 || kind == TASK_ROUTED_L1;
 }
-__device__ __forceinline__ bool is_promote(int kind) {
-  return kind == TASK_ROUTED_L1 || kind == TASK_ROUTED_L2;
-}
 
 template <int BN>
 __device__ UnitInfo decode_unit(const GemmParams& p, const int* s_tile_off, const int* s_off,
@@ -266,7 +263,7 @@ __device__ void run_producer(const GemmParams& p, Smem<BN>& sm, const int* s_til
     if (info.task < 0) break;
     const GemmTask& T = p.task[info.task];
     const bool pair = is_pair(T.kind);
-    const int elems_per_kb = is_promote(T.kind) ? 128 : 64;
+    const int elems_per_kb = T.fp8 ? 128 : 64;
     const int step = (pair || !C::DUAL) ? 1 : 2;
     for (int kb = info.kb0; kb < info.kb1; kb += step) {
       if (p.stall_after > 0 && issued >= p.stall_after) { stalled = true; break; }
@@ -327,10 +324,11 @@ __device__ void run_mma(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_base) {
     mbar_arrive(&sm.uempty[us]);
     if (++us == C::US) { us = 0; uphase ^= 1; }
     if (info.task < 0) break;
-    const int kind = p.task[info.task].kind;
-    const bool pair = is_pair(kind);
-    const bool promote = is_promote(kind);
-    const uint32_t idesc = promote ? idesc_fp8 : idesc_bf16;
+    const GemmTask& T = p.task[info.task];
+    const bool pair = is_pair(T.kind);
+    const bool promote = T.kpg > 0;
+    const bool fp8 = T.fp8 != 0;
+    const uint32_t idesc = fp8 ? idesc_fp8 : idesc_bf16;
     const int step = (pair || !C::DUAL) ? 1 : 2;
     if (!promote) {
       if (!mbar_wait(&sm.tempty[acc], aphase ^ 1, sm.abort_flag, p.err, p.timeout)) break;
@@ -346,7 +344,9 @@ __device__ void run_mma(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_base) {
       const int nsub = min(step, info.kb1 - kb);
       const uint32_t sa = smem_u32(sm.stages + stage * C::STAGE_BYTES);
       for (int sub = 0; sub < nsub; ++sub) {
-        if (promote) {
+        // position of this k-block in its promotion group
+        const int gpos = promote ? (kb + sub - info.kb0) % T.kpg : 0;
+        if (promote && gpos == 0) {
           if (!mbar_wait(&sm.tempty[acc], aphase ^ 1, sm.abort_flag, p.err, p.timeout)) {
             ok = false;
             break;
@@ -357,15 +357,16 @@ __device__ void run_mma(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_base) {
         const uint64_t da = sdesc_sw128(sa + sub * C::A_BYTES);
         const uint64_t du = sdesc_sw128(sa + C::A_BYTES);
         const uint64_t db = sdesc_sw128(sa + 2 * C::A_BYTES + sub * C::B_BYTES);
-        const uint32_t accum = promote ? 0u : static_cast<uint32_t>(kb + sub > info.kb0);
-        if (promote) {
+        const uint32_t accum = promote ? static_cast<uint32_t>(gpos > 0)
+                                       : static_cast<uint32_t>(kb + sub > info.kb0);
+        if (fp8) {
           mma4_fp8(d, da, db, idesc, accum);
           if (pair) mma4_fp8(d + BN, du, db, idesc, accum);
         } else {
           mma4_bf16(d, da, db, idesc, accum);
           if (pair) mma4_bf16(d + BN, du, db, idesc, accum);
         }
-        if (promote) {
+        if (promote && gpos == T.kpg - 1) {
           tc_commit(&sm.tfull[acc]);
           if (++acc == C::NACC) { acc = 0; aphase ^= 1; }
         }
@@ -417,23 +418,23 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
     for (int j = 0; j < COLS; ++j) { g[j] = 0.f; u[j] = 0.f; }
     float* sb = sm.sc + sc_buf * C::SC_FLOATS;
 
-    if (is_promote(kind)) {
-      // Stage this unit's scales in shared memory once: token group scales [kb][column]
-      // and the weight block scale(s) per kb.  Double-buffered by unit parity; the barrier
-      // also guarantees every epilogue thread has finished the previous unit.
+    if (T.kpg > 0) {
+      // Stage this unit's scales in shared memory once: token group scales [group][column]
+      // and the weight block scale(s) per 128-wide K group.  Double-buffered by unit parity;
+      // the barrier also guarantees every epilogue thread has finished the previous unit.
       const float* tok_scale = kind == TASK_ROUTED_L1 ? p.zsT : p.asT;
       sc_buf ^= 1;
-      const int nkb = info.kb1 - info.kb0;
+      const int nkb = (info.kb1 - info.kb0) / T.kpg;  // promotion groups of this unit
+      const int g0 = info.kb0 / T.kpg;
       const int etid = threadIdx.x - 64;
       for (int i = etid; i < nkb * BN; i += C::EPI_THREADS) {
         const int kbi = i / BN, j = i - kbi * BN;
         sb[i] = j < info.rows
-                    ? __ldg(tok_scale + static_cast<size_t>(info.kb0 + kbi) * p.cap +
-                            info.row0 + j)
+                    ? __ldg(tok_scale + static_cast<size_t>(g0 + kbi) * p.cap + info.row0 + j)
                     : 0.f;
       }
       for (int kbi = etid; kbi < nkb; kbi += C::EPI_THREADS) {
-        const int kb = info.kb0 + kbi;
+        const int kb = g0 + kbi;
         float a, b = 0.f;
         if (kind == TASK_ROUTED_L1) {
           const size_t rb = static_cast<size_t>(info.e) * (2 * G_I);
@@ -587,7 +588,11 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
         const float s = amax == 0.f ? 1.0f : amax / 448.0f;
         if (c0 + j < info.rows) {
           const size_t pp = static_cast<size_t>(info.row0 + c0 + j);
-          dst[pp * p.I] = f32_to_e4m3(g[j] / s);
+          const uint8_t code = f32_to_e4m3(g[j] / s);
+          dst[pp * p.I] = code;
+          if (p.aqb != nullptr)
+            p.aqb[pp * p.I + static_cast<size_t>(info.ftile) * 128 + row] =
+                __float2bfloat16_rn(e4m3_to_f32(code));
           if (quad == 0 && lane == 0) p.asT[static_cast<size_t>(info.ftile) * p.cap + pp] = s;
         }
       }

@@ -35,6 +35,7 @@ struct PermParams {
   const uint8_t* zq;   // [M, L]
   const float* zs;     // [M, L/128]
   uint8_t* zq_perm;    // [cap, L]
+  __nv_bfloat16* zqb_perm;  // [cap, L] exact bf16 images of the codes (bf16-operand layers)
   float* zsT;          // [L/128, cap]
   const float* wts;    // [M*k] routing weights by pair i
   float* wperm;        // [cap] routing weight of pair p
@@ -63,6 +64,9 @@ struct GemmTask {
   CUtensorMap tmB[2];  // token operand maps (BN-row boxes); [1] used past kb_split0
   const uint8_t* a_ptr[2];  // weight operands, pre-swizzled tile-major (16 KB per tile)
   int kind;
+  int fp8;             // operands e4m3 (kind::f8f6f4, 128 elements per k-block) or bf16
+                       // (kind::f16, 64 elements per k-block)
+  int kpg;             // k-blocks per promotion group (0: accumulate the unit in TMEM)
   int routed;          // units come from the device tile list (tile_off/off)
   int ftiles;          // 128-row output tiles (gate/up pairs for L1 kinds)
   int kb_total;        // k-blocks of 128 bytes per row
@@ -94,6 +98,7 @@ struct GemmParams {
   const float* w13_s;          // [E, 2I/128, L/128]
   const float* w2_s;           // [E, L/128, I/128]
   uint8_t* aq;                 // [cap, I]
+  __nv_bfloat16* aqb;          // [cap, I] exact bf16 images of aq (bf16-operand layers) or null
   float* asT;                  // [I/128, cap]
   float* r;                    // [M, L]
   __nv_bfloat16* a_s;          // [max_tokens, Is]
@@ -118,6 +123,14 @@ cudaError_t launch_norm(const NormParams& p, cudaStream_t s, bool pdl);
 // ((rb * row_bytes/128) + kb) * 16384 bytes (rows % 128 == 0, row_bytes % 128 == 0), each
 // tile stored in the 128-byte-swizzled K-major image the tensor core reads from shared
 // memory: 16-byte chunk c of row r at r * 128 + (c ^ (r % 8)) * 16.
+// NVFP4 [rows, K/2] packed e2m1 + e4m3 scales [rows, K/16] -> exact bf16 values
+// e2m1 * scale (the per-matrix fp32 scale is applied later) in the same swizzled tile-major
+// image as launch_tile_relayout for a bf16 matrix [rows, K].
+cudaError_t launch_nvfp4_expand(const uint8_t* packed, const uint8_t* sb, void* dst,
+                                long long rows, long long K, cudaStream_t s);
+// dst[e * per + i] = g[e] for i < per (per-128-block promotion scales of NVFP4 layers).
+cudaError_t launch_fill_expert_scale(const float* g, float* dst, int E, long long per,
+                                     cudaStream_t s);
 cudaError_t launch_tile_relayout(const void* src, void* dst, long long rows, long long row_bytes,
                                  cudaStream_t s);
 // bn in {16, 128}; grid = persistent CTAs.

@@ -218,8 +218,23 @@ __global__ void __launch_bounds__(256) perm_gather_kernel(const PermParams p) {
     const int pp = static_cast<int>(c / row16);
     const int ch = static_cast<int>(c - static_cast<long long>(pp) * row16);
     const int t = __ldg(p.gidx + pp);
-    reinterpret_cast<uint4*>(p.zq_perm + static_cast<size_t>(pp) * p.L)[ch] =
-        reinterpret_cast<const uint4*>(p.zq + static_cast<size_t>(t) * p.L)[ch];
+    const uint4 v = reinterpret_cast<const uint4*>(p.zq + static_cast<size_t>(t) * p.L)[ch];
+    if (p.zqb_perm == nullptr) {
+      reinterpret_cast<uint4*>(p.zq_perm + static_cast<size_t>(pp) * p.L)[ch] = v;
+    } else {  // exact bf16 image of every e4m3 code (bf16-operand layers)
+      const uint8_t* b = reinterpret_cast<const uint8_t*>(&v);
+      uint32_t o[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(e4m3_to_f32(b[2 * i]),
+                                                       e4m3_to_f32(b[2 * i + 1]));
+        o[i] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(p.zqb_perm + static_cast<size_t>(pp) * p.L +
+                                            static_cast<size_t>(ch) * 16);
+      dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+      dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
   }
   if (c < Mk * G) {
     const int pp = static_cast<int>(c / G);
@@ -276,6 +291,38 @@ __global__ void __launch_bounds__(256)
       *reinterpret_cast<const uint4*>(src + row * row_bytes + col * 16);
 }
 
+// 16-byte output chunk q = 8 bf16 values of row r at K offset k0 (8 | k0, one scale block).
+__global__ void __launch_bounds__(256)
+    nvfp4_expand_kernel(const uint8_t* packed, const uint8_t* sb, uint8_t* dst, long long rows,
+                        long long K) {
+  const long long c16 = K / 8;
+  const long long q = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
+  if (q >= rows * c16) return;
+  const long long row = q / c16, col = q - row * c16;
+  const long long k0 = col * 8;
+  const uint32_t codes = *reinterpret_cast<const uint32_t*>(packed + row * (K / 2) + k0 / 2);
+  const float scale = e4m3_to_f32(sb[row * (K / 16) + k0 / 16]);
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t byte = codes >> (8 * i);
+    const __nv_bfloat162 h = __floats2bfloat162_rn(e2m1_to_f32(byte & 0xF) * scale,
+                                                   e2m1_to_f32((byte >> 4) & 0xF) * scale);
+    o[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  const long long row_bytes = K * 2;
+  const long long rb = row >> 7, r = row & 127, kb = (k0 * 2) >> 7, ch = ((k0 * 2) & 127) >> 4;
+  const long long dst_off =
+      (((rb * (row_bytes / 128)) + kb) * 128 + r) * 128 + ((ch ^ (r & 7)) * 16);
+  *reinterpret_cast<uint4*>(dst + dst_off) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__global__ void __launch_bounds__(256)
+    fill_expert_scale_kernel(const float* g, float* dst, int E, long long per) {
+  const long long i = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
+  if (i < E * per) dst[i] = g[i / per];
+}
+
 template <typename Kern, typename Param>
 cudaError_t launch_simple(Kern k, dim3 grid, dim3 block, const Param& prm, cudaStream_t s,
                           bool pdl) {
@@ -314,6 +361,20 @@ cudaError_t launch_norm(const NormParams& p, cudaStream_t s, bool pdl) {
   return launch_simple(norm_kernel, dim3(p.M), dim3(128), p, s, pdl);
 }
 
+cudaError_t launch_nvfp4_expand(const uint8_t* packed, const uint8_t* sb, void* dst,
+                                long long rows, long long K, cudaStream_t s) {
+  const long long chunks = rows * (K / 8);
+  nvfp4_expand_kernel<<<static_cast<unsigned>((chunks + 255) / 256), 256, 0, s>>>(
+      packed, sb, static_cast<uint8_t*>(dst), rows, K);
+  return cudaGetLastError();
+}
+cudaError_t launch_fill_expert_scale(const float* g, float* dst, int E, long long per,
+                                     cudaStream_t s) {
+  const long long n = E * per;
+  fill_expert_scale_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(g, dst, E,
+                                                                                    per);
+  return cudaGetLastError();
+}
 cudaError_t launch_tile_relayout(const void* src, void* dst, long long rows, long long row_bytes,
                                  cudaStream_t s) {
   const long long chunks = rows * (row_bytes / 16);

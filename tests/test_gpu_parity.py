@@ -61,6 +61,16 @@ def test_small_shapes(M):
     run_case(configs.SMALL, M=M)
 
 
+@pytest.mark.parametrize("M", [3, 33])
+def test_small_nvfp4(M):
+    run_case(configs.SMALL.with_(routed_fmt="nvfp4", E=6, topk=2, seed=28), M=M)
+
+
+def test_small_nvfp4_wider():
+    run_case(configs.SMALL.with_(routed_fmt="nvfp4", H=384, L=512, I=256, Is=256, E=5,
+                                 topk=3, seed=29), M=45)
+
+
 def test_small_all_experts_selected():
     run_case(configs.SMALL.with_(E=4, topk=4, seed=21), M=9)
 
@@ -172,5 +182,14 @@ def test_prefill_m4096_sampled_tokens():
     cfg = configs.PREFILL_M4096
     rng = np.random.default_rng(0)
     tok = np.sort(rng.choice(cfg.M, 48, replace=False))
+    tok[0], tok[-1] = 0, cfg.M - 1
+    run_case(cfg, tokens=tok)
+
+
+@pytest.mark.slow
+def test_prefill_m8192_nvfp4_sampled_tokens():
+    cfg = configs.PREFILL_M8192_NVFP4
+    rng = np.random.default_rng(1)
+    tok = np.sort(rng.choice(cfg.M, 32, replace=False))
     tok[0], tok[-1] = 0, cfg.M - 1
     run_case(cfg, tokens=tok)
