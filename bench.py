@@ -181,6 +181,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode_m16_e64_k8_fp8")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tile-n", type=int, default=0,
+                    help="token-tile width of the GEMM stages (0 = library choice)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -218,8 +220,13 @@ def main():
     assert tail.status() == B.KLT_OK
     nl = tail.launch_count(M)
 
+    base_dbg = None
+    if args.tile_n:
+        base_dbg = B.KltDebug()
+        base_dbg.force_bn = args.tile_n
+
     def step():
-        tail.forward(act["x"], act["z"], act["logits"], out=out)
+        tail.forward(act["x"], act["z"], act["logits"], out=out, debug=base_dbg)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -260,6 +267,7 @@ def main():
     for i in range(args.steps):
         flush.zero_()
         dbg = B.KltDebug()
+        dbg.force_bn = args.tile_n
         evs[i][0].record(stream)
         for j in range(nl):
             dbg.events[j] = evs[i][j + 1].cuda_event
@@ -289,7 +297,7 @@ def main():
         xd.copy_(xh, non_blocking=True)
         zd.copy_(zh, non_blocking=True)
         ld.copy_(lh, non_blocking=True)
-        tail.forward(xd, zd, ld, out=out)
+        tail.forward(xd, zd, ld, out=out, debug=base_dbg)
         oh.copy_(out, non_blocking=True)
         e1[i].record(stream)
     torch.cuda.synchronize()

@@ -133,7 +133,9 @@ typedef struct klt_routing {
  *     set, each GEMM launch g (0..2) records globaltimer stamps (ns) per CTA c and role r
  *     (0 = weight tile copy issued, 1 = tile consumed by the MMA issuer, 2 = epilogue step
  *     done) at trace[((g * SMs + c) * 3 + r) * trace_entries + i], first trace_entries
- *     events each; unused entries are left untouched. */
+ *     events each; unused entries are left untouched;
+ *   force_bn: token-tile width of the GEMM stages for this call (16, 32, 64 or 128;
+ *     0 = chosen from M), for tuning sweeps. */
 typedef struct klt_debug {
   uint8_t* zq;
   float* zs;
@@ -147,6 +149,7 @@ typedef struct klt_debug {
   int32_t timeout_ms;
   int64_t* trace;
   int32_t trace_entries;
+  int32_t force_bn;
 } klt_debug;
 
 typedef struct klt_handle klt_handle;

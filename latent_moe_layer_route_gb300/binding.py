@@ -52,7 +52,8 @@ class KltDebug(ctypes.Structure):
                 ("as_", ctypes.c_void_p), ("r", ctypes.c_void_p), ("n", ctypes.c_void_p),
                 ("a_s", ctypes.c_void_p), ("events", ctypes.c_void_p * 8),
                 ("stall_after_kblocks", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
-                ("trace", ctypes.c_void_p), ("trace_entries", ctypes.c_int32)]
+                ("trace", ctypes.c_void_p), ("trace_entries", ctypes.c_int32),
+                ("force_bn", ctypes.c_int32)]
 
 
 _LIB: Optional[ctypes.CDLL] = None

@@ -59,8 +59,8 @@ bool encode_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esi
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-constexpr int kNumBN = 2;
-constexpr int kBN[kNumBN] = {16, 128};
+constexpr int kNumBN = 4;
+constexpr int kBN[kNumBN] = {16, 32, 64, 128};
 constexpr int kMaxSplitUnits = 3 * 160;  // split-K tiles*splits bound per task
 constexpr int kMaxCounters = 8192;       // arrival counters per split task
 
@@ -115,7 +115,13 @@ int check_dims(const klt_dims* d) {
   return KLT_OK;
 }
 
-int bn_index(int M) { return M <= 32 ? 0 : 1; }
+// Token-tile width: the smallest tile that holds a decode batch, 64 beyond that (the
+// 128-wide tile is kept for explicit selection).
+int bn_index(int M, int force_bn) {
+  for (int i = 0; i < kNumBN; ++i)
+    if (force_bn == kBN[i]) return i;
+  return M <= 16 ? 0 : (M <= 32 ? 1 : 2);
+}
 
 // k splits for a non-routed task so that a launch has enough units to fill the GPU,
 // keeping split-K partial traffic small next to the weight bytes.
@@ -306,7 +312,7 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
   const bool pdl = !(h->flags & KLT_FLAG_NO_PDL);
   const klt_dims& d = h->d;
   const int E = d.E, k = d.topk, L = d.L, I = d.I, Is = d.Is, H = d.H;
-  const int bi = bn_index(M);
+  const int bi = bn_index(M, dbg ? dbg->force_bn : 0);
   const int BN = kBN[bi];
   const bool nvfp4 = d.routed_fmt == KLT_FMT_NVFP4;
   const int rkb = nvfp4 ? 64 : 128;  // routed K elements per k-block

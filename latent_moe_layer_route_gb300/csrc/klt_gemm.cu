@@ -41,6 +41,7 @@ struct Cfg {
   static constexpr bool DUAL = BN <= 32;
   static constexpr int STAGE_BYTES = 2 * A_BYTES + (DUAL ? 2 : 1) * B_BYTES;
   static constexpr int STAGES = BN == 16 ? 6 : (BN == 128 ? 3 : 5);
+  static_assert(BN == 16 || BN == 32 || BN == 64 || BN == 128, "tile width");
   static constexpr int SLOT_COLS = 2 * BN;
   static constexpr int TMEM_COLS = BN <= 64 ? 256 : 512;
   static constexpr int NACC = TMEM_COLS / SLOT_COLS;
@@ -694,14 +695,23 @@ cudaError_t launch_bn(const GemmParams& p, int grid, cudaStream_t s, bool pdl) {
 
 // dynamic shared memory plus the producer's static offset tables
 static_assert(Smem<16>::bytes() + 2 * (MAX_E + 1) * 4 <= 227 * 1024, "shared memory budget");
+static_assert(Smem<32>::bytes() + 2 * (MAX_E + 1) * 4 <= 227 * 1024, "shared memory budget");
+static_assert(Smem<64>::bytes() + 2 * (MAX_E + 1) * 4 <= 227 * 1024, "shared memory budget");
 static_assert(Smem<128>::bytes() + 2 * (MAX_E + 1) * 4 <= 227 * 1024, "shared memory budget");
 
 int gemm_smem_bytes(int bn) {
-  return bn == 16 ? Smem<16>::bytes() : Smem<128>::bytes();
+  switch (bn) {
+    case 16: return Smem<16>::bytes();
+    case 32: return Smem<32>::bytes();
+    case 64: return Smem<64>::bytes();
+    default: return Smem<128>::bytes();
+  }
 }
 
 cudaError_t launch_gemm(const GemmParams& p, int bn, int grid, cudaStream_t s, bool pdl) {
   if (bn == 16) return launch_bn<16>(p, grid, s, pdl);
+  if (bn == 32) return launch_bn<32>(p, grid, s, pdl);
+  if (bn == 64) return launch_bn<64>(p, grid, s, pdl);
   if (bn == 128) return launch_bn<128>(p, grid, s, pdl);
   return cudaErrorInvalidValue;
 }

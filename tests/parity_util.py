@@ -26,7 +26,7 @@ class Run:
     """One forward with routing and stage outputs captured."""
 
     def __init__(self, tail: B.LatentMoETail, act: Dict, cfg, stall_after: int = 0,
-                 timeout_ms: int = 0):
+                 timeout_ms: int = 0, force_bn: int = 0):
         M = act["x"].shape[0]
         k, E, L, I, Is = cfg.topk, cfg.E, cfg.L, cfg.I, cfg.Is
         dev = "cuda"
@@ -54,6 +54,7 @@ class Run:
         dbg.r, dbg.n, dbg.a_s = self.r.data_ptr(), self.n.data_ptr(), self.a_s.data_ptr()
         dbg.stall_after_kblocks = stall_after
         dbg.timeout_ms = timeout_ms
+        dbg.force_bn = force_bn
         tail.forward(act["x"], act["z"], act["logits"], out=self.out, routing=ro, debug=dbg)
         torch.cuda.synchronize()
 

@@ -36,7 +36,7 @@ def weights_for(cfg):
     return _CACHE[key]
 
 
-def run_case(cfg, M=None, act=None, tokens=None, max_tokens=None, tail=None):
+def run_case(cfg, M=None, act=None, tokens=None, max_tokens=None, tail=None, force_bn=0):
     w_cpu, w_gpu = weights_for(cfg)
     if act is None:
         act = inputs.make_activations(cfg, M)
@@ -44,7 +44,7 @@ def run_case(cfg, M=None, act=None, tokens=None, max_tokens=None, tail=None):
     own = tail is None
     if own:
         tail = B.LatentMoETail(cfg, w_gpu, max_tokens=max_tokens or M)
-    run = PU.Run(tail, PU.to_cuda(act), cfg)
+    run = PU.Run(tail, PU.to_cuda(act), cfg, force_bn=force_bn)
     assert tail.status() == B.KLT_OK
     o = T.tail(act, w_cpu, cfg, tokens=tokens)
     PU.check_routing(run, o, cfg)
@@ -69,6 +69,13 @@ def test_small_nvfp4(M):
 def test_small_nvfp4_wider():
     run_case(configs.SMALL.with_(routed_fmt="nvfp4", H=384, L=512, I=256, Is=256, E=5,
                                  topk=3, seed=29), M=45)
+
+
+@pytest.mark.parametrize("bn", [16, 32, 64, 128])
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+def test_every_token_tile_width(bn, fmt):
+    # ragged M spanning several token tiles of each width
+    run_case(configs.SMALL.with_(routed_fmt=fmt, E=6, topk=3, seed=30), M=150, force_bn=bn)
 
 
 def test_small_all_experts_selected():
