@@ -388,6 +388,78 @@ __device__ void run_mma(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_base) {
 }
 
 // ------------------------------------------------------------------ epilogue
+// One promotion batch of up to MAXNB groups (fewer when COLS is wide or the unit ends):
+// acc += partial * (weight block scale * token group scale), per group.  Returns the
+// number of groups consumed, 0 if a bounded wait expired.
+template <int BN, int COLS, int MAXNB, bool PAIR>
+__device__ __forceinline__ int promote_batch(int left, int kbi, const float* sb, float* g,
+                                             float* u, Smem<BN>& sm, uint32_t tmem_base,
+                                             uint32_t lane_base, int c0, int& acc,
+                                             uint32_t& aphase, const GemmParams& p) {
+  using C = Cfg<BN>;
+  // registers per thread for one batch: NB groups x (PAIR ? 2 : 1) x 16 columns <= 64
+  constexpr int CAP = 64 / ((PAIR ? 2 : 1) * 16);
+  constexpr int NBMAX = (COLS == 16) ? (MAXNB < CAP ? MAXNB : CAP) : 1;
+  const int nb = left < NBMAX ? left : NBMAX;
+  uint32_t tb[4];
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    if (b >= nb) break;
+    int slot = acc + b;
+    uint32_t par = aphase;
+    if (slot >= C::NACC) { slot -= C::NACC; par ^= 1; }
+    if (!mbar_wait(&sm.tfull[slot], par, sm.abort_flag, p.err, p.timeout)) return 0;
+    tb[b] = tmem_base + lane_base + static_cast<uint32_t>(slot * C::SLOT_COLS);
+  }
+  tc_fence_after();
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int ch = 0; ch < COLS / 16; ++ch) {
+    float v[4][16];
+    const int col = c0 + ch * 16;
+    if (PAIR) {
+      if (nb == 2) {
+        tmem_ld16x4(tb[0] + col, tb[0] + BN + col, tb[1] + col, tb[1] + BN + col, v[0], v[1],
+                    v[2], v[3]);
+      } else {
+        tmem_ld16x2(tb[0] + col, tb[0] + BN + col, v[0], v[1]);
+      }
+    } else {
+      if (nb == 4)
+        tmem_ld16x4(tb[0] + col, tb[1] + col, tb[2] + col, tb[3] + col, v[0], v[1], v[2], v[3]);
+      else if (nb >= 2)
+        tmem_ld16x2(tb[0] + col, tb[1] + col, v[0], v[1]);
+      else
+        tmem_ld16(tb[0] + col, v[0]);
+      if (nb == 3) tmem_ld16(tb[2] + col, v[2]);
+    }
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      if (b >= nb) break;
+      const int gk = kbi + b;
+      const float sw_g = sb[MAX_KB * BN + 2 * gk];
+      const float sw_u = sb[MAX_KB * BN + 2 * gk + 1];
+      const float* ts = sb + gk * BN + ch * 16 + c0;
+      const float* pg = PAIR ? v[2 * b] : v[b];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float sa = ts[i];
+        g[ch * 16 + i] = fmaf(pg[i], sw_g * sa, g[ch * 16 + i]);
+        if (PAIR) u[ch * 16 + i] = fmaf(v[2 * b + 1][i], sw_u * sa, u[ch * 16 + i]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncwarp();
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    if (b >= nb) break;
+    if (lane == 0) mbar_arrive(&sm.tempty[acc]);
+    if (++acc == C::NACC) { acc = 0; aphase ^= 1; }
+  }
+  return nb;
+}
+
 template <int BN>
 __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_base) {
   using C = Cfg<BN>;
@@ -456,32 +528,19 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
         }
       }
       named_bar_sync(1, C::EPI_THREADS);
-      for (int kbi = 0; kbi < nkb; ++kbi) {
-        const float sw_g = sb[MAX_KB * BN + 2 * kbi];
-        const float sw_u = sb[MAX_KB * BN + 2 * kbi + 1];
-        const float* ts = sb + kbi * BN + c0;
-        if (!mbar_wait(&sm.tfull[acc], aphase, sm.abort_flag, p.err, p.timeout)) return;
-        tc_fence_after();
-        const uint32_t tb = tmem_base + lane_base + static_cast<uint32_t>(acc * C::SLOT_COLS);
-#pragma unroll
-        for (int ch = 0; ch < COLS / 16; ++ch) {
-          float pg[16], pu[16];
-          if (pair)
-            tmem_ld16x2(tb + c0 + ch * 16, tb + BN + c0 + ch * 16, pg, pu);
-          else
-            tmem_ld16(tb + c0 + ch * 16, pg);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int j = ch * 16 + i;
-            const float sa = ts[j];
-            g[j] = fmaf(pg[i], sw_g * sa, g[j]);
-            if (pair) u[j] = fmaf(pu[i], sw_u * sa, u[j]);
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.tempty[acc]);
-        if (++acc == C::NACC) { acc = 0; aphase ^= 1; }
+      // Promote completed groups in batches: wait for up to NB slots, load them under one
+      // TMEM wait, then scale-and-add, so the per-group latency chain is paid once per batch.
+      for (int kbi = 0; kbi < nkb;) {
+        const int left = nkb - kbi;
+        int nb;
+        if (pair)
+          nb = promote_batch<BN, COLS, 2, true>(left, kbi, sb, g, u, sm, tmem_base, lane_base, c0,
+                                                acc, aphase, p);
+        else
+          nb = promote_batch<BN, COLS, 4, false>(left, kbi, sb, g, u, sm, tmem_base, lane_base,
+                                                 c0, acc, aphase, p);
+        if (nb == 0) return;  // a bounded wait expired
+        kbi += nb;
         if (ew == 0 && lane == 0) trace_mark(p, 2, steps++);
       }
     } else {
