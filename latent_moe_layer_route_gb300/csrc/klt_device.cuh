@@ -94,13 +94,6 @@ KLT_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
-// Prefetch `bytes` (multiple of 16) of global memory into L2.
-KLT_DEV void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(
-                   src)),
-               "r"(bytes)
-               : "memory");
-}
 KLT_DEV uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

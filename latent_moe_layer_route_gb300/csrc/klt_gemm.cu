@@ -239,94 +239,35 @@ __device__ void run_producer(const GemmParams& p, Smem<BN>& sm, const int* s_til
   bool stalled = false;
   const bool streamk = p.task[0].streamk != 0;
   long long sk_x = 0, sk_end = 0;
-  if (streamk && static_cast<int>(blockIdx.x) < p.task[0].sk_grid) {
-    sk_x = sk_begin(p.task[0].sk_total, p.task[0].sk_grid, blockIdx.x);
-    sk_end = sk_begin(p.task[0].sk_total, p.task[0].sk_grid, blockIdx.x + 1);
+  int u = 0;
+  if (streamk) {
+    if (static_cast<int>(blockIdx.x) < p.task[0].sk_grid) {
+      sk_x = sk_begin(p.task[0].sk_total, p.task[0].sk_grid, blockIdx.x);
+      sk_end = sk_begin(p.task[0].sk_total, p.task[0].sk_grid, blockIdx.x + 1);
+    }
+  } else {
+    u = atomicAdd(p.sched, 1);
   }
-  // Units are claimed ahead into a small FIFO by an L2 prefetch cursor that runs up to
-  // PF stages ahead of the copy cursor, so the weight tiles a stage copies into shared
-  // memory are already in L2: DRAM latency is then covered by L2 capacity instead of the
-  // shared-memory ring.
-  constexpr int QN = 4;
-  constexpr int PF = 2 * C::STAGES;
-  UnitInfo q[QN];
-  int qh = 0, qn = 0;          // FIFO head and size
-  bool src_done = false;       // no more units to claim
-  int pf_u = 0, pf_kb = 0;     // prefetch cursor: FIFO offset and k-block
-  bool pf_started = false;
-  int ahead = 0;               // stages prefetched but not yet copied
-  auto claim = [&]() -> bool {
-    if (src_done || qn == QN) return false;
-    UnitInfo in;
-    if (streamk) {
-      in = next_streamk_piece<BN>(p, sk_x, sk_end);
-    } else {
-      const int u = atomicAdd(p.sched, 1);
-      in = decode_unit<BN>(p, s_tile_off, s_off, u);
-    }
-    if (in.task < 0) {
-      src_done = true;
-      return false;
-    }
-    q[(qh + qn) % QN] = in;
-    ++qn;
-    return true;
-  };
-  auto prefetch_ahead = [&]() {
-    while (ahead < PF) {
-      if (pf_u >= qn && !claim()) return;
-      const UnitInfo& pi = q[(qh + pf_u) % QN];
-      if (!pf_started) {
-        pf_kb = pi.kb0;
-        pf_started = true;
-      }
-      const GemmTask& PT = p.task[pi.task];
-      const bool ppair = is_pair(PT.kind);
-      const int pstep = (ppair || !C::DUAL) ? 1 : 2;
-      const int nsub = min(pstep, pi.kb1 - pf_kb);
-      for (int sub = 0; sub < nsub; ++sub) {
-        const int kbs = pf_kb + sub;
-        const int m = kbs < PT.kb_split0 ? 0 : 1;
-        const int kk = m ? kbs - PT.kb_split0 : kbs;
-        bulk_prefetch_l2(
-            PT.a_ptr[m] + (static_cast<size_t>(pi.arb) * PT.a_kb[m] + kk) * C::A_BYTES,
-            C::A_BYTES);
-        if (ppair)
-          bulk_prefetch_l2(PT.a_ptr[m] + (static_cast<size_t>(pi.arb + PT.a_rb_up) *
-                                              PT.a_kb[m] + kk) * C::A_BYTES,
-                           C::A_BYTES);
-      }
-      ++ahead;
-      pf_kb += pstep;
-      if (pf_kb >= pi.kb1) {
-        ++pf_u;
-        pf_started = false;
-      }
-    }
-  };
   for (;;) {
-    prefetch_ahead();
-    if (qn == 0 && !claim()) {
-      UnitInfo end_info;
-      end_info.task = -1;
-      if (mbar_wait(&sm.uempty[us], uphase ^ 1, sm.abort_flag, p.err, p.timeout)) {
-        sm.ring[us] = end_info;
-        mbar_arrive(&sm.ufull[us]);
-      }
-      break;
+    UnitInfo info;
+    if (streamk) {
+      info = next_streamk_piece<BN>(p, sk_x, sk_end);
+    } else {
+      info = decode_unit<BN>(p, s_tile_off, s_off, u);
+      // claim the next unit now so the counter round trip overlaps this unit's copies
+      if (info.task >= 0) u = atomicAdd(p.sched, 1);
     }
-    const UnitInfo info = q[qh];
     if (!mbar_wait(&sm.uempty[us], uphase ^ 1, sm.abort_flag, p.err, p.timeout)) break;
     sm.ring[us] = info;
     mbar_arrive(&sm.ufull[us]);
     if (++us == C::US) { us = 0; uphase ^= 1; }
+    if (info.task < 0) break;
     const GemmTask& T = p.task[info.task];
     const bool pair = is_pair(T.kind);
     const int elems_per_kb = T.fp8 ? 128 : 64;
     const int step = (pair || !C::DUAL) ? 1 : 2;
     for (int kb = info.kb0; kb < info.kb1; kb += step) {
       if (p.stall_after > 0 && issued >= p.stall_after) { stalled = true; break; }
-      prefetch_ahead();
       if (!mbar_wait(&sm.empty[stage], phase ^ 1, sm.abort_flag, p.err, p.timeout)) {
         stalled = true;
         break;
@@ -355,13 +296,9 @@ __device__ void run_producer(const GemmParams& p, Smem<BN>& sm, const int* s_til
       }
       trace_mark(p, 0, static_cast<int>(issued));
       ++issued;
-      if (ahead > 0) --ahead;
       if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
     }
     if (stalled) break;
-    qh = (qh + 1) % QN;
-    --qn;
-    --pf_u;
   }
   // Drain: wait (bounded, ignoring the abort flag) for this thread's last copies, so no
   // TMA write into shared memory outlives the CTA.
