@@ -129,10 +129,11 @@ typedef struct klt_routing {
  *     GEMM stops feeding data after that many k-blocks, so its consumers' bounded waits
  *     run out and klt_status reports KLT_ERR_DEVICE_TIMEOUT;
  *   timeout_ms: bound of every on-device wait for this call (0 = the default, 1000 ms);
- *   trace: optional device int64 buffer of 3 * trace_entries * 3 * (SM count) entries; when
+ *   trace: optional device int64 buffer of 3 * trace_entries * 4 * (SM count) entries; when
  *     set, each GEMM launch g (0..2) records globaltimer stamps (ns) per CTA c and role r
  *     (0 = weight tile copy issued, 1 = tile consumed by the MMA issuer, 2 = epilogue step
- *     done) at trace[((g * SMs + c) * 3 + r) * trace_entries + i], first trace_entries
+ *     done, 3 = MMA issuer starts waiting for a tile) at
+ *     trace[((g * SMs + c) * 4 + r) * trace_entries + i], first trace_entries
  *     events each; unused entries are left untouched;
  *   force_bn: token-tile width of the GEMM stages for this call (16, 32, 64 or 128;
  *     0 = chosen from M), for tuning sweeps. */

@@ -407,7 +407,7 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
   gp.trace_n = dbg ? dbg->trace_entries : 0;
   long long* trace = (dbg && dbg->trace && dbg->trace_entries > 0)
                          ? reinterpret_cast<long long*>(dbg->trace) : nullptr;
-  const long long trace_launch = static_cast<long long>(h->num_sms) * 3 * gp.trace_n;
+  const long long trace_launch = static_cast<long long>(h->num_sms) * 4 * gp.trace_n;
   const int ntiles = (M + BN - 1) / BN;
   const int grid = h->num_sms;
   const size_t ws_task = static_cast<size_t>(kMaxSplitUnits) * 2 * 128 * 128;

@@ -125,7 +125,7 @@ struct Smem {
 // Optional event trace: stamp i of role r for this CTA.
 __device__ __forceinline__ void trace_mark(const GemmParams& p, int role, int i) {
   if (p.trace != nullptr && i < p.trace_n)
-    p.trace[(static_cast<long long>(blockIdx.x) * 3 + role) * p.trace_n + i] = global_ns();
+    p.trace[(static_cast<long long>(blockIdx.x) * 4 + role) * p.trace_n + i] = global_ns();
 }
 
 __device__ __forceinline__ bool is_pair(int kind) {
@@ -336,6 +336,7 @@ __device__ void run_mma(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_base) {
       tc_fence_after();
     }
     for (int kb = info.kb0; kb < info.kb1 && ok; kb += step) {
+      trace_mark(p, 3, consumed);
       if (!mbar_wait(&sm.full[stage], phase, sm.abort_flag, p.err, p.timeout)) {
         ok = false;
         break;
