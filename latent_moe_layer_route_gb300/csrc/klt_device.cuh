@@ -51,16 +51,30 @@ KLT_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// As mbar_try_wait, but the thread is suspended (without taking issue slots from the warps
+// sharing its scheduler) until the phase completes or about `hint_ns` elapse.
+KLT_DEV bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
 
 // Wait for phase `parity` of `bar`, giving up after `timeout` SM cycles or as soon as the
 // CTA's abort flag is raised.  On expiry raises the abort flag and the device error bit.
-// Returns false when the wait did not complete.
+// Returns false when the wait did not complete.  Waiting threads sleep in hardware between
+// checks so they do not steal issue slots from the MMA and copy threads.
 KLT_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                        int* err_word, long long timeout) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, 2000)) return true;
     if (*abort_flag) return false;
     if (clock64() - t0 > timeout) {
       *abort_flag = 1;
