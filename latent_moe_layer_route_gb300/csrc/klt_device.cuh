@@ -194,6 +194,33 @@ KLT_DEV void mma_fp8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t i
       "l"(da), "l"(db), "r"(idesc), "r"(accumulate), "l"(da + 2), "l"(db + 2), "l"(da + 4),  \
       "l"(db + 4), "l"(da + 6), "l"(db + 6)                                                \
       : "memory")
+// Gate and up of one K block (eight MMAs, two accumulators `d` and `d + n_off`) in one
+// asm block.
+#define KLT_MMA8(KIND)                                                                    \
+  asm volatile(                                                                           \
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %5, 0;\n\tsetp.eq.b32 q, 0, 0;\n\t"        \
+      "tcgen05.mma.cta_group::1." KIND " [%0], %2, %4, %6, p;\n\t"                         \
+      "tcgen05.mma.cta_group::1." KIND " [%1], %3, %4, %6, p;\n\t"                         \
+      "tcgen05.mma.cta_group::1." KIND " [%0], %7, %8, %6, q;\n\t"                         \
+      "tcgen05.mma.cta_group::1." KIND " [%1], %9, %8, %6, q;\n\t"                         \
+      "tcgen05.mma.cta_group::1." KIND " [%0], %10, %11, %6, q;\n\t"                       \
+      "tcgen05.mma.cta_group::1." KIND " [%1], %12, %11, %6, q;\n\t"                       \
+      "tcgen05.mma.cta_group::1." KIND " [%0], %13, %14, %6, q;\n\t"                       \
+      "tcgen05.mma.cta_group::1." KIND " [%1], %15, %14, %6, q;\n\t}" ::"r"(d),            \
+      "r"(d + n_off), "l"(da), "l"(du), "l"(db), "r"(accumulate), "r"(idesc), "l"(da + 2), \
+      "l"(db + 2), "l"(du + 2), "l"(da + 4), "l"(db + 4), "l"(du + 4), "l"(da + 6),        \
+      "l"(db + 6), "l"(du + 6)                                                             \
+      : "memory")
+KLT_DEV void mma8_bf16(uint32_t d, uint64_t da, uint64_t du, uint64_t db, uint32_t idesc,
+                       uint32_t accumulate, uint32_t n_off) {
+  KLT_MMA8("kind::f16");
+}
+KLT_DEV void mma8_fp8(uint32_t d, uint64_t da, uint64_t du, uint64_t db, uint32_t idesc,
+                      uint32_t accumulate, uint32_t n_off) {
+  KLT_MMA8("kind::f8f6f4");
+}
+#undef KLT_MMA8
+
 KLT_DEV void mma4_bf16(uint32_t d, uint64_t da, uint64_t db, uint32_t idesc,
                        uint32_t accumulate) {
   KLT_MMA4("kind::f16");

@@ -311,14 +311,22 @@ __device__ void run_producer(const GemmParams& p, Smem<BN>& sm, const int* s_til
 }
 
 // ------------------------------------------------------------------ MMA issuer (1 thread)
+// The issuing thread pays for every instruction it executes between MMAs, so the loop keeps
+// only barrier waits, descriptor adds and the MMAs themselves: per-stage descriptors are
+// precomputed, task fields are read once per unit and group positions are counted.
 template <int BN>
 __device__ void run_mma(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_base) {
   using C = Cfg<BN>;
-  int stage = 0, us = 0, acc = 0, consumed = 0;
+  int stage = 0, us = 0, acc = 0;
   uint32_t phase = 0, uphase = 0, aphase = 0;
   bool ok = true;
   const uint32_t idesc_bf16 = idesc_make(1, 128, BN);
   const uint32_t idesc_fp8 = idesc_make(0, 128, BN);
+  // descriptor of stage 0's A0 tile; every other operand is a fixed offset from it
+  const uint64_t desc0 = sdesc_sw128(smem_u32(sm.stages));
+  constexpr uint64_t STAGE_D = C::STAGE_BYTES >> 4;
+  constexpr uint64_t A_D = C::A_BYTES >> 4;
+  constexpr uint64_t B_D = C::B_BYTES >> 4;
   while (ok) {
     if (!mbar_wait(&sm.ufull[us], uphase, sm.abort_flag, p.err, p.timeout)) break;
     const UnitInfo info = sm.ring[us];
@@ -327,27 +335,26 @@ __device__ void run_mma(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_base) {
     if (info.task < 0) break;
     const GemmTask& T = p.task[info.task];
     const bool pair = is_pair(T.kind);
-    const bool promote = T.kpg > 0;
+    const int kpg = T.kpg;
+    const bool promote = kpg > 0;
     const bool fp8 = T.fp8 != 0;
     const uint32_t idesc = fp8 ? idesc_fp8 : idesc_bf16;
     const int step = (pair || !C::DUAL) ? 1 : 2;
+    const int kb0 = info.kb0, kb1 = info.kb1;
     if (!promote) {
       if (!mbar_wait(&sm.tempty[acc], aphase ^ 1, sm.abort_flag, p.err, p.timeout)) break;
       tc_fence_after();
     }
-    for (int kb = info.kb0; kb < info.kb1 && ok; kb += step) {
-      trace_mark(p, 3, consumed);
+    int gpos = 0;  // position of the next k-block in its promotion group
+    for (int kb = kb0; kb < kb1 && ok; kb += step) {
       if (!mbar_wait(&sm.full[stage], phase, sm.abort_flag, p.err, p.timeout)) {
         ok = false;
         break;
       }
-      trace_mark(p, 1, consumed++);
       tc_fence_after();
-      const int nsub = min(step, info.kb1 - kb);
-      const uint32_t sa = smem_u32(sm.stages + stage * C::STAGE_BYTES);
+      const int nsub = min(step, kb1 - kb);
+      const uint64_t ds = desc0 + static_cast<uint64_t>(stage) * STAGE_D;
       for (int sub = 0; sub < nsub; ++sub) {
-        // position of this k-block in its promotion group
-        const int gpos = promote ? (kb + sub - info.kb0) % T.kpg : 0;
         if (promote && gpos == 0) {
           if (!mbar_wait(&sm.tempty[acc], aphase ^ 1, sm.abort_flag, p.err, p.timeout)) {
             ok = false;
@@ -356,21 +363,24 @@ __device__ void run_mma(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_base) {
           tc_fence_after();
         }
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * C::SLOT_COLS);
-        const uint64_t da = sdesc_sw128(sa + sub * C::A_BYTES);
-        const uint64_t du = sdesc_sw128(sa + C::A_BYTES);
-        const uint64_t db = sdesc_sw128(sa + 2 * C::A_BYTES + sub * C::B_BYTES);
+        const uint64_t da = ds + static_cast<uint64_t>(sub) * A_D;
+        const uint64_t du = ds + A_D;
+        const uint64_t db = ds + 2 * A_D + static_cast<uint64_t>(sub) * B_D;
         const uint32_t accum = promote ? static_cast<uint32_t>(gpos > 0)
-                                       : static_cast<uint32_t>(kb + sub > info.kb0);
+                                       : static_cast<uint32_t>(kb + sub > kb0);
         if (fp8) {
-          mma4_fp8(d, da, db, idesc, accum);
-          if (pair) mma4_fp8(d + BN, du, db, idesc, accum);
+          if (pair) mma8_fp8(d, da, du, db, idesc, accum, BN);
+          else mma4_fp8(d, da, db, idesc, accum);
         } else {
-          mma4_bf16(d, da, db, idesc, accum);
-          if (pair) mma4_bf16(d + BN, du, db, idesc, accum);
+          if (pair) mma8_bf16(d, da, du, db, idesc, accum, BN);
+          else mma4_bf16(d, da, db, idesc, accum);
         }
-        if (promote && gpos == T.kpg - 1) {
-          tc_commit(&sm.tfull[acc]);
-          if (++acc == C::NACC) { acc = 0; aphase ^= 1; }
+        if (promote) {
+          if (++gpos == kpg) {
+            gpos = 0;
+            tc_commit(&sm.tfull[acc]);
+            if (++acc == C::NACC) { acc = 0; aphase ^= 1; }
+          }
         }
       }
       tc_commit(&sm.empty[stage]);
