@@ -62,7 +62,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 constexpr int kNumBN = 4;
 constexpr int kBN[kNumBN] = {16, 32, 64, 128};
 constexpr int kMaxSplitUnits = 3 * 160;  // split-K tiles*splits bound per task
-constexpr int kMaxCounters = 8192;       // arrival counters per split task
+constexpr int kMaxCounters = 8192;       // arrival counters per split launch
+constexpr int kRoutedSplitPairs = 2048;  // routed L1 k-splits only when M * topk <= this
 
 }  // namespace
 
@@ -82,6 +83,7 @@ struct klt_handle {
   __nv_bfloat16 *n, *a_s, *zqb_perm, *aqb;
   int *split_cnt, *sched, *err;
   int cap, max_hist_blocks;
+  long long ws_routed_floats;
   // descriptors per BN variant (token-side maps depend on the box height)
   CUtensorMap tm_zqp[kNumBN], tm_aq[kNumBN], tm_n[kNumBN], tm_as[kNumBN];
   void* allocs[48];
@@ -235,7 +237,14 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
   KLT_ALLOC(h->r, Mx * L * 4);
   KLT_ALLOC(h->n, Mx * L * 2);
   KLT_ALLOC(h->a_s, Mx * Is * 2);
-  KLT_ALLOC(h->ws, 2LL * kMaxSplitUnits * 2 * 128 * 128 * 4);
+  // split-K partials: [shared L1 | routed L1 | output GEMM]
+  h->ws_routed_floats =
+      static_cast<long long>(kRoutedSplitPairs / 16 + E) * (I / 128) * 2 * 2 * 16 * 128;
+  for (int bn = 32; bn <= 128; bn *= 2)
+    h->ws_routed_floats = std::max<long long>(
+        h->ws_routed_floats,
+        static_cast<long long>((kRoutedSplitPairs + bn - 1) / bn + E) * (I / 128) * 2 * 2 * bn * 128);
+  KLT_ALLOC(h->ws, (2LL * kMaxSplitUnits * 2 * 128 * 128 + h->ws_routed_floats) * 4);
   KLT_ALLOC(h->split_cnt, 2LL * kMaxCounters * 4);
   KLT_ALLOC(h->sched, 64 * 4);
   KLT_ALLOC(h->err, 256);
@@ -428,8 +437,14 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
     R.ftiles = I / 128;
     R.kb_total = L / rkb;
     R.kb_split0 = R.kb_total;
-    R.ksplit = 1;
-    R.kb_per_split = R.kb_total;
+    // decode sizes: two k-splits per routed tile so the units are small enough to balance
+    const long long routed_tiles_max = static_cast<long long>((Mk + BN - 1) / BN + E) * R.ftiles;
+    R.ksplit = (Mk <= kRoutedSplitPairs && R.kb_total >= 8 &&
+                routed_tiles_max + kMaxSplitUnits <= kMaxCounters)
+                   ? 2 : 1;
+    R.kb_per_split = (R.kb_total + R.ksplit - 1) / R.ksplit;
+    if (R.kpg > 1) R.kb_per_split = (R.kb_per_split + R.kpg - 1) / R.kpg * R.kpg;
+    R.ksplit = (R.kb_total + R.kb_per_split - 1) / R.kb_per_split;
     R.a_rb_up = I / 128;
     R.a_rb_expert = 2 * I / 128;
     R.a_kb[0] = R.a_kb[1] = L / rkb;
@@ -445,7 +460,11 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
     S.a_rb_up = Is / 128;
     S.a_kb[0] = S.a_kb[1] = H / 64;
     S.ws_tile_base = 0;
+    S.ws_off = 0;
     plan_split(S, ntiles, ntiles * S.ftiles * std::max(1, S.kb_total / 8), BN);
+    // routed partials and counters follow the shared ones
+    R.ws_tile_base = S.ntiles * S.ftiles;
+    R.ws_off = static_cast<long long>(kMaxSplitUnits) * 2 * 128 * 128;
     if (!encode_2d(&S.tmB[0], x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, H, BN))
       return KLT_ERR_CUDA;
     S.a_ptr[0] = S.a_ptr[1] = reinterpret_cast<const uint8_t*>(h->ws13);
@@ -490,7 +509,7 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
     g3.ntasks = 1;
     g3.sched = h->sched + 2;
     g3.trace = trace ? trace + 2 * trace_launch : nullptr;
-    g3.ws = h->ws + ws_task;
+    g3.ws = h->ws + ws_task + h->ws_routed_floats;
     g3.cnt = h->split_cnt + kMaxCounters;
     GemmTask& O = g3.task[0];
     O.kind = TASK_OUT;

@@ -141,10 +141,13 @@ __device__ UnitInfo decode_unit(const GemmParams& p, const int* s_tile_off, cons
     const GemmTask& T = p.task[ti];
     if (T.routed) {
       const int ntiles = s_tile_off[p.E];
-      const int units = ntiles * T.ftiles;
+      const int per_t = T.ftiles * T.ksplit;
+      const int units = ntiles * per_t;
       if (u < units) {
-        const int t = u / T.ftiles;
-        const int ft = u - t * T.ftiles;
+        const int t = u / per_t;
+        const int rem = u - t * per_t;
+        const int ft = rem / T.ksplit;
+        const int sp = rem - ft * T.ksplit;
         int lo = 0, hi = p.E - 1;  // largest e with tile_off[e] <= t
         while (lo < hi) {
           const int mid = (lo + hi + 1) >> 1;
@@ -157,11 +160,11 @@ __device__ UnitInfo decode_unit(const GemmParams& p, const int* s_tile_off, cons
         info.rows = min(BN, s_off[e + 1] - info.row0);
         info.ftile = ft;
         info.arb = e * T.a_rb_expert + ft;
-        info.kb0 = 0;
-        info.kb1 = T.kb_total;
-        info.tile_id = 0;
-        info.split = 0;
-        info.ncontrib = 1;
+        info.kb0 = sp * T.kb_per_split;
+        info.kb1 = min(T.kb_total, info.kb0 + T.kb_per_split);
+        info.tile_id = T.ws_tile_base + t * T.ftiles + ft;
+        info.split = sp;
+        info.ncontrib = T.ksplit;
         info.cfirst = 0;
         info.wslot = 0;
         return info;
@@ -577,9 +580,10 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
     if (info.ncontrib > 1) {
       const int parts = pair ? 2 : 1;
       const size_t tile_floats = static_cast<size_t>(parts) * BN * 128;
-      const size_t own = T.streamk ? static_cast<size_t>(info.wslot)
-                                   : static_cast<size_t>(info.tile_id) * T.ksplit + info.split;
-      float* mine = p.ws + own * tile_floats;
+      const size_t own =
+          T.streamk ? static_cast<size_t>(info.wslot)
+                    : static_cast<size_t>(info.tile_id - T.ws_tile_base) * T.ksplit + info.split;
+      float* mine = p.ws + T.ws_off + own * tile_floats;
 #pragma unroll
       for (int j = 0; j < COLS; ++j) {
         __stcg(mine + static_cast<size_t>(c0 + j) * 128 + row, g[j]);
@@ -603,8 +607,8 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
             T.streamk ? static_cast<size_t>(sk_slot(T.sk_total, T.sk_grid, T.kb_total,
                                                     info.cfirst + s,
                                                     info.tile_id - T.ws_tile_base))
-                      : static_cast<size_t>(info.tile_id) * T.ksplit + s;
-        const float* ps = p.ws + idx * tile_floats;
+                      : static_cast<size_t>(info.tile_id - T.ws_tile_base) * T.ksplit + s;
+        const float* ps = p.ws + T.ws_off + idx * tile_floats;
 #pragma unroll
         for (int j = 0; j < COLS; ++j) {
           g[j] += __ldcg(ps + static_cast<size_t>(c0 + j) * 128 + row);

@@ -78,7 +78,8 @@ struct GemmTask {
   int a_kb[2];         // k-blocks per 128-row block of a_ptr[0], a_ptr[1]
   int ntiles;          // non-routed: token tiles
   int units;           // non-routed: ntiles * ftiles * ksplit
-  int ws_tile_base;    // first split-K workspace tile / counter of this task
+  int ws_tile_base;    // first arrival counter of this task (tile ids start here)
+  long long ws_off;    // float offset of this task's partials in the workspace
   int streamk;         // 1: static stream-K partition of ntiles*ftiles*kb_total k-blocks
                        //    over sk_grid CTAs (non-routed, bf16, sole task of its launch)
   int sk_grid;
