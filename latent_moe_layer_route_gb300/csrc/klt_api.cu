@@ -63,7 +63,8 @@ constexpr int kNumBN = 4;
 constexpr int kBN[kNumBN] = {16, 32, 64, 128};
 constexpr int kMaxSplitUnits = 3 * 160;  // split-K tiles*splits bound per task
 constexpr int kMaxCounters = 8192;       // arrival counters per split launch
-constexpr int kRoutedSplitPairs = 2048;  // routed L1 k-splits only when M * topk <= this
+constexpr int kRoutedSplitPairs = 0;  // routed L1 k-splits when M * topk <= this (off: the
+                                      // split reduce outweighs the balance it buys)
 
 }  // namespace
 
@@ -239,8 +240,10 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
   KLT_ALLOC(h->a_s, Mx * Is * 2);
   // split-K partials: [shared L1 | routed L1 | output GEMM]
   h->ws_routed_floats =
-      static_cast<long long>(kRoutedSplitPairs / 16 + E) * (I / 128) * 2 * 2 * 16 * 128;
-  for (int bn = 32; bn <= 128; bn *= 2)
+      kRoutedSplitPairs == 0
+          ? 0
+          : static_cast<long long>(kRoutedSplitPairs / 16 + E) * (I / 128) * 2 * 2 * 16 * 128;
+  for (int bn = 32; bn <= 128 && kRoutedSplitPairs > 0; bn *= 2)
     h->ws_routed_floats = std::max<long long>(
         h->ws_routed_floats,
         static_cast<long long>((kRoutedSplitPairs + bn - 1) / bn + E) * (I / 128) * 2 * 2 * bn * 128);
