@@ -57,8 +57,11 @@ enum klt_routed_format {
 
 /* klt_create flags. */
 enum klt_flags {
-  KLT_FLAG_NO_PDL = 1u << 0  /* launch the kernels with plain stream ordering instead of
-                                programmatic dependent launch                          */
+  KLT_FLAG_NO_PDL = 1u << 0,  /* launch the kernels with plain stream ordering instead of
+                                 programmatic dependent launch                          */
+  KLT_FLAG_PHASED = 1u << 1   /* run the GEMM stages as three launches plus a norm launch
+                                 instead of one persistent launch with device-side
+                                 dependencies (same results; for comparison)            */
 };
 
 /* Layer shape.  H, L, I, Is must be multiples of 128; 1 <= topk <= min(E, 32);

@@ -83,6 +83,8 @@ struct klt_handle {
   uint8_t *zq, *zq_perm, *aq;
   __nv_bfloat16 *n, *a_s, *zqb_perm, *aqb;
   int *split_cnt, *sched, *err;
+  int* dep_cnt;  // fused-launch dependency counters [routed tiles | l2 | norm tiles | shared]
+  int dep_routed, dep_ntiles;
   int cap, max_hist_blocks;
   long long ws_routed_floats;
   // descriptors per BN variant (token-side maps depend on the box height)
@@ -250,6 +252,9 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
   KLT_ALLOC(h->ws, (2LL * kMaxSplitUnits * 2 * 128 * 128 + h->ws_routed_floats) * 4);
   KLT_ALLOC(h->split_cnt, 2LL * kMaxCounters * 4);
   KLT_ALLOC(h->sched, 64 * 4);
+  h->dep_routed = static_cast<int>((cap + 15) / 16 + E);
+  h->dep_ntiles = static_cast<int>((Mx + 15) / 16);
+  KLT_ALLOC(h->dep_cnt, (static_cast<int64_t>(h->dep_routed) + 1 + 2 * h->dep_ntiles) * 4);
   KLT_ALLOC(h->err, 256);
 #undef KLT_ALLOC
 
@@ -309,7 +314,8 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
 int klt_launch_count(const klt_handle* h, int32_t M) {
   if (!h || M <= 0) return 0;
   const int nblocks = (M * h->d.topk + PERM_BLOCK - 1) / PERM_BLOCK;
-  return 7 + (nblocks > 1 ? 1 : 0);
+  const int gemm_launches = (h->flags & KLT_FLAG_PHASED) ? 4 : 1;  // phased: 3 GEMMs + norm
+  return 3 + gemm_launches + (nblocks > 1 ? 1 : 0);
 }
 
 int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits, int32_t M,
@@ -355,6 +361,8 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
   rp.r = h->r;
   rp.sched = h->sched;
   rp.nsched = 8;
+  rp.zero_buf = h->dep_cnt;
+  rp.zero_n = (h->flags & KLT_FLAG_PHASED) ? 0 : h->dep_routed + 1 + 2 * h->dep_ntiles;
   rp.M = M;
   rp.E = E;
   rp.k = k;
@@ -424,13 +432,10 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
   const int grid = h->num_sms;
   const size_t ws_task = static_cast<size_t>(kMaxSplitUnits) * 2 * 128 * 128;
 
+  const bool fused = !(h->flags & KLT_FLAG_PHASED);
+  GemmParams g1 = gp, g2 = gp, g3 = gp;
   // ---- GEMM 1: shared L1 (bf16, split-K) + routed L1 (fp8, SwiGLU + act quant)
   {
-    GemmParams g1 = gp;
-    g1.ntasks = 2;
-    g1.sched = h->sched + 0;
-    g1.stall_after = dbg ? dbg->stall_after_kblocks : 0;
-    g1.trace = trace;
     // Routed units first, then the shared expert in small k-splits that fill the tail.
     GemmTask& R = g1.task[0];
     R.kind = TASK_ROUTED_L1;
@@ -472,14 +477,9 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
       return KLT_ERR_CUDA;
     S.a_ptr[0] = S.a_ptr[1] = reinterpret_cast<const uint8_t*>(h->ws13);
     S.tmB[1] = S.tmB[0];
-    KLT_LAUNCH(launch_gemm(g1, BN, grid, s, pdl));
   }
   // ---- GEMM 2: routed L2 with the top-k weighted scatter-combine into r
   {
-    GemmParams g2 = gp;
-    g2.ntasks = 1;
-    g2.sched = h->sched + 1;
-    g2.trace = trace ? trace + trace_launch : nullptr;
     GemmTask& R = g2.task[0];
     R.kind = TASK_ROUTED_L2;
     R.fp8 = !nvfp4;
@@ -495,25 +495,9 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
     R.a_ptr[0] = R.a_ptr[1] = h->w2;
     R.tmB[0] = h->tm_aq[bi];
     R.tmB[1] = h->tm_aq[bi];
-    KLT_LAUNCH(launch_gemm(g2, BN, grid, s, pdl));
   }
-  // ---- RMSNorm of the combine
-  NormParams np;
-  np.r = h->r;
-  np.gamma = h->gamma;
-  np.n = h->n;
-  np.M = M;
-  np.L = L;
-  np.eps = d.eps;
-  KLT_LAUNCH(launch_norm(np, s, pdl));
   // ---- GEMM 3: out = bf16([n | a_s] . [W_up | Ws2]^T)
   {
-    GemmParams g3 = gp;
-    g3.ntasks = 1;
-    g3.sched = h->sched + 2;
-    g3.trace = trace ? trace + 2 * trace_launch : nullptr;
-    g3.ws = h->ws + ws_task + h->ws_routed_floats;
-    g3.cnt = h->split_cnt + kMaxCounters;
     GemmTask& O = g3.task[0];
     O.kind = TASK_OUT;
     O.routed = 0;
@@ -527,7 +511,12 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
     O.kb_per_split = O.kb_total;
     O.ntiles = ntiles;
     O.units = ntiles * O.ftiles;
-    if (O.units < 4 * grid) {
+    if (fused) {
+      // units come from the launch-wide counter, after the other tasks' units
+      O.ws_tile_base = kMaxCounters;
+      O.ws_off = static_cast<long long>(ws_task) + h->ws_routed_floats;
+      plan_split(O, ntiles, 2 * grid, BN);
+    } else if (O.units < 4 * grid) {
       // static stream-K: every CTA streams the same number of k-blocks (no more CTAs than
       // k-blocks, so every CTA's range is non-empty)
       O.streamk = 1;
@@ -538,6 +527,68 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
     O.a_ptr[1] = reinterpret_cast<const uint8_t*>(h->ws2);
     O.tmB[0] = h->tm_n[bi];
     O.tmB[1] = h->tm_as[bi];
+  }
+  if (fused) {
+    // One persistent launch: routed L1 and shared L1, routed L2 (after its token tile's L1
+    // units), the RMSNorm (after every L2 unit) and the output GEMM (after its tile's norm
+    // and shared L1), ordered so that every unit depends only on earlier units.
+    GemmParams gf = gp;
+    gf.ntasks = 5;
+    gf.sched = h->sched + 3;
+    gf.stall_after = dbg ? dbg->stall_after_kblocks : 0;
+    gf.trace = trace;
+    gf.cnt = h->split_cnt;
+    gf.task[0] = g1.task[0];
+    gf.task[1] = g1.task[1];
+    gf.task[2] = g2.task[0];
+    gf.task[2].dep = DEP_L1_TILE;
+    GemmTask& N = gf.task[3];
+    N.kind = TASK_NORM;
+    N.dep = DEP_ALL_L2;
+    N.routed = 0;
+    N.ftiles = 1;
+    N.ksplit = 1;
+    N.kb_total = 0;
+    N.kb_per_split = 0;
+    N.ntiles = ntiles;
+    N.units = ntiles;
+    N.tmB[0] = N.tmB[1] = h->tm_n[bi];
+    gf.task[4] = g3.task[0];
+    gf.task[4].dep = DEP_OUT_TILE;
+    gf.l1_done = h->dep_cnt;
+    gf.l2_done = h->dep_cnt + h->dep_routed;
+    gf.norm_done = gf.l2_done + 1;
+    gf.sh_done = gf.norm_done + h->dep_ntiles;
+    gf.l1_target = I / 128;
+    gf.sh_target = Is / 128;
+    gf.l2_ftiles = L / 128;
+    gf.gamma = h->gamma;
+    gf.nrm = h->n;
+    gf.eps = d.eps;
+    KLT_LAUNCH(launch_gemm(gf, BN, grid, s, pdl));
+  } else {
+    g1.ntasks = 2;
+    g1.sched = h->sched + 0;
+    g1.stall_after = dbg ? dbg->stall_after_kblocks : 0;
+    g1.trace = trace;
+    KLT_LAUNCH(launch_gemm(g1, BN, grid, s, pdl));
+    g2.ntasks = 1;
+    g2.sched = h->sched + 1;
+    g2.trace = trace ? trace + trace_launch : nullptr;
+    KLT_LAUNCH(launch_gemm(g2, BN, grid, s, pdl));
+    NormParams np;
+    np.r = h->r;
+    np.gamma = h->gamma;
+    np.n = h->n;
+    np.M = M;
+    np.L = L;
+    np.eps = d.eps;
+    KLT_LAUNCH(launch_norm(np, s, pdl));
+    g3.ntasks = 1;
+    g3.sched = h->sched + 2;
+    g3.trace = trace ? trace + 2 * trace_launch : nullptr;
+    g3.ws = h->ws + ws_task + h->ws_routed_floats;
+    g3.cnt = h->split_cnt + kMaxCounters;
     KLT_LAUNCH(launch_gemm(g3, BN, grid, s, pdl));
   }
 #undef KLT_LAUNCH

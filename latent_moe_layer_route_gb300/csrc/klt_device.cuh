@@ -329,6 +329,21 @@ KLT_DEV uint8_t f32_to_e4m3(float v) {
 
 KLT_DEV int lane_id() { return threadIdx.x & 31; }
 
+// Cross-CTA signalling inside one launch: writers publish with a release add after their
+// data (and a proxy fence when the data is later read by TMA); readers acquire.
+KLT_DEV int ld_acquire_gpu(const int* ptr) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+KLT_DEV void red_release_gpu_add(int* ptr, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+}
+// Orders this thread's generic-proxy global accesses with its async-proxy (TMA) accesses.
+KLT_DEV void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 KLT_DEV long long global_ns() {
   long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

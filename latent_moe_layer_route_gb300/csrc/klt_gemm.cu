@@ -67,6 +67,7 @@ struct UnitInfo {
   int ncontrib;  // units contributing to this tile (1: no partials)
   int cfirst;    // stream-K: first contributing CTA
   int wslot;     // stream-K: this unit's partial slot
+  int dep_idx;   // routed token tile (routed tasks) or token tile (others)
 };
 
 // Stream-K helpers: CTA c owns k-blocks [b(c), b(c+1)) of the task's flattened
@@ -167,6 +168,7 @@ __device__ UnitInfo decode_unit(const GemmParams& p, const int* s_tile_off, cons
         info.ncontrib = T.ksplit;
         info.cfirst = 0;
         info.wslot = 0;
+        info.dep_idx = t;
         return info;
       }
       u -= units;
@@ -190,6 +192,7 @@ __device__ UnitInfo decode_unit(const GemmParams& p, const int* s_tile_off, cons
         info.ncontrib = T.ksplit;
         info.cfirst = 0;
         info.wslot = 0;
+        info.dep_idx = nt;
         return info;
       }
       u -= T.units;
@@ -225,7 +228,38 @@ __device__ UnitInfo next_streamk_piece(const GemmParams& p, long long& x, long l
   info.ncontrib =
       sk_owner(T.sk_total, T.sk_grid, static_cast<long long>(t + 1) * K - 1) - info.cfirst + 1;
   info.wslot = sk_slot(T.sk_total, T.sk_grid, K, blockIdx.x, t);
+  info.dep_idx = nt;
   return info;
+}
+
+// Bounded wait until the unit's inputs produced by other units of this launch are complete.
+// The acquire loads pair with the producers' release adds; the proxy fence orders the
+// acquired data before this thread's TMA reads of it.
+__device__ bool wait_dependency(const GemmParams& p, int dep, int idx, const int* s_tile_off,
+                                volatile int* abort_flag) {
+  if (dep == DEP_NONE) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    bool ready;
+    if (dep == DEP_L1_TILE) {
+      ready = ld_acquire_gpu(p.l1_done + idx) >= p.l1_target;
+    } else if (dep == DEP_ALL_L2) {
+      ready = ld_acquire_gpu(p.l2_done) >= s_tile_off[p.E] * p.l2_ftiles;
+    } else {
+      ready = ld_acquire_gpu(p.norm_done + idx) >= 1 &&
+              ld_acquire_gpu(p.sh_done + idx) >= p.sh_target;
+    }
+    if (ready) break;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > p.timeout) {
+      *abort_flag = 1;
+      atomicOr(p.err, DEV_ERR_TIMEOUT);
+      return false;
+    }
+    __nanosleep(100);
+  }
+  fence_proxy_async_global();
+  return true;
 }
 
 // ------------------------------------------------------------------ producer (1 thread)
@@ -260,26 +294,22 @@ __device__ void run_producer(const GemmParams& p, Smem<BN>& sm, const int* s_til
       // claim the next unit now so the counter round trip overlaps this unit's copies
       if (info.task >= 0) u = atomicAdd(p.sched, 1);
     }
-    if (!mbar_wait(&sm.uempty[us], uphase ^ 1, sm.abort_flag, p.err, p.timeout)) break;
-    sm.ring[us] = info;
-    mbar_arrive(&sm.ufull[us]);
-    if (++us == C::US) { us = 0; uphase ^= 1; }
-    if (info.task < 0) break;
+    if (info.task < 0) {
+      if (mbar_wait(&sm.uempty[us], uphase ^ 1, sm.abort_flag, p.err, p.timeout)) {
+        sm.ring[us] = info;
+        mbar_arrive(&sm.ufull[us]);
+      }
+      break;
+    }
     const GemmTask& T = p.task[info.task];
     const bool pair = is_pair(T.kind);
     const int elems_per_kb = T.fp8 ? 128 : 64;
     const int step = (pair || !C::DUAL) ? 1 : 2;
-    for (int kb = info.kb0; kb < info.kb1; kb += step) {
-      if (p.stall_after > 0 && issued >= p.stall_after) { stalled = true; break; }
-      if (!mbar_wait(&sm.empty[stage], phase ^ 1, sm.abort_flag, p.err, p.timeout)) {
-        stalled = true;
-        break;
-      }
-      const int nsub = min(step, info.kb1 - kb);
-      uint8_t* st = sm.stages + stage * C::STAGE_BYTES;
-      const uint32_t bytes = pair ? 2 * C::A_BYTES + C::B_BYTES
-                                  : static_cast<uint32_t>(nsub) * (C::A_BYTES + C::B_BYTES);
-      mbar_arrive_expect_tx(&sm.full[stage], bytes);
+    auto stage_bytes = [&](int nsub) -> uint32_t {
+      return pair ? 2 * C::A_BYTES + C::B_BYTES
+                  : static_cast<uint32_t>(nsub) * (C::A_BYTES + C::B_BYTES);
+    };
+    auto issue_a = [&](int kb, int nsub, uint8_t* st, uint64_t* bar) {
       for (int sub = 0; sub < nsub; ++sub) {
         const int kbs = kb + sub;
         const int m = kbs < T.kb_split0 ? 0 : 1;
@@ -288,15 +318,63 @@ __device__ void run_producer(const GemmParams& p, Smem<BN>& sm, const int* s_til
         // (row block, kb), copied as is
         bulk_load(st + sub * C::A_BYTES,
                   T.a_ptr[m] + (static_cast<size_t>(info.arb) * T.a_kb[m] + kk) * C::A_BYTES,
-                  C::A_BYTES, &sm.full[stage], pol_w);
+                  C::A_BYTES, bar, pol_w);
         if (pair)
           bulk_load(st + C::A_BYTES,
                     T.a_ptr[m] + (static_cast<size_t>(info.arb + T.a_rb_up) * T.a_kb[m] + kk) *
                                      C::A_BYTES,
-                    C::A_BYTES, &sm.full[stage], pol_w);
-        tma_load_2d(st + 2 * C::A_BYTES + sub * C::B_BYTES, &T.tmB[m], &sm.full[stage],
-                    kk * elems_per_kb, info.row0, pol_t);
+                    C::A_BYTES, bar, pol_w);
       }
+    };
+    auto issue_b = [&](int kb, int nsub, uint8_t* st, uint64_t* bar) {
+      for (int sub = 0; sub < nsub; ++sub) {
+        const int kbs = kb + sub;
+        const int m = kbs < T.kb_split0 ? 0 : 1;
+        const int kk = m ? kbs - T.kb_split0 : kbs;
+        tma_load_2d(st + 2 * C::A_BYTES + sub * C::B_BYTES, &T.tmB[m], bar, kk * elems_per_kb,
+                    info.row0, pol_t);
+      }
+    };
+    int kb = info.kb0;
+    if (T.dep != DEP_NONE) {
+      // Stream the unit's weight tiles into the stages that are free now, then wait for
+      // the token operand's producers, then copy the token tiles of those stages.
+      int pre_kb[C::STAGES], pre_st[C::STAGES], npre = 0;
+      while (kb < info.kb1 && npre < C::STAGES) {
+        if (p.stall_after > 0 && issued >= p.stall_after) break;
+        if (!mbar_try_wait(&sm.empty[stage], phase ^ 1)) break;
+        const int nsub = min(step, info.kb1 - kb);
+        uint8_t* st = sm.stages + stage * C::STAGE_BYTES;
+        mbar_arrive_expect_tx(&sm.full[stage], stage_bytes(nsub));
+        issue_a(kb, nsub, st, &sm.full[stage]);
+        pre_kb[npre] = kb;
+        pre_st[npre] = stage;
+        ++npre;
+        trace_mark(p, 0, static_cast<int>(issued));
+        ++issued;
+        if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+        kb += step;
+      }
+      if (!wait_dependency(p, T.dep, info.dep_idx, s_tile_off, sm.abort_flag)) break;
+      for (int i = 0; i < npre; ++i)
+        issue_b(pre_kb[i], min(step, info.kb1 - pre_kb[i]), sm.stages + pre_st[i] * C::STAGE_BYTES,
+                &sm.full[pre_st[i]]);
+    }
+    if (!mbar_wait(&sm.uempty[us], uphase ^ 1, sm.abort_flag, p.err, p.timeout)) break;
+    sm.ring[us] = info;
+    mbar_arrive(&sm.ufull[us]);
+    if (++us == C::US) { us = 0; uphase ^= 1; }
+    for (; kb < info.kb1; kb += step) {
+      if (p.stall_after > 0 && issued >= p.stall_after) { stalled = true; break; }
+      if (!mbar_wait(&sm.empty[stage], phase ^ 1, sm.abort_flag, p.err, p.timeout)) {
+        stalled = true;
+        break;
+      }
+      const int nsub = min(step, info.kb1 - kb);
+      uint8_t* st = sm.stages + stage * C::STAGE_BYTES;
+      mbar_arrive_expect_tx(&sm.full[stage], stage_bytes(nsub));
+      issue_a(kb, nsub, st, &sm.full[stage]);
+      issue_b(kb, nsub, st, &sm.full[stage]);
       trace_mark(p, 0, static_cast<int>(issued));
       ++issued;
       if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
@@ -337,6 +415,7 @@ __device__ void run_mma(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_base) {
     if (++us == C::US) { us = 0; uphase ^= 1; }
     if (info.task < 0) break;
     const GemmTask& T = p.task[info.task];
+    if (T.kind == TASK_NORM) continue;  // no tensor-core work
     const bool pair = is_pair(T.kind);
     const int kpg = T.kpg;
     const bool promote = kpg > 0;
@@ -402,6 +481,16 @@ __device__ void run_mma(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_base) {
 }
 
 // ------------------------------------------------------------------ epilogue
+// Every epilogue thread has written its part of a unit's output; publish completion with
+// one release add (proxy fence first: the output is read later by TMA).
+__device__ __forceinline__ void signal_done(int* counter, int ew, int lane, int nthreads) {
+  fence_proxy_async_global();
+  __threadfence();
+  named_bar_sync(1, nthreads);
+  if (ew == 0 && lane == 0) red_release_gpu_add(counter, 1);
+}
+
+
 // One promotion batch of up to MAXNB groups (fewer when COLS is wide or the unit ends):
 // acc += partial * (weight block scale * token group scale), per group.  Returns the
 // number of groups consumed, 0 if a bounded wait expired.
@@ -500,6 +589,43 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
     const int kind = T.kind;
     const bool pair = is_pair(kind);
 
+    if (kind == TASK_NORM) {
+      // RMSNorm of token rows [row0, row0 + rows): fp32 statistic on the fp32 combine,
+      // gamma applied, rounded once to bf16 as the output GEMM's token operand.
+      const float4* gsrc = nullptr;
+      (void)gsrc;
+      for (int rr = ew; rr < info.rows; rr += C::EPI_WARPS) {
+        const size_t t = static_cast<size_t>(info.row0 + rr);
+        const float4* rv = reinterpret_cast<const float4*>(p.r + t * p.L);
+        float ss = 0.f;
+        for (int c = lane; c < p.L / 4; c += 32) {
+          const float4 v = __ldcg(rv + c);
+          ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+        const float inv = rsqrtf(ss / static_cast<float>(p.L) + p.eps);
+        const uint2* gg = reinterpret_cast<const uint2*>(p.gamma);
+        uint2* nn = reinterpret_cast<uint2*>(p.nrm + t * p.L);
+        for (int c = lane; c < p.L / 4; c += 32) {
+          const float4 v = __ldcg(rv + c);
+          const uint2 graw = __ldg(gg + c);
+          const __nv_bfloat162 g01 = *reinterpret_cast<const __nv_bfloat162*>(&graw.x);
+          const __nv_bfloat162 g23 = *reinterpret_cast<const __nv_bfloat162*>(&graw.y);
+          const __nv_bfloat162 o01 = __floats2bfloat162_rn(v.x * inv * __low2float(g01),
+                                                           v.y * inv * __high2float(g01));
+          const __nv_bfloat162 o23 = __floats2bfloat162_rn(v.z * inv * __low2float(g23),
+                                                           v.w * inv * __high2float(g23));
+          uint2 o;
+          o.x = *reinterpret_cast<const uint32_t*>(&o01);
+          o.y = *reinterpret_cast<const uint32_t*>(&o23);
+          nn[c] = o;
+        }
+      }
+      signal_done(p.norm_done + info.dep_idx, ew, lane, C::EPI_THREADS);
+      continue;
+    }
+
     float g[COLS], u[COLS];
 #pragma unroll
     for (int j = 0; j < COLS; ++j) { g[j] = 0.f; u[j] = 0.f; }
@@ -517,7 +643,7 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
       for (int i = etid; i < nkb * BN; i += C::EPI_THREADS) {
         const int kbi = i / BN, j = i - kbi * BN;
         sb[i] = j < info.rows
-                    ? __ldg(tok_scale + static_cast<size_t>(g0 + kbi) * p.cap + info.row0 + j)
+                    ? __ldcg(tok_scale + static_cast<size_t>(g0 + kbi) * p.cap + info.row0 + j)
                     : 0.f;
       }
       for (int kbi = etid; kbi < nkb; kbi += C::EPI_THREADS) {
@@ -626,6 +752,7 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
           dst[static_cast<size_t>(info.row0 + c0 + j) * p.Is] =
               __float2bfloat16_rn(silu_f(g[j]) * u[j]);
       }
+      if (p.sh_done != nullptr) signal_done(p.sh_done + info.dep_idx, ew, lane, C::EPI_THREADS);
     } else if (kind == TASK_OUT) {
       __nv_bfloat16* dst = p.out + static_cast<size_t>(info.ftile) * 128 + row;
 #pragma unroll
@@ -643,6 +770,7 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
           atomicAdd(p.r + static_cast<size_t>(tok) * p.L + col, wv * g[j]);
         }
       }
+      if (p.l2_done != nullptr) signal_done(p.l2_done, ew, lane, C::EPI_THREADS);
     } else {  // TASK_ROUTED_L1: SwiGLU, then e4m3 per 128 features of each token
       float* red = sm.red + ew * COLS;
 #pragma unroll
@@ -672,6 +800,7 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
         }
       }
       named_bar_sync(2 + half, 128);
+      if (p.l1_done != nullptr) signal_done(p.l1_done + info.dep_idx, ew, lane, C::EPI_THREADS);
     }
   }
 }

@@ -20,6 +20,8 @@ struct RouteParams {
   float* r;                // [M, L] zeroed here (the routed combine accumulates into it)
   int* sched;              // per-launch tile counters, zeroed here
   int nsched;
+  int* zero_buf;           // dependency counters of the fused launch, zeroed here
+  int zero_n;
   int M, E, k, L;
 };
 
@@ -57,7 +59,17 @@ enum TaskKind : int {
   TASK_ROUTED_L1 = 2,  // fp8 zq_perm . W13_e^T, pair, per-128-K promotion -> SwiGLU ->
                        // per-128 e4m3 quantisation -> aq, asT
   TASK_ROUTED_L2 = 3,  // fp8 aq . W2_e^T, promotion -> r[gidx] += w * y (fp32 atomics)
-  TASK_OUT = 4         // bf16 [n | a_s] . [W_up | Ws2]^T -> out (bf16, one rounding)
+  TASK_OUT = 4,        // bf16 [n | a_s] . [W_up | Ws2]^T -> out (bf16, one rounding)
+  TASK_NORM = 5        // RMSNorm of a token tile of r -> n (epilogue warps, no MMA)
+};
+
+// Dependency of a unit in the fused launch, checked by the producer before it publishes
+// the unit (and before it copies the token operand).
+enum DepKind : int {
+  DEP_NONE = 0,
+  DEP_L1_TILE = 1,   // routed L2 unit: all L1 units of its routed token tile are done
+  DEP_ALL_L2 = 2,    // norm unit: every routed L2 unit is done
+  DEP_OUT_TILE = 3   // output unit: norm and shared L1 of its token tile are done
 };
 
 struct GemmTask {
@@ -78,6 +90,7 @@ struct GemmTask {
   int a_kb[2];         // k-blocks per 128-row block of a_ptr[0], a_ptr[1]
   int ntiles;          // non-routed: token tiles
   int units;           // non-routed: ntiles * ftiles * ksplit
+  int dep;             // DepKind of this task's units
   int ws_tile_base;    // first arrival counter of this task (tile ids start here)
   long long ws_off;    // float offset of this task's partials in the workspace
   int streamk;         // 1: static stream-K partition of ntiles*ftiles*kb_total k-blocks
@@ -87,7 +100,7 @@ struct GemmTask {
 };
 
 struct GemmParams {
-  GemmTask task[2];
+  GemmTask task[5];
   int ntasks;
   int M;                       // tokens of this forward
   int E, L, I, Is, H, cap;     // cap = max_tokens * topk (rows of the permuted buffers)
@@ -110,6 +123,17 @@ struct GemmParams {
   int* err;                    // sticky device error word
   long long timeout;           // SM cycles per bounded wait
   int stall_after;             // test hook (0 = off)
+  // fused launch: dependency counters (zeroed by the routing kernel) and the norm step
+  int* l1_done;                // [routed tiles] L1 units done per routed token tile
+  int* l2_done;                // routed L2 units done
+  int* norm_done;              // [token tiles] norm units done
+  int* sh_done;                // [token tiles] shared L1 tiles finalised
+  int l1_target;               // L1 units per routed token tile (I/128)
+  int sh_target;               // shared L1 tiles per token tile (Is/128)
+  int l2_ftiles;               // routed L2 units per routed token tile (L/128)
+  const __nv_bfloat16* gamma;  // [L]
+  __nv_bfloat16* nrm;          // [max_tokens, L]
+  float eps;
   long long* trace;            // optional timestamp trace (this launch's region)
   int trace_n;                 // entries per (CTA, role)
 };

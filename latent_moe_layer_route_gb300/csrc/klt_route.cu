@@ -31,6 +31,9 @@ __global__ void __launch_bounds__(32 * ROUTE_WARPS)
   pdl_trigger();
   const int lane = lane_id();
   if (blockIdx.x == 0 && threadIdx.x < p.nsched) p.sched[threadIdx.x] = 0;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+       i < p.zero_n; i += static_cast<long long>(gridDim.x) * blockDim.x)
+    p.zero_buf[i] = 0;
   const int G = p.L / 128;
   const long long w = static_cast<long long>(blockIdx.x) * ROUTE_WARPS + (threadIdx.x >> 5);
   const int t = static_cast<int>(w / (G + 1));
