@@ -134,8 +134,8 @@ typedef struct klt_routing {
  *   timeout_ms: bound of every on-device wait for this call (0 = the default, 1000 ms);
  *   trace: optional device int64 buffer of 3 * trace_entries * 4 * (SM count) entries; when
  *     set, each GEMM launch g (0..2) records globaltimer stamps (ns) per CTA c and role r
- *     (0 = weight tile copy issued, 1 = tile consumed by the MMA issuer, 2 = epilogue step
- *     done, 3 = MMA issuer starts waiting for a tile) at
+ *     (0 = weight tile copy issued, 1 = work unit published to the MMA issuer and epilogue,
+ *     2 = epilogue step done, 3 = task index + 1 of that unit, not a time) at
  *     trace[((g * SMs + c) * 4 + r) * trace_entries + i], first trace_entries
  *     events each; unused entries are left untouched;
  *   force_bn: token-tile width of the GEMM stages for this call (16, 32, 64 or 128;

@@ -551,7 +551,7 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
     N.kb_total = 0;
     N.kb_per_split = 0;
     N.ntiles = ntiles;
-    N.units = ntiles;
+    N.units = M;  // one token row per norm unit
     N.tmB[0] = N.tmB[1] = h->tm_n[bi];
     gf.task[4] = g3.task[0];
     gf.task[4].dep = DEP_OUT_TILE;

@@ -173,6 +173,22 @@ __device__ UnitInfo decode_unit(const GemmParams& p, const int* s_tile_off, cons
       }
       u -= units;
     } else {
+      if (u < T.units && T.kind == TASK_NORM) {
+        info.task = ti;
+        info.e = 0;
+        info.row0 = u;
+        info.rows = 1;
+        info.ftile = 0;
+        info.arb = 0;
+        info.kb0 = info.kb1 = 0;
+        info.tile_id = 0;
+        info.split = 0;
+        info.ncontrib = 1;
+        info.cfirst = 0;
+        info.wslot = 0;
+        info.dep_idx = u / BN;
+        return info;
+      }
       if (u < T.units) {
         const int per_n = T.ftiles * T.ksplit;
         const int nt = u / per_n;
@@ -235,6 +251,7 @@ __device__ UnitInfo next_streamk_piece(const GemmParams& p, long long& x, long l
 // Bounded wait until the unit's inputs produced by other units of this launch are complete.
 // The acquire loads pair with the producers' release adds; the proxy fence orders the
 // acquired data before this thread's TMA reads of it.
+template <int BN>
 __device__ bool wait_dependency(const GemmParams& p, int dep, int idx, const int* s_tile_off,
                                 volatile int* abort_flag) {
   if (dep == DEP_NONE) return true;
@@ -246,7 +263,7 @@ __device__ bool wait_dependency(const GemmParams& p, int dep, int idx, const int
     } else if (dep == DEP_ALL_L2) {
       ready = ld_acquire_gpu(p.l2_done) >= s_tile_off[p.E] * p.l2_ftiles;
     } else {
-      ready = ld_acquire_gpu(p.norm_done + idx) >= 1 &&
+      ready = ld_acquire_gpu(p.norm_done + idx) >= min(BN, p.M - idx * BN) &&
               ld_acquire_gpu(p.sh_done + idx) >= p.sh_target;
     }
     if (ready) break;
@@ -272,6 +289,7 @@ __device__ void run_producer(const GemmParams& p, Smem<BN>& sm, const int* s_til
   int stage = 0, us = 0;
   uint32_t phase = 0, uphase = 0;
   long long issued = 0;
+  int published = 0;
   int dummy_abort = 0;
   bool stalled = false;
   const bool streamk = p.task[0].streamk != 0;
@@ -355,7 +373,7 @@ __device__ void run_producer(const GemmParams& p, Smem<BN>& sm, const int* s_til
         if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         kb += step;
       }
-      if (!wait_dependency(p, T.dep, info.dep_idx, s_tile_off, sm.abort_flag)) break;
+      if (!wait_dependency<BN>(p, T.dep, info.dep_idx, s_tile_off, sm.abort_flag)) break;
       for (int i = 0; i < npre; ++i)
         issue_b(pre_kb[i], min(step, info.kb1 - pre_kb[i]), sm.stages + pre_st[i] * C::STAGE_BYTES,
                 &sm.full[pre_st[i]]);
@@ -364,6 +382,12 @@ __device__ void run_producer(const GemmParams& p, Smem<BN>& sm, const int* s_til
     sm.ring[us] = info;
     mbar_arrive(&sm.ufull[us]);
     if (++us == C::US) { us = 0; uphase ^= 1; }
+    if (p.trace != nullptr && published < p.trace_n) {  // unit publish time and task
+      p.trace[(static_cast<long long>(blockIdx.x) * 4 + 1) * p.trace_n + published] = global_ns();
+      p.trace[(static_cast<long long>(blockIdx.x) * 4 + 3) * p.trace_n + published] =
+          info.task + 1;
+    }
+    ++published;
     for (; kb < info.kb1; kb += step) {
       if (p.stall_after > 0 && issued >= p.stall_after) { stalled = true; break; }
       if (!mbar_wait(&sm.empty[stage], phase ^ 1, sm.abort_flag, p.err, p.timeout)) {
@@ -482,9 +506,8 @@ __device__ void run_mma(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_base) {
 
 // ------------------------------------------------------------------ epilogue
 // Every epilogue thread has written its part of a unit's output; publish completion with
-// one release add (proxy fence first: the output is read later by TMA).
+// one release add (the consumer orders its later TMA reads with a proxy fence).
 __device__ __forceinline__ void signal_done(int* counter, int ew, int lane, int nthreads) {
-  fence_proxy_async_global();
   __threadfence();
   named_bar_sync(1, nthreads);
   if (ew == 0 && lane == 0) red_release_gpu_add(counter, 1);
@@ -590,38 +613,58 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
     const bool pair = is_pair(kind);
 
     if (kind == TASK_NORM) {
-      // RMSNorm of token rows [row0, row0 + rows): fp32 statistic on the fp32 combine,
-      // gamma applied, rounded once to bf16 as the output GEMM's token operand.
-      const float4* gsrc = nullptr;
-      (void)gsrc;
-      for (int rr = ew; rr < info.rows; rr += C::EPI_WARPS) {
-        const size_t t = static_cast<size_t>(info.row0 + rr);
-        const float4* rv = reinterpret_cast<const float4*>(p.r + t * p.L);
-        float ss = 0.f;
-        for (int c = lane; c < p.L / 4; c += 32) {
-          const float4 v = __ldcg(rv + c);
-          ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-        }
+      // RMSNorm of one token row (unit rows = 1): fp32 statistic on the fp32 combine,
+      // gamma applied, rounded once to bf16 as the output GEMM's token operand.  The
+      // epilogue threads split the row; each loads its float4s before using them.
+      const size_t t = static_cast<size_t>(info.row0);
+      const float4* rv = reinterpret_cast<const float4*>(p.r + t * p.L);
+      const int etid = threadIdx.x - 64;
+      const int n4 = p.L / 4;
+      constexpr int PER = 8;  // float4s per thread held in registers (L <= 4096 * ... )
+      float4 v[PER];
+      float ss = 0.f;
 #pragma unroll
-        for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
-        const float inv = rsqrtf(ss / static_cast<float>(p.L) + p.eps);
-        const uint2* gg = reinterpret_cast<const uint2*>(p.gamma);
-        uint2* nn = reinterpret_cast<uint2*>(p.nrm + t * p.L);
-        for (int c = lane; c < p.L / 4; c += 32) {
-          const float4 v = __ldcg(rv + c);
-          const uint2 graw = __ldg(gg + c);
-          const __nv_bfloat162 g01 = *reinterpret_cast<const __nv_bfloat162*>(&graw.x);
-          const __nv_bfloat162 g23 = *reinterpret_cast<const __nv_bfloat162*>(&graw.y);
-          const __nv_bfloat162 o01 = __floats2bfloat162_rn(v.x * inv * __low2float(g01),
-                                                           v.y * inv * __high2float(g01));
-          const __nv_bfloat162 o23 = __floats2bfloat162_rn(v.z * inv * __low2float(g23),
-                                                           v.w * inv * __high2float(g23));
-          uint2 o;
-          o.x = *reinterpret_cast<const uint32_t*>(&o01);
-          o.y = *reinterpret_cast<const uint32_t*>(&o23);
-          nn[c] = o;
-        }
+      for (int i = 0; i < PER; ++i) {
+        const int c = etid + i * C::EPI_THREADS;
+        v[i] = c < n4 ? __ldcg(rv + c) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
+#pragma unroll
+      for (int i = 0; i < PER; ++i) ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z +
+                                         v[i].w * v[i].w;
+      for (int c = etid + PER * C::EPI_THREADS; c < n4; c += C::EPI_THREADS) {  // wide rows
+        const float4 w = __ldcg(rv + c);
+        ss += w.x * w.x + w.y * w.y + w.z * w.z + w.w * w.w;
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+      if (lane == 0) sm.red[ew] = ss;
+      named_bar_sync(1, C::EPI_THREADS);
+      float tot = 0.f;
+      for (int w = 0; w < C::EPI_WARPS; ++w) tot += sm.red[w];
+      const float inv = rsqrtf(tot / static_cast<float>(p.L) + p.eps);
+      const uint2* gg = reinterpret_cast<const uint2*>(p.gamma);
+      uint2* nn = reinterpret_cast<uint2*>(p.nrm + t * p.L);
+      auto emit = [&](int c, const float4& x) {
+        const uint2 graw = __ldg(gg + c);
+        const __nv_bfloat162 g01 = *reinterpret_cast<const __nv_bfloat162*>(&graw.x);
+        const __nv_bfloat162 g23 = *reinterpret_cast<const __nv_bfloat162*>(&graw.y);
+        const __nv_bfloat162 o01 = __floats2bfloat162_rn(x.x * inv * __low2float(g01),
+                                                         x.y * inv * __high2float(g01));
+        const __nv_bfloat162 o23 = __floats2bfloat162_rn(x.z * inv * __low2float(g23),
+                                                         x.w * inv * __high2float(g23));
+        uint2 o;
+        o.x = *reinterpret_cast<const uint32_t*>(&o01);
+        o.y = *reinterpret_cast<const uint32_t*>(&o23);
+        nn[c] = o;
+      };
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        const int c = etid + i * C::EPI_THREADS;
+        if (c < n4) emit(c, v[i]);
+      }
+      for (int c = etid + PER * C::EPI_THREADS; c < n4; c += C::EPI_THREADS)
+        emit(c, __ldcg(rv + c));
+      named_bar_sync(1, C::EPI_THREADS);  // sm.red is reused by the next unit
       signal_done(p.norm_done + info.dep_idx, ew, lane, C::EPI_THREADS);
       continue;
     }
