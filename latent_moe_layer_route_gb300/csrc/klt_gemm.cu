@@ -505,10 +505,10 @@ __device__ void run_mma(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_base) {
 }
 
 // ------------------------------------------------------------------ epilogue
-// Every epilogue thread has written its part of a unit's output; publish completion with
-// one release add (the consumer orders its later TMA reads with a proxy fence).
+// Every epilogue thread has written its part of a unit's output; after the CTA barrier one
+// gpu-scope release add publishes all of them (release is cumulative over the barrier; the
+// consumer acquires and orders its later TMA reads with a proxy fence).
 __device__ __forceinline__ void signal_done(int* counter, int ew, int lane, int nthreads) {
-  __threadfence();
   named_bar_sync(1, nthreads);
   if (ew == 0 && lane == 0) red_release_gpu_add(counter, 1);
 }
