@@ -99,6 +99,31 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the dominant
+# kernel, from one ncu capture of `bench.py --steps 2 --warmup 3 --no-cpu-baseline` on the
+# workload, valid only while the kernel sources hash to the recorded digest.
+NCU_TRAFFIC = {
+    ("decode_m16_e64_k8_fp8", "gemm_fused"): (718447872, "4d5da6fe7530ee8a"),
+}
+KERNEL_SOURCES = ("klt_gemm.cu", "klt_device.cuh", "klt_internal.h", "klt_api.cu")
+
+
+def kernel_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "latent_moe_layer_route_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, kernel: str):
+    rec = NCU_TRAFFIC.get((workload, kernel))
+    if rec is None or rec[1] != kernel_digest():
+        return None
+    return rec[0]
+
+
 def algorithmic_bytes(cfg, cnt: np.ndarray, M: int):
     """Bytes each launch must move at least once (weights of touched experts, token
     inputs, stage outputs), per the tail's data flow."""
@@ -158,9 +183,12 @@ def run_reference(cfg, args, ws, rank):
 
 
 def cpu_baseline(cfg, act, w):
+    """The oracle as it stands on the first (at most 16) tokens of the workload, repeated
+    for about 10 s; the routing and permutation still cover the whole batch."""
     from oracle import model as oracle_model
     cores = len(os.sched_getaffinity(0))
-    tok = np.arange(cfg.M)
+    sample = min(cfg.M, 16)
+    tok = np.arange(sample)
     t0 = time.perf_counter()
     n = 0
     while True:
@@ -169,8 +197,8 @@ def cpu_baseline(cfg, act, w):
         if time.perf_counter() - t0 > 10.0 or n >= 5:
             break
     dt = time.perf_counter() - t0
-    return {"value": cfg.M * n / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{n} full step(s) of all {cfg.M} tokens, {dt:.1f} s"}
+    return {"value": sample * n / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} step(s) of the first {sample} of {cfg.M} tokens, {dt:.1f} s"}
 
 
 def main():
@@ -325,10 +353,28 @@ def main():
     else:
         dom = max(("gemm_l1", "gemm_l2", "gemm_out"), key=lambda n: per_launch_us[n])
         dom_bytes = ab[dom]
-    achieved = dom_bytes / (per_launch_us[dom] * 1e-6) / 1e9
     routed_f, dense_f = flops(cfg, M)
-    roof_time_us = max(ab["total"] / (HBM_NOMINAL_GBS * 1e9),
-                       routed_f / (2 * bf16_tf * 1e12) + dense_f / (bf16_tf * 1e12)) * 1e6
+    # fp8 routed contractions run at twice the bf16 rate (the nominal fp8:bf16 ratio applied
+    # to the measured bf16 peak); the fused launch's mixed peak follows from the flop mix
+    t_tensor = routed_f / (2 * bf16_tf * 1e12) + dense_f / (bf16_tf * 1e12)
+    dom_s = per_launch_us[dom] * 1e-6
+    traffic = recorded_traffic(cfg.name, dom)
+    if t_tensor > dom_bytes / (hbm * 1e9):
+        mixed_peak = (routed_f + dense_f) / t_tensor / 1e12
+        achieved = (routed_f + dense_f) / dom_s / 1e12
+        roof = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1),
+                "peak": round(mixed_peak, 1), "unit": "TFLOP/s",
+                "frac": round(achieved / mixed_peak, 4),
+                "peak_source": f"{peak_src} bf16 burst, fp8 share at 2x",
+                "traffic": traffic, "algorithmic_flops": routed_f + dense_f,
+                "algorithmic_bytes": int(dom_bytes)}
+    else:
+        achieved = dom_bytes / dom_s / 1e9
+        roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm,
+                "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                "peak_source": f"{peak_src} copy bandwidth", "traffic": traffic,
+                "algorithmic_bytes": int(dom_bytes)}
+    roof_time_us = max(ab["total"] / (HBM_NOMINAL_GBS * 1e9), t_tensor) * 1e6
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
@@ -341,10 +387,7 @@ def main():
                    "l2": "flushed (512 MB write) before every timed step",
                    "schedule": "phased" if args.phased else "fused",
                    "parallelism": f"replicas x{ws}"},
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
-                     "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                     "peak_source": peak_src, "traffic": None,
-                     "algorithmic_bytes": int(dom_bytes)},
+        "roofline": roof,
         "step_roofline": {"algorithmic_bytes": int(ab["total"]),
                           "touched_experts": ab["touched_experts"],
                           "roofline_us_at_8TBps": round(roof_time_us, 2),
