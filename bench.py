@@ -212,7 +212,8 @@ def main():
     ap.add_argument("--phased", action="store_true",
                     help="one launch per GEMM stage instead of the fused persistent launch")
     ap.add_argument("--tile-n", type=int, default=0,
-                    help="token-tile width of the GEMM stages (0 = library choice)")
+                    help="GEMM engine / token-tile width: 16..128 feature-major, 256 "
+                         "token-major (0 = library choice)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 

@@ -138,8 +138,11 @@ typedef struct klt_routing {
  *     2 = epilogue step done, 3 = task index + 1 of that unit, not a time) at
  *     trace[((g * SMs + c) * 4 + r) * trace_entries + i], first trace_entries
  *     events each; unused entries are left untouched;
- *   force_bn: token-tile width of the GEMM stages for this call (16, 32, 64 or 128;
- *     0 = chosen from M), for tuning sweeps. */
+ *   force_bn: GEMM engine and token-tile width for this call, for tuning sweeps:
+ *     16, 32, 64 or 128 = feature-major engine (128 weight rows x force_bn tokens per
+ *     MMA); 256 = token-major engine (128 tokens x 256 features per MMA; needs H and L
+ *     multiples of 256 and the fused schedule, else KLT_ERR_UNSUPPORTED); 0 = chosen
+ *     from M (token-major from 1024 tokens on when available). */
 typedef struct klt_debug {
   uint8_t* zq;
   float* zs;
@@ -191,6 +194,13 @@ const char* klt_strerror(int code);
 
 /* Number of kernels one klt_forward launches for the given M and handle (0 for M == 0). */
 int klt_launch_count(const klt_handle* h, int32_t M);
+
+/* GEMM configuration klt_forward uses for M tokens when klt_debug.force_bn = force_bn
+ * (0 = automatic): 16, 32, 64 or 128 = the feature-major engine with that token tile,
+ * 256 = the token-major engine (128-token x 256-feature units).  A negative value is the
+ * negated status klt_forward would return: -KLT_ERR_UNSUPPORTED when force_bn = 256 is not
+ * available for this handle, -KLT_ERR_INVALID_ARG for a NULL handle. */
+int klt_gemm_tile(const klt_handle* h, int32_t M, int32_t force_bn);
 
 /* Largest M * topk klt_route_noalloc accepts (its fixed scratch size, about 320 KB). */
 #define KLT_NOALLOC_MAX_PAIRS 65536

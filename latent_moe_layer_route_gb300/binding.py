@@ -27,7 +27,7 @@ KLT_FLAG_NO_PDL = 1
 KLT_FLAG_PHASED = 2
 
 EXPORTS = ("klt_create", "klt_forward", "klt_status", "klt_destroy", "klt_strerror",
-           "klt_launch_count", "klt_route_noalloc")
+           "klt_launch_count", "klt_gemm_tile", "klt_route_noalloc")
 
 
 class KltDims(ctypes.Structure):
@@ -91,6 +91,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.klt_strerror.restype = ctypes.c_char_p
     lib.klt_launch_count.argtypes = [ctypes.c_void_p, ctypes.c_int32]
     lib.klt_launch_count.restype = ctypes.c_int
+    lib.klt_gemm_tile.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32]
+    lib.klt_gemm_tile.restype = ctypes.c_int
     lib.klt_route_noalloc.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                       ctypes.c_int32] + [ctypes.c_void_p] * 8
     lib.klt_route_noalloc.restype = ctypes.c_int
@@ -153,6 +155,10 @@ def klt_launch_count(h, M: int) -> int:
     return load_library().klt_launch_count(h, M)
 
 
+def klt_gemm_tile(h, M: int, force_bn: int = 0) -> int:
+    return load_library().klt_gemm_tile(h, M, force_bn)
+
+
 def klt_route_noalloc(logits, topk: int, ids, weights, cnt, off, gidx, slot, pos,
                       stream: Optional[int] = None) -> int:
     """Routing + permutation with no device allocation (fixed internal scratch); tensors
@@ -191,6 +197,10 @@ class LatentMoETail:
 
     def launch_count(self, M: int) -> int:
         return klt_launch_count(self.handle, M)
+
+    def gemm_tile(self, M: int, force_bn: int = 0) -> int:
+        """256 for the token-major engine, else the feature-major engine's token tile."""
+        return klt_gemm_tile(self.handle, M, force_bn)
 
     def close(self):
         if self.handle is not None and self.handle.value:

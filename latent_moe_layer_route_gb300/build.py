@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG_DIR)
 CSRC = os.path.join(PKG_DIR, "csrc")
 OUT_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libklt.so")
-SOURCES = ["klt_api.cu", "klt_route.cu", "klt_gemm.cu", "klt_noalloc.cu"]
+SOURCES = ["klt_api.cu", "klt_route.cu", "klt_gemm.cu", "klt_wide.cu", "klt_noalloc.cu"]
 HEADERS = ["klt_device.cuh", "klt_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

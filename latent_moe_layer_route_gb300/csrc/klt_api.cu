@@ -63,6 +63,7 @@ constexpr int kNumBN = 4;
 constexpr int kBN[kNumBN] = {16, 32, 64, 128};
 constexpr int kMaxSplitUnits = 3 * 160;  // split-K tiles*splits bound per task
 constexpr int kMaxCounters = 8192;       // arrival counters per split launch
+constexpr int kWideMinTokens = 1024;  // token-major engine from this batch size on
 constexpr int kRoutedSplitPairs = 0;  // routed L1 k-splits when M * topk <= this (off: the
                                       // split reduce outweighs the balance it buys)
 
@@ -86,6 +87,7 @@ struct klt_handle {
   int* dep_cnt;  // fused-launch dependency counters [routed tiles | l2 | norm tiles | shared]
   int dep_routed, dep_ntiles;
   int cap, max_hist_blocks;
+  bool wide_ok;  // token-major engine usable (dims and launch register count)
   long long ws_routed_floats;
   // descriptors per BN variant (token-side maps depend on the box height)
   CUtensorMap tm_zqp[kNumBN], tm_aq[kNumBN], tm_n[kNumBN], tm_as[kNumBN];
@@ -307,6 +309,7 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
     delete h;
     return KLT_ERR_CUDA;
   }
+  h->wide_ok = L % 256 == 0 && H % 256 == 0 && wide_regs_ok(wide_kernel_regs());
   *out = h;
   return KLT_OK;
 }
@@ -316,6 +319,14 @@ int klt_launch_count(const klt_handle* h, int32_t M) {
   const int nblocks = (M * h->d.topk + PERM_BLOCK - 1) / PERM_BLOCK;
   const int gemm_launches = (h->flags & KLT_FLAG_PHASED) ? 4 : 1;  // phased: 3 GEMMs + norm
   return 3 + gemm_launches + (nblocks > 1 ? 1 : 0);
+}
+
+int klt_gemm_tile(const klt_handle* h, int32_t M, int32_t force_bn) {
+  if (!h) return -KLT_ERR_INVALID_ARG;
+  const bool phased = (h->flags & KLT_FLAG_PHASED) != 0;
+  if (force_bn == 256) return h->wide_ok && !phased ? 256 : -KLT_ERR_UNSUPPORTED;
+  if (force_bn == 0 && h->wide_ok && !phased && M >= kWideMinTokens) return 256;
+  return kBN[bn_index(M, force_bn)];
 }
 
 int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits, int32_t M,
@@ -330,7 +341,11 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
   const bool pdl = !(h->flags & KLT_FLAG_NO_PDL);
   const klt_dims& d = h->d;
   const int E = d.E, k = d.topk, L = d.L, I = d.I, Is = d.Is, H = d.H;
-  const int bi = bn_index(M, dbg ? dbg->force_bn : 0);
+  const bool phased = (h->flags & KLT_FLAG_PHASED) != 0;
+  const int tile = klt_gemm_tile(h, M, dbg ? dbg->force_bn : 0);
+  if (tile < 0) return -tile;
+  const bool wide = tile == 256;
+  const int bi = wide ? kNumBN - 1 : bn_index(M, tile);
   const int BN = kBN[bi];
   const bool nvfp4 = d.routed_fmt == KLT_FMT_NVFP4;
   const int rkb = nvfp4 ? 64 : 128;  // routed K elements per k-block
@@ -391,7 +406,7 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
   pp.k = k;
   pp.L = L;
   pp.cap = h->cap;
-  pp.bn = BN;
+  pp.bn = BN;  // routed tile list in BN-token tiles (128 for the token-major engine)
   pp.nblocks = nblocks;
   if (nblocks > 1) KLT_LAUNCH(launch_perm_hist(pp, s, pdl));
   KLT_LAUNCH(launch_perm_scatter(pp, s, pdl));
@@ -432,12 +447,16 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
   const int grid = h->num_sms;
   const size_t ws_task = static_cast<size_t>(kMaxSplitUnits) * 2 * 128 * 128;
 
-  const bool fused = !(h->flags & KLT_FLAG_PHASED);
-  GemmParams g1 = gp, g2 = gp, g3 = gp;
-  // ---- GEMM 1: shared L1 (bf16, split-K) + routed L1 (fp8, SwiGLU + act quant)
-  {
-    // Routed units first, then the shared expert in small k-splits that fill the tail.
-    GemmTask& R = g1.task[0];
+  const bool fused = !phased;
+  if (wide) {
+    // Token-major engine: 128-token tiles, 256 features per unit, the five tasks of the
+    // fused launch with the same dependency counters.
+    GemmParams gw = gp;
+    gw.ntasks = 5;
+    gw.sched = h->sched + 3;
+    gw.stall_after = dbg ? dbg->stall_after_kblocks : 0;
+    gw.trace = trace;
+    GemmTask& R = gw.task[0];  // routed L1: gate and up row blocks of one 128-output tile
     R.kind = TASK_ROUTED_L1;
     R.fp8 = !nvfp4;
     R.kpg = nvfp4 ? 2 : 1;
@@ -445,151 +464,237 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
     R.ftiles = I / 128;
     R.kb_total = L / rkb;
     R.kb_split0 = R.kb_total;
-    // decode sizes: two k-splits per routed tile so the units are small enough to balance
-    const long long routed_tiles_max = static_cast<long long>((Mk + BN - 1) / BN + E) * R.ftiles;
-    R.ksplit = (Mk <= kRoutedSplitPairs && R.kb_total >= 8 &&
-                routed_tiles_max + kMaxSplitUnits <= kMaxCounters)
-                   ? 2 : 1;
-    R.kb_per_split = (R.kb_total + R.ksplit - 1) / R.ksplit;
-    if (R.kpg > 1) R.kb_per_split = (R.kb_per_split + R.kpg - 1) / R.kpg * R.kpg;
-    R.ksplit = (R.kb_total + R.kb_per_split - 1) / R.kb_per_split;
+    R.ksplit = 1;
+    R.kb_per_split = R.kb_total;
     R.a_rb_up = I / 128;
     R.a_rb_expert = 2 * I / 128;
     R.a_kb[0] = R.a_kb[1] = L / rkb;
     R.a_ptr[0] = R.a_ptr[1] = h->w13;
-    R.tmB[0] = h->tm_zqp[bi];
-    R.tmB[1] = h->tm_zqp[bi];
-    GemmTask& S = g1.task[1];
+    R.tmB[0] = R.tmB[1] = h->tm_zqp[bi];
+    GemmTask& S = gw.task[1];  // shared L1 (bf16)
     S.kind = TASK_SHARED_L1;
-    S.routed = 0;
     S.ftiles = Is / 128;
     S.kb_total = H / 64;
     S.kb_split0 = S.kb_total;
+    S.ksplit = 1;
+    S.kb_per_split = S.kb_total;
     S.a_rb_up = Is / 128;
     S.a_kb[0] = S.a_kb[1] = H / 64;
-    S.ws_tile_base = 0;
-    S.ws_off = 0;
-    plan_split(S, ntiles, ntiles * S.ftiles * std::max(1, S.kb_total / 8), BN);
-    // routed partials and counters follow the shared ones
-    R.ws_tile_base = S.ntiles * S.ftiles;
-    R.ws_off = static_cast<long long>(kMaxSplitUnits) * 2 * 128 * 128;
+    S.a_ptr[0] = S.a_ptr[1] = reinterpret_cast<const uint8_t*>(h->ws13);
+    S.ntiles = ntiles;
+    S.units = ntiles * S.ftiles;
     if (!encode_2d(&S.tmB[0], x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, H, BN))
       return KLT_ERR_CUDA;
-    S.a_ptr[0] = S.a_ptr[1] = reinterpret_cast<const uint8_t*>(h->ws13);
     S.tmB[1] = S.tmB[0];
-  }
-  // ---- GEMM 2: routed L2 with the top-k weighted scatter-combine into r
-  {
-    GemmTask& R = g2.task[0];
-    R.kind = TASK_ROUTED_L2;
-    R.fp8 = !nvfp4;
-    R.kpg = nvfp4 ? 2 : 1;
-    R.routed = 1;
-    R.ftiles = L / 128;
-    R.kb_total = I / rkb;
-    R.kb_split0 = R.kb_total;
-    R.ksplit = 1;
-    R.kb_per_split = R.kb_total;
-    R.a_rb_expert = L / 128;
-    R.a_kb[0] = R.a_kb[1] = I / rkb;
-    R.a_ptr[0] = R.a_ptr[1] = h->w2;
-    R.tmB[0] = h->tm_aq[bi];
-    R.tmB[1] = h->tm_aq[bi];
-  }
-  // ---- GEMM 3: out = bf16([n | a_s] . [W_up | Ws2]^T)
-  {
-    GemmTask& O = g3.task[0];
+    GemmTask& R2 = gw.task[2];  // routed L2 + combine: two row blocks of W2 per unit
+    R2.kind = TASK_ROUTED_L2;
+    R2.fp8 = !nvfp4;
+    R2.kpg = nvfp4 ? 2 : 1;
+    R2.routed = 1;
+    R2.ftiles = L / 256;
+    R2.kb_total = I / rkb;
+    R2.kb_split0 = R2.kb_total;
+    R2.ksplit = 1;
+    R2.kb_per_split = R2.kb_total;
+    R2.a_rb_expert = L / 128;
+    R2.a_kb[0] = R2.a_kb[1] = I / rkb;
+    R2.a_ptr[0] = R2.a_ptr[1] = h->w2;
+    R2.tmB[0] = R2.tmB[1] = h->tm_aq[bi];
+    R2.dep = DEP_L1_TILE;
+    GemmTask& N = gw.task[3];  // RMSNorm, one token row per unit
+    N.kind = TASK_NORM;
+    N.dep = DEP_ALL_L2;
+    N.ftiles = 1;
+    N.ksplit = 1;
+    N.ntiles = ntiles;
+    N.units = M;
+    N.tmB[0] = N.tmB[1] = h->tm_n[bi];
+    GemmTask& O = gw.task[4];  // out = bf16([n | a_s] . [W_up | Ws2]^T), 256 outputs per unit
     O.kind = TASK_OUT;
-    O.routed = 0;
-    O.ftiles = H / 128;
+    O.ftiles = H / 256;
     O.kb_total = L / 64 + Is / 64;
     O.kb_split0 = L / 64;
-    O.ws_tile_base = 0;
     O.a_kb[0] = L / 64;
     O.a_kb[1] = Is / 64;
     O.ksplit = 1;
     O.kb_per_split = O.kb_total;
     O.ntiles = ntiles;
     O.units = ntiles * O.ftiles;
-    if (fused) {
-      // units come from the launch-wide counter, after the other tasks' units
-      O.ws_tile_base = kMaxCounters;
-      O.ws_off = static_cast<long long>(ws_task) + h->ws_routed_floats;
-      plan_split(O, ntiles, 2 * grid, BN);
-    } else if (O.units < 4 * grid) {
-      // static stream-K: every CTA streams the same number of k-blocks (no more CTAs than
-      // k-blocks, so every CTA's range is non-empty)
-      O.streamk = 1;
-      O.sk_total = static_cast<long long>(O.units) * O.kb_total;
-      O.sk_grid = static_cast<int>(std::min<long long>(grid, O.sk_total));
-    }
+    O.dep = DEP_OUT_TILE;
     O.a_ptr[0] = reinterpret_cast<const uint8_t*>(h->w_up);
     O.a_ptr[1] = reinterpret_cast<const uint8_t*>(h->ws2);
     O.tmB[0] = h->tm_n[bi];
     O.tmB[1] = h->tm_as[bi];
-  }
-  if (fused) {
-    // One persistent launch: routed L1 and shared L1, routed L2 (after its token tile's L1
-    // units), the RMSNorm (after every L2 unit) and the output GEMM (after its tile's norm
-    // and shared L1), ordered so that every unit depends only on earlier units.
-    GemmParams gf = gp;
-    gf.ntasks = 5;
-    gf.sched = h->sched + 3;
-    gf.stall_after = dbg ? dbg->stall_after_kblocks : 0;
-    gf.trace = trace;
-    gf.cnt = h->split_cnt;
-    gf.task[0] = g1.task[0];
-    gf.task[1] = g1.task[1];
-    gf.task[2] = g2.task[0];
-    gf.task[2].dep = DEP_L1_TILE;
-    GemmTask& N = gf.task[3];
-    N.kind = TASK_NORM;
-    N.dep = DEP_ALL_L2;
-    N.routed = 0;
-    N.ftiles = 1;
-    N.ksplit = 1;
-    N.kb_total = 0;
-    N.kb_per_split = 0;
-    N.ntiles = ntiles;
-    N.units = M;  // one token row per norm unit
-    N.tmB[0] = N.tmB[1] = h->tm_n[bi];
-    gf.task[4] = g3.task[0];
-    gf.task[4].dep = DEP_OUT_TILE;
-    gf.l1_done = h->dep_cnt;
-    gf.l2_done = h->dep_cnt + h->dep_routed;
-    gf.norm_done = gf.l2_done + 1;
-    gf.sh_done = gf.norm_done + h->dep_ntiles;
-    gf.l1_target = I / 128;
-    gf.sh_target = Is / 128;
-    gf.l2_ftiles = L / 128;
-    gf.gamma = h->gamma;
-    gf.nrm = h->n;
-    gf.eps = d.eps;
-    KLT_LAUNCH(launch_gemm(gf, BN, grid, s, pdl));
+    gw.l1_done = h->dep_cnt;
+    gw.l2_done = h->dep_cnt + h->dep_routed;
+    gw.norm_done = gw.l2_done + 1;
+    gw.sh_done = gw.norm_done + h->dep_ntiles;
+    gw.l1_target = I / 128;
+    gw.sh_target = Is / 128;
+    gw.l2_ftiles = L / 256;
+    gw.gamma = h->gamma;
+    gw.nrm = h->n;
+    gw.eps = d.eps;
+    KLT_LAUNCH(launch_wide(gw, grid, s, pdl));
   } else {
-    g1.ntasks = 2;
-    g1.sched = h->sched + 0;
-    g1.stall_after = dbg ? dbg->stall_after_kblocks : 0;
-    g1.trace = trace;
-    KLT_LAUNCH(launch_gemm(g1, BN, grid, s, pdl));
-    g2.ntasks = 1;
-    g2.sched = h->sched + 1;
-    g2.trace = trace ? trace + trace_launch : nullptr;
-    KLT_LAUNCH(launch_gemm(g2, BN, grid, s, pdl));
-    NormParams np;
-    np.r = h->r;
-    np.gamma = h->gamma;
-    np.n = h->n;
-    np.M = M;
-    np.L = L;
-    np.eps = d.eps;
-    KLT_LAUNCH(launch_norm(np, s, pdl));
-    g3.ntasks = 1;
-    g3.sched = h->sched + 2;
-    g3.trace = trace ? trace + 2 * trace_launch : nullptr;
-    g3.ws = h->ws + ws_task + h->ws_routed_floats;
-    g3.cnt = h->split_cnt + kMaxCounters;
-    KLT_LAUNCH(launch_gemm(g3, BN, grid, s, pdl));
+    GemmParams g1 = gp, g2 = gp, g3 = gp;
+    // ---- GEMM 1: shared L1 (bf16, split-K) + routed L1 (fp8, SwiGLU + act quant)
+    {
+      // Routed units first, then the shared expert in small k-splits that fill the tail.
+      GemmTask& R = g1.task[0];
+      R.kind = TASK_ROUTED_L1;
+      R.fp8 = !nvfp4;
+      R.kpg = nvfp4 ? 2 : 1;
+      R.routed = 1;
+      R.ftiles = I / 128;
+      R.kb_total = L / rkb;
+      R.kb_split0 = R.kb_total;
+      // decode sizes: two k-splits per routed tile so the units are small enough to balance
+      const long long routed_tiles_max = static_cast<long long>((Mk + BN - 1) / BN + E) * R.ftiles;
+      R.ksplit = (Mk <= kRoutedSplitPairs && R.kb_total >= 8 &&
+                  routed_tiles_max + kMaxSplitUnits <= kMaxCounters)
+                     ? 2 : 1;
+      R.kb_per_split = (R.kb_total + R.ksplit - 1) / R.ksplit;
+      if (R.kpg > 1) R.kb_per_split = (R.kb_per_split + R.kpg - 1) / R.kpg * R.kpg;
+      R.ksplit = (R.kb_total + R.kb_per_split - 1) / R.kb_per_split;
+      R.a_rb_up = I / 128;
+      R.a_rb_expert = 2 * I / 128;
+      R.a_kb[0] = R.a_kb[1] = L / rkb;
+      R.a_ptr[0] = R.a_ptr[1] = h->w13;
+      R.tmB[0] = h->tm_zqp[bi];
+      R.tmB[1] = h->tm_zqp[bi];
+      GemmTask& S = g1.task[1];
+      S.kind = TASK_SHARED_L1;
+      S.routed = 0;
+      S.ftiles = Is / 128;
+      S.kb_total = H / 64;
+      S.kb_split0 = S.kb_total;
+      S.a_rb_up = Is / 128;
+      S.a_kb[0] = S.a_kb[1] = H / 64;
+      S.ws_tile_base = 0;
+      S.ws_off = 0;
+      plan_split(S, ntiles, ntiles * S.ftiles * std::max(1, S.kb_total / 8), BN);
+      // routed partials and counters follow the shared ones
+      R.ws_tile_base = S.ntiles * S.ftiles;
+      R.ws_off = static_cast<long long>(kMaxSplitUnits) * 2 * 128 * 128;
+      if (!encode_2d(&S.tmB[0], x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, H, BN))
+        return KLT_ERR_CUDA;
+      S.a_ptr[0] = S.a_ptr[1] = reinterpret_cast<const uint8_t*>(h->ws13);
+      S.tmB[1] = S.tmB[0];
+    }
+    // ---- GEMM 2: routed L2 with the top-k weighted scatter-combine into r
+    {
+      GemmTask& R = g2.task[0];
+      R.kind = TASK_ROUTED_L2;
+      R.fp8 = !nvfp4;
+      R.kpg = nvfp4 ? 2 : 1;
+      R.routed = 1;
+      R.ftiles = L / 128;
+      R.kb_total = I / rkb;
+      R.kb_split0 = R.kb_total;
+      R.ksplit = 1;
+      R.kb_per_split = R.kb_total;
+      R.a_rb_expert = L / 128;
+      R.a_kb[0] = R.a_kb[1] = I / rkb;
+      R.a_ptr[0] = R.a_ptr[1] = h->w2;
+      R.tmB[0] = h->tm_aq[bi];
+      R.tmB[1] = h->tm_aq[bi];
+    }
+    // ---- GEMM 3: out = bf16([n | a_s] . [W_up | Ws2]^T)
+    {
+      GemmTask& O = g3.task[0];
+      O.kind = TASK_OUT;
+      O.routed = 0;
+      O.ftiles = H / 128;
+      O.kb_total = L / 64 + Is / 64;
+      O.kb_split0 = L / 64;
+      O.ws_tile_base = 0;
+      O.a_kb[0] = L / 64;
+      O.a_kb[1] = Is / 64;
+      O.ksplit = 1;
+      O.kb_per_split = O.kb_total;
+      O.ntiles = ntiles;
+      O.units = ntiles * O.ftiles;
+      if (fused) {
+        // units come from the launch-wide counter, after the other tasks' units
+        O.ws_tile_base = kMaxCounters;
+        O.ws_off = static_cast<long long>(ws_task) + h->ws_routed_floats;
+        plan_split(O, ntiles, 2 * grid, BN);
+      } else if (O.units < 4 * grid) {
+        // static stream-K: every CTA streams the same number of k-blocks (no more CTAs than
+        // k-blocks, so every CTA's range is non-empty)
+        O.streamk = 1;
+        O.sk_total = static_cast<long long>(O.units) * O.kb_total;
+        O.sk_grid = static_cast<int>(std::min<long long>(grid, O.sk_total));
+      }
+      O.a_ptr[0] = reinterpret_cast<const uint8_t*>(h->w_up);
+      O.a_ptr[1] = reinterpret_cast<const uint8_t*>(h->ws2);
+      O.tmB[0] = h->tm_n[bi];
+      O.tmB[1] = h->tm_as[bi];
+    }
+    if (fused) {
+      // One persistent launch: routed L1 and shared L1, routed L2 (after its token tile's L1
+      // units), the RMSNorm (after every L2 unit) and the output GEMM (after its tile's norm
+      // and shared L1), ordered so that every unit depends only on earlier units.
+      GemmParams gf = gp;
+      gf.ntasks = 5;
+      gf.sched = h->sched + 3;
+      gf.stall_after = dbg ? dbg->stall_after_kblocks : 0;
+      gf.trace = trace;
+      gf.cnt = h->split_cnt;
+      gf.task[0] = g1.task[0];
+      gf.task[1] = g1.task[1];
+      gf.task[2] = g2.task[0];
+      gf.task[2].dep = DEP_L1_TILE;
+      GemmTask& N = gf.task[3];
+      N.kind = TASK_NORM;
+      N.dep = DEP_ALL_L2;
+      N.routed = 0;
+      N.ftiles = 1;
+      N.ksplit = 1;
+      N.kb_total = 0;
+      N.kb_per_split = 0;
+      N.ntiles = ntiles;
+      N.units = M;  // one token row per norm unit
+      N.tmB[0] = N.tmB[1] = h->tm_n[bi];
+      gf.task[4] = g3.task[0];
+      gf.task[4].dep = DEP_OUT_TILE;
+      gf.l1_done = h->dep_cnt;
+      gf.l2_done = h->dep_cnt + h->dep_routed;
+      gf.norm_done = gf.l2_done + 1;
+      gf.sh_done = gf.norm_done + h->dep_ntiles;
+      gf.l1_target = I / 128;
+      gf.sh_target = Is / 128;
+      gf.l2_ftiles = L / 128;
+      gf.gamma = h->gamma;
+      gf.nrm = h->n;
+      gf.eps = d.eps;
+      KLT_LAUNCH(launch_gemm(gf, BN, grid, s, pdl));
+    } else {
+      g1.ntasks = 2;
+      g1.sched = h->sched + 0;
+      g1.stall_after = dbg ? dbg->stall_after_kblocks : 0;
+      g1.trace = trace;
+      KLT_LAUNCH(launch_gemm(g1, BN, grid, s, pdl));
+      g2.ntasks = 1;
+      g2.sched = h->sched + 1;
+      g2.trace = trace ? trace + trace_launch : nullptr;
+      KLT_LAUNCH(launch_gemm(g2, BN, grid, s, pdl));
+      NormParams np;
+      np.r = h->r;
+      np.gamma = h->gamma;
+      np.n = h->n;
+      np.M = M;
+      np.L = L;
+      np.eps = d.eps;
+      KLT_LAUNCH(launch_norm(np, s, pdl));
+      g3.ntasks = 1;
+      g3.sched = h->sched + 2;
+      g3.trace = trace ? trace + 2 * trace_launch : nullptr;
+      g3.ws = h->ws + ws_task + h->ws_routed_floats;
+      g3.cnt = h->split_cnt + kMaxCounters;
+      KLT_LAUNCH(launch_gemm(g3, BN, grid, s, pdl));
+    }
   }
 #undef KLT_LAUNCH
 

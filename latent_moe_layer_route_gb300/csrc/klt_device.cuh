@@ -113,6 +113,11 @@ KLT_DEV uint64_t policy_evict_first() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
+KLT_DEV uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
 KLT_DEV uint64_t policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
@@ -308,6 +313,26 @@ KLT_DEV void tmem_ld16x4(uint32_t t0, uint32_t t1, uint32_t t2, uint32_t t3, flo
 
 // ------------------------------------------------------------------ misc
 KLT_DEV float silu_f(float g) { return g / (1.0f + expf(-g)); }
+// SiLU with the fast exponential and an IEEE reciprocal; exact limits at both ends
+// (exp overflow gives 1/inf = 0).
+KLT_DEV float silu_fast(float g) { return g * __frcp_rn(1.0f + __expf(-g)); }
+
+// Four consecutive fp32 atomically added to global memory (16-byte aligned), one request.
+KLT_DEV void red_add_v4(float* dst, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+
+// Per-warpgroup register budget changes (all four warps of the warpgroup execute them).
+template <int N>
+KLT_DEV void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+KLT_DEV void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
 
 // e4m3 code -> fp32 (exact).
 KLT_DEV float e4m3_to_f32(uint8_t c) {

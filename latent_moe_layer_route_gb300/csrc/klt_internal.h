@@ -161,6 +161,13 @@ cudaError_t launch_tile_relayout(const void* src, void* dst, long long rows, lon
 // bn in {16, 128}; grid = persistent CTAs.
 cudaError_t launch_gemm(const GemmParams& p, int bn, int grid, cudaStream_t s, bool pdl);
 int gemm_smem_bytes(int bn);
+// Token-major engine (128-token x 256-feature units, one persistent launch of the five
+// fused tasks with 128-token tiles).  Its epilogue warps take registers from the control
+// warps at run time, which needs the kernel to launch with exactly the register count it
+// was built for: wide_regs_ok(wide_kernel_regs()) must hold before launch_wide is used.
+cudaError_t launch_wide(const GemmParams& p, int grid, cudaStream_t s, bool pdl);
+int wide_kernel_regs();
+bool wide_regs_ok(int regs);
 
 constexpr int PERM_BLOCK = 1024;  // pairs per permutation block
 constexpr int ROUTE_WARPS = 8;    // warps per routing block

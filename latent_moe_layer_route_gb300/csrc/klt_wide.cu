@@ -1,0 +1,716 @@
+// Token-major tile engine for prefill batches: one persistent launch runs the routed L1
+// (SwiGLU + per-token e4m3 requantisation), the shared-expert L1, the routed L2 with the
+// weighted scatter-combine, the RMSNorm and the output GEMM, like the decode engine, but
+// every unit is a 128-token x 256-feature tile:
+//
+//   D[token, feature] = sum_k A[token, k] * B[feature, k]      (tcgen05.mma M=128, N=256)
+//
+// A is the token tile (TMA, 128 rows x 128 bytes per k-block) and B is two pre-swizzled
+// 128-row weight tiles placed back to back (gate and up of an L1 unit, or two consecutive
+// row blocks of L2 / output weights).  With 256 features per MMA the tensor pipe, not the
+// single issuing thread, sets the pace, and each staged byte feeds twice the MMA work of a
+// 128-feature tile.
+//
+// Warp roles (3 warpgroups): warp 0 = TMA producer, warp 1 = MMA issuer, warps 2-3 idle,
+// warps 4-11 = epilogue.  The control warpgroup hands registers to the epilogue
+// warpgroups (setmaxnreg) so each epilogue thread can hold its 128 fp32 accumulators of
+// one token across the per-128-K promotion of block-scaled FP8 (or NVFP4) products.
+//
+// Epilogue thread (warp w, lane l): token row (w % 4) * 32 + l of the tile (its TMEM lane)
+// and column half h = (w - 4) / 4: for gate/up units gate columns [64h, 64h+64) and up
+// columns [128+64h, 128+64h+64), otherwise columns [128h, 128h+128).
+#include "klt_device.cuh"
+#include "klt_internal.h"
+
+namespace klt {
+
+namespace {
+
+struct W {
+  static constexpr int TM = 128;  // tokens per tile: MMA M, TMEM lanes
+  static constexpr int TN = 256;  // features per unit: MMA N, TMEM columns per slot
+  static constexpr int EPI_WARPS = 8;
+  static constexpr int FIRST_EPI_WARP = 4;
+  static constexpr int THREADS = 12 * 32;
+  static constexpr int EPI_THREADS = EPI_WARPS * 32;
+  static constexpr int W_TILE = 128 * 128;  // one pre-swizzled weight tile
+  static constexpr int T_TILE = TM * 128;   // token tile of one k-block
+  static constexpr int STAGE_BYTES = 2 * W_TILE + T_TILE;
+  static constexpr int STAGES = 4;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int NACC = TMEM_COLS / TN;
+  static constexpr int US = 8;
+  // Registers: 384 threads launch with 168 each (3 warps share a scheduler); the control
+  // warpgroup drops to 80 and the two epilogue warpgroups rise to 200, within the
+  // registers released.
+  static constexpr int LAUNCH_REGS = 168;
+  static constexpr int REGS_CTRL = 80;
+  static constexpr int REGS_EPI = 200;
+  static_assert(4 * (LAUNCH_REGS - REGS_CTRL) >= 8 * (REGS_EPI - LAUNCH_REGS),
+                "register hand-over must balance");
+  static_assert(NACC == 2, "two accumulator slots");
+};
+
+struct WUnit {
+  int task;   // -1: no more work
+  int e;      // routed expert
+  int row0;   // first token row of the tile
+  int rows;   // valid token rows
+  int ftile;  // output feature tile (128 SwiGLU outputs for gate/up kinds, else 256)
+  int rb0, rb1;  // weight row blocks staged as B rows [0, 128) and [128, 256)
+  int kb0, kb1;
+  int dep_idx;  // routed token tile (routed kinds) or token tile (others)
+};
+
+struct WSmem {
+  uint8_t* stages;
+  uint64_t *full, *empty, *tfull, *tempty, *ufull, *uempty, *drain;
+  WUnit* ring;
+  uint32_t* tmem_holder;
+  int* abort_flag;
+  float* amax;  // [2 unit parities][2 column halves][TM]
+  float* part;  // [EPI_WARPS] norm partial sums
+
+  static constexpr int BAR_BYTES = 8 * (2 * W::STAGES + 2 * W::NACC + 2 * W::US + 1);
+  static constexpr int bytes() {
+    return W::STAGES * W::STAGE_BYTES + BAR_BYTES + W::US * (int)sizeof(WUnit) + 64 +
+           4 * W::TM * 4 + W::EPI_WARPS * 4 + 1024 /* alignment slack */;
+  }
+  __device__ explicit WSmem(uint8_t* raw) {
+    uint8_t* base = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    stages = base;
+    uint64_t* b = reinterpret_cast<uint64_t*>(base + W::STAGES * W::STAGE_BYTES);
+    full = b;
+    empty = full + W::STAGES;
+    tfull = empty + W::STAGES;
+    tempty = tfull + W::NACC;
+    ufull = tempty + W::NACC;
+    uempty = ufull + W::US;
+    drain = uempty + W::US;
+    ring = reinterpret_cast<WUnit*>(drain + 1);
+    tmem_holder = reinterpret_cast<uint32_t*>(ring + W::US);
+    abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
+    amax = reinterpret_cast<float*>(tmem_holder + 16);
+    part = amax + 4 * W::TM;
+  }
+};
+
+__device__ __forceinline__ void trace_mark(const GemmParams& p, int role, int i) {
+  if (p.trace != nullptr && i < p.trace_n)
+    p.trace[(static_cast<long long>(blockIdx.x) * 4 + role) * p.trace_n + i] = global_ns();
+}
+
+__device__ __forceinline__ bool is_pair(int kind) {
+  return kind == TASK_SHARED_L1 || kind == TASK_ROUTED_L1;
+}
+
+// Unit u of the launch, tasks in order.  Routed units: token tile t of the device tile
+// list (128 tokens of one expert), feature tile ft, t-major so an expert's token tiles
+// read its weights close together in time.
+__device__ WUnit w_decode(const GemmParams& p, const int* s_tile_off, const int* s_off, int u) {
+  WUnit info;
+  info.task = -1;
+  for (int ti = 0; ti < p.ntasks; ++ti) {
+    const GemmTask& T = p.task[ti];
+    const bool pair = is_pair(T.kind);
+    if (T.routed) {
+      const int units = s_tile_off[p.E] * T.ftiles;
+      if (u < units) {
+        const int t = u / T.ftiles;
+        const int ft = u - t * T.ftiles;
+        int lo = 0, hi = p.E - 1;  // largest e with tile_off[e] <= t
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (s_tile_off[mid] <= t) lo = mid; else hi = mid - 1;
+        }
+        info.task = ti;
+        info.e = lo;
+        info.row0 = s_off[lo] + (t - s_tile_off[lo]) * W::TM;
+        info.rows = min(W::TM, s_off[lo + 1] - info.row0);
+        info.ftile = ft;
+        info.rb0 = lo * T.a_rb_expert + (pair ? ft : 2 * ft);
+        info.rb1 = pair ? info.rb0 + T.a_rb_up : info.rb0 + 1;
+        info.kb0 = 0;
+        info.kb1 = T.kb_total;
+        info.dep_idx = t;
+        return info;
+      }
+      u -= units;
+    } else {
+      if (u < T.units) {
+        info.task = ti;
+        info.e = 0;
+        if (T.kind == TASK_NORM) {  // one token row
+          info.row0 = u;
+          info.rows = 1;
+          info.ftile = 0;
+          info.rb0 = info.rb1 = 0;
+          info.kb0 = info.kb1 = 0;
+          info.dep_idx = u / W::TM;
+        } else {
+          const int nt = u / T.ftiles;
+          const int ft = u - nt * T.ftiles;
+          info.row0 = nt * W::TM;
+          info.rows = min(W::TM, p.M - info.row0);
+          info.ftile = ft;
+          info.rb0 = pair ? ft : 2 * ft;
+          info.rb1 = pair ? info.rb0 + T.a_rb_up : info.rb0 + 1;
+          info.kb0 = 0;
+          info.kb1 = T.kb_total;
+          info.dep_idx = nt;
+        }
+        return info;
+      }
+      u -= T.units;
+    }
+  }
+  return info;
+}
+
+// Bounded wait until the unit's inputs produced by other units of this launch are complete
+// (acquire loads pairing with the producers' release adds; the proxy fence orders the
+// acquired data before this thread's TMA reads of it).
+__device__ bool w_wait_dependency(const GemmParams& p, int dep, int idx, const int* s_tile_off,
+                                  volatile int* abort_flag) {
+  if (dep == DEP_NONE) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    bool ready;
+    if (dep == DEP_L1_TILE) {
+      ready = ld_acquire_gpu(p.l1_done + idx) >= p.l1_target;
+    } else if (dep == DEP_ALL_L2) {
+      ready = ld_acquire_gpu(p.l2_done) >= s_tile_off[p.E] * p.l2_ftiles;
+    } else {
+      ready = ld_acquire_gpu(p.norm_done + idx) >= min(W::TM, p.M - idx * W::TM) &&
+              ld_acquire_gpu(p.sh_done + idx) >= p.sh_target;
+    }
+    if (ready) break;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > p.timeout) {
+      *abort_flag = 1;
+      atomicOr(p.err, DEV_ERR_TIMEOUT);
+      return false;
+    }
+    __nanosleep(100);
+  }
+  fence_proxy_async_global();
+  return true;
+}
+
+// ------------------------------------------------------------------ producer (1 thread)
+__device__ void w_producer(const GemmParams& p, WSmem& sm, const int* s_tile_off,
+                           const int* s_off) {
+  // weights are re-read by every token tile of their expert and tokens by every feature
+  // tile: both stay at normal L2 priority
+  const uint64_t pol = policy_evict_normal();
+  int stage = 0, us = 0;
+  uint32_t phase = 0, uphase = 0;
+  long long issued = 0;
+  int published = 0;
+  int dummy_abort = 0;
+  bool stalled = false;
+  int u = atomicAdd(p.sched, 1);
+  for (;;) {
+    const WUnit info = w_decode(p, s_tile_off, s_off, u);
+    // claim the next unit now so the counter round trip overlaps this unit's copies
+    if (info.task >= 0) u = atomicAdd(p.sched, 1);
+    if (info.task < 0) {
+      if (mbar_wait(&sm.uempty[us], uphase ^ 1, sm.abort_flag, p.err, p.timeout)) {
+        sm.ring[us] = info;
+        mbar_arrive(&sm.ufull[us]);
+      }
+      break;
+    }
+    const GemmTask& T = p.task[info.task];
+    const int elems_per_kb = T.fp8 ? 128 : 64;
+    auto issue_w = [&](int kb, uint8_t* st) {
+      const int m = kb < T.kb_split0 ? 0 : 1;
+      const int kk = m ? kb - T.kb_split0 : kb;
+      const uint8_t* a = T.a_ptr[m];
+      const size_t akb = static_cast<size_t>(T.a_kb[m]);
+      bulk_load(st, a + (static_cast<size_t>(info.rb0) * akb + kk) * W::W_TILE, W::W_TILE,
+                &sm.full[stage], pol);
+      bulk_load(st + W::W_TILE, a + (static_cast<size_t>(info.rb1) * akb + kk) * W::W_TILE,
+                W::W_TILE, &sm.full[stage], pol);
+    };
+    auto issue_t = [&](int kb, uint8_t* st, uint64_t* bar) {
+      const int m = kb < T.kb_split0 ? 0 : 1;
+      const int kk = m ? kb - T.kb_split0 : kb;
+      tma_load_2d(st + 2 * W::W_TILE, &T.tmB[m], bar, kk * elems_per_kb, info.row0, pol);
+    };
+    int kb = info.kb0;
+    if (T.dep != DEP_NONE) {
+      // Stream the unit's weight tiles into the stages that are free now, then wait for
+      // the token operand's producers, then copy the token tiles of those stages.
+      int pre_kb[W::STAGES], pre_st[W::STAGES], npre = 0;
+      while (kb < info.kb1 && npre < W::STAGES) {
+        if (p.stall_after > 0 && issued >= p.stall_after) break;
+        if (!mbar_try_wait(&sm.empty[stage], phase ^ 1)) break;
+        uint8_t* st = sm.stages + stage * W::STAGE_BYTES;
+        mbar_arrive_expect_tx(&sm.full[stage], W::STAGE_BYTES);
+        issue_w(kb, st);
+        pre_kb[npre] = kb;
+        pre_st[npre] = stage;
+        ++npre;
+        trace_mark(p, 0, static_cast<int>(issued));
+        ++issued;
+        if (++stage == W::STAGES) { stage = 0; phase ^= 1; }
+        ++kb;
+      }
+      if (!w_wait_dependency(p, T.dep, info.dep_idx, s_tile_off, sm.abort_flag)) break;
+      for (int i = 0; i < npre; ++i)
+        issue_t(pre_kb[i], sm.stages + pre_st[i] * W::STAGE_BYTES, &sm.full[pre_st[i]]);
+    }
+    if (!mbar_wait(&sm.uempty[us], uphase ^ 1, sm.abort_flag, p.err, p.timeout)) break;
+    sm.ring[us] = info;
+    mbar_arrive(&sm.ufull[us]);
+    if (++us == W::US) { us = 0; uphase ^= 1; }
+    if (p.trace != nullptr && published < p.trace_n) {  // unit publish time and task
+      p.trace[(static_cast<long long>(blockIdx.x) * 4 + 1) * p.trace_n + published] = global_ns();
+      p.trace[(static_cast<long long>(blockIdx.x) * 4 + 3) * p.trace_n + published] =
+          info.task + 1;
+    }
+    ++published;
+    for (; kb < info.kb1; ++kb) {
+      if (p.stall_after > 0 && issued >= p.stall_after) { stalled = true; break; }
+      if (!mbar_wait(&sm.empty[stage], phase ^ 1, sm.abort_flag, p.err, p.timeout)) {
+        stalled = true;
+        break;
+      }
+      uint8_t* st = sm.stages + stage * W::STAGE_BYTES;
+      mbar_arrive_expect_tx(&sm.full[stage], W::STAGE_BYTES);
+      issue_w(kb, st);
+      issue_t(kb, st, &sm.full[stage]);
+      trace_mark(p, 0, static_cast<int>(issued));
+      ++issued;
+      if (++stage == W::STAGES) { stage = 0; phase ^= 1; }
+    }
+    if (stalled) break;
+  }
+  // Drain: wait (bounded, ignoring the abort flag) for this thread's last copies, so no
+  // TMA write into shared memory outlives the CTA.
+  const long long first = issued > W::STAGES ? issued - W::STAGES : 0;
+  for (long long i = first; i < issued; ++i) {
+    const int s = static_cast<int>(i % W::STAGES);
+    const uint32_t par = static_cast<uint32_t>((i / W::STAGES) & 1);
+    mbar_wait(&sm.full[s], par, &dummy_abort, p.err, p.timeout);
+  }
+}
+
+// ------------------------------------------------------------------ MMA issuer (1 thread)
+__device__ void w_mma(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
+  int stage = 0, us = 0, acc = 0;
+  uint32_t phase = 0, uphase = 0, aphase = 0;
+  bool ok = true;
+  const uint32_t idesc_bf16 = idesc_make(1, W::TM, W::TN);
+  const uint32_t idesc_fp8 = idesc_make(0, W::TM, W::TN);
+  // B (weights, 256 rows) at the stage base, A (tokens) after the two weight tiles
+  const uint64_t desc_b0 = sdesc_sw128(smem_u32(sm.stages));
+  const uint64_t desc_a0 = desc_b0 + ((2 * W::W_TILE) >> 4);
+  constexpr uint64_t STAGE_D = W::STAGE_BYTES >> 4;
+  while (ok) {
+    if (!mbar_wait(&sm.ufull[us], uphase, sm.abort_flag, p.err, p.timeout)) break;
+    const WUnit info = sm.ring[us];
+    mbar_arrive(&sm.uempty[us]);
+    if (++us == W::US) { us = 0; uphase ^= 1; }
+    if (info.task < 0) break;
+    const GemmTask& T = p.task[info.task];
+    if (T.kind == TASK_NORM) continue;  // no tensor-core work
+    const int kpg = T.kpg;
+    const bool promote = kpg > 0;
+    const bool fp8 = T.fp8 != 0;
+    const uint32_t idesc = fp8 ? idesc_fp8 : idesc_bf16;
+    const int kb0 = info.kb0, kb1 = info.kb1;
+    if (!promote) {
+      if (!mbar_wait(&sm.tempty[acc], aphase ^ 1, sm.abort_flag, p.err, p.timeout)) break;
+      tc_fence_after();
+    }
+    int gpos = 0;  // position of the next k-block in its promotion group
+    for (int kb = kb0; kb < kb1; ++kb) {
+      if (!mbar_wait(&sm.full[stage], phase, sm.abort_flag, p.err, p.timeout)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (promote && gpos == 0) {
+        if (!mbar_wait(&sm.tempty[acc], aphase ^ 1, sm.abort_flag, p.err, p.timeout)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      const uint32_t d = tmem_base + static_cast<uint32_t>(acc * W::TN);
+      const uint64_t off = static_cast<uint64_t>(stage) * STAGE_D;
+      const uint32_t accum = promote ? static_cast<uint32_t>(gpos > 0)
+                                     : static_cast<uint32_t>(kb > kb0);
+      if (fp8) mma4_fp8(d, desc_a0 + off, desc_b0 + off, idesc, accum);
+      else mma4_bf16(d, desc_a0 + off, desc_b0 + off, idesc, accum);
+      tc_commit(&sm.empty[stage]);
+      if (++stage == W::STAGES) { stage = 0; phase ^= 1; }
+      if (promote && ++gpos == kpg) {
+        gpos = 0;
+        tc_commit(&sm.tfull[acc]);
+        if (++acc == W::NACC) { acc = 0; aphase ^= 1; }
+      }
+    }
+    if (!ok) break;
+    if (!promote) {
+      tc_commit(&sm.tfull[acc]);
+      if (++acc == W::NACC) { acc = 0; aphase ^= 1; }
+    }
+  }
+  // Drain: all MMAs issued by this thread complete before TMEM is released.
+  int dummy_abort = 0;
+  tc_commit(sm.drain);
+  mbar_wait(sm.drain, 0, &dummy_abort, p.err, p.timeout);
+}
+
+// ------------------------------------------------------------------ epilogue
+// After the epilogue barrier one gpu-scope release add publishes every epilogue thread's
+// writes of the unit (release is cumulative over the barrier).
+__device__ __forceinline__ void w_signal(int* counter, int ew, int lane) {
+  named_bar_sync(1, W::EPI_THREADS);
+  if (ew == 0 && lane == 0) red_release_gpu_add(counter, 1);
+}
+
+// RMSNorm of one token row of the fp32 combine: fp32 statistic, gamma applied, one bf16
+// rounding (the output GEMM's token operand).  The epilogue threads split the row.
+__device__ void w_norm_row(const GemmParams& p, WSmem& sm, int row, int ew, int lane) {
+  const size_t t = static_cast<size_t>(row);
+  const float4* rv = reinterpret_cast<const float4*>(p.r + t * p.L);
+  const int etid = ew * 32 + lane;
+  const int n4 = p.L / 4;
+  constexpr int PER = 4;  // float4s per thread held in registers (L <= 4096)
+  float4 v[PER];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int c = etid + i * W::EPI_THREADS;
+    v[i] = c < n4 ? __ldcg(rv + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int i = 0; i < PER; ++i)
+    ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+  if (lane == 0) sm.part[ew] = ss;
+  named_bar_sync(1, W::EPI_THREADS);
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < W::EPI_WARPS; ++w) tot += sm.part[w];
+  const float inv = rsqrtf(tot / static_cast<float>(p.L) + p.eps);
+  const uint2* gg = reinterpret_cast<const uint2*>(p.gamma);
+  uint2* nn = reinterpret_cast<uint2*>(p.nrm + t * p.L);
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int c = etid + i * W::EPI_THREADS;
+    if (c < n4) {
+      const float4 x = v[i];
+      const uint2 graw = __ldg(gg + c);
+      const __nv_bfloat162 g01 = *reinterpret_cast<const __nv_bfloat162*>(&graw.x);
+      const __nv_bfloat162 g23 = *reinterpret_cast<const __nv_bfloat162*>(&graw.y);
+      const __nv_bfloat162 o01 = __floats2bfloat162_rn(x.x * inv * __low2float(g01),
+                                                       x.y * inv * __high2float(g01));
+      const __nv_bfloat162 o23 = __floats2bfloat162_rn(x.z * inv * __low2float(g23),
+                                                       x.w * inv * __high2float(g23));
+      uint2 o;
+      o.x = *reinterpret_cast<const uint32_t*>(&o01);
+      o.y = *reinterpret_cast<const uint32_t*>(&o23);
+      nn[c] = o;
+    }
+  }
+  named_bar_sync(1, W::EPI_THREADS);  // sm.part is reused by the next row
+  w_signal(p.norm_done + row / W::TM, ew, lane);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ew = warp - W::FIRST_EPI_WARP;
+  const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+  const int half = ew >> 2;   // column half of this warp
+  const int tok = quad * 32 + lane;
+  const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+  int us = 0, acc = 0, steps = 0, l1_units = 0;
+  uint32_t uphase = 0, aphase = 0;
+  const int G_L = p.L / 128, G_I = p.I / 128;
+
+  for (;;) {
+    if (!mbar_wait(&sm.ufull[us], uphase, sm.abort_flag, p.err, p.timeout)) return;
+    const WUnit info = sm.ring[us];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.uempty[us]);
+    if (++us == W::US) { us = 0; uphase ^= 1; }
+    if (info.task < 0) return;
+    const GemmTask& T = p.task[info.task];
+    const int kind = T.kind;
+    if (kind == TASK_NORM) {
+      w_norm_row(p, sm, info.row0, ew, lane);
+      continue;
+    }
+    const bool pair = is_pair(kind);
+    const bool valid = tok < info.rows;
+    // TMEM columns of this thread's two 64-column groups
+    const uint32_t col0 = pair ? half * 64 : half * 128;
+    const uint32_t col1 = pair ? 128 + half * 64 : half * 128 + 64;
+    float a[128];
+
+    if (T.kpg > 0) {
+      // Block-scaled products: every promotion group's partial (fresh in TMEM) is added
+      // with scale = token scale x weight block scale of the group.
+#pragma unroll
+      for (int i = 0; i < 128; ++i) a[i] = 0.f;
+      const int ng = (info.kb1 - info.kb0) / T.kpg;
+      const int g0 = info.kb0 / T.kpg;
+      const float* ts =
+          (kind == TASK_ROUTED_L1 ? p.zsT : p.asT) + static_cast<size_t>(g0) * p.cap +
+          info.row0 + tok;
+      const float *sw0, *sw1;
+      if (kind == TASK_ROUTED_L1) {
+        const size_t rb = static_cast<size_t>(info.e) * (2 * G_I);
+        sw0 = p.w13_s + (rb + info.ftile) * G_L + g0;
+        sw1 = p.w13_s + (rb + G_I + info.ftile) * G_L + g0;
+      } else {
+        sw0 = p.w2_s + (static_cast<size_t>(info.e) * G_L + 2 * info.ftile + half) * G_I + g0;
+        sw1 = sw0;
+      }
+      float sa_next = valid ? __ldcg(ts) : 0.f;
+      for (int gi = 0; gi < ng; ++gi) {
+        const float sa = sa_next;
+        if (gi + 1 < ng) sa_next = valid ? __ldcg(ts + static_cast<size_t>(gi + 1) * p.cap) : 0.f;
+        const float s0 = __ldg(sw0 + gi) * sa;
+        const float s1 = __ldg(sw1 + gi) * sa;
+        if (!mbar_wait(&sm.tfull[acc], aphase, sm.abort_flag, p.err, p.timeout)) return;
+        tc_fence_after();
+        const uint32_t tb = tmem_base + lane_base + static_cast<uint32_t>(acc * W::TN);
+        float v[4][16];
+        tmem_ld16x4(tb + col0, tb + col0 + 16, tb + col0 + 32, tb + col0 + 48, v[0], v[1],
+                    v[2], v[3]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 16; ++i) a[c * 16 + i] = fmaf(v[c][i], s0, a[c * 16 + i]);
+        tmem_ld16x4(tb + col1, tb + col1 + 16, tb + col1 + 32, tb + col1 + 48, v[0], v[1],
+                    v[2], v[3]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            a[64 + c * 16 + i] = fmaf(v[c][i], s1, a[64 + c * 16 + i]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.tempty[acc]);
+        if (++acc == W::NACC) { acc = 0; aphase ^= 1; }
+        if (ew == 0 && lane == 0) trace_mark(p, 2, steps++);
+      }
+    } else {
+      if (!mbar_wait(&sm.tfull[acc], aphase, sm.abort_flag, p.err, p.timeout)) return;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + lane_base + static_cast<uint32_t>(acc * W::TN);
+      tmem_ld16x4(tb + col0, tb + col0 + 16, tb + col0 + 32, tb + col0 + 48, a, a + 16,
+                  a + 32, a + 48);
+      tmem_ld16x4(tb + col1, tb + col1 + 16, tb + col1 + 32, tb + col1 + 48, a + 64, a + 80,
+                  a + 96, a + 112);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.tempty[acc]);
+      if (++acc == W::NACC) { acc = 0; aphase ^= 1; }
+      if (ew == 0 && lane == 0) trace_mark(p, 2, steps++);
+    }
+
+    // ---- unit end (this thread: one token, 64 gate/up pairs or 128 features)
+    if (kind == TASK_ROUTED_L1) {
+      // SwiGLU, then e4m3 with one scale per token per 128 outputs (both halves' amax)
+      float m = 0.f;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        a[i] = silu_fast(a[i]) * a[64 + i];
+        m = fmaxf(m, fabsf(a[i]));
+      }
+      float* am = sm.amax + (l1_units & 1) * 2 * W::TM;
+      ++l1_units;
+      am[half * W::TM + tok] = m;
+      named_bar_sync(1, W::EPI_THREADS);
+      const float amax = fmaxf(am[tok], am[W::TM + tok]);
+      const float sc = amax == 0.f ? 1.0f : amax / 448.0f;
+      if (valid) {
+        const size_t pp = static_cast<size_t>(info.row0 + tok);
+        const size_t col = static_cast<size_t>(info.ftile) * 128 + half * 64;
+        uint4* dq = reinterpret_cast<uint4*>(p.aq + pp * p.I + col);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t w4[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int i = c * 16 + q * 4;
+            w4[q] = static_cast<uint32_t>(f32_to_e4m3(a[i] / sc)) |
+                    (static_cast<uint32_t>(f32_to_e4m3(a[i + 1] / sc)) << 8) |
+                    (static_cast<uint32_t>(f32_to_e4m3(a[i + 2] / sc)) << 16) |
+                    (static_cast<uint32_t>(f32_to_e4m3(a[i + 3] / sc)) << 24);
+          }
+          dq[c] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          if (p.aqb != nullptr) {  // exact bf16 images of the codes
+            uint4* db = reinterpret_cast<uint4*>(p.aqb + pp * p.I + col) + 2 * c;
+            uint32_t b8[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const uint32_t wq = w4[q >> 1] >> ((q & 1) * 16);
+              b8[q] = pack_bf16x2(e4m3_to_f32(static_cast<uint8_t>(wq & 0xFFu)),
+                                  e4m3_to_f32(static_cast<uint8_t>((wq >> 8) & 0xFFu)));
+            }
+            db[0] = make_uint4(b8[0], b8[1], b8[2], b8[3]);
+            db[1] = make_uint4(b8[4], b8[5], b8[6], b8[7]);
+          }
+        }
+        if (half == 0) p.asT[static_cast<size_t>(info.ftile) * p.cap + pp] = sc;
+      }
+      if (p.l1_done != nullptr) w_signal(p.l1_done + info.dep_idx, ew, lane);
+    } else if (kind == TASK_SHARED_L1) {
+      if (valid) {
+        uint4* dst = reinterpret_cast<uint4*>(
+            p.a_s + static_cast<size_t>(info.row0 + tok) * p.Is + info.ftile * 128 + half * 64);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t w4[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int i = c * 8 + q * 2;
+            w4[q] = pack_bf16x2(silu_fast(a[i]) * a[64 + i], silu_fast(a[i + 1]) * a[65 + i]);
+          }
+          dst[c] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+      }
+      if (p.sh_done != nullptr) w_signal(p.sh_done + info.dep_idx, ew, lane);
+    } else if (kind == TASK_ROUTED_L2) {
+      // weighted scatter-combine into the token's fp32 row of r
+      if (valid) {
+        const int pp = info.row0 + tok;
+        const int tg = __ldg(p.gidx + pp);
+        const float wv = __ldg(p.wperm + pp);
+        float* dst = p.r + static_cast<size_t>(tg) * p.L + info.ftile * 256 + half * 128;
+#pragma unroll
+        for (int i = 0; i < 128; i += 4)
+          red_add_v4(dst + i, wv * a[i], wv * a[i + 1], wv * a[i + 2], wv * a[i + 3]);
+      }
+      if (p.l2_done != nullptr) w_signal(p.l2_done, ew, lane);
+    } else {  // TASK_OUT
+      if (valid) {
+        uint4* dst = reinterpret_cast<uint4*>(
+            p.out + static_cast<size_t>(info.row0 + tok) * p.H + info.ftile * 256 + half * 128);
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          dst[c] = make_uint4(pack_bf16x2(a[c * 8], a[c * 8 + 1]),
+                              pack_bf16x2(a[c * 8 + 2], a[c * 8 + 3]),
+                              pack_bf16x2(a[c * 8 + 4], a[c * 8 + 5]),
+                              pack_bf16x2(a[c * 8 + 6], a[c * 8 + 7]));
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(W::THREADS, 1) wide_kernel(const __grid_constant__ GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  WSmem sm(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < W::STAGES; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    for (int a = 0; a < W::NACC; ++a) {
+      mbar_init(&sm.tfull[a], 1);
+      mbar_init(&sm.tempty[a], W::EPI_WARPS);
+    }
+    for (int u = 0; u < W::US; ++u) {
+      mbar_init(&sm.ufull[u], 1);
+      mbar_init(&sm.uempty[u], 1 + W::EPI_WARPS);
+    }
+    mbar_init(sm.drain, 1);
+    *sm.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int t = 0; t < p.ntasks; ++t) {
+      tma_prefetch_desc(&p.task[t].tmB[0]);
+      tma_prefetch_desc(&p.task[t].tmB[1]);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(sm.tmem_holder, W::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *sm.tmem_holder;
+
+  // Everything above touches only this CTA's resources; inputs written by the previous
+  // kernel in the stream are read only after this point.
+  pdl_wait();
+  pdl_trigger();
+
+  if (warp < W::FIRST_EPI_WARP) {
+    regs_dec<W::REGS_CTRL>();
+    if (warp == 0) {
+      // routing tile offsets for the producer's unit decode, read once per CTA
+      __shared__ int s_tile_off[MAX_E + 1], s_off[MAX_E + 1];
+      for (int i = lane; i <= p.E; i += 32) {
+        s_tile_off[i] = p.tile_off[i];
+        s_off[i] = p.off[i];
+      }
+      __syncwarp();
+      if (lane == 0) w_producer(p, sm, s_tile_off, s_off);
+    } else if (warp == 1) {
+      if (lane == 0) w_mma(p, sm, tmem_base);
+    }
+  } else {
+    regs_inc<W::REGS_EPI>();
+    w_epilogue(p, sm, tmem_base);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, W::TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+static_assert(WSmem::bytes() + 2 * (MAX_E + 1) * 4 <= 227 * 1024, "shared memory budget");
+
+int wide_kernel_regs() {
+  cudaFuncAttributes a;
+  if (cudaFuncGetAttributes(&a, wide_kernel) != cudaSuccess) return -1;
+  return a.numRegs;
+}
+
+bool wide_regs_ok(int regs) { return regs == W::LAUNCH_REGS; }
+
+cudaError_t launch_wide(const GemmParams& p, int grid, cudaStream_t s, bool pdl) {
+  const int smem = WSmem::bytes();
+  cudaError_t e =
+      cudaFuncSetAttribute(wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(W::THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, wide_kernel, p);
+}
+
+}  // namespace klt

@@ -87,3 +87,4 @@ def test_forward_and_status_reject_null_handle(lib):
     assert lib.klt_status(None) == B.KLT_ERR_INVALID_ARG
     assert lib.klt_destroy(None) == B.KLT_OK
     assert lib.klt_launch_count(None, 16) == 0
+    assert lib.klt_gemm_tile(None, 16, 0) == -B.KLT_ERR_INVALID_ARG

@@ -37,7 +37,7 @@ def weights_for(cfg):
 
 
 def run_case(cfg, M=None, act=None, tokens=None, max_tokens=None, tail=None, force_bn=0,
-             flags=0):
+             flags=0, expect_tile=None):
     w_cpu, w_gpu = weights_for(cfg)
     if act is None:
         act = inputs.make_activations(cfg, M)
@@ -45,6 +45,9 @@ def run_case(cfg, M=None, act=None, tokens=None, max_tokens=None, tail=None, for
     own = tail is None
     if own:
         tail = B.LatentMoETail(cfg, w_gpu, max_tokens=max_tokens or M, flags=flags)
+    # the engine under test is the one the library runs
+    tile = tail.gemm_tile(M, force_bn)
+    assert tile == (expect_tile if expect_tile is not None else (force_bn or tile))
     run = PU.Run(tail, PU.to_cuda(act), cfg, force_bn=force_bn)
     assert tail.status() == B.KLT_OK
     o = T.tail(act, w_cpu, cfg, tokens=tokens)
@@ -72,11 +75,50 @@ def test_small_nvfp4_wider():
                                  topk=3, seed=29), M=45)
 
 
-@pytest.mark.parametrize("bn", [16, 32, 64, 128])
+@pytest.mark.parametrize("bn", [16, 32, 64, 128, 256])
 @pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
 def test_every_token_tile_width(bn, fmt):
-    # ragged M spanning several token tiles of each width
+    # ragged M spanning several token tiles of each width (256: the token-major engine)
     run_case(configs.SMALL.with_(routed_fmt=fmt, E=6, topk=3, seed=30), M=150, force_bn=bn)
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+def test_token_major_engine_on_several_feature_tiles(fmt):
+    # two routed L1 tiles, two L2 and three output tiles of 256 features, two shared L1
+    # tiles, ragged 128-token tiles of 8 experts
+    cfg = configs.SMALL.with_(routed_fmt=fmt, H=768, L=512, I=256, Is=256, E=8, topk=2,
+                              seed=33)
+    w_cpu, w_gpu = weights_for(cfg)
+    tail = B.LatentMoETail(cfg, w_gpu, max_tokens=300)
+    try:
+        assert tail.gemm_tile(300, 256) == 256
+        run_case(cfg, M=300, tail=tail, force_bn=256)
+    finally:
+        tail.close()
+
+
+def test_token_major_engine_is_chosen_for_large_batches_only():
+    cfg = configs.SMALL.with_(seed=34)
+    _, w_gpu = weights_for(cfg)
+    tail = B.LatentMoETail(cfg, w_gpu, max_tokens=2048)
+    phased = B.LatentMoETail(cfg, w_gpu, max_tokens=2048, flags=B.KLT_FLAG_PHASED)
+    try:
+        assert tail.gemm_tile(2048) == 256 and tail.gemm_tile(1024) == 256
+        assert tail.gemm_tile(1023) == 64 and tail.gemm_tile(16) == 16
+        assert tail.gemm_tile(16, 128) == 128
+        assert phased.gemm_tile(2048) == 64
+        assert phased.gemm_tile(2048, 256) == -B.KLT_ERR_UNSUPPORTED
+    finally:
+        tail.close()
+        phased.close()
+    narrow = configs.SMALL.with_(H=384, seed=35)  # H not a multiple of 256
+    _, w_gpu = weights_for(narrow)
+    tail = B.LatentMoETail(narrow, w_gpu, max_tokens=2048)
+    try:
+        assert tail.gemm_tile(2048) == 64
+        assert tail.gemm_tile(8, 256) == -B.KLT_ERR_UNSUPPORTED
+    finally:
+        tail.close()
 
 
 @pytest.mark.parametrize("bn", [16, 64])
@@ -162,16 +204,17 @@ def test_m_zero_is_a_noop_and_bad_m_is_rejected():
         tail.close()
 
 
-def test_bounded_wait_expires_into_status_without_faulting():
+@pytest.mark.parametrize("bn", [0, 256])
+def test_bounded_wait_expires_into_status_without_faulting(bn):
     cfg = configs.SMALL.with_(seed=27)
     w_cpu, w_gpu = weights_for(cfg)
     tail = B.LatentMoETail(cfg, w_gpu, max_tokens=16)
     try:
         act = PU.to_cuda(inputs.make_activations(cfg, 16))
-        PU.Run(tail, act, cfg, stall_after=1, timeout_ms=20)
+        PU.Run(tail, act, cfg, stall_after=1, timeout_ms=20, force_bn=bn)
         assert tail.status() == B.KLT_ERR_DEVICE_TIMEOUT
         # the context is still usable: a fresh handle runs correctly
-        run_case(cfg, M=16)
+        run_case(cfg, M=16, force_bn=bn)
     finally:
         tail.close()
 
@@ -198,12 +241,13 @@ def test_decode_m128():
 
 
 @pytest.mark.slow
-def test_prefill_m4096_sampled_tokens():
+@pytest.mark.parametrize("bn", [0, 64])  # 0: the token-major engine chosen for M=4096
+def test_prefill_m4096_sampled_tokens(bn):
     cfg = configs.PREFILL_M4096
     rng = np.random.default_rng(0)
     tok = np.sort(rng.choice(cfg.M, 48, replace=False))
     tok[0], tok[-1] = 0, cfg.M - 1
-    run_case(cfg, tokens=tok)
+    run_case(cfg, tokens=tok, force_bn=bn, expect_tile=bn or 256)
 
 
 @pytest.mark.slow
@@ -212,4 +256,4 @@ def test_prefill_m8192_nvfp4_sampled_tokens():
     rng = np.random.default_rng(1)
     tok = np.sort(rng.choice(cfg.M, 32, replace=False))
     tok[0], tok[-1] = 0, cfg.M - 1
-    run_case(cfg, tokens=tok)
+    run_case(cfg, tokens=tok, expect_tile=256)
