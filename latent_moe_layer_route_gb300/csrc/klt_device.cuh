@@ -84,6 +84,23 @@ KLT_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
   }
 }
 
+// As mbar_wait, for the latency-critical hand-offs of the tensor pipeline: polls without a
+// suspend-time hint so the waiter resumes as soon as the phase completes.
+KLT_DEV bool mbar_wait_spin(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                            int* err_word, long long timeout) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > timeout) {
+      *abort_flag = 1;
+      atomicOr(err_word, DEV_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 // ------------------------------------------------------------------ TMA
 KLT_DEV void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -311,11 +328,43 @@ KLT_DEV void tmem_ld16x4(uint32_t t0, uint32_t t1, uint32_t t2, uint32_t t3, flo
   }
 }
 
+// Store 16 consecutive fp32 columns of this thread's TMEM lane and wait for the store.
+KLT_DEV void tmem_st16(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+KLT_DEV void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // ------------------------------------------------------------------ misc
-KLT_DEV float silu_f(float g) { return g / (1.0f + expf(-g)); }
-// SiLU with the fast exponential and an IEEE reciprocal; exact limits at both ends
-// (exp overflow gives 1/inf = 0).
-KLT_DEV float silu_fast(float g) { return g * __frcp_rn(1.0f + __expf(-g)); }
+// SiLU g / (1 + e^-g) with the fast exponential and the fast divide (each within 2 ulp).
+// The exponent is clamped at 80 so the divisor stays inside the fast divide's range; for
+// g < -80 the result is below 1e-32 either way.
+KLT_DEV float silu_fast(float g) { return __fdividef(g, 1.0f + __expf(-fmaxf(g, -80.0f))); }
+
+// Correctly rounded fp32 quotient x / s from inv = 1/s (itself correctly rounded), by one
+// residual correction (Markstein's method: q0 = x*inv, r = x - q0*s exactly by FMA,
+// q = q0 + r*inv); valid while x / s and the residual stay in the normal range, as for the
+// e4m3 requantisation (|x / s| <= 448).  Three FMA-pipe operations instead of a full-range
+// division per element.
+KLT_DEV float quot_rn(float x, float s, float inv) {
+  const float q0 = x * inv;
+  const float r = fmaf(-q0, s, x);
+  return fmaf(r, inv, q0);
+}
+// 1/s for normal s: the fast reciprocal refined by one Newton step (error well below
+// 1 ulp), for quot_rn when s differs from element to element.
+KLT_DEV float rcp_nr(float s) {
+  const float y0 = __fdividef(1.0f, s);
+  return fmaf(fmaf(-s, y0, 1.0f), y0, y0);
+}
 
 // Four consecutive fp32 atomically added to global memory (16-byte aligned), one request.
 KLT_DEV void red_add_v4(float* dst, float a, float b, float c, float d) {

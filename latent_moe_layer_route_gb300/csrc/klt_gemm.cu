@@ -793,7 +793,7 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
       for (int j = 0; j < COLS; ++j) {
         if (c0 + j < info.rows)
           dst[static_cast<size_t>(info.row0 + c0 + j) * p.Is] =
-              __float2bfloat16_rn(silu_f(g[j]) * u[j]);
+              __float2bfloat16_rn(silu_fast(g[j]) * u[j]);
       }
       if (p.sh_done != nullptr) signal_done(p.sh_done + info.dep_idx, ew, lane, C::EPI_THREADS);
     } else if (kind == TASK_OUT) {
@@ -818,7 +818,7 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
       float* red = sm.red + ew * COLS;
 #pragma unroll
       for (int j = 0; j < COLS; ++j) {
-        g[j] = silu_f(g[j]) * u[j];
+        g[j] = silu_fast(g[j]) * u[j];
         float a = fabsf(g[j]);
 #pragma unroll
         for (int o = 16; o; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
@@ -831,10 +831,12 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
       for (int j = 0; j < COLS; ++j) {
         const float amax = fmaxf(fmaxf(r0[j], r0[COLS + j]), fmaxf(r0[2 * COLS + j],
                                                                    r0[3 * COLS + j]));
-        const float s = amax == 0.f ? 1.0f : amax / 448.0f;
+        // s = fp32(amax / 448) exactly (quotient by the correctly rounded 1/448)
+        const float s = amax == 0.f ? 1.0f : quot_rn(amax, 448.0f, 1.0f / 448.0f);
+        const float inv = rcp_nr(s);
         if (c0 + j < info.rows) {
           const size_t pp = static_cast<size_t>(info.row0 + c0 + j);
-          const uint8_t code = f32_to_e4m3(g[j] / s);
+          const uint8_t code = f32_to_e4m3(quot_rn(g[j], s, inv));
           dst[pp * p.I] = code;
           if (p.aqb != nullptr)
             p.aqb[pp * p.I + static_cast<size_t>(info.ftile) * 128 + row] =

@@ -41,11 +41,11 @@ struct W {
   static constexpr int NACC = TMEM_COLS / TN;
   static constexpr int US = 8;
   // Registers: 384 threads launch with 168 each (3 warps share a scheduler); the control
-  // warpgroup drops to 80 and the two epilogue warpgroups rise to 200, within the
+  // warpgroup drops to 56 and the two epilogue warpgroups rise to 216, within the
   // registers released.
   static constexpr int LAUNCH_REGS = 168;
-  static constexpr int REGS_CTRL = 80;
-  static constexpr int REGS_EPI = 200;
+  static constexpr int REGS_CTRL = 56;
+  static constexpr int REGS_EPI = 216;
   static_assert(4 * (LAUNCH_REGS - REGS_CTRL) >= 8 * (REGS_EPI - LAUNCH_REGS),
                 "register hand-over must balance");
   static_assert(NACC == 2, "two accumulator slots");
@@ -149,8 +149,10 @@ __device__ WUnit w_decode(const GemmParams& p, const int* s_tile_off, const int*
           info.kb0 = info.kb1 = 0;
           info.dep_idx = u / W::TM;
         } else {
-          const int nt = u / T.ftiles;
-          const int ft = u - nt * T.ftiles;
+          // feature-tile major: every token tile of a weight tile runs close together in
+          // time, so each weight tile is read from DRAM once and stays hot in L2
+          const int ft = u / T.ntiles;
+          const int nt = u - ft * T.ntiles;
           info.row0 = nt * W::TM;
           info.rows = min(W::TM, p.M - info.row0);
           info.ftile = ft;
@@ -201,9 +203,9 @@ __device__ bool w_wait_dependency(const GemmParams& p, int dep, int idx, const i
 // ------------------------------------------------------------------ producer (1 thread)
 __device__ void w_producer(const GemmParams& p, WSmem& sm, const int* s_tile_off,
                            const int* s_off) {
-  // weights are re-read by every token tile of their expert and tokens by every feature
-  // tile: both stay at normal L2 priority
+  // weights are re-read by every token tile of their expert, tokens by every feature tile
   const uint64_t pol = policy_evict_normal();
+  const uint64_t pol_w = policy_evict_last();
   int stage = 0, us = 0;
   uint32_t phase = 0, uphase = 0;
   long long issued = 0;
@@ -230,9 +232,9 @@ __device__ void w_producer(const GemmParams& p, WSmem& sm, const int* s_tile_off
       const uint8_t* a = T.a_ptr[m];
       const size_t akb = static_cast<size_t>(T.a_kb[m]);
       bulk_load(st, a + (static_cast<size_t>(info.rb0) * akb + kk) * W::W_TILE, W::W_TILE,
-                &sm.full[stage], pol);
+                &sm.full[stage], pol_w);
       bulk_load(st + W::W_TILE, a + (static_cast<size_t>(info.rb1) * akb + kk) * W::W_TILE,
-                W::W_TILE, &sm.full[stage], pol);
+                W::W_TILE, &sm.full[stage], pol_w);
     };
     auto issue_t = [&](int kb, uint8_t* st, uint64_t* bar) {
       const int m = kb < T.kb_split0 ? 0 : 1;
@@ -274,7 +276,7 @@ __device__ void w_producer(const GemmParams& p, WSmem& sm, const int* s_tile_off
     ++published;
     for (; kb < info.kb1; ++kb) {
       if (p.stall_after > 0 && issued >= p.stall_after) { stalled = true; break; }
-      if (!mbar_wait(&sm.empty[stage], phase ^ 1, sm.abort_flag, p.err, p.timeout)) {
+      if (!mbar_wait_spin(&sm.empty[stage], phase ^ 1, sm.abort_flag, p.err, p.timeout)) {
         stalled = true;
         break;
       }
@@ -323,18 +325,18 @@ __device__ void w_mma(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
     const uint32_t idesc = fp8 ? idesc_fp8 : idesc_bf16;
     const int kb0 = info.kb0, kb1 = info.kb1;
     if (!promote) {
-      if (!mbar_wait(&sm.tempty[acc], aphase ^ 1, sm.abort_flag, p.err, p.timeout)) break;
+      if (!mbar_wait_spin(&sm.tempty[acc], aphase ^ 1, sm.abort_flag, p.err, p.timeout)) break;
       tc_fence_after();
     }
     int gpos = 0;  // position of the next k-block in its promotion group
     for (int kb = kb0; kb < kb1; ++kb) {
-      if (!mbar_wait(&sm.full[stage], phase, sm.abort_flag, p.err, p.timeout)) {
+      if (!mbar_wait_spin(&sm.full[stage], phase, sm.abort_flag, p.err, p.timeout)) {
         ok = false;
         break;
       }
       tc_fence_after();
       if (promote && gpos == 0) {
-        if (!mbar_wait(&sm.tempty[acc], aphase ^ 1, sm.abort_flag, p.err, p.timeout)) {
+        if (!mbar_wait_spin(&sm.tempty[acc], aphase ^ 1, sm.abort_flag, p.err, p.timeout)) {
           ok = false;
           break;
         }
@@ -455,6 +457,13 @@ __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
     }
     const bool pair = is_pair(kind);
     const bool valid = tok < info.rows;
+    // combine target of a routed L2 row, fetched while the products are computed
+    int tg = 0;
+    float wv = 0.f;
+    if (kind == TASK_ROUTED_L2 && valid) {
+      tg = __ldg(p.gidx + info.row0 + tok);
+      wv = __ldg(p.wperm + info.row0 + tok);
+    }
     // TMEM columns of this thread's two 64-column groups
     const uint32_t col0 = pair ? half * 64 : half * 128;
     const uint32_t col1 = pair ? 128 + half * 64 : half * 128 + 64;
@@ -479,13 +488,24 @@ __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
         sw0 = p.w2_s + (static_cast<size_t>(info.e) * G_L + 2 * info.ftile + half) * G_I + g0;
         sw1 = sw0;
       }
-      float sa_next = valid ? __ldcg(ts) : 0.f;
+      // scales are loaded two groups ahead so no global load sits between the
+      // accumulator hand-offs
+      auto tok_scale = [&](int gi) {
+        return valid && gi < ng ? __ldcg(ts + static_cast<size_t>(gi) * p.cap) : 0.f;
+      };
+      auto w_scale = [&](const float* sw, int gi) { return gi < ng ? __ldg(sw + gi) : 0.f; };
+      float sa1 = tok_scale(0), w01 = w_scale(sw0, 0), w11 = w_scale(sw1, 0);
+      float sa2 = tok_scale(1), w02 = w_scale(sw0, 1), w12 = w_scale(sw1, 1);
       for (int gi = 0; gi < ng; ++gi) {
-        const float sa = sa_next;
-        if (gi + 1 < ng) sa_next = valid ? __ldcg(ts + static_cast<size_t>(gi + 1) * p.cap) : 0.f;
-        const float s0 = __ldg(sw0 + gi) * sa;
-        const float s1 = __ldg(sw1 + gi) * sa;
-        if (!mbar_wait(&sm.tfull[acc], aphase, sm.abort_flag, p.err, p.timeout)) return;
+        const float s0 = w01 * sa1;
+        const float s1 = w11 * sa1;
+        sa1 = sa2;
+        w01 = w02;
+        w11 = w12;
+        sa2 = tok_scale(gi + 2);
+        w02 = w_scale(sw0, gi + 2);
+        w12 = w_scale(sw1, gi + 2);
+        if (!mbar_wait_spin(&sm.tfull[acc], aphase, sm.abort_flag, p.err, p.timeout)) return;
         tc_fence_after();
         const uint32_t tb = tmem_base + lane_base + static_cast<uint32_t>(acc * W::TN);
         float v[4][16];
@@ -497,19 +517,20 @@ __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
           for (int i = 0; i < 16; ++i) a[c * 16 + i] = fmaf(v[c][i], s0, a[c * 16 + i]);
         tmem_ld16x4(tb + col1, tb + col1 + 16, tb + col1 + 32, tb + col1 + 48, v[0], v[1],
                     v[2], v[3]);
+        // the slot's contents are in registers: hand it back before the last FMAs
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.tempty[acc]);
+        if (++acc == W::NACC) { acc = 0; aphase ^= 1; }
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             a[64 + c * 16 + i] = fmaf(v[c][i], s1, a[64 + c * 16 + i]);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.tempty[acc]);
-        if (++acc == W::NACC) { acc = 0; aphase ^= 1; }
         if (ew == 0 && lane == 0) trace_mark(p, 2, steps++);
       }
     } else {
-      if (!mbar_wait(&sm.tfull[acc], aphase, sm.abort_flag, p.err, p.timeout)) return;
+      if (!mbar_wait_spin(&sm.tfull[acc], aphase, sm.abort_flag, p.err, p.timeout)) return;
       tc_fence_after();
       const uint32_t tb = tmem_base + lane_base + static_cast<uint32_t>(acc * W::TN);
       tmem_ld16x4(tb + col0, tb + col0 + 16, tb + col0 + 32, tb + col0 + 48, a, a + 16,
@@ -538,6 +559,7 @@ __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
       named_bar_sync(1, W::EPI_THREADS);
       const float amax = fmaxf(am[tok], am[W::TM + tok]);
       const float sc = amax == 0.f ? 1.0f : amax / 448.0f;
+      const float inv = 1.0f / sc;
       if (valid) {
         const size_t pp = static_cast<size_t>(info.row0 + tok);
         const size_t col = static_cast<size_t>(info.ftile) * 128 + half * 64;
@@ -548,10 +570,10 @@ __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int i = c * 16 + q * 4;
-            w4[q] = static_cast<uint32_t>(f32_to_e4m3(a[i] / sc)) |
-                    (static_cast<uint32_t>(f32_to_e4m3(a[i + 1] / sc)) << 8) |
-                    (static_cast<uint32_t>(f32_to_e4m3(a[i + 2] / sc)) << 16) |
-                    (static_cast<uint32_t>(f32_to_e4m3(a[i + 3] / sc)) << 24);
+            w4[q] = static_cast<uint32_t>(f32_to_e4m3(quot_rn(a[i], sc, inv))) |
+                    (static_cast<uint32_t>(f32_to_e4m3(quot_rn(a[i + 1], sc, inv))) << 8) |
+                    (static_cast<uint32_t>(f32_to_e4m3(quot_rn(a[i + 2], sc, inv))) << 16) |
+                    (static_cast<uint32_t>(f32_to_e4m3(quot_rn(a[i + 3], sc, inv))) << 24);
           }
           dq[c] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           if (p.aqb != nullptr) {  // exact bf16 images of the codes
@@ -589,9 +611,6 @@ __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
     } else if (kind == TASK_ROUTED_L2) {
       // weighted scatter-combine into the token's fp32 row of r
       if (valid) {
-        const int pp = info.row0 + tok;
-        const int tg = __ldg(p.gidx + pp);
-        const float wv = __ldg(p.wperm + pp);
         float* dst = p.r + static_cast<size_t>(tg) * p.L + info.ftile * 256 + half * 128;
 #pragma unroll
         for (int i = 0; i < 128; i += 4)
