@@ -142,7 +142,8 @@ typedef struct klt_routing {
  *     16, 32, 64 or 128 = feature-major engine (128 weight rows x force_bn tokens per
  *     MMA); 256 = token-major engine (128 tokens x 256 features per MMA; needs H and L
  *     multiples of 256 and the fused schedule, else KLT_ERR_UNSUPPORTED); 0 = chosen
- *     from M (token-major from 1024 tokens on when available). */
+ *     from M (feature-major with 16-token tiles up to 16 tokens, token-major above when
+ *     available). */
 typedef struct klt_debug {
   uint8_t* zq;
   float* zs;

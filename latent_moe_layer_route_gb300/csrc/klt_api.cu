@@ -63,7 +63,7 @@ constexpr int kNumBN = 4;
 constexpr int kBN[kNumBN] = {16, 32, 64, 128};
 constexpr int kMaxSplitUnits = 3 * 160;  // split-K tiles*splits bound per task
 constexpr int kMaxCounters = 8192;       // arrival counters per split launch
-constexpr int kWideMinTokens = 1024;  // token-major engine from this batch size on
+constexpr int kWideMinTokens = 17;  // token-major engine above the 16-token decode tile
 constexpr int kRoutedSplitPairs = 0;  // routed L1 k-splits when M * topk <= this (off: the
                                       // split reduce outweighs the balance it buys)
 

@@ -97,14 +97,21 @@ def test_token_major_engine_on_several_feature_tiles(fmt):
         tail.close()
 
 
-def test_token_major_engine_is_chosen_for_large_batches_only():
+def test_token_major_engine_with_long_k():
+    # a small batch with long K: the output GEMM's k loop crosses from the up-projection
+    # into the shared down projection far from the first k-block
+    cfg = configs.SMALL.with_(H=2048, L=1024, I=256, Is=256, E=8, topk=2, seed=36)
+    run_case(cfg, M=40, force_bn=256)
+
+
+def test_token_major_engine_is_chosen_above_the_decode_tile():
     cfg = configs.SMALL.with_(seed=34)
     _, w_gpu = weights_for(cfg)
     tail = B.LatentMoETail(cfg, w_gpu, max_tokens=2048)
     phased = B.LatentMoETail(cfg, w_gpu, max_tokens=2048, flags=B.KLT_FLAG_PHASED)
     try:
-        assert tail.gemm_tile(2048) == 256 and tail.gemm_tile(1024) == 256
-        assert tail.gemm_tile(1023) == 64 and tail.gemm_tile(16) == 16
+        assert tail.gemm_tile(2048) == 256 and tail.gemm_tile(17) == 256
+        assert tail.gemm_tile(16) == 16 and tail.gemm_tile(1) == 16
         assert tail.gemm_tile(16, 128) == 128
         assert phased.gemm_tile(2048) == 64
         assert phased.gemm_tile(2048, 256) == -B.KLT_ERR_UNSUPPORTED
