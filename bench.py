@@ -158,7 +158,7 @@ def run_reference(cfg, args, ws, rank):
     from latent_moe_layer_route_gb300 import inputs
     from oracle import model as oracle_model
     act, w = inputs.make_inputs(cfg)
-    sample = min(cfg.M, 2)
+    sample = 1  # one token per step keeps K + W oracle steps within a few minutes
     tok = np.arange(sample)
     for _ in range(args.warmup):
         oracle_model.tail(act, w, cfg, tokens=tok)
