@@ -64,8 +64,6 @@ constexpr int kBN[kNumBN] = {16, 32, 64, 128};
 constexpr int kMaxSplitUnits = 3 * 160;  // split-K tiles*splits bound per task
 constexpr int kMaxCounters = 8192;       // arrival counters per split launch
 constexpr int kWideMinTokens = 17;  // token-major engine above the 16-token decode tile
-constexpr int kRoutedSplitPairs = 0;  // routed L1 k-splits when M * topk <= this (off: the
-                                      // split reduce outweighs the balance it buys)
 
 }  // namespace
 
@@ -88,7 +86,6 @@ struct klt_handle {
   int dep_routed, dep_ntiles;
   int cap, max_hist_blocks;
   bool wide_ok;  // token-major engine usable (dims and launch register count)
-  long long ws_routed_floats;
   // descriptors per BN variant (token-side maps depend on the box height)
   CUtensorMap tm_zqp[kNumBN], tm_aq[kNumBN], tm_n[kNumBN], tm_as[kNumBN];
   void* allocs[48];
@@ -242,16 +239,8 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
   KLT_ALLOC(h->r, Mx * L * 4);
   KLT_ALLOC(h->n, Mx * L * 2);
   KLT_ALLOC(h->a_s, Mx * Is * 2);
-  // split-K partials: [shared L1 | routed L1 | output GEMM]
-  h->ws_routed_floats =
-      kRoutedSplitPairs == 0
-          ? 0
-          : static_cast<long long>(kRoutedSplitPairs / 16 + E) * (I / 128) * 2 * 2 * 16 * 128;
-  for (int bn = 32; bn <= 128 && kRoutedSplitPairs > 0; bn *= 2)
-    h->ws_routed_floats = std::max<long long>(
-        h->ws_routed_floats,
-        static_cast<long long>((kRoutedSplitPairs + bn - 1) / bn + E) * (I / 128) * 2 * 2 * bn * 128);
-  KLT_ALLOC(h->ws, (2LL * kMaxSplitUnits * 2 * 128 * 128 + h->ws_routed_floats) * 4);
+  // split-K partials: [shared L1 | output GEMM], one half each
+  KLT_ALLOC(h->ws, 2LL * kMaxSplitUnits * 2 * 128 * 128 * 4);
   KLT_ALLOC(h->split_cnt, 2LL * kMaxCounters * 4);
   KLT_ALLOC(h->sched, 64 * 4);
   h->dep_routed = static_cast<int>((cap + 15) / 16 + E);
@@ -549,14 +538,10 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
       R.ftiles = I / 128;
       R.kb_total = L / rkb;
       R.kb_split0 = R.kb_total;
-      // decode sizes: two k-splits per routed tile so the units are small enough to balance
-      const long long routed_tiles_max = static_cast<long long>((Mk + BN - 1) / BN + E) * R.ftiles;
-      R.ksplit = (Mk <= kRoutedSplitPairs && R.kb_total >= 8 &&
-                  routed_tiles_max + kMaxSplitUnits <= kMaxCounters)
-                     ? 2 : 1;
-      R.kb_per_split = (R.kb_total + R.ksplit - 1) / R.ksplit;
-      if (R.kpg > 1) R.kb_per_split = (R.kb_per_split + R.kpg - 1) / R.kpg * R.kpg;
-      R.ksplit = (R.kb_total + R.kb_per_split - 1) / R.kb_per_split;
+      // routed units stay whole in K (measured: a k-split's reduce costs more than the
+      // balance it buys)
+      R.ksplit = 1;
+      R.kb_per_split = R.kb_total;
       R.a_rb_up = I / 128;
       R.a_rb_expert = 2 * I / 128;
       R.a_kb[0] = R.a_kb[1] = L / rkb;
@@ -574,9 +559,6 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
       S.ws_tile_base = 0;
       S.ws_off = 0;
       plan_split(S, ntiles, ntiles * S.ftiles * std::max(1, S.kb_total / 8), BN);
-      // routed partials and counters follow the shared ones
-      R.ws_tile_base = S.ntiles * S.ftiles;
-      R.ws_off = static_cast<long long>(kMaxSplitUnits) * 2 * 128 * 128;
       if (!encode_2d(&S.tmB[0], x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, H, BN))
         return KLT_ERR_CUDA;
       S.a_ptr[0] = S.a_ptr[1] = reinterpret_cast<const uint8_t*>(h->ws13);
@@ -618,7 +600,7 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
       if (fused) {
         // units come from the launch-wide counter, after the other tasks' units
         O.ws_tile_base = kMaxCounters;
-        O.ws_off = static_cast<long long>(ws_task) + h->ws_routed_floats;
+        O.ws_off = static_cast<long long>(ws_task);
         plan_split(O, ntiles, 2 * grid, BN);
       } else if (O.units < 4 * grid) {
         // static stream-K: every CTA streams the same number of k-blocks (no more CTAs than
@@ -691,7 +673,7 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
       g3.ntasks = 1;
       g3.sched = h->sched + 2;
       g3.trace = trace ? trace + 2 * trace_launch : nullptr;
-      g3.ws = h->ws + ws_task + h->ws_routed_floats;
+      g3.ws = h->ws + ws_task;
       g3.cnt = h->split_cnt + kMaxCounters;
       KLT_LAUNCH(launch_gemm(g3, BN, grid, s, pdl));
     }
