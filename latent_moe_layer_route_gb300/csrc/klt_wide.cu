@@ -62,6 +62,10 @@ struct WUnit {
   int dep_idx;  // routed token tile (routed kinds) or token tile (others)
 };
 
+// Row stride (floats) of the combine staging: 16 features + 1, so a column written by the
+// 32 lanes of a warp touches 32 different banks.
+constexpr int STG_LD = 17;
+
 struct WSmem {
   uint8_t* stages;
   uint64_t *full, *empty, *tfull, *tempty, *ufull, *uempty, *drain;
@@ -70,11 +74,13 @@ struct WSmem {
   int* abort_flag;
   float* amax;  // [2 unit parities][2 column halves][TM]
   float* part;  // [EPI_WARPS] norm partial sums
+  float* stg;   // [EPI_WARPS][32 tokens][STG_LD] per-warp transpose staging of the combine
 
   static constexpr int BAR_BYTES = 8 * (2 * W::STAGES + 2 * W::NACC + 2 * W::US + 1);
   static constexpr int bytes() {
     return W::STAGES * W::STAGE_BYTES + BAR_BYTES + W::US * (int)sizeof(WUnit) + 64 +
-           4 * W::TM * 4 + W::EPI_WARPS * 4 + 1024 /* alignment slack */;
+           4 * W::TM * 4 + W::EPI_WARPS * 4 + W::EPI_WARPS * 32 * STG_LD * 4 +
+           1024 /* alignment slack */;
   }
   __device__ explicit WSmem(uint8_t* raw) {
     uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -93,6 +99,7 @@ struct WSmem {
     abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
     amax = reinterpret_cast<float*>(tmem_holder + 16);
     part = amax + 4 * W::TM;
+    stg = part + W::EPI_WARPS;
   }
 };
 
@@ -609,12 +616,29 @@ __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
       }
       if (p.sh_done != nullptr) w_signal(p.sh_done + info.dep_idx, ew, lane);
     } else if (kind == TASK_ROUTED_L2) {
-      // weighted scatter-combine into the token's fp32 row of r
-      if (valid) {
-        float* dst = p.r + static_cast<size_t>(tg) * p.L + info.ftile * 256 + half * 128;
+      // Weighted scatter-combine into the tokens' fp32 rows of r.  A lane holds one token's
+      // 128 features; 16 features of the warp's 32 tokens at a time pass through shared
+      // memory, so each vector reduction instruction covers 8 tokens x 64 contiguous bytes
+      // (8 L2 requests) instead of 32 tokens x 16 bytes.
+      float* st = sm.stg + ew * 32 * STG_LD;
+      const size_t col0 = static_cast<size_t>(info.ftile) * 256 + half * 128;
 #pragma unroll
-        for (int i = 0; i < 128; i += 4)
-          red_add_v4(dst + i, wv * a[i], wv * a[i + 1], wv * a[i + 2], wv * a[i + 3]);
+      for (int c = 0; c < 8; ++c) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) st[lane * STG_LD + i] = wv * a[16 * c + i];
+        __syncwarp();
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+          const int t = it * 8 + (lane >> 2);  // token (lane) of the warp this lane reduces
+          const int q = lane & 3;              // its 4-feature quad within the 16
+          const int tgt = __shfl_sync(0xFFFFFFFFu, tg, t);
+          const bool ok = __shfl_sync(0xFFFFFFFFu, valid ? 1 : 0, t) != 0;
+          const float* sv = st + t * STG_LD + 4 * q;
+          if (ok)
+            red_add_v4(p.r + static_cast<size_t>(tgt) * p.L + col0 + 16 * c + 4 * q, sv[0],
+                       sv[1], sv[2], sv[3]);
+        }
+        __syncwarp();
       }
       if (p.l2_done != nullptr) w_signal(p.l2_done, ew, lane);
     } else {  // TASK_OUT
