@@ -40,6 +40,8 @@ struct W {
   static constexpr int TMEM_COLS = 512;
   static constexpr int NACC = TMEM_COLS / TN;
   static constexpr int US = 8;
+  static constexpr int SIG = 8;             // completion-signal ring (epilogue -> signaller)
+  static constexpr int SIGNAL_WARP = 2;     // control warp that publishes unit completions
   // Registers: 384 threads launch with 168 each (3 warps share a scheduler); the control
   // warpgroup drops to 56 and the two epilogue warpgroups rise to 216, within the
   // registers released.
@@ -68,7 +70,8 @@ constexpr int STG_LD = 17;
 
 struct WSmem {
   uint8_t* stages;
-  uint64_t *full, *empty, *tfull, *tempty, *ufull, *uempty, *drain;
+  uint64_t *full, *empty, *tfull, *tempty, *ufull, *uempty, *sfull, *sempty, *drain;
+  int** sptr;  // [SIG] counter each completion signal increments (null: end of work)
   WUnit* ring;
   uint32_t* tmem_holder;
   int* abort_flag;
@@ -76,7 +79,8 @@ struct WSmem {
   float* part;  // [EPI_WARPS] norm partial sums
   float* stg;   // [EPI_WARPS][32 tokens][STG_LD] per-warp transpose staging of the combine
 
-  static constexpr int BAR_BYTES = 8 * (2 * W::STAGES + 2 * W::NACC + 2 * W::US + 1);
+  static constexpr int BAR_BYTES =
+      8 * (2 * W::STAGES + 2 * W::NACC + 2 * W::US + 2 * W::SIG + 1) + 8 * W::SIG;
   static constexpr int bytes() {
     return W::STAGES * W::STAGE_BYTES + BAR_BYTES + W::US * (int)sizeof(WUnit) + 64 +
            4 * W::TM * 4 + W::EPI_WARPS * 4 + W::EPI_WARPS * 32 * STG_LD * 4 +
@@ -93,8 +97,11 @@ struct WSmem {
     tempty = tfull + W::NACC;
     ufull = tempty + W::NACC;
     uempty = ufull + W::US;
-    drain = uempty + W::US;
-    ring = reinterpret_cast<WUnit*>(drain + 1);
+    sfull = uempty + W::US;
+    sempty = sfull + W::SIG;
+    drain = sempty + W::SIG;
+    sptr = reinterpret_cast<int**>(drain + 1);
+    ring = reinterpret_cast<WUnit*>(sptr + W::SIG);
     tmem_holder = reinterpret_cast<uint32_t*>(ring + W::US);
     abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
     amax = reinterpret_cast<float*>(tmem_holder + 16);
@@ -376,16 +383,41 @@ __device__ void w_mma(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
 }
 
 // ------------------------------------------------------------------ epilogue
-// After the epilogue barrier one gpu-scope release add publishes every epilogue thread's
-// writes of the unit (release is cumulative over the barrier).
-__device__ __forceinline__ void w_signal(int* counter, int ew, int lane) {
-  named_bar_sync(1, W::EPI_THREADS);
-  if (ew == 0 && lane == 0) red_release_gpu_add(counter, 1);
+// Unit completion: every epilogue warp arrives (release, CTA scope) on the next slot of
+// the signal ring once its writes of the unit are issued; the signalling warp acquires the
+// completed phase and publishes with one gpu-scope release add (cumulative over what it
+// acquired), so the epilogue never waits for its own writes to become visible.
+struct SigState {
+  int slot = 0;
+  uint32_t phase = 0;
+};
+__device__ __forceinline__ void w_signal(const GemmParams& p, WSmem& sm, SigState& sg,
+                                         int* counter, int ew, int lane) {
+  if (lane == 0)  // the slot's previous request has been published
+    mbar_wait(&sm.sempty[sg.slot], sg.phase ^ 1, sm.abort_flag, p.err, p.timeout);
+  __syncwarp();
+  if (ew == 0 && lane == 0) sm.sptr[sg.slot] = counter;
+  if (lane == 0) mbar_arrive(&sm.sfull[sg.slot]);
+  if (++sg.slot == W::SIG) { sg.slot = 0; sg.phase ^= 1; }
+}
+
+__device__ void w_signaller(const GemmParams& p, WSmem& sm) {
+  int slot = 0;
+  uint32_t phase = 0;
+  for (;;) {
+    if (!mbar_wait(&sm.sfull[slot], phase, sm.abort_flag, p.err, p.timeout)) return;
+    int* counter = sm.sptr[slot];
+    if (counter == nullptr) return;  // end of work
+    red_release_gpu_add(counter, 1);
+    mbar_arrive(&sm.sempty[slot]);
+    if (++slot == W::SIG) { slot = 0; phase ^= 1; }
+  }
 }
 
 // RMSNorm of one token row of the fp32 combine: fp32 statistic, gamma applied, one bf16
 // rounding (the output GEMM's token operand).  The epilogue threads split the row.
-__device__ void w_norm_row(const GemmParams& p, WSmem& sm, int row, int ew, int lane) {
+__device__ void w_norm_row(const GemmParams& p, WSmem& sm, SigState& sg, int row, int ew,
+                           int lane) {
   const size_t t = static_cast<size_t>(row);
   const float4* rv = reinterpret_cast<const float4*>(p.r + t * p.L);
   const int etid = ew * 32 + lane;
@@ -430,7 +462,7 @@ __device__ void w_norm_row(const GemmParams& p, WSmem& sm, int row, int ew, int 
     }
   }
   named_bar_sync(1, W::EPI_THREADS);  // sm.part is reused by the next row
-  w_signal(p.norm_done + row / W::TM, ew, lane);
+  w_signal(p, sm, sg, p.norm_done + row / W::TM, ew, lane);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
@@ -447,6 +479,7 @@ __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
   const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
   int us = 0, acc = 0, steps = 0, l1_units = 0;
   uint32_t uphase = 0, aphase = 0;
+  SigState sg;
   const int G_L = p.L / 128, G_I = p.I / 128;
 
   for (;;) {
@@ -455,11 +488,14 @@ __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.uempty[us]);
     if (++us == W::US) { us = 0; uphase ^= 1; }
-    if (info.task < 0) return;
+    if (info.task < 0) {
+      w_signal(p, sm, sg, nullptr, ew, lane);  // releases the signalling warp
+      return;
+    }
     const GemmTask& T = p.task[info.task];
     const int kind = T.kind;
     if (kind == TASK_NORM) {
-      w_norm_row(p, sm, info.row0, ew, lane);
+      w_norm_row(p, sm, sg, info.row0, ew, lane);
       continue;
     }
     const bool pair = is_pair(kind);
@@ -598,7 +634,7 @@ __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
         }
         if (half == 0) p.asT[static_cast<size_t>(info.ftile) * p.cap + pp] = sc;
       }
-      if (p.l1_done != nullptr) w_signal(p.l1_done + info.dep_idx, ew, lane);
+      if (p.l1_done != nullptr) w_signal(p, sm, sg, p.l1_done + info.dep_idx, ew, lane);
     } else if (kind == TASK_SHARED_L1) {
       if (valid) {
         uint4* dst = reinterpret_cast<uint4*>(
@@ -614,7 +650,7 @@ __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
           dst[c] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
       }
-      if (p.sh_done != nullptr) w_signal(p.sh_done + info.dep_idx, ew, lane);
+      if (p.sh_done != nullptr) w_signal(p, sm, sg, p.sh_done + info.dep_idx, ew, lane);
     } else if (kind == TASK_ROUTED_L2) {
       // Weighted scatter-combine into the tokens' fp32 rows of r.  A lane holds one token's
       // 128 features; 16 features of the warp's 32 tokens at a time pass through shared
@@ -640,7 +676,7 @@ __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
         }
         __syncwarp();
       }
-      if (p.l2_done != nullptr) w_signal(p.l2_done, ew, lane);
+      if (p.l2_done != nullptr) w_signal(p, sm, sg, p.l2_done, ew, lane);
     } else {  // TASK_OUT
       if (valid) {
         uint4* dst = reinterpret_cast<uint4*>(
@@ -673,6 +709,10 @@ __global__ void __launch_bounds__(W::THREADS, 1) wide_kernel(const __grid_consta
     for (int u = 0; u < W::US; ++u) {
       mbar_init(&sm.ufull[u], 1);
       mbar_init(&sm.uempty[u], 1 + W::EPI_WARPS);
+    }
+    for (int g = 0; g < W::SIG; ++g) {
+      mbar_init(&sm.sfull[g], W::EPI_WARPS);
+      mbar_init(&sm.sempty[g], 1);
     }
     mbar_init(sm.drain, 1);
     *sm.abort_flag = 0;
@@ -711,6 +751,8 @@ __global__ void __launch_bounds__(W::THREADS, 1) wide_kernel(const __grid_consta
       if (lane == 0) w_producer(p, sm, s_tile_off, s_off);
     } else if (warp == 1) {
       if (lane == 0) w_mma(p, sm, tmem_base);
+    } else if (warp == W::SIGNAL_WARP) {
+      if (lane == 0) w_signaller(p, sm);
     }
   } else {
     regs_inc<W::REGS_EPI>();
