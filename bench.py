@@ -103,9 +103,12 @@ class Clocks:
 # kernel, from one ncu capture of `bench.py --steps 2 --warmup 3 --no-cpu-baseline` on the
 # workload, valid only while the kernel sources hash to the recorded digest.
 NCU_TRAFFIC = {
-    ("decode_m16_e64_k8_fp8", "gemm_fused"): (718447872, "4d5da6fe7530ee8a"),
+    ("decode_m16_e64_k8_fp8", "gemm_fused"): (718250752, "021f38001034969e"),
+    ("decode_m128_e64_k8_fp8_biased", "gemm_fused"): (817384448, "021f38001034969e"),
+    ("prefill_m4096_e64_k8_fp8_zipf", "gemm_fused"): (1827365136, "021f38001034969e"),
 }
-KERNEL_SOURCES = ("klt_gemm.cu", "klt_device.cuh", "klt_internal.h", "klt_api.cu")
+KERNEL_SOURCES = ("klt_gemm.cu", "klt_wide.cu", "klt_device.cuh", "klt_internal.h", "klt_api.cu",
+                  "klt_route.cu")
 
 
 def kernel_digest() -> str:
@@ -269,14 +272,23 @@ def main():
     # ---- timed region: device time of each step, L2 flushed between steps
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    def load_for(seconds):  # the same steps, untimed, so clock samples see the timed load
+        t_end = time.perf_counter() + seconds
+        while time.perf_counter() < t_end:
+            for _ in range(10):
+                flush.zero_()
+                step()
+            torch.cuda.synchronize()
+
     with Clocks(local) as clk:
-        torch.cuda.synchronize()
+        load_for(0.5)
         for i in range(args.steps):
             flush.zero_()
             starts[i].record(stream)
             step()
             ends[i].record(stream)
         torch.cuda.synchronize()
+        load_for(0.5)
     if ws > 1:
         dist.barrier()
     ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
@@ -398,7 +410,9 @@ def main():
         "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": nl * args.steps,
-        "clocks": clk.summary(),
+        "clocks": {**clk.summary(),
+                   "window": "nvidia-smi every 200 ms, timed steps bracketed by 0.5 s of the "
+                             "same steps on each side"},
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, act_cpu, w_cpu)
