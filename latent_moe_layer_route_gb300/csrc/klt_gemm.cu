@@ -32,7 +32,10 @@ namespace {
 template <int BN>
 struct Cfg {
   static constexpr int EPI_WARPS = BN >= 64 ? 8 : 4;
-  static constexpr int THREADS = (2 + EPI_WARPS) * 32;
+  // producer, MMA issuer, epilogue warps, completion signaller
+  static constexpr int SIGNAL_WARP = 2 + EPI_WARPS;
+  static constexpr int THREADS = (3 + EPI_WARPS) * 32;
+  static constexpr int SIG = 8;  // completion-signal ring (epilogue -> signaller)
   static constexpr int EPI_THREADS = EPI_WARPS * 32;
   static constexpr int A_BYTES = 128 * 128;
   static constexpr int B_BYTES = BN * 128;
@@ -89,7 +92,8 @@ template <int BN>
 struct Smem {
   using C = Cfg<BN>;
   uint8_t* stages;
-  uint64_t *full, *empty, *tfull, *tempty, *ufull, *uempty, *drain;
+  uint64_t *full, *empty, *tfull, *tempty, *ufull, *uempty, *sfull, *sempty, *drain;
+  int** sptr;  // [SIG] counter each completion signal increments (null: end of work)
   UnitInfo* ring;
   uint32_t* tmem_holder;
   int* abort_flag;
@@ -97,7 +101,8 @@ struct Smem {
   float* red;  // [EPI_WARPS][COLS]
   float* sc;   // [2][SC_FLOATS]
 
-  static constexpr int BAR_BYTES = 8 * (2 * C::STAGES + 2 * C::NACC + 2 * C::US + 1);
+  static constexpr int BAR_BYTES =
+      8 * (2 * C::STAGES + 2 * C::NACC + 2 * C::US + 2 * C::SIG + 1) + 8 * C::SIG;
   static constexpr int bytes() {
     return C::STAGES * C::STAGE_BYTES + BAR_BYTES + C::US * (int)sizeof(UnitInfo) + 64 +
            C::EPI_WARPS * C::COLS * 4 + 2 * C::SC_FLOATS * 4 + 1024 /* alignment slack */;
@@ -113,8 +118,11 @@ struct Smem {
     tempty = tfull + C::NACC;
     ufull = tempty + C::NACC;
     uempty = ufull + C::US;
-    drain = uempty + C::US;
-    ring = reinterpret_cast<UnitInfo*>(drain + 1);
+    sfull = uempty + C::US;
+    sempty = sfull + C::SIG;
+    drain = sempty + C::SIG;
+    sptr = reinterpret_cast<int**>(drain + 1);
+    ring = reinterpret_cast<UnitInfo*>(sptr + C::SIG);
     tmem_holder = reinterpret_cast<uint32_t*>(ring + C::US);
     abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
     last_flag = abort_flag + 1;
@@ -505,12 +513,40 @@ __device__ void run_mma(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_base) {
 }
 
 // ------------------------------------------------------------------ epilogue
-// Every epilogue thread has written its part of a unit's output; after the CTA barrier one
-// gpu-scope release add publishes all of them (release is cumulative over the barrier; the
-// consumer acquires and orders its later TMA reads with a proxy fence).
-__device__ __forceinline__ void signal_done(int* counter, int ew, int lane, int nthreads) {
-  named_bar_sync(1, nthreads);
-  if (ew == 0 && lane == 0) red_release_gpu_add(counter, 1);
+// Unit completion: every epilogue warp arrives (release, CTA scope) on the next slot of the
+// signal ring once its writes of the unit are issued; the signalling warp acquires the
+// completed phase and publishes with one gpu-scope release add (cumulative over what it
+// acquired; the consumer acquires and orders its later TMA reads with a proxy fence), so
+// the epilogue never waits for its own writes to become visible.
+struct SigState {
+  int slot = 0;
+  uint32_t phase = 0;
+};
+template <int BN>
+__device__ __forceinline__ void signal_done(const GemmParams& p, Smem<BN>& sm, SigState& sg,
+                                            int* counter, int ew, int lane) {
+  using C = Cfg<BN>;
+  if (lane == 0)  // the slot's previous request has been published
+    mbar_wait(&sm.sempty[sg.slot], sg.phase ^ 1, sm.abort_flag, p.err, p.timeout);
+  __syncwarp();
+  if (ew == 0 && lane == 0) sm.sptr[sg.slot] = counter;
+  if (lane == 0) mbar_arrive(&sm.sfull[sg.slot]);
+  if (++sg.slot == C::SIG) { sg.slot = 0; sg.phase ^= 1; }
+}
+
+template <int BN>
+__device__ void run_signaller(const GemmParams& p, Smem<BN>& sm) {
+  using C = Cfg<BN>;
+  int slot = 0;
+  uint32_t phase = 0;
+  for (;;) {
+    if (!mbar_wait(&sm.sfull[slot], phase, sm.abort_flag, p.err, p.timeout)) return;
+    int* counter = sm.sptr[slot];
+    if (counter == nullptr) return;  // end of work
+    red_release_gpu_add(counter, 1);
+    mbar_arrive(&sm.sempty[slot]);
+    if (++slot == C::SIG) { slot = 0; phase ^= 1; }
+  }
 }
 
 
@@ -599,6 +635,7 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
   const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
   int us = 0, acc = 0, sc_buf = 0, steps = 0;
   uint32_t uphase = 0, aphase = 0;
+  SigState sg;
   const int G_L = p.L / 128, G_I = p.I / 128;
 
   for (;;) {
@@ -607,7 +644,10 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.uempty[us]);
     if (++us == C::US) { us = 0; uphase ^= 1; }
-    if (info.task < 0) return;
+    if (info.task < 0) {
+      signal_done<BN>(p, sm, sg, nullptr, ew, lane);  // releases the signalling warp
+      return;
+    }
     const GemmTask& T = p.task[info.task];
     const int kind = T.kind;
     const bool pair = is_pair(kind);
@@ -665,7 +705,7 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
       for (int c = etid + PER * C::EPI_THREADS; c < n4; c += C::EPI_THREADS)
         emit(c, __ldcg(rv + c));
       named_bar_sync(1, C::EPI_THREADS);  // sm.red is reused by the next unit
-      signal_done(p.norm_done + info.dep_idx, ew, lane, C::EPI_THREADS);
+      signal_done<BN>(p, sm, sg, p.norm_done + info.dep_idx, ew, lane);
       continue;
     }
 
@@ -795,7 +835,7 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
           dst[static_cast<size_t>(info.row0 + c0 + j) * p.Is] =
               __float2bfloat16_rn(silu_fast(g[j]) * u[j]);
       }
-      if (p.sh_done != nullptr) signal_done(p.sh_done + info.dep_idx, ew, lane, C::EPI_THREADS);
+      if (p.sh_done != nullptr) signal_done<BN>(p, sm, sg, p.sh_done + info.dep_idx, ew, lane);
     } else if (kind == TASK_OUT) {
       __nv_bfloat16* dst = p.out + static_cast<size_t>(info.ftile) * 128 + row;
 #pragma unroll
@@ -813,7 +853,7 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
           atomicAdd(p.r + static_cast<size_t>(tok) * p.L + col, wv * g[j]);
         }
       }
-      if (p.l2_done != nullptr) signal_done(p.l2_done, ew, lane, C::EPI_THREADS);
+      if (p.l2_done != nullptr) signal_done<BN>(p, sm, sg, p.l2_done, ew, lane);
     } else {  // TASK_ROUTED_L1: SwiGLU, then e4m3 per 128 features of each token
       float* red = sm.red + ew * COLS;
 #pragma unroll
@@ -845,7 +885,7 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
         }
       }
       named_bar_sync(2 + half, 128);
-      if (p.l1_done != nullptr) signal_done(p.l1_done + info.dep_idx, ew, lane, C::EPI_THREADS);
+      if (p.l1_done != nullptr) signal_done<BN>(p, sm, sg, p.l1_done + info.dep_idx, ew, lane);
     }
   }
 }
@@ -870,6 +910,10 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
     for (int u = 0; u < C::US; ++u) {
       mbar_init(&sm.ufull[u], 1);
       mbar_init(&sm.uempty[u], 1 + C::EPI_WARPS);
+    }
+    for (int g = 0; g < C::SIG; ++g) {
+      mbar_init(&sm.sfull[g], C::EPI_WARPS);
+      mbar_init(&sm.sempty[g], 1);
     }
     mbar_init(sm.drain, 1);
     *sm.abort_flag = 0;
@@ -906,6 +950,8 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
     if (lane == 0) run_producer<BN>(p, sm, s_tile_off, s_off);
   } else if (warp == 1) {
     if (lane == 0) run_mma<BN>(p, sm, tmem_base);
+  } else if (warp == C::SIGNAL_WARP) {
+    if (lane == 0) run_signaller<BN>(p, sm);
   } else {
     run_epilogue<BN>(p, sm, tmem_base);
   }
