@@ -68,6 +68,10 @@ def test_create_rejects_null_and_bad_shapes(lib):
     assert _create(lib, _dims(eps=0.0), w)[0] == B.KLT_ERR_INVALID_ARG
     assert _create(lib, _dims(max_tokens=0), w)[0] == B.KLT_ERR_INVALID_ARG
     assert _create(lib, _dims(max_tokens=1 << 20, topk=2), w)[0] == B.KLT_ERR_UNSUPPORTED
+    # one past the largest supported sizes: 32 k-blocks of L and I, 32 choices per token
+    assert _create(lib, _dims(L=4224), w)[0] == B.KLT_ERR_UNSUPPORTED
+    assert _create(lib, _dims(I=4224), w)[0] == B.KLT_ERR_UNSUPPORTED
+    assert _create(lib, _dims(E=64, topk=33), w)[0] == B.KLT_ERR_UNSUPPORTED
 
 
 def test_create_rejects_null_and_misaligned_weight_pointers(lib):

@@ -104,6 +104,21 @@ def test_token_major_engine_with_long_k():
     run_case(cfg, M=40, force_bn=256)
 
 
+@pytest.mark.parametrize("bn", [16, 256])
+def test_largest_router_256_experts_top32(bn):
+    # the router's widest expert set and deepest top-k, on both GEMM engines
+    cfg = configs.SMALL.with_(E=256, topk=32, seed=37)
+    run_case(cfg, M=20, force_bn=bn)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("bn", [16, 256])
+def test_longest_latent_and_intermediate_4096(bn):
+    # L = I = 4096: 32 k-blocks per routed unit, the most the engines stage per unit
+    cfg = configs.SMALL.with_(L=4096, I=4096, E=2, topk=2, seed=38)
+    run_case(cfg, M=24, force_bn=bn)
+
+
 def test_token_major_engine_is_chosen_above_the_decode_tile():
     cfg = configs.SMALL.with_(seed=34)
     _, w_gpu = weights_for(cfg)
