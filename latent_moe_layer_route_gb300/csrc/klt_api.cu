@@ -64,6 +64,7 @@ constexpr int kBN[kNumBN] = {16, 32, 64, 128};
 constexpr int kMaxSplitUnits = 3 * 160;  // split-K tiles*splits bound per task
 constexpr int kMaxCounters = 8192;       // arrival counters per split launch
 constexpr int kWideMinTokens = 17;  // token-major engine above the 16-token decode tile
+constexpr int kDualMinTiles = 16;   // token-major units over two token tiles from 2048 tokens
 
 }  // namespace
 
@@ -442,6 +443,11 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
     // fused launch with the same dependency counters.
     GemmParams gw = gp;
     gw.ntasks = 5;
+    // prefill-size batches: pairs of token tiles share each staged weight tile of the
+    // BF16 tasks (3 stages of 64 KB); otherwise 4 stages of 48 KB
+    const bool dual = ntiles >= kDualMinTiles;
+    gw.w_stages = dual ? 3 : 4;
+    gw.w_stage_bytes = dual ? 64 * 1024 : 48 * 1024;
     gw.sched = h->sched + 3;
     gw.stall_after = dbg ? dbg->stall_after_kblocks : 0;
     gw.trace = trace;
@@ -471,7 +477,8 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
     S.a_kb[0] = S.a_kb[1] = H / 64;
     S.a_ptr[0] = S.a_ptr[1] = reinterpret_cast<const uint8_t*>(h->ws13);
     S.ntiles = ntiles;
-    S.units = ntiles * S.ftiles;
+    S.dual = dual;
+    S.units = (S.dual ? (ntiles + 1) / 2 : ntiles) * S.ftiles;
     if (!encode_2d(&S.tmB[0], x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, H, BN))
       return KLT_ERR_CUDA;
     S.tmB[1] = S.tmB[0];
@@ -508,7 +515,8 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
     O.ksplit = 1;
     O.kb_per_split = O.kb_total;
     O.ntiles = ntiles;
-    O.units = ntiles * O.ftiles;
+    O.dual = dual;
+    O.units = (O.dual ? (ntiles + 1) / 2 : ntiles) * O.ftiles;
     O.dep = DEP_OUT_TILE;
     O.a_ptr[0] = reinterpret_cast<const uint8_t*>(h->w_up);
     O.a_ptr[1] = reinterpret_cast<const uint8_t*>(h->ws2);

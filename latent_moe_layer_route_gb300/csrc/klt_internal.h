@@ -89,6 +89,8 @@ struct GemmTask {
   int a_rb_expert;     // routed: 128-row blocks per expert
   int a_kb[2];         // k-blocks per 128-row block of a_ptr[0], a_ptr[1]
   int ntiles;          // non-routed: token tiles
+  int dual;            // token-major engine, non-promoted: a unit covers two token tiles
+                       // that share its weight tiles (units = ceil(ntiles / 2) * ftiles)
   int units;           // non-routed: ntiles * ftiles * ksplit
   int dep;             // DepKind of this task's units
   int ws_tile_base;    // first arrival counter of this task (tile ids start here)
@@ -134,6 +136,8 @@ struct GemmParams {
   const __nv_bfloat16* gamma;  // [L]
   __nv_bfloat16* nrm;          // [max_tokens, L]
   float eps;
+  int w_stages;                // token-major engine: stage ring depth (4 x 48 KB or 3 x 64 KB)
+  int w_stage_bytes;           //   and stage size (64 KB when units carry two token tiles)
   long long* trace;            // optional timestamp trace (this launch's region)
   int trace_n;                 // entries per (CTA, role)
 };

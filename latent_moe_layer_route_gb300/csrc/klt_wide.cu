@@ -35,8 +35,14 @@ struct W {
   static constexpr int EPI_THREADS = EPI_WARPS * 32;
   static constexpr int W_TILE = 128 * 128;  // one pre-swizzled weight tile
   static constexpr int T_TILE = TM * 128;   // token tile of one k-block
+  // The stage ring is 192 KB, either 4 stages of two weight tiles + one token tile or 3
+  // stages with room for a second token tile (dual units of the BF16 tasks); the launch
+  // chooses (GemmParams::w_stages, w_stage_bytes).  Barriers are sized for the deeper ring.
   static constexpr int STAGE_BYTES = 2 * W_TILE + T_TILE;
   static constexpr int STAGES = 4;
+  static constexpr int DUAL_STAGE_BYTES = 2 * W_TILE + 2 * T_TILE;
+  static constexpr int DUAL_STAGES = 3;
+  static_assert(STAGES * STAGE_BYTES == DUAL_STAGES * DUAL_STAGE_BYTES, "one ring size");
   static constexpr int TMEM_COLS = 512;
   static constexpr int NACC = TMEM_COLS / TN;
   static constexpr int US = 8;
@@ -60,8 +66,8 @@ struct WUnit {
   int rows;   // valid token rows
   int ftile;  // output feature tile (128 SwiGLU outputs for gate/up kinds, else 256)
   int rb0, rb1;  // weight row blocks staged as B rows [0, 128) and [128, 256)
-  int kb0, kb1;
   int dep_idx;  // routed token tile (routed kinds) or token tile (others)
+  int dual;     // 1: a second token tile follows (rows from row0 + TM, token tile dep_idx + 1)
 };
 
 // Row stride (floats) of the combine staging: 16 features + 1, so a column written by the
@@ -145,9 +151,8 @@ __device__ WUnit w_decode(const GemmParams& p, const int* s_tile_off, const int*
         info.ftile = ft;
         info.rb0 = lo * T.a_rb_expert + (pair ? ft : 2 * ft);
         info.rb1 = pair ? info.rb0 + T.a_rb_up : info.rb0 + 1;
-        info.kb0 = 0;
-        info.kb1 = T.kb_total;
         info.dep_idx = t;
+        info.dual = 0;
         return info;
       }
       u -= units;
@@ -155,26 +160,27 @@ __device__ WUnit w_decode(const GemmParams& p, const int* s_tile_off, const int*
       if (u < T.units) {
         info.task = ti;
         info.e = 0;
+        info.dual = 0;
         if (T.kind == TASK_NORM) {  // one token row
           info.row0 = u;
           info.rows = 1;
           info.ftile = 0;
           info.rb0 = info.rb1 = 0;
-          info.kb0 = info.kb1 = 0;
           info.dep_idx = u / W::TM;
         } else {
           // feature-tile major: every token tile of a weight tile runs close together in
           // time, so each weight tile is read from DRAM once and stays hot in L2
-          const int ft = u / T.ntiles;
-          const int nt = u - ft * T.ntiles;
+          const int per_ft = T.dual ? (T.ntiles + 1) / 2 : T.ntiles;
+          const int ft = u / per_ft;
+          const int j = u - ft * per_ft;
+          const int nt = T.dual ? 2 * j : j;
           info.row0 = nt * W::TM;
           info.rows = min(W::TM, p.M - info.row0);
           info.ftile = ft;
           info.rb0 = pair ? ft : 2 * ft;
           info.rb1 = pair ? info.rb0 + T.a_rb_up : info.rb0 + 1;
-          info.kb0 = 0;
-          info.kb1 = T.kb_total;
           info.dep_idx = nt;
+          info.dual = T.dual && nt + 1 < T.ntiles;
         }
         return info;
       }
@@ -220,6 +226,7 @@ __device__ void w_producer(const GemmParams& p, WSmem& sm, const int* s_tile_off
   // weights are re-read by every token tile of their expert, tokens by every feature tile
   const uint64_t pol = policy_evict_normal();
   const uint64_t pol_w = policy_evict_last();
+  const int nst = p.w_stages, sbytes = p.w_stage_bytes;
   int stage = 0, us = 0;
   uint32_t phase = 0, uphase = 0;
   long long issued = 0;
@@ -254,29 +261,40 @@ __device__ void w_producer(const GemmParams& p, WSmem& sm, const int* s_tile_off
       const int m = kb < T.kb_split0 ? 0 : 1;
       const int kk = m ? kb - T.kb_split0 : kb;
       tma_load_2d(st + 2 * W::W_TILE, &T.tmB[m], bar, kk * elems_per_kb, info.row0, pol);
+      if (info.dual)
+        tma_load_2d(st + 2 * W::W_TILE + W::T_TILE, &T.tmB[m], bar, kk * elems_per_kb,
+                    info.row0 + W::TM, pol);
     };
-    int kb = info.kb0;
+    const uint32_t stage_tx =
+        2 * W::W_TILE + (info.dual ? 2 : 1) * static_cast<uint32_t>(W::T_TILE);
+    const int kb_end = T.kb_total;
+    int kb = 0;
     if (T.dep != DEP_NONE) {
       // Stream the unit's weight tiles into the stages that are free now, then wait for
       // the token operand's producers, then copy the token tiles of those stages.
-      int pre_kb[W::STAGES], pre_st[W::STAGES], npre = 0;
-      while (kb < info.kb1 && npre < W::STAGES) {
+      // the early stages are consecutive ring slots holding k-blocks 0, 1, ...
+      const int st0 = stage;
+      int npre = 0;
+      while (kb < kb_end && npre < nst) {
         if (p.stall_after > 0 && issued >= p.stall_after) break;
         if (!mbar_try_wait(&sm.empty[stage], phase ^ 1)) break;
-        uint8_t* st = sm.stages + stage * W::STAGE_BYTES;
-        mbar_arrive_expect_tx(&sm.full[stage], W::STAGE_BYTES);
+        uint8_t* st = sm.stages + stage * sbytes;
+        mbar_arrive_expect_tx(&sm.full[stage], stage_tx);
         issue_w(kb, st);
-        pre_kb[npre] = kb;
-        pre_st[npre] = stage;
         ++npre;
         trace_mark(p, 0, static_cast<int>(issued));
         ++issued;
-        if (++stage == W::STAGES) { stage = 0; phase ^= 1; }
+        if (++stage == nst) { stage = 0; phase ^= 1; }
         ++kb;
       }
       if (!w_wait_dependency(p, T.dep, info.dep_idx, s_tile_off, sm.abort_flag)) break;
-      for (int i = 0; i < npre; ++i)
-        issue_t(pre_kb[i], sm.stages + pre_st[i] * W::STAGE_BYTES, &sm.full[pre_st[i]]);
+      if (info.dual &&
+          !w_wait_dependency(p, T.dep, info.dep_idx + 1, s_tile_off, sm.abort_flag))
+        break;
+      for (int i = 0, s = st0; i < npre; ++i) {
+        issue_t(i, sm.stages + s * sbytes, &sm.full[s]);
+        if (++s == nst) s = 0;
+      }
     }
     if (!mbar_wait(&sm.uempty[us], uphase ^ 1, sm.abort_flag, p.err, p.timeout)) break;
     sm.ring[us] = info;
@@ -288,28 +306,28 @@ __device__ void w_producer(const GemmParams& p, WSmem& sm, const int* s_tile_off
           info.task + 1;
     }
     ++published;
-    for (; kb < info.kb1; ++kb) {
+    for (; kb < kb_end; ++kb) {
       if (p.stall_after > 0 && issued >= p.stall_after) { stalled = true; break; }
       if (!mbar_wait_spin(&sm.empty[stage], phase ^ 1, sm.abort_flag, p.err, p.timeout)) {
         stalled = true;
         break;
       }
-      uint8_t* st = sm.stages + stage * W::STAGE_BYTES;
-      mbar_arrive_expect_tx(&sm.full[stage], W::STAGE_BYTES);
+      uint8_t* st = sm.stages + stage * sbytes;
+      mbar_arrive_expect_tx(&sm.full[stage], stage_tx);
       issue_w(kb, st);
       issue_t(kb, st, &sm.full[stage]);
       trace_mark(p, 0, static_cast<int>(issued));
       ++issued;
-      if (++stage == W::STAGES) { stage = 0; phase ^= 1; }
+      if (++stage == nst) { stage = 0; phase ^= 1; }
     }
     if (stalled) break;
   }
   // Drain: wait (bounded, ignoring the abort flag) for this thread's last copies, so no
   // TMA write into shared memory outlives the CTA.
-  const long long first = issued > W::STAGES ? issued - W::STAGES : 0;
+  const long long first = issued > nst ? issued - nst : 0;
   for (long long i = first; i < issued; ++i) {
-    const int s = static_cast<int>(i % W::STAGES);
-    const uint32_t par = static_cast<uint32_t>((i / W::STAGES) & 1);
+    const int s = static_cast<int>(i % nst);
+    const uint32_t par = static_cast<uint32_t>((i / nst) & 1);
     mbar_wait(&sm.full[s], par, &dummy_abort, p.err, p.timeout);
   }
 }
@@ -324,7 +342,7 @@ __device__ void w_mma(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
   // B (weights, 256 rows) at the stage base, A (tokens) after the two weight tiles
   const uint64_t desc_b0 = sdesc_sw128(smem_u32(sm.stages));
   const uint64_t desc_a0 = desc_b0 + ((2 * W::W_TILE) >> 4);
-  constexpr uint64_t STAGE_D = W::STAGE_BYTES >> 4;
+  const uint64_t STAGE_D = static_cast<uint64_t>(p.w_stage_bytes) >> 4;
   while (ok) {
     if (!mbar_wait(&sm.ufull[us], uphase, sm.abort_flag, p.err, p.timeout)) break;
     const WUnit info = sm.ring[us];
@@ -337,13 +355,20 @@ __device__ void w_mma(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
     const bool promote = kpg > 0;
     const bool fp8 = T.fp8 != 0;
     const uint32_t idesc = fp8 ? idesc_fp8 : idesc_bf16;
-    const int kb0 = info.kb0, kb1 = info.kb1;
+    const int kb1 = T.kb_total;
+    const bool dual = info.dual != 0;  // two token tiles share the weight operand
+    // the slot after `acc` (the second tile of a dual unit) and its phase parity
+    const int acc2 = acc + 1 == W::NACC ? 0 : acc + 1;
+    const uint32_t aphase2 = acc + 1 == W::NACC ? aphase ^ 1 : aphase;
     if (!promote) {
       if (!mbar_wait_spin(&sm.tempty[acc], aphase ^ 1, sm.abort_flag, p.err, p.timeout)) break;
+      if (dual &&
+          !mbar_wait_spin(&sm.tempty[acc2], aphase2 ^ 1, sm.abort_flag, p.err, p.timeout))
+        break;
       tc_fence_after();
     }
     int gpos = 0;  // position of the next k-block in its promotion group
-    for (int kb = kb0; kb < kb1; ++kb) {
+    for (int kb = 0; kb < kb1; ++kb) {
       if (!mbar_wait_spin(&sm.full[stage], phase, sm.abort_flag, p.err, p.timeout)) {
         ok = false;
         break;
@@ -359,11 +384,17 @@ __device__ void w_mma(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
       const uint32_t d = tmem_base + static_cast<uint32_t>(acc * W::TN);
       const uint64_t off = static_cast<uint64_t>(stage) * STAGE_D;
       const uint32_t accum = promote ? static_cast<uint32_t>(gpos > 0)
-                                     : static_cast<uint32_t>(kb > kb0);
+                                     : static_cast<uint32_t>(kb > 0);
       if (fp8) mma4_fp8(d, desc_a0 + off, desc_b0 + off, idesc, accum);
       else mma4_bf16(d, desc_a0 + off, desc_b0 + off, idesc, accum);
+      if (dual) {  // second token tile, same weights, into the next slot
+        const uint32_t d2 = tmem_base + static_cast<uint32_t>(acc2 * W::TN);
+        const uint64_t da2 = desc_a0 + off + (W::T_TILE >> 4);
+        if (fp8) mma4_fp8(d2, da2, desc_b0 + off, idesc, accum);
+        else mma4_bf16(d2, da2, desc_b0 + off, idesc, accum);
+      }
       tc_commit(&sm.empty[stage]);
-      if (++stage == W::STAGES) { stage = 0; phase ^= 1; }
+      if (++stage == p.w_stages) { stage = 0; phase ^= 1; }
       if (promote && ++gpos == kpg) {
         gpos = 0;
         tc_commit(&sm.tfull[acc]);
@@ -374,6 +405,10 @@ __device__ void w_mma(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
     if (!promote) {
       tc_commit(&sm.tfull[acc]);
       if (++acc == W::NACC) { acc = 0; aphase ^= 1; }
+      if (dual) {
+        tc_commit(&sm.tfull[acc]);
+        if (++acc == W::NACC) { acc = 0; aphase ^= 1; }
+      }
     }
   }
   // Drain: all MMAs issued by this thread complete before TMEM is released.
@@ -498,195 +533,201 @@ __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
       w_norm_row(p, sm, sg, info.row0, ew, lane);
       continue;
     }
-    const bool pair = is_pair(kind);
-    const bool valid = tok < info.rows;
-    // combine target of a routed L2 row, fetched while the products are computed
-    int tg = 0;
-    float wv = 0.f;
-    if (kind == TASK_ROUTED_L2 && valid) {
-      tg = __ldg(p.gidx + info.row0 + tok);
-      wv = __ldg(p.wperm + info.row0 + tok);
-    }
-    // TMEM columns of this thread's two 64-column groups
-    const uint32_t col0 = pair ? half * 64 : half * 128;
-    const uint32_t col1 = pair ? 128 + half * 64 : half * 128 + 64;
-    float a[128];
-
-    if (T.kpg > 0) {
-      // Block-scaled products: every promotion group's partial (fresh in TMEM) is added
-      // with scale = token scale x weight block scale of the group.
-#pragma unroll
-      for (int i = 0; i < 128; ++i) a[i] = 0.f;
-      const int ng = (info.kb1 - info.kb0) / T.kpg;
-      const int g0 = info.kb0 / T.kpg;
-      const float* ts =
-          (kind == TASK_ROUTED_L1 ? p.zsT : p.asT) + static_cast<size_t>(g0) * p.cap +
-          info.row0 + tok;
-      const float *sw0, *sw1;
-      if (kind == TASK_ROUTED_L1) {
-        const size_t rb = static_cast<size_t>(info.e) * (2 * G_I);
-        sw0 = p.w13_s + (rb + info.ftile) * G_L + g0;
-        sw1 = p.w13_s + (rb + G_I + info.ftile) * G_L + g0;
-      } else {
-        sw0 = p.w2_s + (static_cast<size_t>(info.e) * G_L + 2 * info.ftile + half) * G_I + g0;
-        sw1 = sw0;
+    // a dual unit (two token tiles sharing the weight operand, accumulated in consecutive
+    // slots) is finished as two single-tile units
+    const int nsub = info.dual ? 2 : 1;
+    for (int si = 0; si < nsub; ++si) {
+      const int row0 = info.row0 + si * W::TM;
+      const int rows = si ? min(W::TM, p.M - row0) : info.rows;
+      const int dep_idx = info.dep_idx + si;
+      const bool pair = is_pair(kind);
+      const bool valid = tok < rows;
+      // combine target of a routed L2 row, fetched while the products are computed
+      int tg = 0;
+      float wv = 0.f;
+      if (kind == TASK_ROUTED_L2 && valid) {
+        tg = __ldg(p.gidx + row0 + tok);
+        wv = __ldg(p.wperm + row0 + tok);
       }
-      // scales are loaded two groups ahead so no global load sits between the
-      // accumulator hand-offs
-      auto tok_scale = [&](int gi) {
-        return valid && gi < ng ? __ldcg(ts + static_cast<size_t>(gi) * p.cap) : 0.f;
-      };
-      auto w_scale = [&](const float* sw, int gi) { return gi < ng ? __ldg(sw + gi) : 0.f; };
-      float sa1 = tok_scale(0), w01 = w_scale(sw0, 0), w11 = w_scale(sw1, 0);
-      float sa2 = tok_scale(1), w02 = w_scale(sw0, 1), w12 = w_scale(sw1, 1);
-      for (int gi = 0; gi < ng; ++gi) {
-        const float s0 = w01 * sa1;
-        const float s1 = w11 * sa1;
-        sa1 = sa2;
-        w01 = w02;
-        w11 = w12;
-        sa2 = tok_scale(gi + 2);
-        w02 = w_scale(sw0, gi + 2);
-        w12 = w_scale(sw1, gi + 2);
+      // TMEM columns of this thread's two 64-column groups
+      const uint32_t col0 = pair ? half * 64 : half * 128;
+      const uint32_t col1 = pair ? 128 + half * 64 : half * 128 + 64;
+      float a[128];
+
+      if (T.kpg > 0) {
+        // Block-scaled products: every promotion group's partial (fresh in TMEM) is added
+        // with scale = token scale x weight block scale of the group.
+  #pragma unroll
+        for (int i = 0; i < 128; ++i) a[i] = 0.f;
+        const int ng = T.kb_total / T.kpg;
+        const float* ts =
+            (kind == TASK_ROUTED_L1 ? p.zsT : p.asT) + row0 + tok;
+        const float *sw0, *sw1;
+        if (kind == TASK_ROUTED_L1) {
+          const size_t rb = static_cast<size_t>(info.e) * (2 * G_I);
+          sw0 = p.w13_s + (rb + info.ftile) * G_L;
+          sw1 = p.w13_s + (rb + G_I + info.ftile) * G_L;
+        } else {
+          sw0 = p.w2_s + (static_cast<size_t>(info.e) * G_L + 2 * info.ftile + half) * G_I;
+          sw1 = sw0;
+        }
+        // scales are loaded two groups ahead so no global load sits between the
+        // accumulator hand-offs
+        auto tok_scale = [&](int gi) {
+          return valid && gi < ng ? __ldcg(ts + static_cast<size_t>(gi) * p.cap) : 0.f;
+        };
+        auto w_scale = [&](const float* sw, int gi) { return gi < ng ? __ldg(sw + gi) : 0.f; };
+        float sa1 = tok_scale(0), w01 = w_scale(sw0, 0), w11 = w_scale(sw1, 0);
+        float sa2 = tok_scale(1), w02 = w_scale(sw0, 1), w12 = w_scale(sw1, 1);
+        for (int gi = 0; gi < ng; ++gi) {
+          const float s0 = w01 * sa1;
+          const float s1 = w11 * sa1;
+          sa1 = sa2;
+          w01 = w02;
+          w11 = w12;
+          sa2 = tok_scale(gi + 2);
+          w02 = w_scale(sw0, gi + 2);
+          w12 = w_scale(sw1, gi + 2);
+          if (!mbar_wait_spin(&sm.tfull[acc], aphase, sm.abort_flag, p.err, p.timeout)) return;
+          tc_fence_after();
+          const uint32_t tb = tmem_base + lane_base + static_cast<uint32_t>(acc * W::TN);
+          float v[4][16];
+          tmem_ld16x4(tb + col0, tb + col0 + 16, tb + col0 + 32, tb + col0 + 48, v[0], v[1],
+                      v[2], v[3]);
+  #pragma unroll
+          for (int c = 0; c < 4; ++c)
+  #pragma unroll
+            for (int i = 0; i < 16; ++i) a[c * 16 + i] = fmaf(v[c][i], s0, a[c * 16 + i]);
+          tmem_ld16x4(tb + col1, tb + col1 + 16, tb + col1 + 32, tb + col1 + 48, v[0], v[1],
+                      v[2], v[3]);
+          // the slot's contents are in registers: hand it back before the last FMAs
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.tempty[acc]);
+          if (++acc == W::NACC) { acc = 0; aphase ^= 1; }
+  #pragma unroll
+          for (int c = 0; c < 4; ++c)
+  #pragma unroll
+            for (int i = 0; i < 16; ++i)
+              a[64 + c * 16 + i] = fmaf(v[c][i], s1, a[64 + c * 16 + i]);
+          if (ew == 0 && lane == 0) trace_mark(p, 2, steps++);
+        }
+      } else {
         if (!mbar_wait_spin(&sm.tfull[acc], aphase, sm.abort_flag, p.err, p.timeout)) return;
         tc_fence_after();
         const uint32_t tb = tmem_base + lane_base + static_cast<uint32_t>(acc * W::TN);
-        float v[4][16];
-        tmem_ld16x4(tb + col0, tb + col0 + 16, tb + col0 + 32, tb + col0 + 48, v[0], v[1],
-                    v[2], v[3]);
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int i = 0; i < 16; ++i) a[c * 16 + i] = fmaf(v[c][i], s0, a[c * 16 + i]);
-        tmem_ld16x4(tb + col1, tb + col1 + 16, tb + col1 + 32, tb + col1 + 48, v[0], v[1],
-                    v[2], v[3]);
-        // the slot's contents are in registers: hand it back before the last FMAs
+        tmem_ld16x4(tb + col0, tb + col0 + 16, tb + col0 + 32, tb + col0 + 48, a, a + 16,
+                    a + 32, a + 48);
+        tmem_ld16x4(tb + col1, tb + col1 + 16, tb + col1 + 32, tb + col1 + 48, a + 64, a + 80,
+                    a + 96, a + 112);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.tempty[acc]);
         if (++acc == W::NACC) { acc = 0; aphase ^= 1; }
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            a[64 + c * 16 + i] = fmaf(v[c][i], s1, a[64 + c * 16 + i]);
         if (ew == 0 && lane == 0) trace_mark(p, 2, steps++);
       }
-    } else {
-      if (!mbar_wait_spin(&sm.tfull[acc], aphase, sm.abort_flag, p.err, p.timeout)) return;
-      tc_fence_after();
-      const uint32_t tb = tmem_base + lane_base + static_cast<uint32_t>(acc * W::TN);
-      tmem_ld16x4(tb + col0, tb + col0 + 16, tb + col0 + 32, tb + col0 + 48, a, a + 16,
-                  a + 32, a + 48);
-      tmem_ld16x4(tb + col1, tb + col1 + 16, tb + col1 + 32, tb + col1 + 48, a + 64, a + 80,
-                  a + 96, a + 112);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.tempty[acc]);
-      if (++acc == W::NACC) { acc = 0; aphase ^= 1; }
-      if (ew == 0 && lane == 0) trace_mark(p, 2, steps++);
-    }
 
-    // ---- unit end (this thread: one token, 64 gate/up pairs or 128 features)
-    if (kind == TASK_ROUTED_L1) {
-      // SwiGLU, then e4m3 with one scale per token per 128 outputs (both halves' amax)
-      float m = 0.f;
-#pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        a[i] = silu_fast(a[i]) * a[64 + i];
-        m = fmaxf(m, fabsf(a[i]));
-      }
-      float* am = sm.amax + (l1_units & 1) * 2 * W::TM;
-      ++l1_units;
-      am[half * W::TM + tok] = m;
-      named_bar_sync(1, W::EPI_THREADS);
-      const float amax = fmaxf(am[tok], am[W::TM + tok]);
-      const float sc = amax == 0.f ? 1.0f : amax / 448.0f;
-      const float inv = 1.0f / sc;
-      if (valid) {
-        const size_t pp = static_cast<size_t>(info.row0 + tok);
-        const size_t col = static_cast<size_t>(info.ftile) * 128 + half * 64;
-        uint4* dq = reinterpret_cast<uint4*>(p.aq + pp * p.I + col);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t w4[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int i = c * 16 + q * 4;
-            w4[q] = static_cast<uint32_t>(f32_to_e4m3(quot_rn(a[i], sc, inv))) |
-                    (static_cast<uint32_t>(f32_to_e4m3(quot_rn(a[i + 1], sc, inv))) << 8) |
-                    (static_cast<uint32_t>(f32_to_e4m3(quot_rn(a[i + 2], sc, inv))) << 16) |
-                    (static_cast<uint32_t>(f32_to_e4m3(quot_rn(a[i + 3], sc, inv))) << 24);
-          }
-          dq[c] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-          if (p.aqb != nullptr) {  // exact bf16 images of the codes
-            uint4* db = reinterpret_cast<uint4*>(p.aqb + pp * p.I + col) + 2 * c;
-            uint32_t b8[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const uint32_t wq = w4[q >> 1] >> ((q & 1) * 16);
-              b8[q] = pack_bf16x2(e4m3_to_f32(static_cast<uint8_t>(wq & 0xFFu)),
-                                  e4m3_to_f32(static_cast<uint8_t>((wq >> 8) & 0xFFu)));
+      // ---- unit end (this thread: one token, 64 gate/up pairs or 128 features)
+      if (kind == TASK_ROUTED_L1) {
+        // SwiGLU, then e4m3 with one scale per token per 128 outputs (both halves' amax)
+        float m = 0.f;
+  #pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          a[i] = silu_fast(a[i]) * a[64 + i];
+          m = fmaxf(m, fabsf(a[i]));
+        }
+        float* am = sm.amax + (l1_units & 1) * 2 * W::TM;
+        ++l1_units;
+        am[half * W::TM + tok] = m;
+        named_bar_sync(1, W::EPI_THREADS);
+        const float amax = fmaxf(am[tok], am[W::TM + tok]);
+        const float sc = amax == 0.f ? 1.0f : amax / 448.0f;
+        const float inv = 1.0f / sc;
+        if (valid) {
+          const size_t pp = static_cast<size_t>(row0 + tok);
+          const size_t col = static_cast<size_t>(info.ftile) * 128 + half * 64;
+          uint4* dq = reinterpret_cast<uint4*>(p.aq + pp * p.I + col);
+  #pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t w4[4];
+  #pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int i = c * 16 + q * 4;
+              w4[q] = static_cast<uint32_t>(f32_to_e4m3(quot_rn(a[i], sc, inv))) |
+                      (static_cast<uint32_t>(f32_to_e4m3(quot_rn(a[i + 1], sc, inv))) << 8) |
+                      (static_cast<uint32_t>(f32_to_e4m3(quot_rn(a[i + 2], sc, inv))) << 16) |
+                      (static_cast<uint32_t>(f32_to_e4m3(quot_rn(a[i + 3], sc, inv))) << 24);
             }
-            db[0] = make_uint4(b8[0], b8[1], b8[2], b8[3]);
-            db[1] = make_uint4(b8[4], b8[5], b8[6], b8[7]);
+            dq[c] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            if (p.aqb != nullptr) {  // exact bf16 images of the codes
+              uint4* db = reinterpret_cast<uint4*>(p.aqb + pp * p.I + col) + 2 * c;
+              uint32_t b8[8];
+  #pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                const uint32_t wq = w4[q >> 1] >> ((q & 1) * 16);
+                b8[q] = pack_bf16x2(e4m3_to_f32(static_cast<uint8_t>(wq & 0xFFu)),
+                                    e4m3_to_f32(static_cast<uint8_t>((wq >> 8) & 0xFFu)));
+              }
+              db[0] = make_uint4(b8[0], b8[1], b8[2], b8[3]);
+              db[1] = make_uint4(b8[4], b8[5], b8[6], b8[7]);
+            }
+          }
+          if (half == 0) p.asT[static_cast<size_t>(info.ftile) * p.cap + pp] = sc;
+        }
+        if (p.l1_done != nullptr) w_signal(p, sm, sg, p.l1_done + dep_idx, ew, lane);
+      } else if (kind == TASK_SHARED_L1) {
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(
+              p.a_s + static_cast<size_t>(row0 + tok) * p.Is + info.ftile * 128 + half * 64);
+  #pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint32_t w4[4];
+  #pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int i = c * 8 + q * 2;
+              w4[q] = pack_bf16x2(silu_fast(a[i]) * a[64 + i], silu_fast(a[i + 1]) * a[65 + i]);
+            }
+            dst[c] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
         }
-        if (half == 0) p.asT[static_cast<size_t>(info.ftile) * p.cap + pp] = sc;
-      }
-      if (p.l1_done != nullptr) w_signal(p, sm, sg, p.l1_done + info.dep_idx, ew, lane);
-    } else if (kind == TASK_SHARED_L1) {
-      if (valid) {
-        uint4* dst = reinterpret_cast<uint4*>(
-            p.a_s + static_cast<size_t>(info.row0 + tok) * p.Is + info.ftile * 128 + half * 64);
-#pragma unroll
+        if (p.sh_done != nullptr) w_signal(p, sm, sg, p.sh_done + dep_idx, ew, lane);
+      } else if (kind == TASK_ROUTED_L2) {
+        // Weighted scatter-combine into the tokens' fp32 rows of r.  A lane holds one token's
+        // 128 features; 16 features of the warp's 32 tokens at a time pass through shared
+        // memory, so each vector reduction instruction covers 8 tokens x 64 contiguous bytes
+        // (8 L2 requests) instead of 32 tokens x 16 bytes.
+        float* st = sm.stg + ew * 32 * STG_LD;
+        const size_t col0 = static_cast<size_t>(info.ftile) * 256 + half * 128;
+  #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          uint32_t w4[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int i = c * 8 + q * 2;
-            w4[q] = pack_bf16x2(silu_fast(a[i]) * a[64 + i], silu_fast(a[i + 1]) * a[65 + i]);
+  #pragma unroll
+          for (int i = 0; i < 16; ++i) st[lane * STG_LD + i] = wv * a[16 * c + i];
+          __syncwarp();
+  #pragma unroll
+          for (int it = 0; it < 4; ++it) {
+            const int t = it * 8 + (lane >> 2);  // token (lane) of the warp this lane reduces
+            const int q = lane & 3;              // its 4-feature quad within the 16
+            const int tgt = __shfl_sync(0xFFFFFFFFu, tg, t);
+            const bool ok = __shfl_sync(0xFFFFFFFFu, valid ? 1 : 0, t) != 0;
+            const float* sv = st + t * STG_LD + 4 * q;
+            if (ok)
+              red_add_v4(p.r + static_cast<size_t>(tgt) * p.L + col0 + 16 * c + 4 * q, sv[0],
+                         sv[1], sv[2], sv[3]);
           }
-          dst[c] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          __syncwarp();
         }
-      }
-      if (p.sh_done != nullptr) w_signal(p, sm, sg, p.sh_done + info.dep_idx, ew, lane);
-    } else if (kind == TASK_ROUTED_L2) {
-      // Weighted scatter-combine into the tokens' fp32 rows of r.  A lane holds one token's
-      // 128 features; 16 features of the warp's 32 tokens at a time pass through shared
-      // memory, so each vector reduction instruction covers 8 tokens x 64 contiguous bytes
-      // (8 L2 requests) instead of 32 tokens x 16 bytes.
-      float* st = sm.stg + ew * 32 * STG_LD;
-      const size_t col0 = static_cast<size_t>(info.ftile) * 256 + half * 128;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) st[lane * STG_LD + i] = wv * a[16 * c + i];
-        __syncwarp();
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-          const int t = it * 8 + (lane >> 2);  // token (lane) of the warp this lane reduces
-          const int q = lane & 3;              // its 4-feature quad within the 16
-          const int tgt = __shfl_sync(0xFFFFFFFFu, tg, t);
-          const bool ok = __shfl_sync(0xFFFFFFFFu, valid ? 1 : 0, t) != 0;
-          const float* sv = st + t * STG_LD + 4 * q;
-          if (ok)
-            red_add_v4(p.r + static_cast<size_t>(tgt) * p.L + col0 + 16 * c + 4 * q, sv[0],
-                       sv[1], sv[2], sv[3]);
+        if (p.l2_done != nullptr) w_signal(p, sm, sg, p.l2_done, ew, lane);
+      } else {  // TASK_OUT
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(
+              p.out + static_cast<size_t>(row0 + tok) * p.H + info.ftile * 256 + half * 128);
+  #pragma unroll
+          for (int c = 0; c < 16; ++c)
+            dst[c] = make_uint4(pack_bf16x2(a[c * 8], a[c * 8 + 1]),
+                                pack_bf16x2(a[c * 8 + 2], a[c * 8 + 3]),
+                                pack_bf16x2(a[c * 8 + 4], a[c * 8 + 5]),
+                                pack_bf16x2(a[c * 8 + 6], a[c * 8 + 7]));
         }
-        __syncwarp();
-      }
-      if (p.l2_done != nullptr) w_signal(p, sm, sg, p.l2_done, ew, lane);
-    } else {  // TASK_OUT
-      if (valid) {
-        uint4* dst = reinterpret_cast<uint4*>(
-            p.out + static_cast<size_t>(info.row0 + tok) * p.H + info.ftile * 256 + half * 128);
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          dst[c] = make_uint4(pack_bf16x2(a[c * 8], a[c * 8 + 1]),
-                              pack_bf16x2(a[c * 8 + 2], a[c * 8 + 3]),
-                              pack_bf16x2(a[c * 8 + 4], a[c * 8 + 5]),
-                              pack_bf16x2(a[c * 8 + 6], a[c * 8 + 7]));
       }
     }
   }

@@ -119,6 +119,15 @@ def test_longest_latent_and_intermediate_4096(bn):
     run_case(cfg, M=24, force_bn=bn)
 
 
+def test_token_major_engine_dual_token_tiles():
+    # from 16 token tiles on, the shared L1 and output units take two token tiles each
+    # (3 stages of 64 KB): 17 tiles, the last one ragged and unpaired
+    cfg = configs.SMALL.with_(E=8, topk=2, seed=39)
+    rng = np.random.default_rng(2)
+    tok = np.sort(np.concatenate([rng.choice(2048, 40, replace=False), np.arange(2048, 2100)]))
+    run_case(cfg, M=2100, tokens=tok, force_bn=256)
+
+
 def test_token_major_engine_is_chosen_above_the_decode_tile():
     cfg = configs.SMALL.with_(seed=34)
     _, w_gpu = weights_for(cfg)
