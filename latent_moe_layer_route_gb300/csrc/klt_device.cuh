@@ -400,6 +400,11 @@ KLT_DEV float e2m1_to_f32(uint32_t c) {
 KLT_DEV uint8_t f32_to_e4m3(float v) {
   return static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
 }
+// Two values in one conversion: `lo` in bits 0-7, `hi` in bits 8-15.
+KLT_DEV uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  return static_cast<uint32_t>(
+      __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
+}
 
 KLT_DEV int lane_id() { return threadIdx.x & 31; }
 

@@ -70,9 +70,11 @@ struct WUnit {
   int dual;     // 1: a second token tile follows (rows from row0 + TM, token tile dep_idx + 1)
 };
 
-// Row stride (floats) of the combine staging: 16 features + 1, so a column written by the
-// 32 lanes of a warp touches 32 different banks.
-constexpr int STG_LD = 17;
+// Combine staging: per warp 32 tokens x 16 features (fp32), each row's four 16-byte quads
+// stored at quad position j ^ ((row >> 1) & 3), so that both the row-wise 16-byte stores
+// of 8 lanes and the quad-wise 16-byte loads of 8 lanes touch 32 different banks.
+constexpr int STG_LD = 16;
+__device__ __forceinline__ int stg_quad(int row, int j) { return row * STG_LD + 4 * (j ^ ((row >> 1) & 3)); }
 
 struct WSmem {
   uint8_t* stages;
@@ -84,13 +86,14 @@ struct WSmem {
   float* amax;  // [2 unit parities][2 column halves][TM]
   float* part;  // [EPI_WARPS] norm partial sums
   float* stg;   // [EPI_WARPS][32 tokens][STG_LD] per-warp transpose staging of the combine
+                // (16-byte aligned)
 
   static constexpr int BAR_BYTES =
       8 * (2 * W::STAGES + 2 * W::NACC + 2 * W::US + 2 * W::SIG + 1) + 8 * W::SIG;
   static constexpr int bytes() {
     return W::STAGES * W::STAGE_BYTES + BAR_BYTES + W::US * (int)sizeof(WUnit) + 64 +
            4 * W::TM * 4 + W::EPI_WARPS * 4 + W::EPI_WARPS * 32 * STG_LD * 4 +
-           1024 /* alignment slack */;
+           16 + 1024 /* alignment slack */;
   }
   __device__ explicit WSmem(uint8_t* raw) {
     uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -112,7 +115,8 @@ struct WSmem {
     abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
     amax = reinterpret_cast<float*>(tmem_holder + 16);
     part = amax + 4 * W::TM;
-    stg = part + W::EPI_WARPS;
+    stg = reinterpret_cast<float*>(
+        (reinterpret_cast<uintptr_t>(part + W::EPI_WARPS) + 15) & ~static_cast<uintptr_t>(15));
   }
 };
 
@@ -653,10 +657,9 @@ __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
   #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const int i = c * 16 + q * 4;
-              w4[q] = static_cast<uint32_t>(f32_to_e4m3(quot_rn(a[i], sc, inv))) |
-                      (static_cast<uint32_t>(f32_to_e4m3(quot_rn(a[i + 1], sc, inv))) << 8) |
-                      (static_cast<uint32_t>(f32_to_e4m3(quot_rn(a[i + 2], sc, inv))) << 16) |
-                      (static_cast<uint32_t>(f32_to_e4m3(quot_rn(a[i + 3], sc, inv))) << 24);
+              w4[q] = f32x2_to_e4m3x2(quot_rn(a[i], sc, inv), quot_rn(a[i + 1], sc, inv)) |
+                      (f32x2_to_e4m3x2(quot_rn(a[i + 2], sc, inv), quot_rn(a[i + 3], sc, inv))
+                       << 16);
             }
             dq[c] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
             if (p.aqb != nullptr) {  // exact bf16 images of the codes
@@ -695,24 +698,34 @@ __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
         // Weighted scatter-combine into the tokens' fp32 rows of r.  A lane holds one token's
         // 128 features; 16 features of the warp's 32 tokens at a time pass through shared
         // memory, so each vector reduction instruction covers 8 tokens x 64 contiguous bytes
-        // (8 L2 requests) instead of 32 tokens x 16 bytes.
+        // (8 L2 requests) instead of 32 tokens x 16 bytes.  Lane l reduces quad l % 4 of
+        // tokens l / 4 + 8i (i < 4); their target rows are fetched once per unit.
         float* st = sm.stg + ew * 32 * STG_LD;
-        const size_t col0 = static_cast<size_t>(info.ftile) * 256 + half * 128;
+        const int qd = lane & 3;
+        const size_t col0 = static_cast<size_t>(info.ftile) * 256 + half * 128 + 4 * qd;
+        float* dst[4];
+        int src[4];
+        bool ok[4];
+  #pragma unroll
+        for (int it = 0; it < 4; ++it) {
+          const int t = it * 8 + (lane >> 2);
+          const int tgt = __shfl_sync(0xFFFFFFFFu, tg, t);
+          ok[it] = __shfl_sync(0xFFFFFFFFu, valid ? 1 : 0, t) != 0;
+          dst[it] = p.r + static_cast<size_t>(tgt) * p.L + col0;
+          src[it] = stg_quad(t, qd);
+        }
   #pragma unroll
         for (int c = 0; c < 8; ++c) {
   #pragma unroll
-          for (int i = 0; i < 16; ++i) st[lane * STG_LD + i] = wv * a[16 * c + i];
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<float4*>(st + stg_quad(lane, j)) =
+                make_float4(wv * a[16 * c + 4 * j], wv * a[16 * c + 4 * j + 1],
+                            wv * a[16 * c + 4 * j + 2], wv * a[16 * c + 4 * j + 3]);
           __syncwarp();
   #pragma unroll
           for (int it = 0; it < 4; ++it) {
-            const int t = it * 8 + (lane >> 2);  // token (lane) of the warp this lane reduces
-            const int q = lane & 3;              // its 4-feature quad within the 16
-            const int tgt = __shfl_sync(0xFFFFFFFFu, tg, t);
-            const bool ok = __shfl_sync(0xFFFFFFFFu, valid ? 1 : 0, t) != 0;
-            const float* sv = st + t * STG_LD + 4 * q;
-            if (ok)
-              red_add_v4(p.r + static_cast<size_t>(tgt) * p.L + col0 + 16 * c + 4 * q, sv[0],
-                         sv[1], sv[2], sv[3]);
+            const float4 v = *reinterpret_cast<const float4*>(st + src[it]);
+            if (ok[it]) red_add_v4(dst[it] + 16 * c, v.x, v.y, v.z, v.w);
           }
           __syncwarp();
         }
