@@ -569,6 +569,30 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
       plan_split(S, ntiles, ntiles * S.ftiles * std::max(1, S.kb_total / 8), BN);
       if (!encode_2d(&S.tmB[0], x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, H, BN))
         return KLT_ERR_CUDA;
+      // A batch that touches few experts has fewer routed L1 units than SMs: split them in
+      // K (whole promotion groups) so the routed weights stream through every SM.  The
+      // splits' partials go to the workspace after the shared expert's; the last split of
+      // a tile sums them in a fixed order and runs the SwiGLU/requantisation epilogue.
+      {
+        const int ntr_est = std::min(E, Mk);                   // touched experts, at most
+        const int ntr_ub = ntr_est + (Mk + BN - 1) / BN;        // routed tiles, at most
+        const int r_units = ntr_est * R.ftiles;
+        const size_t tile_floats = 2ull * BN * 128;
+        const size_t s_slots = static_cast<size_t>(S.units);
+        const int base = S.ntiles * S.ftiles;
+        int ks = r_units < grid ? (grid + r_units - 1) / r_units : 1;
+        ks = std::min(ks, std::max(1, R.kb_total / (4 * R.kpg)));
+        while (ks > 1 &&
+               (s_slots + static_cast<size_t>(ntr_ub) * R.ftiles * ks) * tile_floats > ws_task)
+          --ks;
+        if (ks > 1 && base + ntr_ub * R.ftiles <= kMaxCounters) {
+          const int groups = R.kb_total / R.kpg;
+          R.kb_per_split = ((groups + ks - 1) / ks) * R.kpg;
+          R.ksplit = (R.kb_total + R.kb_per_split - 1) / R.kb_per_split;
+          R.ws_tile_base = base;
+          R.ws_off = static_cast<long long>(s_slots * tile_floats);
+        }
+      }
       S.a_ptr[0] = S.a_ptr[1] = reinterpret_cast<const uint8_t*>(h->ws13);
       S.tmB[1] = S.tmB[0];
     }

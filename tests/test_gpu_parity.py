@@ -75,6 +75,15 @@ def test_small_nvfp4_wider():
                                  topk=3, seed=29), M=45)
 
 
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+@pytest.mark.parametrize("M", [3, 9])
+def test_routed_l1_k_split(fmt, M):
+    # few touched experts: the routed L1 units are split in K (two splits of whole promotion
+    # groups), the last split of each tile sums the partials and runs the epilogue
+    cfg = configs.SMALL.with_(L=1024, E=4, topk=2, routed_fmt=fmt, seed=41)
+    run_case(cfg, M=M, force_bn=16)
+
+
 @pytest.mark.parametrize("bn", [16, 32, 64, 128, 256])
 @pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
 def test_every_token_tile_width(bn, fmt):
