@@ -503,7 +503,7 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
     N.ftiles = 1;
     N.ksplit = 1;
     N.ntiles = ntiles;
-    N.units = M;
+    N.units = (M + kWideNormRows - 1) / kWideNormRows;  // a token row per epilogue warp
     N.tmB[0] = N.tmB[1] = h->tm_n[bi];
     GemmTask& O = gw.task[4];  // out = bf16([n | a_s] . [W_up | Ws2]^T), 256 outputs per unit
     O.kind = TASK_OUT;

@@ -169,6 +169,8 @@ int gemm_smem_bytes(int bn);
 // fused tasks with 128-token tiles).  Its epilogue warps take registers from the control
 // warps at run time, which needs the kernel to launch with exactly the register count it
 // was built for: wide_regs_ok(wide_kernel_regs()) must hold before launch_wide is used.
+// Token-major engine: RMSNorm rows per norm unit (one per epilogue warp).
+constexpr int kWideNormRows = 8;
 cudaError_t launch_wide(const GemmParams& p, int grid, cudaStream_t s, bool pdl);
 int wide_kernel_regs();
 bool wide_regs_ok(int regs);

@@ -33,6 +33,8 @@ struct W {
   static constexpr int FIRST_EPI_WARP = 4;
   static constexpr int THREADS = 12 * 32;
   static constexpr int EPI_THREADS = EPI_WARPS * 32;
+  static constexpr int NORM_ROWS = kWideNormRows;  // one token row per epilogue warp
+  static_assert(NORM_ROWS == EPI_WARPS && TM % NORM_ROWS == 0, "norm rows per unit");
   static constexpr int W_TILE = 128 * 128;  // one pre-swizzled weight tile
   static constexpr int T_TILE = TM * 128;   // token tile of one k-block
   // The stage ring is 192 KB, either 4 stages of two weight tiles + one token tile or 3
@@ -84,7 +86,6 @@ struct WSmem {
   uint32_t* tmem_holder;
   int* abort_flag;
   float* amax;  // [2 unit parities][2 column halves][TM]
-  float* part;  // [EPI_WARPS] norm partial sums
   float* stg;   // [EPI_WARPS][32 tokens][STG_LD] per-warp transpose staging of the combine
                 // (16-byte aligned)
 
@@ -92,7 +93,7 @@ struct WSmem {
       8 * (2 * W::STAGES + 2 * W::NACC + 2 * W::US + 2 * W::SIG + 1) + 8 * W::SIG;
   static constexpr int bytes() {
     return W::STAGES * W::STAGE_BYTES + BAR_BYTES + W::US * (int)sizeof(WUnit) + 64 +
-           4 * W::TM * 4 + W::EPI_WARPS * 4 + W::EPI_WARPS * 32 * STG_LD * 4 +
+           4 * W::TM * 4 + W::EPI_WARPS * 32 * STG_LD * 4 +
            16 + 1024 /* alignment slack */;
   }
   __device__ explicit WSmem(uint8_t* raw) {
@@ -114,9 +115,8 @@ struct WSmem {
     tmem_holder = reinterpret_cast<uint32_t*>(ring + W::US);
     abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
     amax = reinterpret_cast<float*>(tmem_holder + 16);
-    part = amax + 4 * W::TM;
     stg = reinterpret_cast<float*>(
-        (reinterpret_cast<uintptr_t>(part + W::EPI_WARPS) + 15) & ~static_cast<uintptr_t>(15));
+        (reinterpret_cast<uintptr_t>(amax + 4 * W::TM) + 15) & ~static_cast<uintptr_t>(15));
   }
 };
 
@@ -165,12 +165,12 @@ __device__ WUnit w_decode(const GemmParams& p, const int* s_tile_off, const int*
         info.task = ti;
         info.e = 0;
         info.dual = 0;
-        if (T.kind == TASK_NORM) {  // one token row
-          info.row0 = u;
-          info.rows = 1;
+        if (T.kind == TASK_NORM) {  // NORM_ROWS token rows, all in one token tile
+          info.row0 = u * W::NORM_ROWS;
+          info.rows = min(W::NORM_ROWS, p.M - info.row0);
           info.ftile = 0;
           info.rb0 = info.rb1 = 0;
-          info.dep_idx = u / W::TM;
+          info.dep_idx = info.row0 / W::TM;
         } else {
           // feature-tile major: every token tile of a weight tile runs close together in
           // time, so each weight tile is read from DRAM once and stays hot in L2
@@ -208,7 +208,8 @@ __device__ bool w_wait_dependency(const GemmParams& p, int dep, int idx, const i
     } else if (dep == DEP_ALL_L2) {
       ready = ld_acquire_gpu(p.l2_done) >= s_tile_off[p.E] * p.l2_ftiles;
     } else {
-      ready = ld_acquire_gpu(p.norm_done + idx) >= min(W::TM, p.M - idx * W::TM) &&
+      ready = ld_acquire_gpu(p.norm_done + idx) >=
+                  (min(W::TM, p.M - idx * W::TM) + W::NORM_ROWS - 1) / W::NORM_ROWS &&
               ld_acquire_gpu(p.sh_done + idx) >= p.sh_target;
     }
     if (ready) break;
@@ -453,55 +454,51 @@ __device__ void w_signaller(const GemmParams& p, WSmem& sm) {
   }
 }
 
-// RMSNorm of one token row of the fp32 combine: fp32 statistic, gamma applied, one bf16
-// rounding (the output GEMM's token operand).  The epilogue threads split the row.
-__device__ void w_norm_row(const GemmParams& p, WSmem& sm, SigState& sg, int row, int ew,
-                           int lane) {
-  const size_t t = static_cast<size_t>(row);
-  const float4* rv = reinterpret_cast<const float4*>(p.r + t * p.L);
-  const int etid = ew * 32 + lane;
-  const int n4 = p.L / 4;
-  constexpr int PER = 4;  // float4s per thread held in registers (L <= 4096)
-  float4 v[PER];
-  float ss = 0.f;
+// RMSNorm of up to NORM_ROWS token rows of the fp32 combine, one row per epilogue warp:
+// fp32 statistic (lane partials, then a shuffle tree), gamma applied, one bf16 rounding (the
+// output GEMM's token operand).  No barrier between the warps.
+__device__ void w_norm_rows(const GemmParams& p, WSmem& sm, SigState& sg, int row0, int rows,
+                            int ew, int lane) {
+  if (ew < rows) {
+    const size_t t = static_cast<size_t>(row0 + ew);
+    const float4* rv = reinterpret_cast<const float4*>(p.r + t * p.L);
+    const int n4 = p.L / 4;
+    constexpr int PER = 32;  // float4s per lane held in registers (L <= 4096)
+    float4 v[PER];
+    float ss = 0.f;
 #pragma unroll
-  for (int i = 0; i < PER; ++i) {
-    const int c = etid + i * W::EPI_THREADS;
-    v[i] = c < n4 ? __ldcg(rv + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
+    for (int i = 0; i < PER; ++i) {
+      const int c = lane + i * 32;
+      v[i] = c < n4 ? __ldcg(rv + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
 #pragma unroll
-  for (int i = 0; i < PER; ++i)
-    ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+    for (int i = 0; i < PER; ++i)
+      ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
 #pragma unroll
-  for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
-  if (lane == 0) sm.part[ew] = ss;
-  named_bar_sync(1, W::EPI_THREADS);
-  float tot = 0.f;
+    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+    const float inv = rsqrtf(ss / static_cast<float>(p.L) + p.eps);
+    const uint2* gg = reinterpret_cast<const uint2*>(p.gamma);
+    uint2* nn = reinterpret_cast<uint2*>(p.nrm + t * p.L);
 #pragma unroll
-  for (int w = 0; w < W::EPI_WARPS; ++w) tot += sm.part[w];
-  const float inv = rsqrtf(tot / static_cast<float>(p.L) + p.eps);
-  const uint2* gg = reinterpret_cast<const uint2*>(p.gamma);
-  uint2* nn = reinterpret_cast<uint2*>(p.nrm + t * p.L);
-#pragma unroll
-  for (int i = 0; i < PER; ++i) {
-    const int c = etid + i * W::EPI_THREADS;
-    if (c < n4) {
-      const float4 x = v[i];
-      const uint2 graw = __ldg(gg + c);
-      const __nv_bfloat162 g01 = *reinterpret_cast<const __nv_bfloat162*>(&graw.x);
-      const __nv_bfloat162 g23 = *reinterpret_cast<const __nv_bfloat162*>(&graw.y);
-      const __nv_bfloat162 o01 = __floats2bfloat162_rn(x.x * inv * __low2float(g01),
-                                                       x.y * inv * __high2float(g01));
-      const __nv_bfloat162 o23 = __floats2bfloat162_rn(x.z * inv * __low2float(g23),
-                                                       x.w * inv * __high2float(g23));
-      uint2 o;
-      o.x = *reinterpret_cast<const uint32_t*>(&o01);
-      o.y = *reinterpret_cast<const uint32_t*>(&o23);
-      nn[c] = o;
+    for (int i = 0; i < PER; ++i) {
+      const int c = lane + i * 32;
+      if (c < n4) {
+        const float4 x = v[i];
+        const uint2 graw = __ldg(gg + c);
+        const __nv_bfloat162 g01 = *reinterpret_cast<const __nv_bfloat162*>(&graw.x);
+        const __nv_bfloat162 g23 = *reinterpret_cast<const __nv_bfloat162*>(&graw.y);
+        const __nv_bfloat162 o01 = __floats2bfloat162_rn(x.x * inv * __low2float(g01),
+                                                         x.y * inv * __high2float(g01));
+        const __nv_bfloat162 o23 = __floats2bfloat162_rn(x.z * inv * __low2float(g23),
+                                                         x.w * inv * __high2float(g23));
+        uint2 o;
+        o.x = *reinterpret_cast<const uint32_t*>(&o01);
+        o.y = *reinterpret_cast<const uint32_t*>(&o23);
+        nn[c] = o;
+      }
     }
   }
-  named_bar_sync(1, W::EPI_THREADS);  // sm.part is reused by the next row
-  w_signal(p, sm, sg, p.norm_done + row / W::TM, ew, lane);
+  w_signal(p, sm, sg, p.norm_done + row0 / W::TM, ew, lane);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
@@ -534,7 +531,7 @@ __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
     const GemmTask& T = p.task[info.task];
     const int kind = T.kind;
     if (kind == TASK_NORM) {
-      w_norm_row(p, sm, sg, info.row0, ew, lane);
+      w_norm_rows(p, sm, sg, info.row0, info.rows, ew, lane);
       continue;
     }
     // a dual unit (two token tiles sharing the weight operand, accumulated in consecutive
