@@ -9,10 +9,11 @@
 // 128-row weight tiles placed back to back (gate and up of an L1 unit, or two consecutive
 // row blocks of L2 / output weights).  With 256 features per MMA the tensor pipe, not the
 // single issuing thread, sets the pace, and each staged byte feeds twice the MMA work of a
-// 128-feature tile.
+// 128-feature tile.  From 16 token tiles on, the BF16 tasks (shared L1, output GEMM) run
+// dual units: two token tiles share each staged weight tile and fill both TMEM slots.
 //
-// Warp roles (3 warpgroups): warp 0 = TMA producer, warp 1 = MMA issuer, warps 2-3 idle,
-// warps 4-11 = epilogue.  The control warpgroup hands registers to the epilogue
+// Warp roles (3 warpgroups): warp 0 = TMA producer, warp 1 = MMA issuer, warp 2 = unit
+// completion signaller, warp 3 idle, warps 4-11 = epilogue.  The control warpgroup hands registers to the epilogue
 // warpgroups (setmaxnreg) so each epilogue thread can hold its 128 fp32 accumulators of
 // one token across the per-128-K promotion of block-scaled FP8 (or NVFP4) products.
 //
