@@ -46,7 +46,7 @@ struct Cfg {
   static constexpr int STAGES = BN == 16 ? 6 : (BN == 128 ? 3 : 5);
   static_assert(BN == 16 || BN == 32 || BN == 64 || BN == 128, "tile width");
   static constexpr int SLOT_COLS = 2 * BN;
-  static constexpr int TMEM_COLS = BN <= 64 ? 256 : 512;
+  static constexpr int TMEM_COLS = 512;  // the whole TMEM: 16 accumulator slots at BN=16
   static constexpr int NACC = TMEM_COLS / SLOT_COLS;
   static constexpr int US = 8;
   static constexpr int COLS = BN / (EPI_WARPS / 4);
