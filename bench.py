@@ -300,6 +300,39 @@ def main():
     value = ws * M * args.steps / (ms / 1e3)
     assert tail.status() == B.KLT_OK
 
+    # ---- the same step captured once in a CUDA graph (kernels chained by programmatic
+    # dependent launch edges) and replayed, L2 flushed before each replay
+    try:
+        graph_obj = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            step()
+        torch.cuda.current_stream().wait_stream(side)
+        with torch.cuda.graph(graph_obj):
+            step()
+        torch.cuda.synchronize()
+        gs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ge = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            gs[i].record(stream)
+            graph_obj.replay()
+            ge[i].record(stream)
+        torch.cuda.synchronize()
+        assert tail.status() == B.KLT_OK
+        gms = sum(a.elapsed_time(b) for a, b in zip(gs, ge))
+        if ws > 1:
+            t = torch.tensor([gms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            gms = float(t.item())
+        graph = {"value": ws * M * args.steps / (gms / 1e3), "unit": "tokens/s",
+                 "ms_per_step": gms / args.steps,
+                 "how": "one klt_forward captured in a CUDA graph, replayed per step"}
+        del graph_obj
+    except Exception as exc:  # report, do not fail the line
+        graph = {"unavailable": f"{type(exc).__name__}: {str(exc)[:160]}"}
+
     # ---- per-launch breakdown (events between launches; separate loop)
     nev = nl + 1
     assert nl <= 8
@@ -410,6 +443,7 @@ def main():
         "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": nl * args.steps,
+        "graph": graph,
         "clocks": {**clk.summary(),
                    "window": "nvidia-smi every 200 ms, timed steps bracketed by 0.5 s of the "
                              "same steps on each side"},

@@ -218,6 +218,50 @@ def test_repeated_calls_and_smaller_m_reuse_the_workspace():
         tail.close()
 
 
+@pytest.mark.parametrize("M,bn", [(12, 0), (40, 256)])
+def test_two_consecutive_forwards_replayed_from_a_cuda_graph(M, bn):
+    # two layers' tails captured in one CUDA graph (the launches of each forward, and of the
+    # second after the first, chained by programmatic dependent launch edges), replayed
+    # twice: every output matches the oracle, and the replays match each other
+    cfg = configs.SMALL.with_(E=8, topk=3, seed=44)
+    w_cpu, w_gpu = weights_for(cfg)
+    tail = B.LatentMoETail(cfg, w_gpu, max_tokens=M)
+    try:
+        acts = [inputs.make_activations(cfg.with_(seed=44 + i), M) for i in range(2)]
+        dev = [PU.to_cuda(a) for a in acts]
+        outs = [torch.empty((M, cfg.H), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+        dbg = B.KltDebug()
+        dbg.force_bn = bn
+
+        def layers():
+            for a, o in zip(dev, outs):
+                tail.forward(a["x"], a["z"], a["logits"], out=o, debug=dbg)
+
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            layers()
+        torch.cuda.current_stream().wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            layers()
+        got = []
+        for _ in range(2):
+            for o in outs:
+                o.fill_(0)
+            g.replay()
+            torch.cuda.synchronize()
+            assert tail.status() == B.KLT_OK
+            got.append([o.float().cpu().numpy().astype(np.float64) for o in outs])
+        for a, y in zip(acts, got[0]):
+            PU.assert_output_close(y, T.tail(a, w_cpu, cfg)["out"])
+        for y0, y1 in zip(got[0], got[1]):
+            assert PU.rel_fro(y1, y0) <= 1e-3  # the fp32 combine adds in arrival order
+        del g
+    finally:
+        tail.close()
+
+
 def test_m_zero_is_a_noop_and_bad_m_is_rejected():
     cfg = configs.SMALL
     _, w_gpu = weights_for(cfg)
