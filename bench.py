@@ -214,6 +214,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--phased", action="store_true",
                     help="one launch per GEMM stage instead of the fused persistent launch")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="fixed-order combine of the routed experts (KLT_FLAG_DETERMINISTIC)")
     ap.add_argument("--tile-n", type=int, default=0,
                     help="GEMM engine / token-tile width: 16..128 feature-major, 256 "
                          "token-major (0 = library choice)")
@@ -242,7 +244,9 @@ def main():
     act_cpu, w_cpu = inputs.make_inputs(cfg)
     w = {k: v.cuda() for k, v in w_cpu.items()}
     act = {k: v.cuda() for k, v in act_cpu.items()}
-    tail = B.LatentMoETail(cfg, w, flags=B.KLT_FLAG_PHASED if args.phased else 0)
+    flags = (B.KLT_FLAG_PHASED if args.phased else 0) | \
+        (B.KLT_FLAG_DETERMINISTIC if args.deterministic else 0)
+    tail = B.LatentMoETail(cfg, w, flags=flags)
     del w
     out = torch.empty((M, cfg.H), dtype=torch.bfloat16, device="cuda")
     stream = torch.cuda.current_stream()
@@ -432,6 +436,7 @@ def main():
                    "topk": cfg.topk, "I": cfg.I, "Is": cfg.Is, "routed_fmt": cfg.routed_fmt,
                    "l2": "flushed (512 MB write) before every timed step",
                    "schedule": "phased" if args.phased else "fused",
+                   "combine": "fixed order" if args.deterministic else "arrival order",
                    "parallelism": f"replicas x{ws}"},
         "roofline": roof,
         "step_roofline": {"algorithmic_bytes": int(ab["total"]),

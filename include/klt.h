@@ -59,9 +59,17 @@ enum klt_routed_format {
 enum klt_flags {
   KLT_FLAG_NO_PDL = 1u << 0,  /* launch the kernels with plain stream ordering instead of
                                  programmatic dependent launch                          */
-  KLT_FLAG_PHASED = 1u << 1   /* run the GEMM stages as three launches plus a norm launch
+  KLT_FLAG_PHASED = 1u << 1,  /* run the GEMM stages as three launches plus a norm launch
                                  instead of one persistent launch with device-side
                                  dependencies (same results; for comparison)            */
+  KLT_FLAG_DETERMINISTIC = 1u << 2 /* combine the routed experts' outputs in a fixed order:
+                                 each (token, choice) slot's weighted output is stored and
+                                 the norm sums a token's topk slots in choice order, so the
+                                 output is bitwise reproducible run to run (by default the
+                                 routed L2 units add into an fp32 row as they finish).
+                                 Costs max_tokens * topk * L * 4 bytes of workspace and
+                                 that traffic per forward.  Not combinable with
+                                 KLT_FLAG_PHASED (klt_create: KLT_ERR_UNSUPPORTED).       */
 };
 
 /* Layer shape.  H, L, I, Is must be multiples of 128; 1 <= topk <= min(E, 32);

@@ -25,6 +25,7 @@ KLT_FMT_FP8_B128 = 0
 KLT_FMT_NVFP4 = 1
 KLT_FLAG_NO_PDL = 1
 KLT_FLAG_PHASED = 2
+KLT_FLAG_DETERMINISTIC = 4
 
 EXPORTS = ("klt_create", "klt_forward", "klt_status", "klt_destroy", "klt_strerror",
            "klt_launch_count", "klt_gemm_tile", "klt_route_noalloc")

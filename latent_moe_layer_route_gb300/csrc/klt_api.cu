@@ -80,6 +80,7 @@ struct klt_handle {
   // workspace
   int32_t *ids, *cnt, *off, *tile_off, *gidx, *slot, *pos, *hist;
   float *wts, *wperm, *zs, *zsT, *asT, *r, *ws;
+  float* yw;  // deterministic combine: weighted output per (token, choice) slot, or null
   uint8_t *zq, *zq_perm, *aq;
   __nv_bfloat16 *n, *a_s, *zqb_perm, *aqb;
   int *split_cnt, *sched, *err;
@@ -169,6 +170,7 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
   if (!d || !w) return KLT_ERR_INVALID_ARG;
   int rc = check_dims(d);
   if (rc) return rc;
+  if ((flags & KLT_FLAG_DETERMINISTIC) && (flags & KLT_FLAG_PHASED)) return KLT_ERR_UNSUPPORTED;
   const bool nvfp4 = d->routed_fmt == KLT_FMT_NVFP4;
   if (nvfp4 && (!w->w13_global || !w->w2_global)) return KLT_ERR_INVALID_ARG;
   if (nvfp4 && (!aligned16(w->w13_global) || !aligned16(w->w2_global))) return KLT_ERR_ALIGN;
@@ -238,6 +240,7 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
   KLT_ALLOC(h->aq, cap * I);
   KLT_ALLOC(h->asT, (I / 128) * cap * 4);
   KLT_ALLOC(h->r, Mx * L * 4);
+  if (flags & KLT_FLAG_DETERMINISTIC) KLT_ALLOC(h->yw, cap * L * 4);
   KLT_ALLOC(h->n, Mx * L * 2);
   KLT_ALLOC(h->a_s, Mx * Is * 2);
   // split-K partials: [shared L1 | output GEMM], one half each
@@ -423,6 +426,9 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
   gp.aqb = nvfp4 ? h->aqb : nullptr;
   gp.asT = h->asT;
   gp.r = h->r;
+  gp.yw = (h->flags & KLT_FLAG_DETERMINISTIC) ? h->yw : nullptr;
+  gp.pos = h->pos;
+  gp.topk = k;
   gp.a_s = h->a_s;
   gp.out = static_cast<__nv_bfloat16*>(out);
   gp.ws = h->ws;

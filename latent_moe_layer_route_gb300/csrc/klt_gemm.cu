@@ -622,7 +622,7 @@ __device__ __forceinline__ int promote_batch(int left, int kbi, const float* sb,
   return nb;
 }
 
-template <int BN>
+template <int BN, bool DET>
 __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_base) {
   using C = Cfg<BN>;
   constexpr int COLS = C::COLS;
@@ -658,6 +658,25 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
       // epilogue threads split the row; each loads its float4s before using them.
       const size_t t = static_cast<size_t>(info.row0);
       const float4* rv = reinterpret_cast<const float4*>(p.r + t * p.L);
+      // the combined row: r (added into by the routed L2 units), or the token's topk
+      // weighted slots summed in choice order (deterministic combine)
+      auto row4 = [&](int c) {
+        if constexpr (!DET) {
+          return __ldcg(rv + c);
+        } else {
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int j = 0; j < p.topk; ++j) {
+            const int pj = __ldg(p.pos + t * p.topk + j);
+            const float4 y =
+                __ldcg(reinterpret_cast<const float4*>(p.yw + static_cast<size_t>(pj) * p.L) + c);
+            acc.x += y.x;
+            acc.y += y.y;
+            acc.z += y.z;
+            acc.w += y.w;
+          }
+          return acc;
+        }
+      };
       const int etid = threadIdx.x - 64;
       const int n4 = p.L / 4;
       constexpr int PER = 8;  // float4s per thread held in registers (L <= 4096 * ... )
@@ -666,13 +685,13 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
 #pragma unroll
       for (int i = 0; i < PER; ++i) {
         const int c = etid + i * C::EPI_THREADS;
-        v[i] = c < n4 ? __ldcg(rv + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[i] = c < n4 ? row4(c) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int i = 0; i < PER; ++i) ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z +
                                          v[i].w * v[i].w;
       for (int c = etid + PER * C::EPI_THREADS; c < n4; c += C::EPI_THREADS) {  // wide rows
-        const float4 w = __ldcg(rv + c);
+        const float4 w = row4(c);
         ss += w.x * w.x + w.y * w.y + w.z * w.z + w.w * w.w;
       }
 #pragma unroll
@@ -703,7 +722,7 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
         if (c < n4) emit(c, v[i]);
       }
       for (int c = etid + PER * C::EPI_THREADS; c < n4; c += C::EPI_THREADS)
-        emit(c, __ldcg(rv + c));
+        emit(c, row4(c));
       named_bar_sync(1, C::EPI_THREADS);  // sm.red is reused by the next unit
       signal_done<BN>(p, sm, sg, p.norm_done + info.dep_idx, ew, lane);
       continue;
@@ -850,7 +869,10 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
         if (c0 + j < info.rows) {
           const int tok = __float_as_int(sb[MAX_KB * BN + 2 * MAX_KB + c0 + j]);
           const float wv = sb[MAX_KB * BN + 2 * MAX_KB + BN + c0 + j];
-          atomicAdd(p.r + static_cast<size_t>(tok) * p.L + col, wv * g[j]);
+          if constexpr (DET)  // this pair's weighted output, summed later in choice order
+            p.yw[static_cast<size_t>(info.row0 + c0 + j) * p.L + col] = wv * g[j];
+          else
+            atomicAdd(p.r + static_cast<size_t>(tok) * p.L + col, wv * g[j]);
         }
       }
       if (p.l2_done != nullptr) signal_done<BN>(p, sm, sg, p.l2_done, ew, lane);
@@ -890,7 +912,7 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
   }
 }
 
-template <int BN>
+template <int BN, bool DET>
 __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
     gemm_kernel(const __grid_constant__ GemmParams p) {
   using C = Cfg<BN>;
@@ -953,7 +975,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
   } else if (warp == C::SIGNAL_WARP) {
     if (lane == 0) run_signaller<BN>(p, sm);
   } else {
-    run_epilogue<BN>(p, sm, tmem_base);
+    run_epilogue<BN, DET>(p, sm, tmem_base);
   }
 
   tc_fence_before();
@@ -969,7 +991,9 @@ template <int BN>
 cudaError_t launch_bn(const GemmParams& p, int grid, cudaStream_t s, bool pdl) {
   using C = Cfg<BN>;
   const int smem = Smem<BN>::bytes();
-  cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN>,
+  // the deterministic combine is a separate instantiation (no code in the default one)
+  const bool det = p.yw != nullptr;
+  cudaError_t e = cudaFuncSetAttribute(det ? gemm_kernel<BN, true> : gemm_kernel<BN, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -982,7 +1006,8 @@ cudaError_t launch_bn(const GemmParams& p, int grid, cudaStream_t s, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<BN>, p);
+  return det ? cudaLaunchKernelEx(&cfg, gemm_kernel<BN, true>, p)
+             : cudaLaunchKernelEx(&cfg, gemm_kernel<BN, false>, p);
 }
 
 }  // namespace

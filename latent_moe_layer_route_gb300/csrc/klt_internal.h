@@ -117,6 +117,11 @@ struct GemmParams {
   __nv_bfloat16* aqb;          // [cap, I] exact bf16 images of aq (bf16-operand layers) or null
   float* asT;                  // [I/128, cap]
   float* r;                    // [M, L]
+  // deterministic combine (null yw: the routed L2 units add into r): the routed L2 units
+  // store w * y per permuted pair into yw and the norm sums a token's topk slots in order
+  float* yw;                   // [cap, L] or null
+  const int32_t* pos;          // [M, topk] permuted pair of (token, choice)
+  int topk;
   __nv_bfloat16* a_s;          // [max_tokens, Is]
   __nv_bfloat16* out;          // [M, H]
   float* ws;                   // split-K partials

@@ -458,11 +458,31 @@ __device__ void w_signaller(const GemmParams& p, WSmem& sm) {
 // RMSNorm of up to NORM_ROWS token rows of the fp32 combine, one row per epilogue warp:
 // fp32 statistic (lane partials, then a shuffle tree), gamma applied, one bf16 rounding (the
 // output GEMM's token operand).  No barrier between the warps.
+template <bool DET>
 __device__ void w_norm_rows(const GemmParams& p, WSmem& sm, SigState& sg, int row0, int rows,
                             int ew, int lane) {
   if (ew < rows) {
     const size_t t = static_cast<size_t>(row0 + ew);
     const float4* rv = reinterpret_cast<const float4*>(p.r + t * p.L);
+    // the combined row: r (added into by the routed L2 units), or the token's topk weighted
+    // slots summed in choice order (deterministic combine)
+    auto row4 = [&](int c) {
+      if constexpr (!DET) {
+        return __ldcg(rv + c);
+      } else {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < p.topk; ++j) {
+          const int pj = __ldg(p.pos + t * p.topk + j);
+          const float4 y =
+              __ldcg(reinterpret_cast<const float4*>(p.yw + static_cast<size_t>(pj) * p.L) + c);
+          acc.x += y.x;
+          acc.y += y.y;
+          acc.z += y.z;
+          acc.w += y.w;
+        }
+        return acc;
+      }
+    };
     const int n4 = p.L / 4;
     constexpr int PER = 32;  // float4s per lane held in registers (L <= 4096)
     float4 v[PER];
@@ -470,7 +490,7 @@ __device__ void w_norm_rows(const GemmParams& p, WSmem& sm, SigState& sg, int ro
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
       const int c = lane + i * 32;
-      v[i] = c < n4 ? __ldcg(rv + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[i] = c < n4 ? row4(c) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int i = 0; i < PER; ++i)
@@ -507,6 +527,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+template <bool DET>
 __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ew = warp - W::FIRST_EPI_WARP;
@@ -532,7 +553,7 @@ __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
     const GemmTask& T = p.task[info.task];
     const int kind = T.kind;
     if (kind == TASK_NORM) {
-      w_norm_rows(p, sm, sg, info.row0, info.rows, ew, lane);
+      w_norm_rows<DET>(p, sm, sg, info.row0, info.rows, ew, lane);
       continue;
     }
     // a dual unit (two token tiles sharing the weight operand, accumulated in consecutive
@@ -693,6 +714,18 @@ __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
         }
         if (p.sh_done != nullptr) w_signal(p, sm, sg, p.sh_done + dep_idx, ew, lane);
       } else if (kind == TASK_ROUTED_L2) {
+        if constexpr (DET) {
+          // this pair's weighted output, summed in choice order by the norm: 128 features
+          // of one permuted row per thread, 16-byte stores
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(
+                p.yw + static_cast<size_t>(row0 + tok) * p.L + info.ftile * 256 + half * 128);
+  #pragma unroll
+            for (int c = 0; c < 32; ++c)
+              dst[c] = make_float4(wv * a[4 * c], wv * a[4 * c + 1], wv * a[4 * c + 2],
+                                   wv * a[4 * c + 3]);
+          }
+        } else {
         // Weighted scatter-combine into the tokens' fp32 rows of r.  A lane holds one token's
         // 128 features; 16 features of the warp's 32 tokens at a time pass through shared
         // memory, so each vector reduction instruction covers 8 tokens x 64 contiguous bytes
@@ -727,6 +760,7 @@ __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
           }
           __syncwarp();
         }
+        }
         if (p.l2_done != nullptr) w_signal(p, sm, sg, p.l2_done, ew, lane);
       } else {  // TASK_OUT
         if (valid) {
@@ -744,6 +778,7 @@ __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
   }
 }
 
+template <bool DET>
 __global__ void __launch_bounds__(W::THREADS, 1) wide_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   WSmem sm(smem_raw);
@@ -808,7 +843,7 @@ __global__ void __launch_bounds__(W::THREADS, 1) wide_kernel(const __grid_consta
     }
   } else {
     regs_inc<W::REGS_EPI>();
-    w_epilogue(p, sm, tmem_base);
+    w_epilogue<DET>(p, sm, tmem_base);
   }
 
   tc_fence_before();
@@ -824,18 +859,20 @@ __global__ void __launch_bounds__(W::THREADS, 1) wide_kernel(const __grid_consta
 
 static_assert(WSmem::bytes() + 2 * (MAX_E + 1) * 4 <= 227 * 1024, "shared memory budget");
 
-int wide_kernel_regs() {
-  cudaFuncAttributes a;
-  if (cudaFuncGetAttributes(&a, wide_kernel) != cudaSuccess) return -1;
-  return a.numRegs;
+int wide_kernel_regs() {  // both instantiations must launch with the planned registers
+  cudaFuncAttributes a, b;
+  if (cudaFuncGetAttributes(&a, wide_kernel<false>) != cudaSuccess) return -1;
+  if (cudaFuncGetAttributes(&b, wide_kernel<true>) != cudaSuccess) return -1;
+  return a.numRegs == b.numRegs ? a.numRegs : -1;
 }
 
 bool wide_regs_ok(int regs) { return regs == W::LAUNCH_REGS; }
 
 cudaError_t launch_wide(const GemmParams& p, int grid, cudaStream_t s, bool pdl) {
   const int smem = WSmem::bytes();
-  cudaError_t e =
-      cudaFuncSetAttribute(wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const bool det = p.yw != nullptr;  // deterministic combine: its own instantiation
+  cudaError_t e = cudaFuncSetAttribute(det ? wide_kernel<true> : wide_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -847,7 +884,8 @@ cudaError_t launch_wide(const GemmParams& p, int grid, cudaStream_t s, bool pdl)
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, wide_kernel, p);
+  return det ? cudaLaunchKernelEx(&cfg, wide_kernel<true>, p)
+             : cudaLaunchKernelEx(&cfg, wide_kernel<false>, p);
 }
 
 }  // namespace klt

@@ -91,8 +91,10 @@ def check_routing(run: Run, o: Dict, cfg, tokens: Optional[np.ndarray] = None):
     np.testing.assert_array_equal(run.host("pos").numpy(), o["pos"])
 
 
-def check_stages(run: Run, o: Dict, cfg):
-    """Every stage for the oracle's selected tokens (o['tokens'])."""
+def check_stages(run: Run, o: Dict, cfg, combine_buffer: bool = True):
+    """Every stage for the oracle's selected tokens (o['tokens']).  `combine_buffer` False:
+    the forward ran the fixed-order combine, which keeps no fp32 combine row (its sum is
+    checked through the normalised latent and the output)."""
     tok = o["tokens"]
     zq = run.host("zq").numpy()[tok]
     np.testing.assert_array_equal(zq, o["zq"])
@@ -107,7 +109,8 @@ def check_stages(run: Run, o: Dict, cfg):
     assert rel_fro(deq_g, deq_o) < 2e-2
     code_diff = (aq != o["aq"]).mean()
     assert code_diff < 0.02, f"routed activation codes differ in {code_diff:.3%}"
-    assert rel_fro(run.host("r").numpy()[tok].astype(np.float64), o["r"]) < REL_FRO
+    if combine_buffer:
+        assert rel_fro(run.host("r").numpy()[tok].astype(np.float64), o["r"]) < REL_FRO
     a_s = run.host("a_s").float().numpy()[tok].astype(np.float64)
     assert rel_fro(a_s, o["a_s"]) < REL_FRO
     nn = run.host("n").float().numpy()[tok].astype(np.float64)

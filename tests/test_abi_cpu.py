@@ -74,6 +74,15 @@ def test_create_rejects_null_and_bad_shapes(lib):
     assert _create(lib, _dims(E=64, topk=33), w)[0] == B.KLT_ERR_UNSUPPORTED
 
 
+def test_create_rejects_the_deterministic_combine_with_phased_launches(lib):
+    w = B.KltWeights(*([0x1000] * 10))
+    h = ctypes.c_void_p()
+    flags = B.KLT_FLAG_DETERMINISTIC | B.KLT_FLAG_PHASED
+    assert lib.klt_create(ctypes.byref(_dims()), ctypes.byref(w), flags, ctypes.byref(h)) == \
+        B.KLT_ERR_UNSUPPORTED
+    assert not h.value
+
+
 def test_create_rejects_null_and_misaligned_weight_pointers(lib):
     ptrs = [0x1000] * 10
     ptrs[2] = ptrs[5] = 0  # fp8 layers do not use the global scales

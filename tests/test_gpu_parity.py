@@ -52,7 +52,7 @@ def run_case(cfg, M=None, act=None, tokens=None, max_tokens=None, tail=None, for
     assert tail.status() == B.KLT_OK
     o = T.tail(act, w_cpu, cfg, tokens=tokens)
     PU.check_routing(run, o, cfg)
-    rf = PU.check_stages(run, o, cfg)
+    rf = PU.check_stages(run, o, cfg, combine_buffer=not flags & B.KLT_FLAG_DETERMINISTIC)
     if own:
         tail.close()
     return run, o, rf
@@ -258,6 +258,29 @@ def test_two_consecutive_forwards_replayed_from_a_cuda_graph(M, bn):
         for y0, y1 in zip(got[0], got[1]):
             assert PU.rel_fro(y1, y0) <= 1e-3  # the fp32 combine adds in arrival order
         del g
+    finally:
+        tail.close()
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+@pytest.mark.parametrize("M,bn", [(12, 0), (40, 256), (300, 256)])
+def test_deterministic_combine_matches_the_oracle_and_repeats_bitwise(fmt, M, bn):
+    # each (token, choice) slot's weighted output stored, summed in choice order by the norm
+    cfg = configs.SMALL.with_(E=8, topk=3, routed_fmt=fmt, seed=45)
+    run_case(cfg, M=M, force_bn=bn, flags=B.KLT_FLAG_DETERMINISTIC)
+    w_cpu, w_gpu = weights_for(cfg)
+    tail = B.LatentMoETail(cfg, w_gpu, max_tokens=M, flags=B.KLT_FLAG_DETERMINISTIC)
+    try:
+        a = PU.to_cuda(inputs.make_activations(cfg, M))
+        dbg = B.KltDebug()
+        dbg.force_bn = bn
+        outs = []
+        for _ in range(3):
+            outs.append(tail.forward(a["x"], a["z"], a["logits"], debug=dbg).clone())
+        torch.cuda.synchronize()
+        assert tail.status() == B.KLT_OK
+        for o in outs[1:]:
+            assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
     finally:
         tail.close()
 
