@@ -133,7 +133,8 @@ typedef struct klt_routing {
  *   zq e4m3 [M, L], zs f32 [M, L/128]: quantised latent input;
  *   aq e4m3 [M * topk, I], as f32 [M * topk, I/128]: quantised routed SwiGLU output,
  *     rows in pair order p;
- *   r f32 [M, L]: routed combine; n bf16 [M, L]: RMSNorm output (gamma applied);
+ *   r f32 [M, L]: routed combine (not formed with KLT_FLAG_DETERMINISTIC, whose norm sums
+ *     the per-pair outputs directly); n bf16 [M, L]: RMSNorm output (gamma applied);
  *   a_s bf16 [M, Is]: shared-expert SwiGLU output;
  *   events: up to 8 cudaEvent_t handles, events[i] recorded after launch i (NULL skips);
  *   stall_after_kblocks: test hook, 0 = off; when > 0 the tile producer of the first
