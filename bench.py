@@ -40,6 +40,23 @@ def _peaks():
         return 6800.0, 1900.0, "fallback"
 
 
+def max_over_ranks(value: float, ws: int, device: str = "cuda") -> float:
+    """The largest of every rank's value: a replicated job runs as long as its slowest
+    replica."""
+    if ws <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(ws: int, m: int, steps: int, ms_total: float) -> float:
+    """Tokens per second of the whole job: every replica processes m tokens a step."""
+    return ws * m * steps / (ms_total / 1e3)
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -295,13 +312,9 @@ def main():
         load_for(0.5)
     if ws > 1:
         dist.barrier()
-    ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
-    if ws > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(starts, ends)), ws)
     ms_step = ms / args.steps
-    value = ws * M * args.steps / (ms / 1e3)
+    value = job_throughput(ws, M, args.steps, ms)
     assert tail.status() == B.KLT_OK
 
     # ---- the same step captured once in a CUDA graph (kernels chained by programmatic
@@ -325,12 +338,8 @@ def main():
             ge[i].record(stream)
         torch.cuda.synchronize()
         assert tail.status() == B.KLT_OK
-        gms = sum(a.elapsed_time(b) for a, b in zip(gs, ge))
-        if ws > 1:
-            t = torch.tensor([gms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            gms = float(t.item())
-        graph = {"value": ws * M * args.steps / (gms / 1e3), "unit": "tokens/s",
+        gms = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(gs, ge)), ws)
+        graph = {"value": job_throughput(ws, M, args.steps, gms), "unit": "tokens/s",
                  "ms_per_step": gms / args.steps,
                  "how": "one klt_forward captured in a CUDA graph, replayed per step"}
         del graph_obj
@@ -384,12 +393,8 @@ def main():
         oh.copy_(out, non_blocking=True)
         e1[i].record(stream)
     torch.cuda.synchronize()
-    ems = sum(a.elapsed_time(b) for a, b in zip(e0, e1))
-    if ws > 1:
-        t = torch.tensor([ems], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ems = float(t.item())
-    e2e = ws * M * args.steps / (ems / 1e3)
+    ems = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(e0, e1)), ws)
+    e2e = job_throughput(ws, M, args.steps, ems)
     h2d = xh.numel() * 2 + zh.numel() * 2 + lh.numel() * 4
     d2h = oh.numel() * 2
 
