@@ -1,17 +1,20 @@
 """Benchmark of the latent-MoE layer tail on GB300.
 
-One step = one klt_forward (routing, permutation, routed FP8 experts, combine, RMSNorm,
-up-projection + BF16 shared expert) over one batch of synthetic tokens.  Prints one JSON
-line.  Default workload: decode batch of 16 tokens, E=64, top-8, routed intermediate
-1024 (FP8 128x128 block scales), shared intermediate 2048, H=7168, L=3584.
+One step = one klt_forward (routing, permutation, routed FP8/NVFP4 experts, combine,
+RMSNorm, up-projection + BF16 shared expert) over one batch of synthetic tokens.  Prints
+one JSON line.  By default every workload is measured in the same run (tiny M=4, decode
+M=16, decode M=128, prefill M=4096, prefill M=8192 NVFP4); the line's top-level figures
+are the decode batch of 16 tokens (E=64, top-8, routed intermediate 1024 with FP8 128x128
+block scales, shared intermediate 2048, H=7168, L=3584) and `workloads` holds every
+workload's record (roofline, end to end, clocks, the oracle on the host cores).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME]
+                    [--workload all|NAME]
 
 Multi-GPU (under torchrun): the tail has no exchange step, so every rank runs an
 independent replica on its own tokens (weak scaling); time = max over ranks.
-`--impl reference` times the CPU float64 oracle (the only other implementation) on a
-bounded token sample of the same workload.
+`--impl reference` times the CPU float64 oracle (the only other implementation) on the
+headline workload (the whole decode batch per step).
 """
 from __future__ import annotations
 
@@ -171,14 +174,24 @@ def flops(cfg, M: int):
     return routed, dense
 
 
+HEADLINE = "decode_m16_e64_k8_fp8"
+
+
+def dtype_of(cfg) -> str:
+    if cfg.routed_fmt == "fp8":
+        return "fp8e4m3+bf16 (fp32 accumulate)"
+    return "nvfp4 weights (bf16-exact MMA) + fp8e4m3 activations + bf16 (fp32 accumulate)"
+
+
 def run_reference(cfg, args, ws, rank):
-    """The CPU float64 oracle as it stands, on a bounded token sample per step."""
+    """The CPU float64 oracle as it stands, on a bounded token sample per step (the whole
+    batch for decode workloads)."""
     if rank != 0:
         return
     from latent_moe_layer_route_gb300 import inputs
     from oracle import model as oracle_model
     act, w = inputs.make_inputs(cfg)
-    sample = 1  # one token per step keeps K + W oracle steps within a few minutes
+    sample = min(cfg.M, 16)  # a decode batch whole; prefill batches: 16 tokens per step
     tok = np.arange(sample)
     for _ in range(args.warmup):
         oracle_model.tail(act, w, cfg, tokens=tok)
@@ -193,7 +206,8 @@ def run_reference(cfg, args, ws, rank):
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": cfg.name, "M": cfg.M, "sample_tokens": sample},
+        "config": {"workload": cfg.name, "M": cfg.M, "sample_tokens": sample,
+                   "same_config": sample == cfg.M},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": f"first {sample} of {cfg.M} tokens per step"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -221,42 +235,13 @@ def cpu_baseline(cfg, act, w):
             "sample": f"{n} step(s) of the first {sample} of {cfg.M} tokens, {dt:.1f} s"}
 
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode_m16_e64_k8_fp8")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--phased", action="store_true",
-                    help="one launch per GEMM stage instead of the fused persistent launch")
-    ap.add_argument("--deterministic", action="store_true",
-                    help="fixed-order combine of the routed experts (KLT_FLAG_DETERMINISTIC)")
-    ap.add_argument("--tile-n", type=int, default=0,
-                    help="GEMM engine / token-tile width: 16..128 feature-major, 256 "
-                         "token-major (0 = library choice)")
-    args = ap.parse_args()
-    args.warmup = max(args.warmup, 3)
-
-    from latent_moe_layer_route_gb300 import configs
-    cfg = configs.BY_NAME[args.workload]
-    ws, rank, local = _dist()
-
-    if args.impl == "reference":
-        run_reference(cfg, args, ws, rank)
-        return
-
+def measure(cfg, args, ws, rank, local, flush, with_cpu: bool):
+    """Every figure of one workload: device-timed steps, graph replay, per-launch times,
+    end to end with host buffers, roofline of the dominant launch, oracle on the host."""
     import torch
-    import torch.distributed as dist
     from latent_moe_layer_route_gb300 import binding as B
-    from latent_moe_layer_route_gb300 import build, inputs
+    from latent_moe_layer_route_gb300 import inputs
 
-    torch.cuda.set_device(local)
-    if ws > 1:
-        dist.init_process_group("nccl")
-    build.build()
-    B.load_library()
     M = cfg.M
     act_cpu, w_cpu = inputs.make_inputs(cfg)
     w = {k: v.cuda() for k, v in w_cpu.items()}
@@ -267,7 +252,6 @@ def main():
     del w
     out = torch.empty((M, cfg.H), dtype=torch.bfloat16, device="cuda")
     stream = torch.cuda.current_stream()
-    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
     cnt = torch.zeros(cfg.E, dtype=torch.int32, device="cuda")
     ro = B.KltRouting(None, None, cnt.data_ptr(), None, None, None, None)
     tail.forward(act["x"], act["z"], act["logits"], out=out, routing=ro)
@@ -288,11 +272,13 @@ def main():
         step()
     torch.cuda.synchronize()
     if ws > 1:
+        import torch.distributed as dist
         dist.barrier()
 
     # ---- timed region: device time of each step, L2 flushed between steps
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+
     def load_for(seconds):  # the same steps, untimed, so clock samples see the timed load
         t_end = time.perf_counter() + seconds
         while time.perf_counter() < t_end:
@@ -431,14 +417,12 @@ def main():
                 "algorithmic_bytes": int(dom_bytes)}
     roof_time_us = max(ab["total"] / (HBM_NOMINAL_GBS * 1e9), t_tensor) * 1e6
 
-    line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-        "us_per_layer": ms_step * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "fp8e4m3+bf16 (fp32 accumulate)",
-        "data": "synthetic (seeded numpy draws, random-init weights)",
+    rec = {
+        "value": value, "unit": "tokens/s", "ms_per_step": ms_step,
+        "us_per_layer": ms_step * 1e3, "dtype": dtype_of(cfg),
         "config": {"workload": cfg.name, "M": M, "H": cfg.H, "L": cfg.L, "E": cfg.E,
                    "topk": cfg.topk, "I": cfg.I, "Is": cfg.Is, "routed_fmt": cfg.routed_fmt,
+                   "router": cfg.router, "gemm_engine": tail.gemm_tile(M, args.tile_n),
                    "l2": "flushed (512 MB write) before every timed step",
                    "schedule": "phased" if args.phased else "fused",
                    "combine": "fixed order" if args.deterministic else "arrival order",
@@ -458,9 +442,75 @@ def main():
                    "window": "nvidia-smi every 200 ms, timed steps bracketed by 0.5 s of the "
                              "same steps on each side"},
     }
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(cfg, act_cpu, w_cpu)
     tail.close()
+    del act, out, xd, zd, ld
+    torch.cuda.empty_cache()
+    if with_cpu:
+        rec["cpu_baseline"] = cpu_baseline(cfg, act_cpu, w_cpu)
+    return rec
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="all",
+                    help="one workload name, or 'all' (default): every workload measured in "
+                         "this run, decode M=16 as the headline of the printed line")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--phased", action="store_true",
+                    help="one launch per GEMM stage instead of the fused persistent launch")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="fixed-order combine of the routed experts (KLT_FLAG_DETERMINISTIC)")
+    ap.add_argument("--tile-n", type=int, default=0,
+                    help="GEMM engine / token-tile width: 16..128 feature-major, 256 "
+                         "token-major (0 = library choice)")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from latent_moe_layer_route_gb300 import configs
+    if args.workload == "all":
+        cfgs = list(configs.ALL)
+        head = configs.BY_NAME[HEADLINE]
+    else:
+        head = configs.BY_NAME[args.workload]
+        cfgs = [head]
+    ws, rank, local = _dist()
+
+    if args.impl == "reference":
+        run_reference(head, args, ws, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+    from latent_moe_layer_route_gb300 import binding as B
+    from latent_moe_layer_route_gb300 import build
+
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl")
+    build.build()
+    B.load_library()
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    with_cpu = rank == 0 and ws == 1 and not args.no_cpu_baseline
+    recs = {}
+    for cfg in cfgs:
+        recs[cfg.name] = measure(cfg, args, ws, rank, local, flush, with_cpu)
+    h = recs[head.name]
+    line = {
+        "metric": METRIC, "value": h["value"], "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": h["ms_per_step"],
+        "us_per_layer": h["us_per_layer"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": h["dtype"],
+        "data": "synthetic (seeded numpy draws, random-init weights)",
+    }
+    line.update({k: v for k, v in h.items() if k not in line})
+    if len(recs) > 1:
+        line["workloads"] = {
+            n: {k: v for k, v in r.items() if k not in ("graph",)} for n, r in recs.items()}
+        line["gpu_launches_all_workloads"] = sum(r["gpu_launches"] for r in recs.values())
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:

@@ -171,7 +171,13 @@ typedef struct klt_debug {
 
 typedef struct klt_handle klt_handle;
 
-/* Create a tail for one layer on the current device.  Synchronous.  Copies and re-lays out
+/* Create a tail for one layer on the current device.
+ * Defined by: DeepGEMM PR 416 "Fuse and publish Kimi K3's BF16 shared expert", Summary
+ * (routed FP8/FP4 experts scheduled with a BF16 shared expert's L1/L2), and the vLLM pull
+ * request "Fuse BF16 shared experts into latent MegaMoE tail", Summary (the routed result's
+ * RMSNorm and 3584 -> 7168 up-projection before the two branches are added); the weight
+ * formats are the readings of those pages' "FP8/FP4" listed with klt_weights.
+ * Synchronous.  Copies and re-lays out
  * the weights, allocates the workspace for `d->max_tokens` tokens and encodes the TMA
  * descriptors.  Errors: KLT_ERR_INVALID_ARG (null d/w/out or a null weight pointer),
  * KLT_ERR_UNSUPPORTED (shape rules above; device is not compute capability 10.3),
@@ -179,6 +185,11 @@ typedef struct klt_handle klt_handle;
 int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_handle** out);
 
 /* Run the tail for M tokens, asynchronously on `stream`.
+ * Defined by: the vLLM pull request "Fuse BF16 shared experts into latent MegaMoE tail",
+ * Summary (route, routed experts in the 3584-wide latent space, routed RMSNorm, 3584 -> 7168
+ * up-projection, shared-expert output added in FP32, BF16 result) and tokenspeed PR 1062
+ * "MNNVL CuTe-DSL finalize tail", commit notes (top-k weighted combine as the finalize step;
+ * fp32-internal norm, one rounding).
  *   x      device bf16 [M, H]  hidden state (shared-expert input);
  *   z      device bf16 [M, L]  latent state (routed-expert input);
  *   logits device f32  [M, E]  router logits (finite values);
@@ -224,8 +235,11 @@ int klt_gemm_tile(const klt_handle* h, int32_t M, int32_t force_bn);
  * memory, caller owned, 16-byte aligned, none NULL.  Internal buffers live in one
  * fixed-size device array (KLT_NOALLOC_MAX_PAIRS pairs) that every GPU loading the library
  * holds until exit; calls share it, so calls whose kernels overlap on the GPU race; order
- * them on one stream.  The first call on a device resolves the array's device address;
- * make that first call before any stream capture.  Asynchronous on `stream`.
+ * them on one stream.  The first call on a device resolves the array's device address
+ * and caches it for the life of the process; make that first call before any stream
+ * capture.  A device reset (cudaDeviceReset) after that first call is not supported: the
+ * library may then load the array at another address while the cache keeps the old one.
+ * Asynchronous on `stream`.
  * Errors: KLT_ERR_INVALID_ARG (M < 0, E or topk < 1, NULL pointer), KLT_ERR_UNSUPPORTED
  * (E > 256, topk > E, topk > 32), KLT_ERR_TOO_LARGE (M * topk > KLT_NOALLOC_MAX_PAIRS),
  * KLT_ERR_ALIGN, KLT_ERR_CUDA.  M == 0 launches nothing. */

@@ -1,4 +1,5 @@
-"""klt_route_noalloc, the allocation-free routing entry point, against klt_forward.
+"""klt_route_noalloc, the allocation-free routing entry point, against klt_forward and
+the float64 oracle.
 
 Some callers cannot allocate device memory where they route (they run inside another
 framework's memory pool, or pin every allocation at start-up); klt_route_noalloc serves
@@ -7,11 +8,13 @@ the ones klt_forward reports for the same logits, on consecutive calls that reus
 shared scratch.  This file is collected last so that a failure here never hides the other
 tests' results; it also passes when run alone in a fresh process.
 """
+import numpy as np
 import pytest
 import torch
 
 from latent_moe_layer_route_gb300 import binding as B
 from latent_moe_layer_route_gb300 import build, configs, inputs
+from oracle import model as T
 
 pytestmark = pytest.mark.gpu
 
@@ -65,9 +68,21 @@ def _same(a, b):
     torch.testing.assert_close(a["weights"], b["weights"], rtol=1e-6, atol=1e-7)
 
 
-@pytest.mark.parametrize("M", [37, 700])  # one and two permutation blocks (k = 2)
-def test_noalloc_routing_matches_forward_on_two_calls_in_a_row(M):
-    cfg = configs.SMALL.with_(E=8, topk=2, seed=31)
+def _matches_oracle(buf, logits, k, E):
+    ids, w = T.route(logits.cpu().numpy(), k)
+    np.testing.assert_array_equal(buf["ids"].cpu().numpy(), ids)
+    np.testing.assert_allclose(buf["weights"].cpu().numpy().astype(np.float64), w, rtol=1e-6,
+                               atol=1e-7)
+    for name, ref in zip(("cnt", "off", "gidx", "slot", "pos"), T.permutation(ids, E)):
+        np.testing.assert_array_equal(buf[name].cpu().numpy(), ref, err_msg=name)
+
+
+# one and two permutation blocks (k = 2), and exactly the scratch capacity: 8192 tokens x
+# top-8 = KLT_NOALLOC_MAX_PAIRS pairs, 64 permutation blocks in the histogram region
+@pytest.mark.parametrize("M,E,k", [(37, 8, 2), (700, 8, 2), (8192, 64, 8)])
+def test_noalloc_routing_matches_forward_on_two_calls_in_a_row(M, E, k):
+    cfg = configs.SMALL.with_(E=E, topk=k, seed=31)
+    assert M * k <= B.KLT_NOALLOC_MAX_PAIRS
     w_gpu = {n: v.cuda() for n, v in inputs.make_weights(cfg).items()}
     act = {n: v.cuda() for n, v in inputs.make_activations(cfg, M).items()}
     ref = _via_forward(cfg, act, w_gpu)
@@ -75,6 +90,21 @@ def test_noalloc_routing_matches_forward_on_two_calls_in_a_row(M):
     second = _via_noalloc(act["logits"], cfg.topk)
     _same(first, ref)
     _same(second, ref)
+    _matches_oracle(second, act["logits"], k, E)
+
+
+def test_noalloc_accepts_exactly_its_capacity_and_rejects_one_more_pair():
+    E = 8
+    rng = np.random.default_rng(3)
+    logits = torch.from_numpy(
+        rng.standard_normal((B.KLT_NOALLOC_MAX_PAIRS + 1, E), dtype=np.float32)).cuda()
+    full = logits[:B.KLT_NOALLOC_MAX_PAIRS]
+    got = _via_noalloc(full, 1)
+    _matches_oracle(got, full, 1, E)
+    buf = _routing_buffers(B.KLT_NOALLOC_MAX_PAIRS + 1, E, 1)
+    rc = B.klt_route_noalloc(logits, 1, buf["ids"], buf["weights"], buf["cnt"], buf["off"],
+                             buf["gidx"], buf["slot"], buf["pos"])
+    assert rc == B.KLT_ERR_TOO_LARGE
 
 
 def test_noalloc_rejects_requests_beyond_its_scratch():
