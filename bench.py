@@ -474,9 +474,9 @@ def main():
     if args.workload == "all":
         cfgs = list(configs.ALL)
         head = configs.BY_NAME[HEADLINE]
-    else:
-        head = configs.BY_NAME[args.workload]
-        cfgs = [head]
+    else:  # one name, or several separated by commas (the first is the headline)
+        cfgs = [configs.BY_NAME[n] for n in args.workload.split(",")]
+        head = cfgs[0]
     ws, rank, local = _dist()
 
     if args.impl == "reference":

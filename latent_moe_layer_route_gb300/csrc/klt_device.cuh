@@ -125,6 +125,25 @@ KLT_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
+// Asks L2 to fetch `bytes` (a multiple of 16) contiguous bytes from global memory
+// (16-byte aligned); no shared memory and no completion tracking.
+KLT_DEV void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
+               "r"(bytes)
+               : "memory");
+}
+// This CTA's share of [p.pf_ptr, p.pf_ptr + p.pf_bytes), in 64 KB requests.
+template <typename P>
+KLT_DEV void prefetch_share_l2(const P& p) {
+  if (p.pf_ptr == nullptr || p.pf_bytes <= 0) return;
+  const long long per = ((p.pf_bytes + gridDim.x - 1) / gridDim.x + 15) & ~15ll;
+  const long long lo = per * blockIdx.x;
+  const long long hi = lo + per < p.pf_bytes ? lo + per : p.pf_bytes;
+  for (long long o = lo; o < hi; o += 65536) {
+    const long long n = hi - o < 65536 ? hi - o : 65536;
+    bulk_prefetch_l2(p.pf_ptr + o, static_cast<uint32_t>(n));
+  }
+}
 KLT_DEV uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

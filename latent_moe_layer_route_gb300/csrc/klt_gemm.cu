@@ -10,11 +10,13 @@
 // one TMEM lane each) and the tokens are the "B" operand (BN columns), so a decode batch
 // of a few tokens still fills the 128-row MMA and the kernel streams weights.
 //
-// Roles per CTA (1 CTA per SM):
+// Roles per CTA (1 CTA per SM, 12 warps):
 //   warp 0      TMA producer: decodes units, publishes them to a ring, streams A/B tiles
 //               (128-byte swizzled K-major, 128 bytes of K per stage) into STAGES buffers;
 //   warp 1      MMA issuer (one thread): tcgen05.mma into TMEM accumulator slots;
-//   warps 2..   epilogue: TMEM -> registers, then the task's fused epilogue.
+//   warps 2, 3  completion signallers (one per epilogue group);
+//   warps 4-11  epilogue: TMEM -> registers, then the task's fused epilogue; up to 32-token
+//               tiles two groups of four warps take alternate units.
 //
 // FP8 routed tasks use per-128-K promotion: every 128-wide K block is accumulated by the
 // tensor core into its own TMEM slot and the epilogue adds it into fp32 registers scaled
@@ -31,12 +33,28 @@ namespace {
 
 template <int BN>
 struct Cfg {
-  static constexpr int EPI_WARPS = BN >= 64 ? 8 : 4;
-  // producer, MMA issuer, epilogue warps, completion signaller
-  static constexpr int SIGNAL_WARP = 2 + EPI_WARPS;
-  static constexpr int THREADS = (3 + EPI_WARPS) * 32;
-  static constexpr int SIG = 8;  // completion-signal ring (epilogue -> signaller)
+  // Warp roles (3 warpgroups): warp 0 = TMA producer, warp 1 = MMA issuer, warps 2 and 3 =
+  // completion signallers (one per epilogue group), warps 4..11 = epilogue.  Up to 32-token
+  // tiles the eight epilogue warps form two groups of four that take alternate work units,
+  // so two units' epilogues (scale staging, promotion, combine, signal) overlap on every
+  // SM; wider tiles use one group of eight split by column halves.
+  static constexpr int EPI_WARPS = 8;
+  static constexpr int FIRST_EPI_WARP = 4;
+  static constexpr int NGROUPS = BN <= 32 ? 2 : 1;
+  static constexpr int GROUP_WARPS = EPI_WARPS / NGROUPS;
+  static constexpr int GROUP_THREADS = GROUP_WARPS * 32;
+  static constexpr int SIGNAL_WARP = 2;  // + group index
+  static constexpr int THREADS = 12 * 32;
+  static constexpr int SIG = 8;  // completion-signal ring per group (epilogue -> signaller)
   static constexpr int EPI_THREADS = EPI_WARPS * 32;
+  // Registers: 384 threads launch with 168 each; the control warpgroup (producer, MMA
+  // issuer, signallers) drops to 88 and the two epilogue warpgroups rise to 208, within
+  // the registers released.
+  static constexpr int LAUNCH_REGS = 168;
+  static constexpr int REGS_CTRL = 88;
+  static constexpr int REGS_EPI = 208;
+  static_assert(4 * (LAUNCH_REGS - REGS_CTRL) >= 8 * (REGS_EPI - LAUNCH_REGS),
+                "register hand-over must balance");
   static constexpr int A_BYTES = 128 * 128;
   static constexpr int B_BYTES = BN * 128;
   // Single-tile tasks carry two k-blocks per stage (A0/A1 + B0/B1) when the stage fits,
@@ -49,7 +67,7 @@ struct Cfg {
   static constexpr int TMEM_COLS = 512;  // the whole TMEM: 16 accumulator slots at BN=16
   static constexpr int NACC = TMEM_COLS / SLOT_COLS;
   static constexpr int US = 8;
-  static constexpr int COLS = BN / (EPI_WARPS / 4);
+  static constexpr int COLS = BN / (GROUP_WARPS / 4);
   // per-unit scale staging: token group scales [MAX_KB][BN] + weight scales [MAX_KB][2]
   // plus, for the combine, the token index and routing weight of each column [2][BN]
   static constexpr int SC_FLOATS = MAX_KB * BN + 2 * MAX_KB + 2 * BN;
@@ -93,19 +111,21 @@ struct Smem {
   using C = Cfg<BN>;
   uint8_t* stages;
   uint64_t *full, *empty, *tfull, *tempty, *ufull, *uempty, *sfull, *sempty, *drain;
-  int** sptr;  // [SIG] counter each completion signal increments (null: end of work)
+  int** sptr;  // [NGROUPS][SIG] counter each completion signal increments (null: end)
   UnitInfo* ring;
   uint32_t* tmem_holder;
   int* abort_flag;
-  int* last_flag;
+  int* last_flag;  // [NGROUPS]
   float* red;  // [EPI_WARPS][COLS]
-  float* sc;   // [2][SC_FLOATS]
+  float* sc;   // [NGROUPS][SC_FLOATS] per-unit scale staging of each group
 
+  static constexpr int NSIG = C::NGROUPS * C::SIG;
   static constexpr int BAR_BYTES =
-      8 * (2 * C::STAGES + 2 * C::NACC + 2 * C::US + 2 * C::SIG + 1) + 8 * C::SIG;
+      8 * (2 * C::STAGES + 2 * C::NACC + 2 * C::US + 2 * NSIG + 1) + 8 * NSIG;
   static constexpr int bytes() {
     return C::STAGES * C::STAGE_BYTES + BAR_BYTES + C::US * (int)sizeof(UnitInfo) + 64 +
-           C::EPI_WARPS * C::COLS * 4 + 2 * C::SC_FLOATS * 4 + 1024 /* alignment slack */;
+           C::EPI_WARPS * C::COLS * 4 + C::NGROUPS * C::SC_FLOATS * 4 +
+           1024 /* alignment slack */;
   }
   __device__ explicit Smem(uint8_t* raw) {
     uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -119,10 +139,10 @@ struct Smem {
     ufull = tempty + C::NACC;
     uempty = ufull + C::US;
     sfull = uempty + C::US;
-    sempty = sfull + C::SIG;
-    drain = sempty + C::SIG;
+    sempty = sfull + NSIG;
+    drain = sempty + NSIG;
     sptr = reinterpret_cast<int**>(drain + 1);
-    ring = reinterpret_cast<UnitInfo*>(sptr + C::SIG);
+    ring = reinterpret_cast<UnitInfo*>(sptr + NSIG);
     tmem_holder = reinterpret_cast<uint32_t*>(ring + C::US);
     abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
     last_flag = abort_flag + 1;
@@ -135,10 +155,6 @@ struct Smem {
 __device__ __forceinline__ void trace_mark(const GemmParams& p, int role, int i) {
   if (p.trace != nullptr && i < p.trace_n)
     p.trace[(static_cast<long long>(blockIdx.x) * 4 + role) * p.trace_n + i] = global_ns();
-}
-
-__device__ __forceinline__ bool is_pair(int kind) {
-  return kind == TASK_SHARED_L1 || kind == TASK_ROUTED_L1;
 }
 
 template <int BN>
@@ -168,7 +184,7 @@ __device__ UnitInfo decode_unit(const GemmParams& p, const int* s_tile_off, cons
         info.row0 = s_off[e] + (t - s_tile_off[e]) * BN;
         info.rows = min(BN, s_off[e + 1] - info.row0);
         info.ftile = ft;
-        info.arb = e * T.a_rb_expert + ft;
+        info.arb = e * T.a_rb_expert + ft * T.a_rb_step;
         info.kb0 = sp * T.kb_per_split;
         info.kb1 = min(T.kb_total, info.kb0 + T.kb_per_split);
         info.tile_id = T.ws_tile_base + t * T.ftiles + ft;
@@ -209,11 +225,13 @@ __device__ UnitInfo decode_unit(const GemmParams& p, const int* s_tile_off, cons
         info.rows = min(BN, p.M - info.row0);
         info.ftile = ft;
         info.arb = ft;
-        info.kb0 = sp * T.kb_per_split;
+        info.kb0 = T.kb_lo + sp * T.kb_per_split;
         info.kb1 = min(T.kb_total, info.kb0 + T.kb_per_split);
         info.tile_id = T.ws_tile_base + nt * T.ftiles + ft;
-        info.split = sp;
-        info.ncontrib = T.ksplit;
+        // a tile's K range may be shared out between two tasks: contributions are numbered
+        // over both, so the last arriver sums every partial in one fixed order
+        info.split = T.split_base + sp;
+        info.ncontrib = T.ncontrib > 0 ? T.ncontrib : T.ksplit;
         info.cfirst = 0;
         info.wslot = 0;
         info.dep_idx = nt;
@@ -259,22 +277,28 @@ __device__ UnitInfo next_streamk_piece(const GemmParams& p, long long& x, long l
 // Bounded wait until the unit's inputs produced by other units of this launch are complete.
 // The acquire loads pair with the producers' release adds; the proxy fence orders the
 // acquired data before this thread's TMA reads of it.
+// One look at whether the unit's inputs produced by other units of this launch are
+// complete (acquire loads pairing with the producers' release adds).
+template <int BN>
+__device__ __forceinline__ bool dep_ready(const GemmParams& p, int dep, int idx,
+                                          const int* s_tile_off) {
+  if (dep == DEP_L1_TILE) return ld_acquire_gpu(p.l1_done + idx) >= p.l1_target;
+  if (dep == DEP_ALL_L2) return ld_acquire_gpu(p.l2_done) >= s_tile_off[p.E] * p.l2_ftiles;
+  if (dep == DEP_SH_TILE) return ld_acquire_gpu(p.sh_done + idx) >= p.sh_target;
+  if (dep == DEP_NORM_TILE)
+    return ld_acquire_gpu(p.norm_done + idx) >= min(BN, p.M - idx * BN);
+  return ld_acquire_gpu(p.norm_done + idx) >= min(BN, p.M - idx * BN) &&
+         ld_acquire_gpu(p.sh_done + idx) >= p.sh_target;
+}
+
+// Bounded wait until the unit's inputs produced by other units of this launch are complete.
+// The proxy fence orders the acquired data before this thread's TMA reads of it.
 template <int BN>
 __device__ bool wait_dependency(const GemmParams& p, int dep, int idx, const int* s_tile_off,
                                 volatile int* abort_flag) {
   if (dep == DEP_NONE) return true;
   const long long t0 = clock64();
-  for (;;) {
-    bool ready;
-    if (dep == DEP_L1_TILE) {
-      ready = ld_acquire_gpu(p.l1_done + idx) >= p.l1_target;
-    } else if (dep == DEP_ALL_L2) {
-      ready = ld_acquire_gpu(p.l2_done) >= s_tile_off[p.E] * p.l2_ftiles;
-    } else {
-      ready = ld_acquire_gpu(p.norm_done + idx) >= min(BN, p.M - idx * BN) &&
-              ld_acquire_gpu(p.sh_done + idx) >= p.sh_target;
-    }
-    if (ready) break;
+  while (!dep_ready<BN>(p, dep, idx, s_tile_off)) {
     if (*abort_flag) return false;
     if (clock64() - t0 > p.timeout) {
       *abort_flag = 1;
@@ -328,7 +352,7 @@ __device__ void run_producer(const GemmParams& p, Smem<BN>& sm, const int* s_til
       break;
     }
     const GemmTask& T = p.task[info.task];
-    const bool pair = is_pair(T.kind);
+    const bool pair = T.pair != 0;
     const int elems_per_kb = T.fp8 ? 128 : 64;
     const int step = (pair || !C::DUAL) ? 1 : 2;
     auto stage_bytes = [&](int nsub) -> uint32_t {
@@ -362,10 +386,16 @@ __device__ void run_producer(const GemmParams& p, Smem<BN>& sm, const int* s_til
       }
     };
     int kb = info.kb0;
-    if (T.dep != DEP_NONE) {
+    if (T.dep != DEP_NONE && dep_ready<BN>(p, T.dep, info.dep_idx, s_tile_off)) {
+      // inputs already complete: publish at once, stream weight and token tiles together
+      fence_proxy_async_global();
+    } else if (T.dep != DEP_NONE) {
       // Stream the unit's weight tiles into the stages that are free now, then wait for
       // the token operand's producers, then copy the token tiles of those stages.
-      int pre_kb[C::STAGES], pre_st[C::STAGES], npre = 0;
+      // the early stages are consecutive ring slots from st0 holding k-blocks kb0, kb0 +
+      // step, ...
+      const int st0 = stage;
+      int npre = 0;
       while (kb < info.kb1 && npre < C::STAGES) {
         if (p.stall_after > 0 && issued >= p.stall_after) break;
         if (!mbar_try_wait(&sm.empty[stage], phase ^ 1)) break;
@@ -373,8 +403,6 @@ __device__ void run_producer(const GemmParams& p, Smem<BN>& sm, const int* s_til
         uint8_t* st = sm.stages + stage * C::STAGE_BYTES;
         mbar_arrive_expect_tx(&sm.full[stage], stage_bytes(nsub));
         issue_a(kb, nsub, st, &sm.full[stage]);
-        pre_kb[npre] = kb;
-        pre_st[npre] = stage;
         ++npre;
         trace_mark(p, 0, static_cast<int>(issued));
         ++issued;
@@ -382,9 +410,10 @@ __device__ void run_producer(const GemmParams& p, Smem<BN>& sm, const int* s_til
         kb += step;
       }
       if (!wait_dependency<BN>(p, T.dep, info.dep_idx, s_tile_off, sm.abort_flag)) break;
-      for (int i = 0; i < npre; ++i)
-        issue_b(pre_kb[i], min(step, info.kb1 - pre_kb[i]), sm.stages + pre_st[i] * C::STAGE_BYTES,
-                &sm.full[pre_st[i]]);
+      for (int i = 0, s = st0, k = info.kb0; i < npre; ++i, k += step) {
+        issue_b(k, min(step, info.kb1 - k), sm.stages + s * C::STAGE_BYTES, &sm.full[s]);
+        if (++s == C::STAGES) s = 0;
+      }
     }
     if (!mbar_wait(&sm.uempty[us], uphase ^ 1, sm.abort_flag, p.err, p.timeout)) break;
     sm.ring[us] = info;
@@ -448,7 +477,7 @@ __device__ void run_mma(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_base) {
     if (info.task < 0) break;
     const GemmTask& T = p.task[info.task];
     if (T.kind == TASK_NORM) continue;  // no tensor-core work
-    const bool pair = is_pair(T.kind);
+    const bool pair = T.pair != 0;
     const int kpg = T.kpg;
     const bool promote = kpg > 0;
     const bool fp8 = T.fp8 != 0;
@@ -522,29 +551,33 @@ struct SigState {
   int slot = 0;
   uint32_t phase = 0;
 };
+// Epilogue group `grp` publishes one unit on its own ring; `gw` is the warp within the group.
 template <int BN>
 __device__ __forceinline__ void signal_done(const GemmParams& p, Smem<BN>& sm, SigState& sg,
-                                            int* counter, int ew, int lane) {
+                                            int* counter, int grp, int gw, int lane) {
   using C = Cfg<BN>;
+  const int slot = grp * C::SIG + sg.slot;
   if (lane == 0)  // the slot's previous request has been published
-    mbar_wait(&sm.sempty[sg.slot], sg.phase ^ 1, sm.abort_flag, p.err, p.timeout);
+    mbar_wait(&sm.sempty[slot], sg.phase ^ 1, sm.abort_flag, p.err, p.timeout);
   __syncwarp();
-  if (ew == 0 && lane == 0) sm.sptr[sg.slot] = counter;
-  if (lane == 0) mbar_arrive(&sm.sfull[sg.slot]);
+  if (gw == 0 && lane == 0) sm.sptr[slot] = counter;
+  if (lane == 0) mbar_arrive(&sm.sfull[slot]);
   if (++sg.slot == C::SIG) { sg.slot = 0; sg.phase ^= 1; }
 }
 
+// Publishes the completions of epilogue group `grp`, in its order, until its end marker.
 template <int BN>
-__device__ void run_signaller(const GemmParams& p, Smem<BN>& sm) {
+__device__ void run_signaller(const GemmParams& p, Smem<BN>& sm, int grp) {
   using C = Cfg<BN>;
   int slot = 0;
   uint32_t phase = 0;
   for (;;) {
-    if (!mbar_wait(&sm.sfull[slot], phase, sm.abort_flag, p.err, p.timeout)) return;
-    int* counter = sm.sptr[slot];
+    const int s = grp * C::SIG + slot;
+    if (!mbar_wait(&sm.sfull[s], phase, sm.abort_flag, p.err, p.timeout)) return;
+    int* counter = sm.sptr[s];
     if (counter == nullptr) return;  // end of work
     red_release_gpu_add(counter, 1);
-    mbar_arrive(&sm.sempty[slot]);
+    mbar_arrive(&sm.sempty[s]);
     if (++slot == C::SIG) { slot = 0; phase ^= 1; }
   }
 }
@@ -627,15 +660,21 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
   using C = Cfg<BN>;
   constexpr int COLS = C::COLS;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int ew = warp - 2;
+  const int ew = warp - C::FIRST_EPI_WARP;    // epilogue warp 0..7
+  const int grp = ew / C::GROUP_WARPS;        // epilogue group (takes every NGROUPS-th unit)
+  const int gw = ew - grp * C::GROUP_WARPS;   // warp within the group
+  const int gtid = gw * 32 + lane;            // thread within the group
   const int quad = warp & 3;            // TMEM lane quadrant this warp may access
-  const int half = ew >> 2;             // column group of this warp
+  const int half = gw >> 2;             // column group of this warp (groups of eight)
   const int row = quad * 32 + lane;     // output feature within the tile
   const int c0 = half * COLS;
   const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-  int us = 0, acc = 0, sc_buf = 0, steps = 0;
+  // named barriers of this group: all its threads, then one per column half
+  const int bar_grp = 1 + grp * 3;
+  int us = 0, acc = 0, steps = 0, seq = 0;
   uint32_t uphase = 0, aphase = 0;
   SigState sg;
+  float* const sb = sm.sc + grp * C::SC_FLOATS;  // this group's per-unit scale staging
   const int G_L = p.L / 128, G_I = p.I / 128;
 
   for (;;) {
@@ -645,12 +684,22 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
     if (lane == 0) mbar_arrive(&sm.uempty[us]);
     if (++us == C::US) { us = 0; uphase ^= 1; }
     if (info.task < 0) {
-      signal_done<BN>(p, sm, sg, nullptr, ew, lane);  // releases the signalling warp
+      signal_done<BN>(p, sm, sg, nullptr, grp, gw, lane);  // releases the group's signaller
       return;
     }
     const GemmTask& T = p.task[info.task];
     const int kind = T.kind;
-    const bool pair = is_pair(kind);
+    const bool pair = T.pair != 0;
+    if (C::NGROUPS > 1 && (seq++ % C::NGROUPS) != grp) {
+      // the other group's unit: step past the accumulator slots the MMA issuer fills for
+      // it (one per promotion group, one for a whole-K unit, none for a norm unit)
+      acc += kind == TASK_NORM ? 0 : (T.kpg > 0 ? (info.kb1 - info.kb0) / T.kpg : 1);
+      while (acc >= C::NACC) {
+        acc -= C::NACC;
+        aphase ^= 1;
+      }
+      continue;
+    }
 
     if (kind == TASK_NORM) {
       // RMSNorm of one token row (unit rows = 1): fp32 statistic on the fp32 combine,
@@ -677,29 +726,28 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
           return acc;
         }
       };
-      const int etid = threadIdx.x - 64;
       const int n4 = p.L / 4;
-      constexpr int PER = 8;  // float4s per thread held in registers (L <= 4096 * ... )
+      constexpr int PER = 8;  // float4s per thread held in registers
       float4 v[PER];
       float ss = 0.f;
 #pragma unroll
       for (int i = 0; i < PER; ++i) {
-        const int c = etid + i * C::EPI_THREADS;
+        const int c = gtid + i * C::GROUP_THREADS;
         v[i] = c < n4 ? row4(c) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int i = 0; i < PER; ++i) ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z +
                                          v[i].w * v[i].w;
-      for (int c = etid + PER * C::EPI_THREADS; c < n4; c += C::EPI_THREADS) {  // wide rows
+      for (int c = gtid + PER * C::GROUP_THREADS; c < n4; c += C::GROUP_THREADS) {  // wide rows
         const float4 w = row4(c);
         ss += w.x * w.x + w.y * w.y + w.z * w.z + w.w * w.w;
       }
 #pragma unroll
       for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
-      if (lane == 0) sm.red[ew] = ss;
-      named_bar_sync(1, C::EPI_THREADS);
+      if (lane == 0) sm.red[ew * COLS] = ss;  // the first entry of this warp's own row
+      named_bar_sync(bar_grp, C::GROUP_THREADS);
       float tot = 0.f;
-      for (int w = 0; w < C::EPI_WARPS; ++w) tot += sm.red[w];
+      for (int w = 0; w < C::GROUP_WARPS; ++w) tot += sm.red[(grp * C::GROUP_WARPS + w) * COLS];
       const float inv = rsqrtf(tot / static_cast<float>(p.L) + p.eps);
       const uint2* gg = reinterpret_cast<const uint2*>(p.gamma);
       uint2* nn = reinterpret_cast<uint2*>(p.nrm + t * p.L);
@@ -718,37 +766,36 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
       };
 #pragma unroll
       for (int i = 0; i < PER; ++i) {
-        const int c = etid + i * C::EPI_THREADS;
+        const int c = gtid + i * C::GROUP_THREADS;
         if (c < n4) emit(c, v[i]);
       }
-      for (int c = etid + PER * C::EPI_THREADS; c < n4; c += C::EPI_THREADS)
+      for (int c = gtid + PER * C::GROUP_THREADS; c < n4; c += C::GROUP_THREADS)
         emit(c, row4(c));
-      named_bar_sync(1, C::EPI_THREADS);  // sm.red is reused by the next unit
-      signal_done<BN>(p, sm, sg, p.norm_done + info.dep_idx, ew, lane);
+      named_bar_sync(bar_grp, C::GROUP_THREADS);  // sm.red is reused by the next unit
+      signal_done<BN>(p, sm, sg, p.norm_done + info.dep_idx, grp, gw, lane);
       continue;
     }
 
     float g[COLS], u[COLS];
 #pragma unroll
     for (int j = 0; j < COLS; ++j) { g[j] = 0.f; u[j] = 0.f; }
-    float* sb = sm.sc + sc_buf * C::SC_FLOATS;
 
     if (T.kpg > 0) {
       // Stage this unit's scales in shared memory once: token group scales [group][column]
-      // and the weight block scale(s) per 128-wide K group.  Double-buffered by unit parity;
-      // the barrier also guarantees every epilogue thread has finished the previous unit.
+      // and the weight block scale(s) per 128-wide K group.  The group's staging buffer is
+      // rewritten only after every thread of the group has finished its previous unit.
       const float* tok_scale = kind == TASK_ROUTED_L1 ? p.zsT : p.asT;
-      sc_buf ^= 1;
+      named_bar_sync(bar_grp, C::GROUP_THREADS);
       const int nkb = (info.kb1 - info.kb0) / T.kpg;  // promotion groups of this unit
       const int g0 = info.kb0 / T.kpg;
-      const int etid = threadIdx.x - 64;
-      for (int i = etid; i < nkb * BN; i += C::EPI_THREADS) {
+      const int etid = gtid;
+      for (int i = etid; i < nkb * BN; i += C::GROUP_THREADS) {
         const int kbi = i / BN, j = i - kbi * BN;
         sb[i] = j < info.rows
                     ? __ldcg(tok_scale + static_cast<size_t>(g0 + kbi) * p.cap + info.row0 + j)
                     : 0.f;
       }
-      for (int kbi = etid; kbi < nkb; kbi += C::EPI_THREADS) {
+      for (int kbi = etid; kbi < nkb; kbi += C::GROUP_THREADS) {
         const int kb = g0 + kbi;
         float a, b = 0.f;
         if (kind == TASK_ROUTED_L1) {
@@ -756,20 +803,23 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
           a = __ldg(p.w13_s + (rb + info.ftile) * G_L + kb);
           b = __ldg(p.w13_s + (rb + G_I + info.ftile) * G_L + kb);
         } else {
-          a = __ldg(p.w2_s + (static_cast<size_t>(info.e) * G_L + info.ftile) * G_I + kb);
+          // one 128-row block, or two consecutive ones (paired units)
+          const size_t rb = static_cast<size_t>(info.e) * G_L + info.ftile * T.a_rb_step;
+          a = __ldg(p.w2_s + rb * G_I + kb);
+          if (pair) b = __ldg(p.w2_s + (rb + 1) * G_I + kb);
         }
         sb[MAX_KB * BN + 2 * kbi] = a;
         sb[MAX_KB * BN + 2 * kbi + 1] = b;
       }
       if (kind == TASK_ROUTED_L2) {  // combine targets of each column
-        for (int j = etid; j < BN; j += C::EPI_THREADS) {
+        for (int j = etid; j < BN; j += C::GROUP_THREADS) {
           const int pp = info.row0 + j;
           sb[MAX_KB * BN + 2 * MAX_KB + j] =
               __int_as_float(j < info.rows ? __ldg(p.gidx + pp) : 0);
           sb[MAX_KB * BN + 2 * MAX_KB + BN + j] = j < info.rows ? __ldg(p.wperm + pp) : 0.f;
         }
       }
-      named_bar_sync(1, C::EPI_THREADS);
+      named_bar_sync(bar_grp, C::GROUP_THREADS);
       // Promote completed groups in batches: wait for up to NB slots, load them under one
       // TMEM wait, then scale-and-add, so the per-group latency chain is paid once per batch.
       for (int kbi = 0; kbi < nkb;) {
@@ -810,7 +860,8 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
       const size_t tile_floats = static_cast<size_t>(parts) * BN * 128;
       const size_t own =
           T.streamk ? static_cast<size_t>(info.wslot)
-                    : static_cast<size_t>(info.tile_id - T.ws_tile_base) * T.ksplit + info.split;
+                    : static_cast<size_t>(info.tile_id - T.ws_tile_base) * info.ncontrib +
+                          info.split;
       float* mine = p.ws + T.ws_off + own * tile_floats;
 #pragma unroll
       for (int j = 0; j < COLS; ++j) {
@@ -818,15 +869,15 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
         if (pair) __stcg(mine + static_cast<size_t>(BN + c0 + j) * 128 + row, u[j]);
       }
       __threadfence();
-      named_bar_sync(1, C::EPI_THREADS);
-      if (ew == 0 && lane == 0) {
+      named_bar_sync(bar_grp, C::GROUP_THREADS);
+      if (gw == 0 && lane == 0) {
         const int old = atomicAdd(p.cnt + info.tile_id, 1);
         const int last = old == info.ncontrib - 1;
         if (last) p.cnt[info.tile_id] = 0;
-        *sm.last_flag = last;
+        sm.last_flag[grp] = last;
       }
-      named_bar_sync(1, C::EPI_THREADS);
-      if (!*sm.last_flag) continue;
+      named_bar_sync(bar_grp, C::GROUP_THREADS);
+      if (!sm.last_flag[grp]) continue;
       __threadfence();
 #pragma unroll
       for (int j = 0; j < COLS; ++j) { g[j] = 0.f; u[j] = 0.f; }
@@ -835,7 +886,7 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
             T.streamk ? static_cast<size_t>(sk_slot(T.sk_total, T.sk_grid, T.kb_total,
                                                     info.cfirst + s,
                                                     info.tile_id - T.ws_tile_base))
-                      : static_cast<size_t>(info.tile_id - T.ws_tile_base) * T.ksplit + s;
+                      : static_cast<size_t>(info.tile_id - T.ws_tile_base) * info.ncontrib + s;
         const float* ps = p.ws + T.ws_off + idx * tile_floats;
 #pragma unroll
         for (int j = 0; j < COLS; ++j) {
@@ -854,7 +905,8 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
           dst[static_cast<size_t>(info.row0 + c0 + j) * p.Is] =
               __float2bfloat16_rn(silu_fast(g[j]) * u[j]);
       }
-      if (p.sh_done != nullptr) signal_done<BN>(p, sm, sg, p.sh_done + info.dep_idx, ew, lane);
+      if (p.sh_done != nullptr)
+        signal_done<BN>(p, sm, sg, p.sh_done + info.dep_idx, grp, gw, lane);
     } else if (kind == TASK_OUT) {
       __nv_bfloat16* dst = p.out + static_cast<size_t>(info.ftile) * 128 + row;
 #pragma unroll
@@ -863,19 +915,25 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
           dst[static_cast<size_t>(info.row0 + c0 + j) * p.H] = __float2bfloat16_rn(g[j]);
       }
     } else if (kind == TASK_ROUTED_L2) {
-      const int col = info.ftile * 128 + row;
+      // g: the unit's first 128 output rows; u: the next 128 (paired units)
+      const int col = info.ftile * 128 * T.a_rb_step + row;
 #pragma unroll
       for (int j = 0; j < COLS; ++j) {
         if (c0 + j < info.rows) {
           const int tok = __float_as_int(sb[MAX_KB * BN + 2 * MAX_KB + c0 + j]);
           const float wv = sb[MAX_KB * BN + 2 * MAX_KB + BN + c0 + j];
-          if constexpr (DET)  // this pair's weighted output, summed later in choice order
-            p.yw[static_cast<size_t>(info.row0 + c0 + j) * p.L + col] = wv * g[j];
-          else
-            atomicAdd(p.r + static_cast<size_t>(tok) * p.L + col, wv * g[j]);
+          if constexpr (DET) {  // this pair's weighted output, summed later in choice order
+            float* y = p.yw + static_cast<size_t>(info.row0 + c0 + j) * p.L + col;
+            y[0] = wv * g[j];
+            if (pair) y[128] = wv * u[j];
+          } else {
+            float* y = p.r + static_cast<size_t>(tok) * p.L + col;
+            atomicAdd(y, wv * g[j]);
+            if (pair) atomicAdd(y + 128, wv * u[j]);
+          }
         }
       }
-      if (p.l2_done != nullptr) signal_done<BN>(p, sm, sg, p.l2_done, ew, lane);
+      if (p.l2_done != nullptr) signal_done<BN>(p, sm, sg, p.l2_done, grp, gw, lane);
     } else {  // TASK_ROUTED_L1: SwiGLU, then e4m3 per 128 features of each token
       float* red = sm.red + ew * COLS;
 #pragma unroll
@@ -886,8 +944,8 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
         for (int o = 16; o; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
         if (lane == 0) red[j] = a;
       }
-      named_bar_sync(2 + half, 128);
-      const float* r0 = sm.red + (half * 4) * COLS;
+      named_bar_sync(bar_grp + 1 + half, 128);
+      const float* r0 = sm.red + (grp * C::GROUP_WARPS + half * 4) * COLS;
       uint8_t* dst = p.aq + static_cast<size_t>(info.ftile) * 128 + row;
 #pragma unroll
       for (int j = 0; j < COLS; ++j) {
@@ -906,8 +964,9 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
           if (quad == 0 && lane == 0) p.asT[static_cast<size_t>(info.ftile) * p.cap + pp] = s;
         }
       }
-      named_bar_sync(2 + half, 128);
-      if (p.l1_done != nullptr) signal_done<BN>(p, sm, sg, p.l1_done + info.dep_idx, ew, lane);
+      named_bar_sync(bar_grp + 1 + half, 128);
+      if (p.l1_done != nullptr)
+        signal_done<BN>(p, sm, sg, p.l1_done + info.dep_idx, grp, gw, lane);
     }
   }
 }
@@ -927,14 +986,14 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
     }
     for (int a = 0; a < C::NACC; ++a) {
       mbar_init(&sm.tfull[a], 1);
-      mbar_init(&sm.tempty[a], C::EPI_WARPS);
+      mbar_init(&sm.tempty[a], C::GROUP_WARPS);  // the warps of the group that owns the unit
     }
     for (int u = 0; u < C::US; ++u) {
       mbar_init(&sm.ufull[u], 1);
       mbar_init(&sm.uempty[u], 1 + C::EPI_WARPS);
     }
-    for (int g = 0; g < C::SIG; ++g) {
-      mbar_init(&sm.sfull[g], C::EPI_WARPS);
+    for (int g = 0; g < Smem<BN>::NSIG; ++g) {
+      mbar_init(&sm.sfull[g], C::GROUP_WARPS);
       mbar_init(&sm.sempty[g], 1);
     }
     mbar_init(sm.drain, 1);
@@ -956,25 +1015,32 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *sm.tmem_holder;
 
-  // Everything above touches only this CTA's resources; inputs written by the previous
-  // kernel in the stream are read only after this point.
+  // Everything above touches only this CTA's resources, and the L2 prefetch below only
+  // handle-owned weights that no kernel writes; inputs written by the previous kernels in
+  // the stream are read only after the wait.  The routing kernels let this launch start
+  // while they run, so the prefetch of routing-independent weights overlaps them.
+  if (warp == 0 && lane == 0) prefetch_share_l2(p);
   pdl_wait();
   pdl_trigger();
 
-  if (warp == 0) {
-    // routing tile offsets for the producer's unit decode, read once per CTA
-    __shared__ int s_tile_off[MAX_E + 1], s_off[MAX_E + 1];
-    for (int i = lane; i <= p.E; i += 32) {
-      s_tile_off[i] = p.tile_off[i];
-      s_off[i] = p.off[i];
+  if (warp < C::FIRST_EPI_WARP) {
+    regs_dec<C::REGS_CTRL>();
+    if (warp == 0) {
+      // routing tile offsets for the producer's unit decode, read once per CTA
+      __shared__ int s_tile_off[MAX_E + 1], s_off[MAX_E + 1];
+      for (int i = lane; i <= p.E; i += 32) {
+        s_tile_off[i] = p.tile_off[i];
+        s_off[i] = p.off[i];
+      }
+      __syncwarp();
+      if (lane == 0) run_producer<BN>(p, sm, s_tile_off, s_off);
+    } else if (warp == 1) {
+      if (lane == 0) run_mma<BN>(p, sm, tmem_base);
+    } else if (warp - C::SIGNAL_WARP < C::NGROUPS && lane == 0) {
+      run_signaller<BN>(p, sm, warp - C::SIGNAL_WARP);
     }
-    __syncwarp();
-    if (lane == 0) run_producer<BN>(p, sm, s_tile_off, s_off);
-  } else if (warp == 1) {
-    if (lane == 0) run_mma<BN>(p, sm, tmem_base);
-  } else if (warp == C::SIGNAL_WARP) {
-    if (lane == 0) run_signaller<BN>(p, sm);
   } else {
+    regs_inc<C::REGS_EPI>();
     run_epilogue<BN, DET>(p, sm, tmem_base);
   }
 
@@ -1017,6 +1083,25 @@ static_assert(Smem<16>::bytes() + 2 * (MAX_E + 1) * 4 <= 227 * 1024, "shared mem
 static_assert(Smem<32>::bytes() + 2 * (MAX_E + 1) * 4 <= 227 * 1024, "shared memory budget");
 static_assert(Smem<64>::bytes() + 2 * (MAX_E + 1) * 4 <= 227 * 1024, "shared memory budget");
 static_assert(Smem<128>::bytes() + 2 * (MAX_E + 1) * 4 <= 227 * 1024, "shared memory budget");
+
+// Every instantiation must launch with the register count its hand-over was planned for.
+bool gemm_regs_ok() {
+  const void* k[] = {
+      reinterpret_cast<const void*>(gemm_kernel<16, false>),
+      reinterpret_cast<const void*>(gemm_kernel<16, true>),
+      reinterpret_cast<const void*>(gemm_kernel<32, false>),
+      reinterpret_cast<const void*>(gemm_kernel<32, true>),
+      reinterpret_cast<const void*>(gemm_kernel<64, false>),
+      reinterpret_cast<const void*>(gemm_kernel<64, true>),
+      reinterpret_cast<const void*>(gemm_kernel<128, false>),
+      reinterpret_cast<const void*>(gemm_kernel<128, true>)};
+  for (const void* f : k) {
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, f) != cudaSuccess || a.numRegs != Cfg<16>::LAUNCH_REGS)
+      return false;
+  }
+  return true;
+}
 
 int gemm_smem_bytes(int bn) {
   switch (bn) {

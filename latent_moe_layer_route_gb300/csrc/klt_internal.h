@@ -69,7 +69,11 @@ enum DepKind : int {
   DEP_NONE = 0,
   DEP_L1_TILE = 1,   // routed L2 unit: all L1 units of its routed token tile are done
   DEP_ALL_L2 = 2,    // norm unit: every routed L2 unit is done
-  DEP_OUT_TILE = 3   // output unit: norm and shared L1 of its token tile are done
+  DEP_OUT_TILE = 3,  // output unit: norm and shared L1 of its token tile are done
+  DEP_SH_TILE = 4,   // output unit over the shared down-projection's k-blocks only: the
+                     // shared L1 tiles of its token tile are done
+  DEP_NORM_TILE = 5  // output unit over the up-projection's k-blocks only: the norm rows
+                     // of its token tile are done
 };
 
 struct GemmTask {
@@ -81,11 +85,19 @@ struct GemmTask {
   int kpg;             // k-blocks per promotion group (0: accumulate the unit in TMEM)
   int routed;          // units come from the device tile list (tile_off/off)
   int ftiles;          // 128-row output tiles (gate/up pairs for L1 kinds)
-  int kb_total;        // k-blocks of 128 bytes per row
+  int kb_total;        // k-blocks of 128 bytes per row (end of this task's k range)
   int kb_split0;       // k-blocks served by map pair 0
-  int ksplit;          // k splits (non-routed only); >1 => partials + last-arriver reduce
+  int kb_lo;           // first k-block of this task's k range (0 unless a tile's K range
+                       // is shared out between two tasks)
+  int ksplit;          // k splits of [kb_lo, kb_total); >1 => partials + last-arriver reduce
   int kb_per_split;
-  int a_rb_up;         // 128-row blocks from a gate tile to its up tile (pair kinds)
+  int split_base;      // index of this task's first split among its tile's contributions
+  int ncontrib;        // contributions per tile over all tasks sharing it (0: ksplit)
+  int pair;            // feature-major engine: each unit reads two 128-row weight tiles per
+                       // k-block into one accumulator slot of 2 x BN columns (gate and up
+                       // of the L1 kinds, or two consecutive row blocks of W2)
+  int a_rb_up;         // 128-row blocks from a unit's first weight tile to its second (pairs)
+  int a_rb_step;       // 128-row blocks per output tile index (2 for paired W2 units, else 1)
   int a_rb_expert;     // routed: 128-row blocks per expert
   int a_kb[2];         // k-blocks per 128-row block of a_ptr[0], a_ptr[1]
   int ntiles;          // non-routed: token tiles
@@ -101,8 +113,10 @@ struct GemmTask {
   long long sk_total;
 };
 
+constexpr int kMaxTasks = 6;
+
 struct GemmParams {
-  GemmTask task[5];
+  GemmTask task[kMaxTasks];
   int ntasks;
   int M;                       // tokens of this forward
   int E, L, I, Is, H, cap;     // cap = max_tokens * topk (rows of the permuted buffers)
@@ -143,6 +157,10 @@ struct GemmParams {
   float eps;
   int w_stages;                // token-major engine: stage ring depth (4 x 48 KB or 3 x 64 KB)
   int w_stage_bytes;           //   and stage size (64 KB when units carry two token tiles)
+  // routing-independent weights prefetched into L2 before the launch waits for the
+  // preceding kernel (16-byte aligned, a multiple of 16 bytes; null/0: none)
+  const uint8_t* pf_ptr;
+  long long pf_bytes;
   long long* trace;            // optional timestamp trace (this launch's region)
   int trace_n;                 // entries per (CTA, role)
 };
@@ -170,6 +188,9 @@ cudaError_t launch_tile_relayout(const void* src, void* dst, long long rows, lon
 // bn in {16, 128}; grid = persistent CTAs.
 cudaError_t launch_gemm(const GemmParams& p, int bn, int grid, cudaStream_t s, bool pdl);
 int gemm_smem_bytes(int bn);
+// The feature-major engine hands registers from its control warps to its epilogue warps at
+// run time: every instantiation must launch with the register count that was planned.
+bool gemm_regs_ok();
 // Token-major engine (128-token x 256-feature units, one persistent launch of the five
 // fused tasks with 128-token tiles).  Its epilogue warps take registers from the control
 // warps at run time, which needs the kernel to launch with exactly the register count it

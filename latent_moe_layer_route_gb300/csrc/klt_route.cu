@@ -27,8 +27,8 @@ __device__ __forceinline__ uint32_t ordered_key(float v) {
 // its 128-column group g of z and zeroes the matching 128 floats of the combine buffer.
 __global__ void __launch_bounds__(32 * ROUTE_WARPS)
     route_quant_kernel(const RouteParams p) {
+  pdl_trigger();  // dependents may launch now; they wait for this grid before reading
   pdl_wait();
-  pdl_trigger();
   const int lane = lane_id();
   if (blockIdx.x == 0 && threadIdx.x < p.nsched) p.sched[threadIdx.x] = 0;
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -115,8 +115,8 @@ __global__ void __launch_bounds__(32 * ROUTE_WARPS)
 
 __global__ void __launch_bounds__(PERM_BLOCK) perm_hist_kernel(const PermParams p) {
   __shared__ int hist[MAX_E];
+  pdl_trigger();  // dependents may launch now; they wait for this grid before reading
   pdl_wait();
-  pdl_trigger();
   for (int e = threadIdx.x; e < p.E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
   const int i = blockIdx.x * PERM_BLOCK + threadIdx.x;
@@ -131,8 +131,8 @@ __global__ void __launch_bounds__(PERM_BLOCK) perm_scatter_kernel(const PermPara
   __shared__ int base[MAX_E];
   __shared__ int total[MAX_E];
   __shared__ int tiles[MAX_E];
+  pdl_trigger();  // dependents may launch now; they wait for this grid before reading
   pdl_wait();
-  pdl_trigger();
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int Mk = p.M * p.k;
   for (int c = tid; c < (PERM_BLOCK / 32) * MAX_E; c += PERM_BLOCK)
@@ -211,8 +211,8 @@ __global__ void __launch_bounds__(PERM_BLOCK) perm_scatter_kernel(const PermPara
 // into pair order, so the routed L1 GEMM streams an expert's token rows as plain tiles.
 // One thread per 16-byte chunk.
 __global__ void __launch_bounds__(256) perm_gather_kernel(const PermParams p) {
+  pdl_trigger();  // dependents may launch now; they wait for this grid before reading
   pdl_wait();
-  pdl_trigger();
   const int G = p.L / 128;
   const int row16 = p.L / 16;
   const long long Mk = static_cast<long long>(p.M) * p.k;
@@ -249,8 +249,8 @@ __global__ void __launch_bounds__(256) perm_gather_kernel(const PermParams p) {
 
 __global__ void __launch_bounds__(128) norm_kernel(const NormParams p) {
   __shared__ float red[4];
+  pdl_trigger();  // dependents may launch now; they wait for this grid before reading
   pdl_wait();
-  pdl_trigger();
   const int t = blockIdx.x;
   const float4* rr = reinterpret_cast<const float4*>(p.r + static_cast<size_t>(t) * p.L);
   float ss = 0.f;

@@ -820,8 +820,10 @@ __global__ void __launch_bounds__(W::THREADS, 1) wide_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem_base = *sm.tmem_holder;
 
-  // Everything above touches only this CTA's resources; inputs written by the previous
-  // kernel in the stream are read only after this point.
+  // Everything above touches only this CTA's resources, and the L2 prefetch below only
+  // handle-owned weights that no kernel writes; inputs written by the previous kernels in
+  // the stream are read only after the wait.
+  if (warp == 0 && lane == 0) prefetch_share_l2(p);
   pdl_wait();
   pdl_trigger();
 
