@@ -704,11 +704,20 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
       // and run while the routed experts stream, while the W_up k-blocks wait for the norm.
       // Both tasks add partials into the same tiles (one fixed-order reduce).
       {
-        const GemmTask& O = g3.task[0];
+        GemmTask O = g3.task[0];
+        // 256 output features per unit (two 128-row tiles per k-block, one 2 x BN slot)
+        if ((H / 128) % 2 == 0) {
+          O.pair = 1;
+          O.a_rb_up = 1;
+          O.a_rb_step = 2;
+          O.ftiles = H / 256;
+        }
         const int kb_up = L / 64, kb_sh = Is / 64;
         const int tiles = O.ntiles * O.ftiles;
-        const int want = std::max(1, (2 * grid + tiles - 1) / tiles);  // contributions
-        const int kps = std::max(4, (kb_up + kb_sh + want - 1) / want);
+        // The W_up units run after the norm, on the critical path: at most one per SM (a
+        // second wave would double the tail).  The Ws2 units take splits of the same size.
+        const int ks_want = std::max(1, grid / tiles);
+        const int kps = std::max(4, (kb_up + ks_want - 1) / ks_want);
         const int ks_up = (kb_up + kps - 1) / kps, ks_sh = (kb_sh + kps - 1) / kps;
         if (tiles * (ks_up + ks_sh) <= kMaxSplitUnits) {
           GemmTask up = O, sh = O;

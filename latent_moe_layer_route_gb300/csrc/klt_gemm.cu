@@ -224,7 +224,7 @@ __device__ UnitInfo decode_unit(const GemmParams& p, const int* s_tile_off, cons
         info.row0 = nt * BN;
         info.rows = min(BN, p.M - info.row0);
         info.ftile = ft;
-        info.arb = ft;
+        info.arb = ft * (T.a_rb_step > 0 ? T.a_rb_step : 1);
         info.kb0 = T.kb_lo + sp * T.kb_per_split;
         info.kb1 = min(T.kb_total, info.kb0 + T.kb_per_split);
         info.tile_id = T.ws_tile_base + nt * T.ftiles + ft;
@@ -728,12 +728,15 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
       };
       const int n4 = p.L / 4;
       constexpr int PER = 8;  // float4s per thread held in registers
+      const uint2* gg = reinterpret_cast<const uint2*>(p.gamma);
       float4 v[PER];
+      uint2 gv[PER];  // gamma, loaded together with the row
       float ss = 0.f;
 #pragma unroll
       for (int i = 0; i < PER; ++i) {
         const int c = gtid + i * C::GROUP_THREADS;
         v[i] = c < n4 ? row4(c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        gv[i] = c < n4 ? __ldg(gg + c) : make_uint2(0u, 0u);
       }
 #pragma unroll
       for (int i = 0; i < PER; ++i) ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z +
@@ -749,10 +752,8 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
       float tot = 0.f;
       for (int w = 0; w < C::GROUP_WARPS; ++w) tot += sm.red[(grp * C::GROUP_WARPS + w) * COLS];
       const float inv = rsqrtf(tot / static_cast<float>(p.L) + p.eps);
-      const uint2* gg = reinterpret_cast<const uint2*>(p.gamma);
       uint2* nn = reinterpret_cast<uint2*>(p.nrm + t * p.L);
-      auto emit = [&](int c, const float4& x) {
-        const uint2 graw = __ldg(gg + c);
+      auto emit = [&](int c, const float4& x, const uint2 graw) {
         const __nv_bfloat162 g01 = *reinterpret_cast<const __nv_bfloat162*>(&graw.x);
         const __nv_bfloat162 g23 = *reinterpret_cast<const __nv_bfloat162*>(&graw.y);
         const __nv_bfloat162 o01 = __floats2bfloat162_rn(x.x * inv * __low2float(g01),
@@ -767,10 +768,10 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
 #pragma unroll
       for (int i = 0; i < PER; ++i) {
         const int c = gtid + i * C::GROUP_THREADS;
-        if (c < n4) emit(c, v[i]);
+        if (c < n4) emit(c, v[i], gv[i]);
       }
       for (int c = gtid + PER * C::GROUP_THREADS; c < n4; c += C::GROUP_THREADS)
-        emit(c, row4(c));
+        emit(c, row4(c), __ldg(gg + c));
       named_bar_sync(bar_grp, C::GROUP_THREADS);  // sm.red is reused by the next unit
       signal_done<BN>(p, sm, sg, p.norm_done + info.dep_idx, grp, gw, lane);
       continue;
@@ -908,11 +909,15 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
       if (p.sh_done != nullptr)
         signal_done<BN>(p, sm, sg, p.sh_done + info.dep_idx, grp, gw, lane);
     } else if (kind == TASK_OUT) {
-      __nv_bfloat16* dst = p.out + static_cast<size_t>(info.ftile) * 128 + row;
+      // g: the unit's first 128 output features; u: the next 128 (paired units)
+      __nv_bfloat16* dst = p.out + static_cast<size_t>(info.arb) * 128 + row;
 #pragma unroll
       for (int j = 0; j < COLS; ++j) {
-        if (c0 + j < info.rows)
-          dst[static_cast<size_t>(info.row0 + c0 + j) * p.H] = __float2bfloat16_rn(g[j]);
+        if (c0 + j < info.rows) {
+          __nv_bfloat16* o = dst + static_cast<size_t>(info.row0 + c0 + j) * p.H;
+          o[0] = __float2bfloat16_rn(g[j]);
+          if (pair) o[128] = __float2bfloat16_rn(u[j]);
+        }
       }
     } else if (kind == TASK_ROUTED_L2) {
       // g: the unit's first 128 output rows; u: the next 128 (paired units)
