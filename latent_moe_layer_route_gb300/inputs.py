@@ -28,8 +28,8 @@ import torch
 
 from .configs import FMT_FP8, FMT_NVFP4, TailConfig
 
-__all__ = ["make_activations", "make_weights", "make_inputs", "fp8_block_quantize",
-           "nvfp4_quantize", "expert_load"]
+__all__ = ["make_activations", "make_weights", "make_inputs", "make_projection_weights",
+           "fp8_block_quantize", "nvfp4_quantize", "expert_load"]
 
 
 def _rng(seed: int, stream: int) -> np.random.Generator:
@@ -150,6 +150,16 @@ def make_weights(cfg: TailConfig) -> Dict[str, torch.Tensor]:
     w["ws2"] = _normal(rng, (H, Is), 1 / math.sqrt(Is)).to(torch.bfloat16)
     w["w_up"] = _normal(rng, (H, L), 1 / math.sqrt(L)).to(torch.bfloat16)
     return w
+
+
+def make_projection_weights(cfg: TailConfig) -> Dict[str, torch.Tensor]:
+    """Weights of the step before the tail (hidden state -> latent input and router
+    logits), drawn from their own stream ``default_rng([seed, 2])`` so that the tail's own
+    draws are unchanged: w_lat [L, H] and w_gate [E, H], both ~ N(0, 1/H) stored as bf16."""
+    rng = _rng(cfg.seed, 2)
+    w_lat = _normal(rng, (cfg.L, cfg.H), 1 / math.sqrt(cfg.H)).to(torch.bfloat16)
+    w_gate = _normal(rng, (cfg.E, cfg.H), 1 / math.sqrt(cfg.H)).to(torch.bfloat16)
+    return {"w_lat": w_lat, "w_gate": w_gate}
 
 
 def make_inputs(cfg: TailConfig, M: Optional[int] = None):

@@ -35,7 +35,8 @@ import numpy as np
 from .codecs import e2m1_decode, e4m3_decode, e4m3_encode, unpack_e2m1
 
 __all__ = ["route", "permutation", "quant_per128", "silu", "dequant_fp8_blocks",
-           "dequant_nvfp4", "rmsnorm", "swiglu_mlp", "tail", "to_f64"]
+           "dequant_nvfp4", "rmsnorm", "swiglu_mlp", "tail", "to_f64", "latent_inputs",
+           "bf16_round"]
 
 
 def to_f64(t) -> np.ndarray:
@@ -55,6 +56,27 @@ def _rows_f64(t, rows) -> np.ndarray:
 
 def _np(t) -> np.ndarray:
     return t.detach().numpy() if hasattr(t, "detach") else np.asarray(t)
+
+
+# ---------------------------------------------------------------- step 0: inputs from x
+
+def bf16_round(v) -> np.ndarray:
+    """float64 -> nearest bfloat16 value (ties to even), returned as float64."""
+    import torch
+    return torch.from_numpy(np.asarray(v, dtype=np.float64)).to(torch.bfloat16).to(
+        torch.float64).numpy()
+
+
+def latent_inputs(x, w_lat, w_gate):
+    """The step before the tail (tokenspeed PR 1062, commit notes: the model's latent input
+    projections feed the latent MoE).  Reading: both come from the hidden state x; the
+    latent input is z = x W_lat^T (H -> L), stored as bf16 (the tail's z is a bf16 tensor),
+    and the router logits are x W_gate^T kept in full precision.  Returns (z as float64
+    holding bf16 values [M, L], logits float64 [M, E])."""
+    xv = to_f64(x)
+    z = bf16_round(xv @ to_f64(w_lat).T)
+    logits = xv @ to_f64(w_gate).T
+    return z, logits
 
 
 # ---------------------------------------------------------------- step 1: route

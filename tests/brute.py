@@ -103,3 +103,24 @@ def tail_token(logits, z, x, k, experts, gamma, eps, ws13, ws2, w_up):
     a_s = [silu(hs[i]) * hs[inter_s + i] for i in range(inter_s)]
     s_out = matvec(ws2, a_s)
     return [up[i] + s_out[i] for i in range(len(up))], order, wts
+
+
+def bf16_value(v: float) -> float:
+    """Nearest bfloat16 value (8 significant bits), ties to an even significand, derived
+    from the significand/exponent split of the float64 value."""
+    if v == 0.0 or math.isinf(v) or math.isnan(v):
+        return v
+    m, e = math.frexp(v)            # v = m * 2**e, 0.5 <= |m| < 1
+    q = m * 256.0                   # significand with 8 bits before the point
+    r = math.floor(q)
+    frac = q - r
+    if frac > 0.5 or (frac == 0.5 and r % 2 == 1):
+        r += 1
+    return math.ldexp(r, e - 8)
+
+
+def latent_inputs_token(x, w_lat, w_gate):
+    """Latent input z (bf16 values) and router logits of one token by explicit loops."""
+    z = [bf16_value(sum(wr[i] * x[i] for i in range(len(x)))) for wr in w_lat]
+    logits = [sum(wr[i] * x[i] for i in range(len(x))) for wr in w_gate]
+    return z, logits

@@ -274,3 +274,54 @@ def test_tail_matches_scalar_brute_force(kw):
         assert o["ids"][t].tolist() == order
         np.testing.assert_allclose(o["w"][t], wts, rtol=1e-13)
         np.testing.assert_allclose(o["out"][t], ref, rtol=1e-9, atol=1e-9)
+
+
+# ---------------------------------------------------------------- the step before the tail
+
+def test_bf16_round_matches_significand_rule_and_ties_to_even():
+    rng = np.random.default_rng(7)
+    v = np.concatenate([rng.standard_normal(2000) * 10.0 ** rng.integers(-8, 8, 2000),
+                        [0.0, -0.0, 1.0, -3.5, 1e-30]])
+    got = T.bf16_round(v)
+    want = np.array([brute.bf16_value(float(a)) for a in v])
+    np.testing.assert_array_equal(got, want)
+    # exact halfway points between neighbouring bf16 values go to the even significand
+    for b in [1.0, 1.0078125, 3.0, -5.0, 0.15625, 255.0]:  # bf16-representable
+        ulp = 2.0 ** (np.floor(np.log2(abs(b))) - 7)
+        h = b + np.sign(b) * ulp / 2  # halfway to the next bf16 value away from zero
+        r = T.bf16_round(np.array([h]))[0]
+        assert r in (b, b + np.sign(b) * ulp), (b, r)
+        sig = abs(r) / 2.0 ** np.floor(np.log2(abs(r))) * 128  # 8-bit significand
+        assert float(sig).is_integer() and int(sig) % 2 == 0, (b, r)
+
+
+def test_latent_inputs_match_scalar_brute_force():
+    rng = np.random.default_rng(8)
+    H, L, E, M = 64, 32, 8, 3
+    x = torch.from_numpy(rng.standard_normal((M, H)).astype(np.float32)).to(torch.bfloat16)
+    w_lat = torch.from_numpy((rng.standard_normal((L, H)) / 8).astype(np.float32)).to(
+        torch.bfloat16)
+    w_gate = torch.from_numpy((rng.standard_normal((E, H)) / 8).astype(np.float32)).to(
+        torch.bfloat16)
+    z, lg = T.latent_inputs(x, w_lat, w_gate)
+    xs, wl, wg = (t.to(torch.float64).tolist() for t in (x, w_lat, w_gate))
+    for t in range(M):
+        zb, lb = brute.latent_inputs_token(xs[t], wl, wg)
+        np.testing.assert_array_equal(z[t], np.array(zb))
+        np.testing.assert_allclose(lg[t], np.array(lb), rtol=1e-13, atol=1e-13)
+
+
+def test_latent_inputs_zero_and_linear_in_x():
+    rng = np.random.default_rng(9)
+    H, L, E = 32, 16, 4
+    w_lat = rng.standard_normal((L, H))
+    w_gate = rng.standard_normal((E, H))
+    z0, l0 = T.latent_inputs(np.zeros((2, H)), w_lat, w_gate)
+    assert not z0.any() and not l0.any()
+    x = rng.standard_normal((3, H))
+    _, l1 = T.latent_inputs(x, w_lat, w_gate)
+    _, l2 = T.latent_inputs(4.0 * x, w_lat, w_gate)
+    np.testing.assert_allclose(l2, 4.0 * l1, rtol=1e-12)
+    z1, _ = T.latent_inputs(x, w_lat, w_gate)
+    z2, _ = T.latent_inputs(4.0 * x, w_lat, w_gate)  # power-of-two scaling commutes with bf16
+    np.testing.assert_array_equal(z2, 4.0 * z1)
