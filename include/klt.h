@@ -108,6 +108,11 @@ typedef struct klt_weights {
   const void* ws2;
   const void* w_up;
   const void* gamma;
+  /* Optional: the step before the tail (both or neither; NULL = klt_forward_hidden is not
+   * available on the handle).  w_lat bf16 [L, H] maps the hidden state to the latent
+   * input; w_gate bf16 [E, H] gives the router logits. */
+  const void* w_lat;
+  const void* w_gate;
 } klt_weights;
 
 /* Optional routing outputs of klt_forward (every pointer may be NULL; device memory,
@@ -167,6 +172,10 @@ typedef struct klt_debug {
   int64_t* trace;
   int32_t trace_entries;
   int32_t force_bn;
+  /* klt_forward_hidden only: the latent input bf16 [M, L] and router logits f32 [M, E]
+   * it computed from the hidden state */
+  void* z;
+  float* logits;
 } klt_debug;
 
 typedef struct klt_handle klt_handle;
@@ -201,6 +210,20 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
  * reported later by klt_status. */
 int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits, int32_t M,
                 void* out, klt_routing* routing_out, klt_debug* dbg, void* stream);
+
+/* Run the step before the tail and then the tail for M tokens, from the hidden state alone,
+ * asynchronously on `stream`.
+ * Defined by: tokenspeed PR 1062 "MNNVL CuTe-DSL finalize tail", commit notes (the model's
+ * latent input projections feeding the latent MoE).  Computes, on the GPU,
+ *   z      = bf16( x W_lat^T )     bf16 [M, L]  (fp32 accumulation, one rounding)
+ *   logits = x W_gate^T            f32  [M, E]
+ * into the handle's workspace and then runs exactly what klt_forward runs on them.
+ *   x   device bf16 [M, H];  out device bf16 [M, H].
+ * Launches one kernel more than klt_forward (the projection, first).  The handle must have
+ * been created with w_lat and w_gate.  Errors: as klt_forward, and KLT_ERR_UNSUPPORTED
+ * when the handle has no projection weights. */
+int klt_forward_hidden(klt_handle* h, const void* x, int32_t M, void* out,
+                       klt_routing* routing_out, klt_debug* dbg, void* stream);
 
 /* Sticky device status of the handle: KLT_OK or KLT_ERR_DEVICE_TIMEOUT.  Reads device
  * memory synchronously, so call it after the forward's stream has been synchronised.  A

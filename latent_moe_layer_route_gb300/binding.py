@@ -27,8 +27,8 @@ KLT_FLAG_NO_PDL = 1
 KLT_FLAG_PHASED = 2
 KLT_FLAG_DETERMINISTIC = 4
 
-EXPORTS = ("klt_create", "klt_forward", "klt_status", "klt_destroy", "klt_strerror",
-           "klt_launch_count", "klt_gemm_tile", "klt_route_noalloc")
+EXPORTS = ("klt_create", "klt_forward", "klt_forward_hidden", "klt_status", "klt_destroy",
+           "klt_strerror", "klt_launch_count", "klt_gemm_tile", "klt_route_noalloc")
 
 
 class KltDims(ctypes.Structure):
@@ -41,7 +41,7 @@ class KltDims(ctypes.Structure):
 class KltWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "w13", "w13_scale", "w13_global", "w2", "w2_scale", "w2_global", "ws13", "ws2",
-        "w_up", "gamma")]
+        "w_up", "gamma", "w_lat", "w_gate")]
 
 
 class KltRouting(ctypes.Structure):
@@ -55,7 +55,8 @@ class KltDebug(ctypes.Structure):
                 ("a_s", ctypes.c_void_p), ("events", ctypes.c_void_p * 8),
                 ("stall_after_kblocks", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
                 ("trace", ctypes.c_void_p), ("trace_entries", ctypes.c_int32),
-                ("force_bn", ctypes.c_int32)]
+                ("force_bn", ctypes.c_int32), ("z", ctypes.c_void_p),
+                ("logits", ctypes.c_void_p)]
 
 
 _LIB: Optional[ctypes.CDLL] = None
@@ -84,6 +85,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                 ctypes.POINTER(KltRouting), ctypes.POINTER(KltDebug),
                                 ctypes.c_void_p]
     lib.klt_forward.restype = ctypes.c_int
+    lib.klt_forward_hidden.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                       ctypes.c_void_p, ctypes.POINTER(KltRouting),
+                                       ctypes.POINTER(KltDebug), ctypes.c_void_p]
+    lib.klt_forward_hidden.restype = ctypes.c_int
     lib.klt_status.argtypes = [ctypes.c_void_p]
     lib.klt_status.restype = ctypes.c_int
     lib.klt_destroy.argtypes = [ctypes.c_void_p]
@@ -116,14 +121,16 @@ def dims_of(cfg, max_tokens: Optional[int] = None) -> KltDims:
 
 
 def weights_of(w: Dict) -> KltWeights:
-    """Weight dict (CUDA tensors, names as produced by ``inputs.make_weights``)."""
+    """Weight dict (CUDA tensors, names as produced by ``inputs.make_weights``, plus the
+    optional ``w_lat``/``w_gate`` of ``inputs.make_projection_weights``)."""
+    proj = (_ptr(w.get("w_lat")), _ptr(w.get("w_gate")))
     if "w13_s" in w:
         return KltWeights(_ptr(w["w13_q"]), _ptr(w["w13_s"]), None, _ptr(w["w2_q"]),
                           _ptr(w["w2_s"]), None, _ptr(w["ws13"]), _ptr(w["ws2"]),
-                          _ptr(w["w_up"]), _ptr(w["gamma"]))
+                          _ptr(w["w_up"]), _ptr(w["gamma"]), *proj)
     return KltWeights(_ptr(w["w13_q"]), _ptr(w["w13_sb"]), _ptr(w["w13_g"]), _ptr(w["w2_q"]),
                       _ptr(w["w2_sb"]), _ptr(w["w2_g"]), _ptr(w["ws13"]), _ptr(w["ws2"]),
-                      _ptr(w["w_up"]), _ptr(w["gamma"]))
+                      _ptr(w["w_up"]), _ptr(w["gamma"]), *proj)
 
 
 def klt_create(dims: KltDims, weights: KltWeights, flags: int = 0) -> ctypes.c_void_p:
@@ -142,6 +149,14 @@ def klt_forward(h, x, z, logits, M: int, out, routing: Optional[KltRouting] = No
                            ctypes.byref(routing) if routing is not None else None,
                            ctypes.byref(debug) if debug is not None else None,
                            stream)
+
+
+def klt_forward_hidden(h, x, M: int, out, routing: Optional[KltRouting] = None,
+                       debug: Optional[KltDebug] = None, stream: Optional[int] = None) -> int:
+    lib = load_library()
+    return lib.klt_forward_hidden(h, _ptr(x), M, _ptr(out),
+                                  ctypes.byref(routing) if routing is not None else None,
+                                  ctypes.byref(debug) if debug is not None else None, stream)
 
 
 def klt_status(h) -> int:
@@ -192,6 +207,21 @@ class LatentMoETail:
         return out
 
     __call__ = forward
+
+    def forward_hidden(self, x, out=None, routing: Optional[KltRouting] = None,
+                       debug: Optional[KltDebug] = None, stream=None):
+        """The step before the tail (latent input and router logits from x), then the
+        tail; the handle must have been created with ``w_lat`` and ``w_gate``."""
+        import torch
+        M = x.shape[0]
+        if out is None:
+            out = torch.empty((M, self.cfg.H), dtype=torch.bfloat16, device=x.device)
+        if stream is None:
+            stream = torch.cuda.current_stream(x.device).cuda_stream
+        rc = klt_forward_hidden(self.handle, x, M, out, routing, debug, stream)
+        if rc != KLT_OK:
+            raise KltError(rc, "klt_forward_hidden")
+        return out
 
     def status(self) -> int:
         return klt_status(self.handle)

@@ -85,6 +85,11 @@ struct klt_handle {
   __nv_bfloat16 *n, *a_s, *zqb_perm, *aqb;
   int *split_cnt, *sched, *err;
   int* dep_cnt;  // fused-launch dependency counters [routed tiles | l2 | norm tiles | shared]
+  // the step before the tail (optional): [W_lat | W_gate | zero rows] bf16, tile-major,
+  // proj_rows x H, and its outputs
+  __nv_bfloat16 *w_proj, *zp;
+  float* lgp;
+  int proj_rows;
   int dep_routed, dep_ntiles;
   int cap, max_hist_blocks;
   bool wide_ok;  // token-major engine usable (dims and launch register count)
@@ -174,6 +179,8 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
   const bool nvfp4 = d->routed_fmt == KLT_FMT_NVFP4;
   if (nvfp4 && (!w->w13_global || !w->w2_global)) return KLT_ERR_INVALID_ARG;
   if (nvfp4 && (!aligned16(w->w13_global) || !aligned16(w->w2_global))) return KLT_ERR_ALIGN;
+  if ((w->w_lat == nullptr) != (w->w_gate == nullptr)) return KLT_ERR_INVALID_ARG;
+  if (w->w_lat && (!aligned16(w->w_lat) || !aligned16(w->w_gate))) return KLT_ERR_ALIGN;
   const void* ptrs[] = {w->w13, w->w13_scale, w->w2, w->w2_scale, w->ws13, w->ws2,
                         w->w_up, w->gamma};
   for (const void* p : ptrs)
@@ -252,6 +259,14 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
   h->dep_ntiles = static_cast<int>((Mx + 15) / 16);
   KLT_ALLOC(h->dep_cnt, (static_cast<int64_t>(h->dep_routed) + 1 + 2 * h->dep_ntiles) * 4);
   KLT_ALLOC(h->err, 256);
+  if (w->w_lat) {
+    // rows: W_lat (L), W_gate (E), zero rows up to a multiple of 256 (two 128-row tiles per
+    // projection unit)
+    h->proj_rows = static_cast<int>((L + E + 255) / 256 * 256);
+    KLT_ALLOC(h->w_proj, static_cast<int64_t>(h->proj_rows) * H * 2);
+    KLT_ALLOC(h->zp, Mx * L * 2);
+    KLT_ALLOC(h->lgp, Mx * E * 4);
+  }
 #undef KLT_ALLOC
 
   // Weights are copied tile-major (one contiguous 16 KB block per 128 rows x 128 bytes of
@@ -277,6 +292,23 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
   ok &= launch_tile_relayout(w->ws13, h->ws13, 2 * Is, H * 2, 0) == cudaSuccess;
   ok &= launch_tile_relayout(w->ws2, h->ws2, H, Is * 2, 0) == cudaSuccess;
   ok &= launch_tile_relayout(w->w_up, h->w_up, H, L * 2, 0) == cudaSuccess;
+  if (w->w_lat) {
+    ok &= launch_tile_relayout(w->w_lat, h->w_proj, L, H * 2, 0) == cudaSuccess;
+    // the gate rows and the zero rows after them, as one block of 128-row tiles
+    const int64_t gate_rows = h->proj_rows - L;
+    void* tmp = nullptr;
+    if (cudaMalloc(&tmp, gate_rows * H * 2) != cudaSuccess) {
+      free_all(h);
+      delete h;
+      return KLT_ERR_OOM;
+    }
+    ok &= cudaMemset(tmp, 0, gate_rows * H * 2) == cudaSuccess;
+    ok &= cudaMemcpy(tmp, w->w_gate, E * H * 2, cudaMemcpyDeviceToDevice) == cudaSuccess;
+    ok &= launch_tile_relayout(tmp, reinterpret_cast<uint8_t*>(h->w_proj) + L * H * 2,
+                               gate_rows, H * 2, 0) == cudaSuccess;
+    ok &= cudaDeviceSynchronize() == cudaSuccess;
+    cudaFree(tmp);
+  }
   if (!nvfp4) {
     ok &= cudaMemcpy(h->w13_s, w->w13_scale, E * (2 * I / 128) * (L / 128) * 4,
                      cudaMemcpyDeviceToDevice) == cudaSuccess;
@@ -323,11 +355,22 @@ int klt_gemm_tile(const klt_handle* h, int32_t M, int32_t force_bn) {
   return kBN[bn_index(M, force_bn)];
 }
 
-int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits, int32_t M,
-                void* out, klt_routing* ro, klt_debug* dbg, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// One forward: the tail on (x, z, logits), or, with `from_hidden`, the projection of x into
+// the handle's z and logits first.
+int forward_impl(klt_handle* h, const void* x, const void* z, const float* logits, int32_t M,
+                 void* out, klt_routing* ro, klt_debug* dbg, void* stream, bool from_hidden) {
   if (!h) return KLT_ERR_INVALID_ARG;
   if (M < 0 || M > h->d.max_tokens) return KLT_ERR_INVALID_ARG;
+  if (from_hidden && !h->w_proj) return KLT_ERR_UNSUPPORTED;
   if (M == 0) return KLT_OK;
+  if (from_hidden) {
+    z = h->zp;
+    logits = h->lgp;
+  }
   if (!x || !z || !logits || !out) return KLT_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(z) || !aligned16(logits) || !aligned16(out))
     return KLT_ERR_ALIGN;
@@ -358,6 +401,47 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
     if ((expr) != cudaSuccess) return KLT_ERR_CUDA; \
     mark();                                   \
   } while (0)
+
+  // ---- the step before the tail: [z | logits] = x . [W_lat | W_gate]^T (feature-major
+  // engine, split in K to fill the GPU; its tile counter was zeroed by the previous
+  // forward's routing kernel or at create)
+  if (from_hidden) {
+    const int pbn = kBN[bn_index(M, 0)];
+    GemmParams gpj;
+    std::memset(&gpj, 0, sizeof(gpj));
+    gpj.ntasks = 1;
+    gpj.M = M;
+    gpj.E = E;
+    gpj.L = L;
+    gpj.I = I;
+    gpj.Is = Is;
+    gpj.H = H;
+    gpj.cap = h->cap;
+    gpj.tile_off = h->tile_off;
+    gpj.off = h->off;
+    gpj.ws = h->ws;
+    gpj.cnt = h->split_cnt;
+    gpj.sched = h->sched + 6;
+    gpj.err = h->err;
+    gpj.timeout = timeout_cycles;
+    gpj.zp = h->zp;
+    gpj.lgp = h->lgp;
+    GemmTask& P = gpj.task[0];
+    P.kind = TASK_PROJ;
+    P.pair = 1;
+    P.a_rb_up = 1;
+    P.a_rb_step = 2;
+    P.ftiles = h->proj_rows / 256;
+    P.kb_total = H / 64;
+    P.kb_split0 = P.kb_total;
+    P.a_kb[0] = P.a_kb[1] = H / 64;
+    P.a_ptr[0] = P.a_ptr[1] = reinterpret_cast<const uint8_t*>(h->w_proj);
+    if (!encode_2d(&P.tmB[0], x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, H, pbn))
+      return KLT_ERR_CUDA;
+    P.tmB[1] = P.tmB[0];
+    plan_split(P, (M + pbn - 1) / pbn, h->num_sms, pbn);
+    KLT_LAUNCH(launch_gemm(gpj, pbn, h->num_sms, s, pdl));
+  }
 
   // ---- K0: routing + latent quantisation + zero r + zero tile counters
   RouteParams rp;
@@ -801,6 +885,10 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
     ok &= cp(ro->pos, h->pos, static_cast<size_t>(Mk) * 4);
   }
   if (dbg) {
+    if (from_hidden) {
+      ok &= cp(dbg->z, h->zp, static_cast<size_t>(M) * L * 2);
+      ok &= cp(dbg->logits, h->lgp, static_cast<size_t>(M) * E * 4);
+    }
     ok &= cp(dbg->zq, h->zq, static_cast<size_t>(M) * L);
     ok &= cp(dbg->zs, h->zs, static_cast<size_t>(M) * (L / 128) * 4);
     ok &= cp(dbg->r, h->r, static_cast<size_t>(M) * L * 4);
@@ -817,6 +905,20 @@ int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits
     }
   }
   return ok ? KLT_OK : KLT_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int klt_forward(klt_handle* h, const void* x, const void* z, const float* logits, int32_t M,
+                void* out, klt_routing* ro, klt_debug* dbg, void* stream) {
+  return forward_impl(h, x, z, logits, M, out, ro, dbg, stream, false);
+}
+
+int klt_forward_hidden(klt_handle* h, const void* x, int32_t M, void* out, klt_routing* ro,
+                       klt_debug* dbg, void* stream) {
+  return forward_impl(h, x, nullptr, nullptr, M, out, ro, dbg, stream, true);
 }
 
 int klt_status(klt_handle* h) {

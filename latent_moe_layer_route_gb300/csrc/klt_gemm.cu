@@ -908,6 +908,26 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
       }
       if (p.sh_done != nullptr)
         signal_done<BN>(p, sm, sg, p.sh_done + info.dep_idx, grp, gw, lane);
+    } else if (kind == TASK_PROJ) {
+      // projection rows [0, L): the latent input (bf16); [L, L + E): router logits (fp32);
+      // beyond: zero padding of the weight image, not stored
+      const int f0 = info.arb * 128 + row;
+#pragma unroll
+      for (int j = 0; j < COLS; ++j) {
+        if (c0 + j < info.rows) {
+          const size_t t = static_cast<size_t>(info.row0 + c0 + j);
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            if (h2 == 1 && !pair) break;
+            const int f = f0 + 128 * h2;
+            const float v = h2 ? u[j] : g[j];
+            if (f < p.L)
+              p.zp[t * p.L + f] = __float2bfloat16_rn(v);
+            else if (f < p.L + p.E)
+              p.lgp[t * p.E + (f - p.L)] = v;
+          }
+        }
+      }
     } else if (kind == TASK_OUT) {
       // g: the unit's first 128 output features; u: the next 128 (paired units)
       __nv_bfloat16* dst = p.out + static_cast<size_t>(info.arb) * 128 + row;

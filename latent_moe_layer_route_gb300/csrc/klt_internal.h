@@ -60,7 +60,9 @@ enum TaskKind : int {
                        // per-128 e4m3 quantisation -> aq, asT
   TASK_ROUTED_L2 = 3,  // fp8 aq . W2_e^T, promotion -> r[gidx] += w * y (fp32 atomics)
   TASK_OUT = 4,        // bf16 [n | a_s] . [W_up | Ws2]^T -> out (bf16, one rounding)
-  TASK_NORM = 5        // RMSNorm of a token tile of r -> n (epilogue warps, no MMA)
+  TASK_NORM = 5,       // RMSNorm of a token tile of r -> n (epilogue warps, no MMA)
+  TASK_PROJ = 6        // bf16 x . [W_lat | W_gate]^T -> latent input z (bf16, rows < L)
+                       // and router logits (fp32, rows L .. L+E-1); the step before the tail
 };
 
 // Dependency of a unit in the fused launch, checked by the producer before it publishes
@@ -161,6 +163,8 @@ struct GemmParams {
   // preceding kernel (16-byte aligned, a multiple of 16 bytes; null/0: none)
   const uint8_t* pf_ptr;
   long long pf_bytes;
+  __nv_bfloat16* zp;           // projection outputs: latent input [M, L]
+  float* lgp;                  //   and router logits [M, E]
   long long* trace;            // optional timestamp trace (this launch's region)
   int trace_n;                 // entries per (CTA, role)
 };

@@ -26,7 +26,7 @@ class Run:
     """One forward with routing and stage outputs captured."""
 
     def __init__(self, tail: B.LatentMoETail, act: Dict, cfg, stall_after: int = 0,
-                 timeout_ms: int = 0, force_bn: int = 0):
+                 timeout_ms: int = 0, force_bn: int = 0, hidden: bool = False):
         M = act["x"].shape[0]
         k, E, L, I, Is = cfg.topk, cfg.E, cfg.L, cfg.I, cfg.Is
         dev = "cuda"
@@ -55,7 +55,14 @@ class Run:
         dbg.stall_after_kblocks = stall_after
         dbg.timeout_ms = timeout_ms
         dbg.force_bn = force_bn
-        tail.forward(act["x"], act["z"], act["logits"], out=self.out, routing=ro, debug=dbg)
+        if hidden:  # latent input and logits computed from x by the library
+            self.z = torch.zeros((M, L), dtype=torch.bfloat16, device=dev)
+            self.logits = torch.full((M, E), float("nan"), dtype=torch.float32, device=dev)
+            dbg.z, dbg.logits = self.z.data_ptr(), self.logits.data_ptr()
+            tail.forward_hidden(act["x"], out=self.out, routing=ro, debug=dbg)
+        else:
+            tail.forward(act["x"], act["z"], act["logits"], out=self.out, routing=ro,
+                         debug=dbg)
         torch.cuda.synchronize()
 
     def host(self, name):

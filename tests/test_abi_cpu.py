@@ -101,3 +101,20 @@ def test_forward_and_status_reject_null_handle(lib):
     assert lib.klt_destroy(None) == B.KLT_OK
     assert lib.klt_launch_count(None, 16) == 0
     assert lib.klt_gemm_tile(None, 16, 0) == -B.KLT_ERR_INVALID_ARG
+
+
+def test_forward_hidden_rejects_null_handle(lib):
+    assert lib.klt_forward_hidden(None, None, 4, None, None, None, None) == \
+        B.KLT_ERR_INVALID_ARG
+
+
+def test_create_wants_both_projection_weights_or_neither(lib):
+    ptrs = [0x1000] * 12
+    ptrs[2] = ptrs[5] = 0
+    for i in (10, 11):  # only one of w_lat / w_gate
+        p = list(ptrs)
+        p[i] = 0
+        assert _create(lib, _dims(), B.KltWeights(*p))[0] == B.KLT_ERR_INVALID_ARG, i
+    p = list(ptrs)
+    p[11] = 0x1008
+    assert _create(lib, _dims(), B.KltWeights(*p))[0] == B.KLT_ERR_ALIGN
