@@ -235,15 +235,19 @@ def cpu_baseline(cfg, act, w):
             "sample": f"{n} step(s) of the first {sample} of {cfg.M} tokens, {dt:.1f} s"}
 
 
-def measure(cfg, args, ws, rank, local, flush, with_cpu: bool):
+def measure(cfg, args, ws, rank, local, flush, with_cpu: bool, hidden: bool = False):
     """Every figure of one workload: device-timed steps, graph replay, per-launch times,
-    end to end with host buffers, roofline of the dominant launch, oracle on the host."""
+    end to end with host buffers, roofline of the dominant launch, oracle on the host.
+    `hidden`: the step runs from the hidden state alone (klt_forward_hidden: the latent
+    input and router logits are computed by the library first)."""
     import torch
     from latent_moe_layer_route_gb300 import binding as B
     from latent_moe_layer_route_gb300 import inputs
 
     M = cfg.M
     act_cpu, w_cpu = inputs.make_inputs(cfg)
+    if hidden:
+        w_cpu.update(inputs.make_projection_weights(cfg))
     w = {k: v.cuda() for k, v in w_cpu.items()}
     act = {k: v.cuda() for k, v in act_cpu.items()}
     flags = (B.KLT_FLAG_PHASED if args.phased else 0) | \
@@ -254,10 +258,13 @@ def measure(cfg, args, ws, rank, local, flush, with_cpu: bool):
     stream = torch.cuda.current_stream()
     cnt = torch.zeros(cfg.E, dtype=torch.int32, device="cuda")
     ro = B.KltRouting(None, None, cnt.data_ptr(), None, None, None, None)
-    tail.forward(act["x"], act["z"], act["logits"], out=out, routing=ro)
+    if hidden:
+        tail.forward_hidden(act["x"], out=out, routing=ro)
+    else:
+        tail.forward(act["x"], act["z"], act["logits"], out=out, routing=ro)
     torch.cuda.synchronize()
     assert tail.status() == B.KLT_OK
-    nl = tail.launch_count(M)
+    nl = tail.launch_count(M) + (1 if hidden else 0)
 
     base_dbg = None
     if args.tile_n:
@@ -265,7 +272,10 @@ def measure(cfg, args, ws, rank, local, flush, with_cpu: bool):
         base_dbg.force_bn = args.tile_n
 
     def step():
-        tail.forward(act["x"], act["z"], act["logits"], out=out, debug=base_dbg)
+        if hidden:
+            tail.forward_hidden(act["x"], out=out, debug=base_dbg)
+        else:
+            tail.forward(act["x"], act["z"], act["logits"], out=out, debug=base_dbg)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -347,16 +357,21 @@ def measure(cfg, args, ws, rank, local, flush, with_cpu: bool):
         evs[i][0].record(stream)
         for j in range(nl):
             dbg.events[j] = evs[i][j + 1].cuda_event
-        tail.forward(act["x"], act["z"], act["logits"], out=out, debug=dbg)
+        if hidden:
+            tail.forward_hidden(act["x"], out=out, debug=dbg)
+        else:
+            tail.forward(act["x"], act["z"], act["logits"], out=out, debug=dbg)
     torch.cuda.synchronize()
     per = np.zeros(nl)
     for i in range(args.steps):
         for j in range(nl):
             per[j] += evs[i][j].elapsed_time(evs[i][j + 1])
     per /= args.steps
-    fused = nl <= 5
-    hist = nl in (5, 8)
-    names = (["route"] + (["perm_hist"] if hist else []) + ["perm_scatter", "perm_gather"] +
+    nt = nl - (1 if hidden else 0)  # launches of the tail itself
+    fused = nt <= 5
+    hist = nt in (5, 8)
+    names = ((["proj"] if hidden else []) + ["route"] + (["perm_hist"] if hist else []) +
+             ["perm_scatter", "perm_gather"] +
              (["gemm_fused"] if fused else ["gemm_l1", "gemm_l2", "norm", "gemm_out"]))
     per_launch_us = {n: round(float(v) * 1e3, 2) for n, v in zip(names, per)}
 
@@ -373,15 +388,18 @@ def measure(cfg, args, ws, rank, local, flush, with_cpu: bool):
         flush.zero_()
         e0[i].record(stream)
         xd.copy_(xh, non_blocking=True)
-        zd.copy_(zh, non_blocking=True)
-        ld.copy_(lh, non_blocking=True)
-        tail.forward(xd, zd, ld, out=out, debug=base_dbg)
+        if hidden:
+            tail.forward_hidden(xd, out=out, debug=base_dbg)
+        else:
+            zd.copy_(zh, non_blocking=True)
+            ld.copy_(lh, non_blocking=True)
+            tail.forward(xd, zd, ld, out=out, debug=base_dbg)
         oh.copy_(out, non_blocking=True)
         e1[i].record(stream)
     torch.cuda.synchronize()
     ems = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(e0, e1)), ws)
     e2e = job_throughput(ws, M, args.steps, ems)
-    h2d = xh.numel() * 2 + zh.numel() * 2 + lh.numel() * 4
+    h2d = xh.numel() * 2 + (0 if hidden else zh.numel() * 2 + lh.numel() * 4)
     d2h = oh.numel() * 2
 
     # ---- roofline of the dominant launch
@@ -395,6 +413,9 @@ def measure(cfg, args, ws, rank, local, flush, with_cpu: bool):
         dom = max(("gemm_l1", "gemm_l2", "gemm_out"), key=lambda n: per_launch_us[n])
         dom_bytes = ab[dom]
     routed_f, dense_f = flops(cfg, M)
+    if hidden:  # the projection: its weights, x again, z and logits written
+        ab["total"] += (cfg.L + cfg.E) * cfg.H * 2 + M * cfg.H * 2 + M * (cfg.L * 2 + cfg.E * 4)
+        dense_f += 2.0 * M * cfg.H * (cfg.L + cfg.E)
     # fp8 routed contractions run at twice the bf16 rate (the nominal fp8:bf16 ratio applied
     # to the measured bf16 peak); the fused launch's mixed peak follows from the flop mix
     t_tensor = routed_f / (2 * bf16_tf * 1e12) + dense_f / (bf16_tf * 1e12)
@@ -420,7 +441,10 @@ def measure(cfg, args, ws, rank, local, flush, with_cpu: bool):
     rec = {
         "value": value, "unit": "tokens/s", "ms_per_step": ms_step,
         "us_per_layer": ms_step * 1e3, "dtype": dtype_of(cfg),
-        "config": {"workload": cfg.name, "M": M, "H": cfg.H, "L": cfg.L, "E": cfg.E,
+        "config": {"workload": cfg.name + ("+hidden" if hidden else ""), "M": M, "H": cfg.H,
+                   "L": cfg.L, "E": cfg.E,
+                   "inputs": "hidden state x only (latent input and router logits computed "
+                             "by the library)" if hidden else "x, z, logits",
                    "topk": cfg.topk, "I": cfg.I, "Is": cfg.Is, "routed_fmt": cfg.routed_fmt,
                    "router": cfg.router, "gemm_engine": tail.gemm_tile(M, args.tile_n),
                    "l2": "flushed (512 MB write) before every timed step",
@@ -471,12 +495,13 @@ def main():
     args.warmup = max(args.warmup, 3)
 
     from latent_moe_layer_route_gb300 import configs
+    # a workload name with "+hidden" runs that workload from the hidden state alone
     if args.workload == "all":
-        cfgs = list(configs.ALL)
-        head = configs.BY_NAME[HEADLINE]
+        names = [c.name for c in configs.ALL] + [HEADLINE + "+hidden"]
     else:  # one name, or several separated by commas (the first is the headline)
-        cfgs = [configs.BY_NAME[n] for n in args.workload.split(",")]
-        head = cfgs[0]
+        names = args.workload.split(",")
+    cfgs = [(configs.BY_NAME[n.split("+")[0]], n.endswith("+hidden")) for n in names]
+    head = configs.BY_NAME[HEADLINE] if args.workload == "all" else cfgs[0][0]
     ws, rank, local = _dist()
 
     if args.impl == "reference":
@@ -496,9 +521,10 @@ def main():
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
     with_cpu = rank == 0 and ws == 1 and not args.no_cpu_baseline
     recs = {}
-    for cfg in cfgs:
-        recs[cfg.name] = measure(cfg, args, ws, rank, local, flush, with_cpu)
-    h = recs[head.name]
+    for cfg, hid in cfgs:
+        recs[cfg.name + ("+hidden" if hid else "")] = measure(cfg, args, ws, rank, local,
+                                                              flush, with_cpu and not hid, hid)
+    h = recs[head.name] if head.name in recs else next(iter(recs.values()))
     line = {
         "metric": METRIC, "value": h["value"], "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": h["ms_per_step"],
