@@ -12,6 +12,7 @@ from dataclasses import dataclass, replace
 
 FMT_FP8 = "fp8"      # e4m3 codes with one fp32 scale per 128x128 block
 FMT_NVFP4 = "nvfp4"  # e2m1 codes, e4m3 scale per 16 K-elements, fp32 per-matrix scale
+FMT_MXFP8 = "mxfp8"  # e4m3 codes, one power-of-two (UE8M0) scale per 32 K-elements
 
 
 @dataclass(frozen=True)
@@ -43,7 +44,14 @@ PREFILL_M8192_NVFP4 = TailConfig("prefill_m8192_e128_k8_nvfp4", M=8192, E=128, t
                                  I=1024, routed_fmt=FMT_NVFP4, seed=4)
 
 ALL = [TINY_M4, DECODE_M16, DECODE_M128, PREFILL_M4096, PREFILL_M8192_NVFP4]
-BY_NAME = {c.name: c for c in ALL}
+
+# The power-of-two-scale variants (MXFP8 routed weights and activations) of the decode and
+# prefill workloads, for comparison with the FP8 128x128-block path on the same shapes.
+DECODE_M16_MX = DECODE_M16.with_(name="decode_m16_e64_k8_mxfp8", routed_fmt=FMT_MXFP8)
+PREFILL_M4096_MX = PREFILL_M4096.with_(name="prefill_m4096_e64_k8_mxfp8_zipf",
+                                       routed_fmt=FMT_MXFP8)
+VARIANTS = [DECODE_M16_MX, PREFILL_M4096_MX]
+BY_NAME = {c.name: c for c in ALL + VARIANTS}
 
 # Small shapes (every width one or two 128-tiles) used by fast parity and oracle tests.
 SMALL = TailConfig("small_h256_l256_e4_k2", M=6, E=4, topk=2, I=128, H=256, L=256, Is=128,

@@ -26,10 +26,10 @@ from typing import Dict, Optional
 import numpy as np
 import torch
 
-from .configs import FMT_FP8, FMT_NVFP4, TailConfig
+from .configs import FMT_FP8, FMT_MXFP8, FMT_NVFP4, TailConfig
 
 __all__ = ["make_activations", "make_weights", "make_inputs", "make_projection_weights",
-           "fp8_block_quantize", "nvfp4_quantize", "expert_load"]
+           "fp8_block_quantize", "mx_quantize", "nvfp4_quantize", "expert_load"]
 
 
 def _rng(seed: int, stream: int) -> np.random.Generator:
@@ -57,6 +57,22 @@ def fp8_block_quantize(w: torch.Tensor):
     v = (b / s[:, None, :, None]).clamp_(-448.0, 448.0)
     q = v.to(torch.float8_e4m3fn).view(torch.uint8).reshape(R, C)
     return q, s.contiguous()
+
+
+def mx_quantize(w: torch.Tensor):
+    """[R, C] fp32 -> (e4m3 codes uint8 [R, C], UE8M0 scale bytes uint8 [R, C/32]).
+
+    One power-of-two scale per 32 consecutive K-elements of a row: 2^(floor(log2 amax) - 8)
+    (1 for an all-zero block), the byte holding exponent + 127; codes are the clamped
+    quotient cast by PyTorch (round to nearest even)."""
+    R, C = w.shape
+    b = w.reshape(R, C // 32, 32)
+    amax = b.abs().amax(dim=-1)
+    _, ex = torch.frexp(amax)
+    e = torch.where(amax > 0, ex - 9, torch.zeros_like(ex)).clamp_(-127, 127)
+    v = (b / torch.ldexp(torch.ones_like(amax), e)[..., None]).clamp_(-448.0, 448.0)
+    q = v.to(torch.float8_e4m3fn).view(torch.uint8).reshape(R, C)
+    return q, (e + 127).to(torch.uint8).contiguous()
 
 
 def _e2m1_codes(v: torch.Tensor) -> torch.Tensor:
@@ -131,6 +147,16 @@ def make_weights(cfg: TailConfig) -> Dict[str, torch.Tensor]:
         for e in range(E):
             w2_q[e], w2_s[e] = fp8_block_quantize(_normal(rng, (L, I), 1 / math.sqrt(I)))
         w.update(w13_q=w13_q, w13_s=w13_s, w2_q=w2_q, w2_s=w2_s)
+    elif cfg.routed_fmt == FMT_MXFP8:
+        w13_q = torch.empty((E, 2 * I, L), dtype=torch.uint8)
+        w13_sx = torch.empty((E, 2 * I, L // 32), dtype=torch.uint8)
+        for e in range(E):
+            w13_q[e], w13_sx[e] = mx_quantize(_normal(rng, (2 * I, L), 1 / math.sqrt(L)))
+        w2_q = torch.empty((E, L, I), dtype=torch.uint8)
+        w2_sx = torch.empty((E, L, I // 32), dtype=torch.uint8)
+        for e in range(E):
+            w2_q[e], w2_sx[e] = mx_quantize(_normal(rng, (L, I), 1 / math.sqrt(I)))
+        w.update(w13_q=w13_q, w13_sx=w13_sx, w2_q=w2_q, w2_sx=w2_sx)
     elif cfg.routed_fmt == FMT_NVFP4:
         w13_q = torch.empty((E, 2 * I, L // 2), dtype=torch.uint8)
         w13_sb = torch.empty((E, 2 * I, L // 16), dtype=torch.uint8)

@@ -36,7 +36,7 @@ from .codecs import e2m1_decode, e4m3_decode, e4m3_encode, unpack_e2m1
 
 __all__ = ["route", "permutation", "quant_per128", "silu", "dequant_fp8_blocks",
            "dequant_nvfp4", "rmsnorm", "swiglu_mlp", "tail", "to_f64", "latent_inputs",
-           "bf16_round"]
+           "bf16_round", "quant_mx", "dequant_mx"]
 
 
 def to_f64(t) -> np.ndarray:
@@ -128,6 +128,32 @@ def quant_per128(v32):
     return q, s
 
 
+def quant_mx(v32):
+    """MX e4m3 quantisation (OCP Microscaling formats v1.0, e4m3 elements): per row, per 32
+    columns, one shared power-of-two scale X = 2^(floor(log2(amax)) - 8) (8 = the largest
+    e4m3 exponent), stored as an UE8M0 byte (exponent + 127, clamped to 0..254); elements
+    q = e4m3(v / X), nearest even, saturating at +-448.  An all-zero block takes X = 1.
+    Returns (codes uint8 [n,C], scale bytes uint8 [n,C/32])."""
+    v = np.asarray(v32, dtype=np.float32)
+    n, C = v.shape
+    g = v.reshape(n, C // 32, 32)
+    amax = np.abs(g).max(axis=-1).astype(np.float64)
+    _, ex = np.frexp(amax)                   # amax = m * 2^ex, 0.5 <= m < 1
+    e = np.where(amax > 0, ex - 1 - 8, 0)    # floor(log2(amax)) - 8
+    e = np.clip(e, -127, 127)
+    quot = (g.astype(np.float64) / np.ldexp(1.0, e)[..., None]).astype(np.float32)
+    q = e4m3_encode(quot).reshape(n, C)
+    return q, (e + 127).astype(np.uint8)
+
+
+def dequant_mx(q, sb) -> np.ndarray:
+    """MX e4m3 codes [n,C] with UE8M0 bytes [n,C/32] -> float64 (exact)."""
+    q = np.asarray(q)
+    n, C = q.shape
+    scale = np.ldexp(1.0, np.asarray(sb, dtype=np.int64) - 127)
+    return (e4m3_decode(q).reshape(n, C // 32, 32) * scale[..., None]).reshape(n, C)
+
+
 def dequant_act(q, s) -> np.ndarray:
     q = np.asarray(q)
     n, C = q.shape
@@ -180,6 +206,9 @@ def _expert_weights(w: Dict, fmt: str, e: int):
     if fmt == "fp8":
         return (dequant_fp8_blocks(w["w13_q"][e], w["w13_s"][e]),
                 dequant_fp8_blocks(w["w2_q"][e], w["w2_s"][e]))
+    if fmt == "mxfp8":
+        return (dequant_mx(_np(w["w13_q"][e]), _np(w["w13_sx"][e])),
+                dequant_mx(_np(w["w2_q"][e]), _np(w["w2_sx"][e])))
     return (dequant_nvfp4(w["w13_q"][e], w["w13_sb"][e], float(w["w13_g"][e])),
             dequant_nvfp4(w["w2_q"][e], w["w2_sb"][e], float(w["w2_g"][e])))
 
@@ -196,23 +225,26 @@ def tail(act: Dict, w: Dict, cfg, tokens: Optional[Iterable[int]] = None) -> Dic
     tok = np.arange(M) if tokens is None else np.asarray(list(tokens), dtype=np.int64)
     n = len(tok)
 
+    # activation quantiser: fp32 amax/448 per 128 columns, or MX (power-of-two per 32)
+    mx = cfg.routed_fmt == "mxfp8"
+    quant, deq, G = (quant_mx, dequant_mx, 32) if mx else (quant_per128, dequant_act, 128)
     z = _rows_f64(act["z"], tok)
-    zq, zs = quant_per128(z.astype(np.float32))
-    zdq = dequant_act(zq, zs)
+    zq, zs = quant(z.astype(np.float32))
+    zdq = deq(zq, zs)
 
     # Routed experts, one expert at a time (bounded memory).
     r = np.zeros((n, cfg.L))
     aq = np.zeros((n, k, I), dtype=np.uint8)
-    as_ = np.zeros((n, k, I // 128), dtype=np.float32)
+    as_ = np.zeros((n, k, I // G), dtype=np.uint8 if mx else np.float32)
     sel_ids = ids[tok]
     for e in np.unique(sel_ids):
         rows, js = np.nonzero(sel_ids == e)
         w13, w2 = _expert_weights(w, cfg.routed_fmt, int(e))
         h = zdq[rows] @ w13.T
         a = silu(h[:, :I]) * h[:, I:]
-        q, s = quant_per128(a.astype(np.float32))
+        q, s = quant(a.astype(np.float32))
         aq[rows, js], as_[rows, js] = q, s
-        y = dequant_act(q, s) @ w2.T
+        y = deq(q, s) @ w2.T
         np.add.at(r, rows, wts[tok][rows, js][:, None] * y)
 
     gamma = to_f64(w["gamma"])

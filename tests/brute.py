@@ -61,6 +61,22 @@ def quant_group(vals):
     return [e4m3_round(f32(v / s)) for v in vals], s
 
 
+def quant_group_mx(vals):
+    """One 32-wide group -> (codes, scale): scale 2**(e - 8) with 2**e <= amax < 2**(e+1),
+    found by exact doubling/halving; 1 for an all-zero group."""
+    amax = max(abs(v) for v in vals)
+    if amax == 0:
+        return [e4m3_round(0.0) for _ in vals], 1.0
+    e, p = 0, 1.0
+    while p > amax:
+        p, e = p / 2.0, e - 1
+    while p * 2.0 <= amax:
+        p, e = p * 2.0, e + 1
+    e = max(-127, min(127, e - 8))
+    s = math.ldexp(1.0, e)
+    return [e4m3_round(f32(v / s)) for v in vals], s
+
+
 def silu(v: float) -> float:
     return v / (1.0 + math.exp(-v))
 
@@ -69,16 +85,18 @@ def matvec(w, x):
     return [sum(wr[i] * x[i] for i in range(len(x))) for wr in w]
 
 
-def tail_token(logits, z, x, k, experts, gamma, eps, ws13, ws2, w_up):
-    """Output vector of one token.  ``experts[e] = (w13 rows, w2 rows)`` dequantised."""
+def tail_token(logits, z, x, k, experts, gamma, eps, ws13, ws2, w_up, mx=False):
+    """Output vector of one token.  ``experts[e] = (w13 rows, w2 rows)`` dequantised.
+    ``mx``: activations quantised per 32 with power-of-two scales instead of per 128."""
+    G, qg = (32, quant_group_mx) if mx else (128, quant_group)
     order = sorted(range(len(logits)), key=lambda e: (-logits[e], e))[:k]
     mx = logits[order[0]]
     ex = [math.exp(logits[e] - mx) for e in order]
     tot = sum(ex)
     wts = [v / tot for v in ex]
     zd = []
-    for g0 in range(0, len(z), 128):
-        q, s = quant_group([f32(v) for v in z[g0:g0 + 128]])
+    for g0 in range(0, len(z), G):
+        q, s = qg([f32(v) for v in z[g0:g0 + G]])
         zd += [e4m3_value(c) * s for c in q]
     L = len(z)
     r = [0.0] * L
@@ -88,8 +106,8 @@ def tail_token(logits, z, x, k, experts, gamma, eps, ws13, ws2, w_up):
         h = matvec(w13, zd)
         a = [silu(h[i]) * h[inter + i] for i in range(inter)]
         ad = []
-        for g0 in range(0, inter, 128):
-            q, s = quant_group([f32(v) for v in a[g0:g0 + 128]])
+        for g0 in range(0, inter, G):
+            q, s = qg([f32(v) for v in a[g0:g0 + G]])
             ad += [e4m3_value(c) * s for c in q]
         y = matvec(w2, ad)
         for c in range(L):

@@ -325,3 +325,96 @@ def test_latent_inputs_zero_and_linear_in_x():
     z1, _ = T.latent_inputs(x, w_lat, w_gate)
     z2, _ = T.latent_inputs(4.0 * x, w_lat, w_gate)  # power-of-two scaling commutes with bf16
     np.testing.assert_array_equal(z2, 4.0 * z1)
+
+
+# ---------------------------------------------------------------- power-of-two (MX) scales
+
+def _mx_blocks(seed):
+    rng = np.random.default_rng(seed)
+    v = rng.standard_normal((6, 256)).astype(np.float32)
+    v[0] *= 1e-6                       # small magnitudes
+    v[1] *= 3e4                        # large magnitudes (quotients reach the e4m3 top)
+    v[2, :32] = 0.0                    # an all-zero block
+    v[3, 32:64] = np.float32(2.0 ** -20)  # a constant block at an exact power of two
+    v[4, 64:96] *= 2.0 ** 40
+    return v
+
+
+def test_quant_mx_matches_scalar_rule():
+    v = _mx_blocks(21)
+    q, sb = T.quant_mx(v)
+    for r in range(v.shape[0]):
+        for g in range(v.shape[1] // 32):
+            codes, s = brute.quant_group_mx([float(a) for a in v[r, 32 * g:32 * g + 32]])
+            assert q[r, 32 * g:32 * g + 32].tolist() == codes, (r, g)
+            assert 2.0 ** (int(sb[r, g]) - 127) == s, (r, g)
+
+
+def test_quant_mx_scale_and_range_properties():
+    v = _mx_blocks(22)
+    q, sb = T.quant_mx(v)
+    d = T.dequant_mx(q, sb)
+    for r in range(v.shape[0]):
+        for g in range(v.shape[1] // 32):
+            blk = v[r, 32 * g:32 * g + 32].astype(np.float64)
+            amax = np.abs(blk).max()
+            if amax == 0:
+                assert sb[r, g] == 127 and not q[r, 32 * g:32 * g + 32].any()
+                continue
+            e = int(np.floor(np.log2(amax)))
+            assert int(sb[r, g]) == e - 8 + 127
+            # the block maximum lands in [256, 448] after scaling (saturating above 448)
+            top = np.abs(d[r, 32 * g:32 * g + 32]).max() / 2.0 ** (e - 8)
+            assert 256.0 <= top <= 448.0
+            # per element error: half an e4m3 step, or the saturation at 448
+            err = np.abs(d[r, 32 * g:32 * g + 32] - blk)
+            assert (err <= np.maximum(np.abs(blk) * 2.0 ** -4, 2.0 ** (e - 8 - 9)) +
+                    np.maximum(np.abs(blk) - 448 * 2.0 ** (e - 8), 0)).all()
+    # scaling a row by a power of two shifts the scale bytes and keeps the codes
+    q2, sb2 = T.quant_mx(v[5:6] * np.float32(2.0 ** 5))
+    np.testing.assert_array_equal(q2, q[5:6])
+    np.testing.assert_array_equal(sb2.astype(int), sb[5:6].astype(int) + 5)
+
+
+def test_dequant_mx_matches_loops():
+    rng = np.random.default_rng(23)
+    q = rng.integers(0, 256, (3, 64)).astype(np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0  # no NaN codes
+    sb = rng.integers(100, 150, (3, 2)).astype(np.uint8)
+    d = T.dequant_mx(q, sb)
+    for r in range(3):
+        for c in range(64):
+            assert d[r, c] == brute.e4m3_value(int(q[r, c])) * 2.0 ** (int(sb[r, c // 32]) - 127)
+
+
+def test_generator_mx_roundtrip_of_representable_weights():
+    # weights that are e4m3 values times a power of two per block are stored exactly
+    rng = np.random.default_rng(24)
+    codes = rng.integers(0, 0x7F, (128, 64)).astype(np.uint8)
+    codes[:, ::32] = 0x7E  # each block holds 448 (its maximum)
+    sign = np.where(rng.random((128, 64)) < 0.5, -1.0, 1.0)
+    scale = 2.0 ** rng.integers(-20, 5, (128, 2))
+    w = np.array([[brute.e4m3_value(int(c)) for c in row] for row in codes]) * sign
+    w = w * np.repeat(scale, 32, axis=1)
+    q, sb = inputs.mx_quantize(torch.from_numpy(w.astype(np.float32)))
+    np.testing.assert_array_equal(T.dequant_mx(q.numpy(), sb.numpy()), w)
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(M=2, E=5, topk=3, seed=12)])
+def test_tail_mx_matches_scalar_brute_force(kw):
+    cfg, act, w = _small(routed_fmt="mxfp8", **kw)
+    o = T.tail(act, w, cfg)
+    lg = act["logits"].numpy()
+    z = T.to_f64(act["z"])
+    x = T.to_f64(act["x"])
+    experts = {e: (T.dequant_mx(w["w13_q"][e].numpy(), w["w13_sx"][e].numpy()).tolist(),
+                   T.dequant_mx(w["w2_q"][e].numpy(), w["w2_sx"][e].numpy()).tolist())
+               for e in range(cfg.E)}
+    gamma = T.to_f64(w["gamma"]).tolist()
+    ws13, ws2, wup = (T.to_f64(w[k]).tolist() for k in ("ws13", "ws2", "w_up"))
+    for t in range(cfg.M):
+        ref, order, wts = brute.tail_token([float(v) for v in lg[t]], z[t].tolist(),
+                                           x[t].tolist(), cfg.topk, experts, gamma, cfg.eps,
+                                           ws13, ws2, wup, mx=True)
+        assert o["ids"][t].tolist() == order
+        np.testing.assert_allclose(o["out"][t], ref, rtol=1e-9, atol=1e-9)
