@@ -23,6 +23,7 @@ KLT_ERR_TOO_LARGE = 7
 KLT_NOALLOC_MAX_PAIRS = 65536
 KLT_FMT_FP8_B128 = 0
 KLT_FMT_NVFP4 = 1
+KLT_FMT_MXFP8 = 2
 KLT_FLAG_NO_PDL = 1
 KLT_FLAG_PHASED = 2
 KLT_FLAG_DETERMINISTIC = 4
@@ -56,7 +57,7 @@ class KltDebug(ctypes.Structure):
                 ("stall_after_kblocks", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
                 ("trace", ctypes.c_void_p), ("trace_entries", ctypes.c_int32),
                 ("force_bn", ctypes.c_int32), ("z", ctypes.c_void_p),
-                ("logits", ctypes.c_void_p)]
+                ("logits", ctypes.c_void_p), ("zsx", ctypes.c_void_p)]
 
 
 _LIB: Optional[ctypes.CDLL] = None
@@ -115,7 +116,8 @@ def _ptr(t) -> Optional[int]:
 
 
 def dims_of(cfg, max_tokens: Optional[int] = None) -> KltDims:
-    fmt = KLT_FMT_NVFP4 if cfg.routed_fmt == "nvfp4" else KLT_FMT_FP8_B128
+    fmt = {"nvfp4": KLT_FMT_NVFP4, "mxfp8": KLT_FMT_MXFP8}.get(cfg.routed_fmt,
+                                                             KLT_FMT_FP8_B128)
     return KltDims(cfg.H, cfg.L, cfg.E, cfg.topk, cfg.I, cfg.Is, fmt, cfg.eps,
                    cfg.M if max_tokens is None else max_tokens)
 
@@ -124,6 +126,10 @@ def weights_of(w: Dict) -> KltWeights:
     """Weight dict (CUDA tensors, names as produced by ``inputs.make_weights``, plus the
     optional ``w_lat``/``w_gate`` of ``inputs.make_projection_weights``)."""
     proj = (_ptr(w.get("w_lat")), _ptr(w.get("w_gate")))
+    if "w13_sx" in w:  # MXFP8: UE8M0 scale bytes per 32 K-elements
+        return KltWeights(_ptr(w["w13_q"]), _ptr(w["w13_sx"]), None, _ptr(w["w2_q"]),
+                          _ptr(w["w2_sx"]), None, _ptr(w["ws13"]), _ptr(w["ws2"]),
+                          _ptr(w["w_up"]), _ptr(w["gamma"]), *proj)
     if "w13_s" in w:
         return KltWeights(_ptr(w["w13_q"]), _ptr(w["w13_s"]), None, _ptr(w["w2_q"]),
                           _ptr(w["w2_s"]), None, _ptr(w["ws13"]), _ptr(w["ws2"]),

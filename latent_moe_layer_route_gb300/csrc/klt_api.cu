@@ -85,6 +85,11 @@ struct klt_handle {
   __nv_bfloat16 *n, *a_s, *zqb_perm, *aqb;
   int *split_cnt, *sched, *err;
   int* dep_cnt;  // fused-launch dependency counters [routed tiles | l2 | norm tiles | shared]
+  // MXFP8 layers: weight scale tiles (512 bytes per 128-row block and k-block, the
+  // tcgen05.cp layout), the latent input's scale bytes, and the token scale tiles of the
+  // routed L1 and L2 units (one per routed tile of 128 pairs and k-block)
+  uint8_t *w13_sf, *w2_sf, *zsx, *zsf_t, *asf_t;
+  int sf_tiles;
   // the step before the tail (optional): [W_lat | W_gate | zero rows] bf16, tile-major,
   // proj_rows x H, and its outputs
   __nv_bfloat16 *w_proj, *zp;
@@ -120,8 +125,11 @@ int check_dims(const klt_dims* d) {
   if (d->H % 128 || d->L % 128 || d->I % 128 || d->Is % 128) return KLT_ERR_UNSUPPORTED;
   if (d->E > MAX_E || d->topk > d->E || d->topk > MAX_TOPK) return KLT_ERR_UNSUPPORTED;
   if (d->L > 128 * MAX_KB || d->I > 128 * MAX_KB) return KLT_ERR_UNSUPPORTED;
-  if (d->routed_fmt != KLT_FMT_FP8_B128 && d->routed_fmt != KLT_FMT_NVFP4)
+  if (d->routed_fmt != KLT_FMT_FP8_B128 && d->routed_fmt != KLT_FMT_NVFP4 &&
+      d->routed_fmt != KLT_FMT_MXFP8)
     return KLT_ERR_UNSUPPORTED;
+  // MXFP8 runs on the token-major engine only (256-wide units)
+  if (d->routed_fmt == KLT_FMT_MXFP8 && (d->H % 256 || d->L % 256)) return KLT_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(d->max_tokens) * d->topk > (1 << 20)) return KLT_ERR_UNSUPPORTED;
   return KLT_OK;
 }
@@ -177,6 +185,8 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
   if (rc) return rc;
   if ((flags & KLT_FLAG_DETERMINISTIC) && (flags & KLT_FLAG_PHASED)) return KLT_ERR_UNSUPPORTED;
   const bool nvfp4 = d->routed_fmt == KLT_FMT_NVFP4;
+  const bool mx = d->routed_fmt == KLT_FMT_MXFP8;
+  if (mx && (flags & KLT_FLAG_PHASED)) return KLT_ERR_UNSUPPORTED;
   if (nvfp4 && (!w->w13_global || !w->w2_global)) return KLT_ERR_INVALID_ARG;
   if (nvfp4 && (!aligned16(w->w13_global) || !aligned16(w->w2_global))) return KLT_ERR_ALIGN;
   if ((w->w_lat == nullptr) != (w->w_gate == nullptr)) return KLT_ERR_INVALID_ARG;
@@ -259,6 +269,14 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
   h->dep_ntiles = static_cast<int>((Mx + 15) / 16);
   KLT_ALLOC(h->dep_cnt, (static_cast<int64_t>(h->dep_routed) + 1 + 2 * h->dep_ntiles) * 4);
   KLT_ALLOC(h->err, 256);
+  if (mx) {
+    h->sf_tiles = static_cast<int>(cap / 128 + E);
+    KLT_ALLOC(h->w13_sf, E * 2 * I * (L / 32));
+    KLT_ALLOC(h->w2_sf, E * L * (I / 32));
+    KLT_ALLOC(h->zsx, Mx * (L / 32));
+    KLT_ALLOC(h->zsf_t, static_cast<int64_t>(h->sf_tiles) * (L / 128) * 512);
+    KLT_ALLOC(h->asf_t, static_cast<int64_t>(h->sf_tiles) * (I / 128) * 512);
+  }
   if (w->w_lat) {
     // rows: W_lat (L), W_gate (E), zero rows up to a multiple of 256 (two 128-row tiles per
     // projection unit)
@@ -289,6 +307,12 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
     ok &= launch_tile_relayout(w->w13, h->w13, E * 2 * I, L, 0) == cudaSuccess;
     ok &= launch_tile_relayout(w->w2, h->w2, E * L, I, 0) == cudaSuccess;
   }
+  if (mx) {
+    ok &= launch_sf_relayout(static_cast<const uint8_t*>(w->w13_scale), h->w13_sf, E * 2 * I, L,
+                             0) == cudaSuccess;
+    ok &= launch_sf_relayout(static_cast<const uint8_t*>(w->w2_scale), h->w2_sf, E * L, I, 0) ==
+          cudaSuccess;
+  }
   ok &= launch_tile_relayout(w->ws13, h->ws13, 2 * Is, H * 2, 0) == cudaSuccess;
   ok &= launch_tile_relayout(w->ws2, h->ws2, H, Is * 2, 0) == cudaSuccess;
   ok &= launch_tile_relayout(w->w_up, h->w_up, H, L * 2, 0) == cudaSuccess;
@@ -309,7 +333,7 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
     ok &= cudaDeviceSynchronize() == cudaSuccess;
     cudaFree(tmp);
   }
-  if (!nvfp4) {
+  if (!nvfp4 && !mx) {
     ok &= cudaMemcpy(h->w13_s, w->w13_scale, E * (2 * I / 128) * (L / 128) * 4,
                      cudaMemcpyDeviceToDevice) == cudaSuccess;
     ok &= cudaMemcpy(h->w2_s, w->w2_scale, E * (L / 128) * (I / 128) * 4,
@@ -336,6 +360,11 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
     return KLT_ERR_CUDA;
   }
   h->wide_ok = L % 256 == 0 && H % 256 == 0 && wide_regs_ok(wide_kernel_regs());
+  if (mx && !h->wide_ok) {
+    free_all(h);
+    delete h;
+    return KLT_ERR_UNSUPPORTED;
+  }
   *out = h;
   return KLT_OK;
 }
@@ -350,6 +379,9 @@ int klt_launch_count(const klt_handle* h, int32_t M) {
 int klt_gemm_tile(const klt_handle* h, int32_t M, int32_t force_bn) {
   if (!h) return -KLT_ERR_INVALID_ARG;
   const bool phased = (h->flags & KLT_FLAG_PHASED) != 0;
+  if (h->d.routed_fmt == KLT_FMT_MXFP8)  // block-scaled units exist in the token-major engine
+    return (force_bn == 0 || force_bn == 256) && h->wide_ok && !phased ? 256
+                                                                      : -KLT_ERR_UNSUPPORTED;
   if (force_bn == 256) return h->wide_ok && !phased ? 256 : -KLT_ERR_UNSUPPORTED;
   if (force_bn == 0 && h->wide_ok && !phased && M >= kWideMinTokens) return 256;
   return kBN[bn_index(M, force_bn)];
@@ -460,6 +492,9 @@ int forward_impl(klt_handle* h, const void* x, const void* z, const float* logit
   rp.E = E;
   rp.k = k;
   rp.L = L;
+  const bool mx = d.routed_fmt == KLT_FMT_MXFP8;
+  rp.mx = mx ? 1 : 0;
+  rp.zsx = h->zsx;
   KLT_LAUNCH(launch_route(rp, s, pdl));
 
   // ---- K1: permutation
@@ -486,6 +521,9 @@ int forward_impl(klt_handle* h, const void* x, const void* z, const float* logit
   pp.cap = h->cap;
   pp.bn = BN;  // routed tile list in BN-token tiles (128 for the token-major engine)
   pp.nblocks = nblocks;
+  pp.zsx = h->zsx;
+  pp.zsf_t = mx ? h->zsf_t : nullptr;
+  pp.sf_tiles = h->sf_tiles;
   if (nblocks > 1) KLT_LAUNCH(launch_perm_hist(pp, s, pdl));
   KLT_LAUNCH(launch_perm_scatter(pp, s, pdl));
   KLT_LAUNCH(launch_perm_gather(pp, s, pdl));
@@ -536,7 +574,11 @@ int forward_impl(klt_handle* h, const void* x, const void* z, const float* logit
     gw.ntasks = 5;
     // prefill-size batches: pairs of token tiles share each staged weight tile of the
     // BF16 tasks (3 stages of 64 KB); otherwise 4 stages of 48 KB
-    const bool dual = ntiles >= kDualMinTiles;
+    // MX launches keep one accumulator slot: the other half of TMEM holds the scale ring
+    // (so no dual units either)
+    const bool dual = !mx && ntiles >= kDualMinTiles;
+    gw.mx = mx ? 1 : 0;
+    gw.asf_t = h->asf_t;
     gw.w_stages = dual ? 3 : 4;
     gw.w_stage_bytes = dual ? 64 * 1024 : 48 * 1024;
     gw.sched = h->sched + 3;
@@ -545,7 +587,7 @@ int forward_impl(klt_handle* h, const void* x, const void* z, const float* logit
     GemmTask& R = gw.task[0];  // routed L1: gate and up row blocks of one 128-output tile
     R.kind = TASK_ROUTED_L1;
     R.fp8 = !nvfp4;
-    R.kpg = nvfp4 ? 2 : 1;
+    R.kpg = mx ? 0 : (nvfp4 ? 2 : 1);  // MX: scales applied by the tensor core
     R.routed = 1;
     R.ftiles = I / 128;
     R.kb_total = L / rkb;
@@ -557,6 +599,8 @@ int forward_impl(klt_handle* h, const void* x, const void* z, const float* logit
     R.a_kb[0] = R.a_kb[1] = L / rkb;
     R.a_ptr[0] = R.a_ptr[1] = h->w13;
     R.tmB[0] = R.tmB[1] = h->tm_zqp[bi];
+    R.a_sf = mx ? h->w13_sf : nullptr;
+    R.t_sf = mx ? h->zsf_t : nullptr;
     GemmTask& S = gw.task[1];  // shared L1 (bf16)
     S.kind = TASK_SHARED_L1;
     S.ftiles = Is / 128;
@@ -576,7 +620,9 @@ int forward_impl(klt_handle* h, const void* x, const void* z, const float* logit
     GemmTask& R2 = gw.task[2];  // routed L2 + combine: two row blocks of W2 per unit
     R2.kind = TASK_ROUTED_L2;
     R2.fp8 = !nvfp4;
-    R2.kpg = nvfp4 ? 2 : 1;
+    R2.kpg = mx ? 0 : (nvfp4 ? 2 : 1);
+    R2.a_sf = mx ? h->w2_sf : nullptr;
+    R2.t_sf = mx ? h->asf_t : nullptr;
     R2.routed = 1;
     R2.ftiles = L / 256;
     R2.kb_total = I / rkb;
@@ -885,6 +931,7 @@ int forward_impl(klt_handle* h, const void* x, const void* z, const float* logit
     ok &= cp(ro->pos, h->pos, static_cast<size_t>(Mk) * 4);
   }
   if (dbg) {
+    if (mx) ok &= cp(dbg->zsx, h->zsx, static_cast<size_t>(M) * (L / 32));
     if (from_hidden) {
       ok &= cp(dbg->z, h->zp, static_cast<size_t>(M) * L * 2);
       ok &= cp(dbg->logits, h->lgp, static_cast<size_t>(M) * E * 4);

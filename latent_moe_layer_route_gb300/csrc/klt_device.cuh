@@ -222,6 +222,36 @@ KLT_DEV void mma_fp8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t i
       : "memory");
 }
 
+// Block-scaled FP8 MMA (kind::mxf8f6f4, one UE8M0 scale per 32 K-elements, applied by the
+// tensor core): K = 32 per instruction.  The scales are read from TMEM: row m of A at lane m,
+// column sfa + m/32; column n of B at lane n%32, column sfb + n/32; the byte within the
+// 32-bit word is the instruction descriptor's scale id (bits 29-30 for A, 4-5 for B).
+KLT_DEV void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                    uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, "
+      "[%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+// Instruction descriptor of kind::mxf8f6f4 with e4m3 A and B, UE8M0 scales, fp32
+// accumulation, both operands K-major, shape M x N, scale ids for A and B.
+__host__ __device__ constexpr uint32_t idesc_mx(int m, int n, uint32_t a_sf_id,
+                                                uint32_t b_sf_id) {
+  return (b_sf_id << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) |
+         (static_cast<uint32_t>(m >> 4) << 24) | (a_sf_id << 29);
+}
+// Copies a 32-row x 16-byte shared-memory tile (row r at +16r) into TMEM columns
+// taddr .. taddr+3, lane r of every lane quadrant (tcgen05.cp 32x128b, warpx4).
+KLT_DEV void tmem_cp_32x128b_x4(uint32_t taddr, uint32_t saddr) {
+  const uint64_t desc = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+                        (static_cast<uint64_t>(128 >> 4) << 16) |
+                        (static_cast<uint64_t>(128 >> 4) << 32) | (static_cast<uint64_t>(1) << 46);
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc)
+               : "memory");
+}
+
 // The four MMAs of one 128-byte K block (K = 4 x 32 bytes) into one accumulator, issued
 // from a single asm block: the first accumulates iff `accumulate`, the rest always do.
 // `kind` is the tcgen05.mma kind string (kind::f16 or kind::f8f6f4).
@@ -383,6 +413,22 @@ KLT_DEV float quot_rn(float x, float s, float inv) {
 KLT_DEV float rcp_nr(float s) {
   const float y0 = __fdividef(1.0f, s);
   return fmaf(fmaf(-s, y0, 1.0f), y0, y0);
+}
+
+// MX (OCP Microscaling, e4m3 elements) shared exponent of a block whose largest magnitude
+// is amax: floor(log2 amax) - 8, clamped to the UE8M0 range [-127, 127]; 0 for amax == 0.
+// Read from the IEEE fields (a subnormal amax has floor(log2 amax) <= -127).
+KLT_DEV int mx_exponent(float amax) {
+  const uint32_t b = __float_as_uint(amax) & 0x7FFFFFFFu;
+  if (b == 0) return 0;
+  const int f = static_cast<int>(b >> 23);  // biased exponent field
+  if (f == 0) return -127;
+  const int e = f - 127 - 8;
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+// 2^n as an fp32 value, exact for -127 <= n <= 127 (2^-127 is the subnormal 0x00400000).
+KLT_DEV float pow2_exact(int n) {
+  return n >= -126 ? __int_as_float((n + 127) << 23) : __int_as_float(0x00400000);
 }
 
 // Four consecutive fp32 atomically added to global memory (16-byte aligned), one request.

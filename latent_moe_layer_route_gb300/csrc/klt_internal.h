@@ -23,6 +23,8 @@ struct RouteParams {
   int* zero_buf;           // dependency counters of the fused launch, zeroed here
   int zero_n;
   int M, E, k, L;
+  int mx;                  // MX quantisation: UE8M0 byte per 32 columns into zsx
+  uint8_t* zsx;            // [M, L/32]
 };
 
 struct PermParams {
@@ -42,6 +44,12 @@ struct PermParams {
   const float* wts;    // [M*k] routing weights by pair i
   float* wperm;        // [cap] routing weight of pair p
   int M, E, k, L, cap, bn, nblocks;
+  // MX layers: the gathered token scale bytes as one 512-byte tile per (routed tile of bn
+  // = 128 pairs, 128-column k-block), laid out for tcgen05.cp: byte r%32*16 + 4*(r/32) + j
+  // = scale of tile row r, 32-column group j of the k-block (rows past the tile: scale 1)
+  const uint8_t* zsx;  // [M, L/32]
+  uint8_t* zsf_t;      // [tile capacity, L/128, 512]
+  int sf_tiles;        // tile capacity (grid bound; tile_off[E] of the batch is <= it)
 };
 
 struct NormParams {
@@ -107,6 +115,11 @@ struct GemmTask {
                        // that share its weight tiles (units = ceil(ntiles / 2) * ftiles)
   int units;           // non-routed: ntiles * ftiles * ksplit
   int dep;             // DepKind of this task's units
+  // MX block-scaled units (token-major engine): scale tiles of 512 bytes in the tcgen05.cp
+  // layout, the weights' per (128-row block, k-block) like their data tiles, the tokens'
+  // per (routed tile, k-block); null for other tasks
+  const uint8_t* a_sf;
+  const uint8_t* t_sf;
   int ws_tile_base;    // first arrival counter of this task (tile ids start here)
   long long ws_off;    // float offset of this task's partials in the workspace
   int streamk;         // 1: static stream-K partition of ntiles*ftiles*kb_total k-blocks
@@ -163,6 +176,10 @@ struct GemmParams {
   // preceding kernel (16-byte aligned, a multiple of 16 bytes; null/0: none)
   const uint8_t* pf_ptr;
   long long pf_bytes;
+  int mx;                      // token-major engine, MX layer: block-scaled routed units
+                               // (one accumulator slot; the scale ring takes the other half
+                               // of TMEM) and the routed L1 epilogue requantises per 32 with
+  uint8_t* asf_t;              //   power-of-two scales into these tiles [tiles, I/128, 512]
   __nv_bfloat16* zp;           // projection outputs: latent input [M, L]
   float* lgp;                  //   and router logits [M, E]
   long long* trace;            // optional timestamp trace (this launch's region)
@@ -189,6 +206,11 @@ cudaError_t launch_fill_expert_scale(const float* g, float* dst, int E, long lon
                                      cudaStream_t s);
 cudaError_t launch_tile_relayout(const void* src, void* dst, long long rows, long long row_bytes,
                                  cudaStream_t s);
+// UE8M0 scale bytes [rows, K/32] (rows % 128 == 0, K % 128 == 0) -> 512-byte tiles per
+// (128-row block rb, k-block kb) at (rb * K/128 + kb) * 512, byte (r%32)*16 + 4*((r%128)/32)
+// + j = scale of row r, 32-column group 4*kb + j (the tcgen05.cp 32x128b layout).
+cudaError_t launch_sf_relayout(const uint8_t* src, uint8_t* dst, long long rows, long long K,
+                               cudaStream_t s);
 // bn in {16, 128}; grid = persistent CTAs.
 cudaError_t launch_gemm(const GemmParams& p, int bn, int grid, cudaStream_t s, bool pdl);
 int gemm_smem_bytes(int bn);

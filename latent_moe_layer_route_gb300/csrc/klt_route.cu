@@ -99,15 +99,32 @@ __global__ void __launch_bounds__(32 * ROUTE_WARPS)
   const float v0 = __low2float(b01), v1 = __high2float(b01);
   const float v2 = __low2float(b23), v3 = __high2float(b23);
   float amax = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
+  uint32_t q;
+  if (p.mx) {
+    // MX: one power-of-two scale per 32 columns (8 lanes): 2^(floor(log2 amax) - 8); the
+    // quotient by a power of two is exact, so the codes equal e4m3(v / scale)
 #pragma unroll
-  for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-  const float s = amax == 0.f ? 1.0f : amax / 448.0f;
-  const uint32_t q = static_cast<uint32_t>(f32_to_e4m3(v0 / s)) |
-                     (static_cast<uint32_t>(f32_to_e4m3(v1 / s)) << 8) |
-                     (static_cast<uint32_t>(f32_to_e4m3(v2 / s)) << 16) |
-                     (static_cast<uint32_t>(f32_to_e4m3(v3 / s)) << 24);
+    for (int o = 4; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const int e = mx_exponent(amax);
+    const float inv = pow2_exact(-e);
+    q = static_cast<uint32_t>(f32_to_e4m3(v0 * inv)) |
+        (static_cast<uint32_t>(f32_to_e4m3(v1 * inv)) << 8) |
+        (static_cast<uint32_t>(f32_to_e4m3(v2 * inv)) << 16) |
+        (static_cast<uint32_t>(f32_to_e4m3(v3 * inv)) << 24);
+    if ((lane & 7) == 0)
+      p.zsx[static_cast<size_t>(t) * (p.L / 32) + g * 4 + (lane >> 3)] =
+          static_cast<uint8_t>(e + 127);
+  } else {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const float s = amax == 0.f ? 1.0f : amax / 448.0f;
+    q = static_cast<uint32_t>(f32_to_e4m3(v0 / s)) |
+        (static_cast<uint32_t>(f32_to_e4m3(v1 / s)) << 8) |
+        (static_cast<uint32_t>(f32_to_e4m3(v2 / s)) << 16) |
+        (static_cast<uint32_t>(f32_to_e4m3(v3 / s)) << 24);
+    if (lane == 0) p.zs[static_cast<size_t>(t) * G + g] = s;
+  }
   *reinterpret_cast<uint32_t*>(p.zq + static_cast<size_t>(t) * p.L + g * 128 + lane * 4) = q;
-  if (lane == 0) p.zs[static_cast<size_t>(t) * G + g] = s;
   // ---- zero the matching 128 floats of the combine buffer
   reinterpret_cast<float4*>(p.r + static_cast<size_t>(t) * p.L + g * 128)[lane] =
       make_float4(0.f, 0.f, 0.f, 0.f);
@@ -239,11 +256,32 @@ __global__ void __launch_bounds__(256) perm_gather_kernel(const PermParams p) {
       dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
     }
   }
-  if (c < Mk * G) {
+  if (p.zsf_t == nullptr && c < Mk * G) {
     const int pp = static_cast<int>(c / G);
     const int g = static_cast<int>(c - static_cast<long long>(pp) * G);
     p.zsT[static_cast<size_t>(g) * p.cap + pp] =
         p.zs[static_cast<size_t>(__ldg(p.gidx + pp)) * G + g];
+  }
+  // MX layers: the token scale tiles of every routed tile (one 4-byte word per tile row and
+  // k-block); rows past the tile's pairs get scale 1 (their products are never stored)
+  if (p.zsf_t != nullptr && c < static_cast<long long>(p.sf_tiles) * 128 * G) {
+    const int tile = static_cast<int>(c / (128LL * G));
+    const int rem = static_cast<int>(c - static_cast<long long>(tile) * 128 * G);
+    const int kb = rem / 128, r = rem - (rem / 128) * 128;
+    if (tile < p.tile_off[p.E]) {
+      int lo = 0, hi = p.E - 1;  // largest e with tile_off[e] <= tile
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(p.tile_off + mid) <= tile) lo = mid; else hi = mid - 1;
+      }
+      const int pp = __ldg(p.off + lo) + (tile - __ldg(p.tile_off + lo)) * p.bn + r;
+      uint32_t word = 0x7F7F7F7Fu;
+      if (pp < __ldg(p.off + lo + 1))
+        word = *reinterpret_cast<const uint32_t*>(
+            p.zsx + static_cast<size_t>(__ldg(p.gidx + pp)) * (p.L / 32) + 4 * kb);
+      *reinterpret_cast<uint32_t*>(p.zsf_t + (static_cast<size_t>(tile) * G + kb) * 512 +
+                                   (r & 31) * 16 + 4 * (r >> 5)) = word;
+    }
   }
 }
 
@@ -321,6 +359,17 @@ __global__ void __launch_bounds__(256)
 }
 
 __global__ void __launch_bounds__(256)
+    sf_relayout_kernel(const uint8_t* src, uint8_t* dst, long long rows, long long K) {
+  const long long kbs = K / 128;
+  const long long q = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
+  if (q >= rows * kbs) return;
+  const long long row = q / kbs, kb = q - row * kbs;
+  const uint32_t word = *reinterpret_cast<const uint32_t*>(src + row * (K / 32) + 4 * kb);
+  const long long rb = row >> 7, r = row & 127;
+  *reinterpret_cast<uint32_t*>(dst + (rb * kbs + kb) * 512 + (r & 31) * 16 + 4 * (r >> 5)) = word;
+}
+
+__global__ void __launch_bounds__(256)
     fill_expert_scale_kernel(const float* g, float* dst, int E, long long per) {
   const long long i = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
   if (i < E * per) dst[i] = g[i / per];
@@ -356,7 +405,11 @@ cudaError_t launch_perm_scatter(const PermParams& p, cudaStream_t s, bool pdl) {
   return launch_simple(perm_scatter_kernel, dim3(p.nblocks), dim3(PERM_BLOCK), p, s, pdl);
 }
 cudaError_t launch_perm_gather(const PermParams& p, cudaStream_t s, bool pdl) {
-  const long long chunks = static_cast<long long>(p.M) * p.k * (p.L / 16);
+  long long chunks = static_cast<long long>(p.M) * p.k * (p.L / 16);
+  if (p.zsf_t != nullptr)
+    chunks = chunks > static_cast<long long>(p.sf_tiles) * 128 * (p.L / 128)
+                 ? chunks
+                 : static_cast<long long>(p.sf_tiles) * 128 * (p.L / 128);
   return launch_simple(perm_gather_kernel, dim3(static_cast<unsigned>((chunks + 255) / 256)),
                        dim3(256), p, s, pdl);
 }
@@ -376,6 +429,12 @@ cudaError_t launch_fill_expert_scale(const float* g, float* dst, int E, long lon
   const long long n = E * per;
   fill_expert_scale_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(g, dst, E,
                                                                                     per);
+  return cudaGetLastError();
+}
+cudaError_t launch_sf_relayout(const uint8_t* src, uint8_t* dst, long long rows, long long K,
+                               cudaStream_t s) {
+  const long long n = rows * (K / 128);
+  sf_relayout_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(src, dst, rows, K);
   return cudaGetLastError();
 }
 cudaError_t launch_tile_relayout(const void* src, void* dst, long long rows, long long row_bytes,

@@ -47,7 +47,10 @@ struct W {
   static constexpr int DUAL_STAGES = 3;
   static_assert(STAGES * STAGE_BYTES == DUAL_STAGES * DUAL_STAGE_BYTES, "one ring size");
   static constexpr int TMEM_COLS = 512;
-  static constexpr int NACC = TMEM_COLS / TN;
+  static constexpr int NACC = TMEM_COLS / TN;  // accumulator slots (MX launches use one)
+  static constexpr int SF_STAGE = 3 * 512;     // MX scale tiles per stage
+  static constexpr int SF_COLS = 12;           // TMEM columns of one stage's scales
+  static_assert(TN + STAGES * SF_COLS <= TMEM_COLS, "MX scale ring beside one slot");
   static constexpr int US = 8;
   static constexpr int SIG = 8;             // completion-signal ring (epilogue -> signaller)
   static constexpr int SIGNAL_WARP = 2;     // control warp that publishes unit completions
@@ -89,12 +92,14 @@ struct WSmem {
   float* amax;  // [2 unit parities][2 column halves][TM]
   float* stg;   // [EPI_WARPS][32 tokens][STG_LD] per-warp transpose staging of the combine
                 // (16-byte aligned)
+  uint8_t* sf;  // [STAGES][SF_STAGE] MX scale tiles of each stage: tokens, weight rows
+                // 0-127, weight rows 128-255 (512 bytes each, 16-byte aligned)
 
   static constexpr int BAR_BYTES =
       8 * (2 * W::STAGES + 2 * W::NACC + 2 * W::US + 2 * W::SIG + 1) + 8 * W::SIG;
   static constexpr int bytes() {
     return W::STAGES * W::STAGE_BYTES + BAR_BYTES + W::US * (int)sizeof(WUnit) + 64 +
-           4 * W::TM * 4 + W::EPI_WARPS * 32 * STG_LD * 4 +
+           4 * W::TM * 4 + W::EPI_WARPS * 32 * STG_LD * 4 + W::STAGES * W::SF_STAGE +
            16 + 1024 /* alignment slack */;
   }
   __device__ explicit WSmem(uint8_t* raw) {
@@ -118,6 +123,7 @@ struct WSmem {
     amax = reinterpret_cast<float*>(tmem_holder + 16);
     stg = reinterpret_cast<float*>(
         (reinterpret_cast<uintptr_t>(amax + 4 * W::TM) + 15) & ~static_cast<uintptr_t>(15));
+    sf = reinterpret_cast<uint8_t*>(stg + W::EPI_WARPS * 32 * STG_LD);
   }
 };
 
@@ -227,6 +233,9 @@ __device__ bool w_wait_dependency(const GemmParams& p, int dep, int idx, const i
 }
 
 // ------------------------------------------------------------------ producer (1 thread)
+// MX: the launch carries block-scaled routed units (their own kernel instantiation, so the
+// other launches keep their code and registers unchanged).
+template <bool MX>
 __device__ void w_producer(const GemmParams& p, WSmem& sm, const int* s_tile_off,
                            const int* s_off) {
   // weights are re-read by every token tile of their expert, tokens by every feature tile
@@ -253,6 +262,7 @@ __device__ void w_producer(const GemmParams& p, WSmem& sm, const int* s_tile_off
     }
     const GemmTask& T = p.task[info.task];
     const int elems_per_kb = T.fp8 ? 128 : 64;
+    const bool mxu = MX && T.a_sf != nullptr;  // block-scaled unit: scale tiles ride along
     auto issue_w = [&](int kb, uint8_t* st) {
       const int m = kb < T.kb_split0 ? 0 : 1;
       const int kk = m ? kb - T.kb_split0 : kb;
@@ -262,17 +272,29 @@ __device__ void w_producer(const GemmParams& p, WSmem& sm, const int* s_tile_off
                 &sm.full[stage], pol_w);
       bulk_load(st + W::W_TILE, a + (static_cast<size_t>(info.rb1) * akb + kk) * W::W_TILE,
                 W::W_TILE, &sm.full[stage], pol_w);
+      if (mxu) {
+        uint8_t* sf = sm.sf + stage * W::SF_STAGE;
+        bulk_load(sf + 512, T.a_sf + (static_cast<size_t>(info.rb0) * akb + kk) * 512, 512,
+                  &sm.full[stage], pol_w);
+        bulk_load(sf + 1024, T.a_sf + (static_cast<size_t>(info.rb1) * akb + kk) * 512, 512,
+                  &sm.full[stage], pol_w);
+      }
     };
-    auto issue_t = [&](int kb, uint8_t* st, uint64_t* bar) {
+    auto issue_t = [&](int kb, uint8_t* st, uint64_t* bar, int stg_idx) {
       const int m = kb < T.kb_split0 ? 0 : 1;
       const int kk = m ? kb - T.kb_split0 : kb;
       tma_load_2d(st + 2 * W::W_TILE, &T.tmB[m], bar, kk * elems_per_kb, info.row0, pol);
       if (info.dual)
         tma_load_2d(st + 2 * W::W_TILE + W::T_TILE, &T.tmB[m], bar, kk * elems_per_kb,
                     info.row0 + W::TM, pol);
+      if (mxu)  // this routed tile's token scales for the k-block
+        bulk_load(sm.sf + stg_idx * W::SF_STAGE,
+                  T.t_sf + (static_cast<size_t>(info.dep_idx) * T.kb_total + kk) * 512, 512, bar,
+                  pol);
     };
-    const uint32_t stage_tx =
-        2 * W::W_TILE + (info.dual ? 2 : 1) * static_cast<uint32_t>(W::T_TILE);
+    const uint32_t stage_tx = 2 * W::W_TILE +
+                              (info.dual ? 2 : 1) * static_cast<uint32_t>(W::T_TILE) +
+                              (mxu ? W::SF_STAGE : 0);
     const int kb_end = T.kb_total;
     int kb = 0;
     if (T.dep != DEP_NONE) {
@@ -298,7 +320,7 @@ __device__ void w_producer(const GemmParams& p, WSmem& sm, const int* s_tile_off
           !w_wait_dependency(p, T.dep, info.dep_idx + 1, s_tile_off, sm.abort_flag))
         break;
       for (int i = 0, s = st0; i < npre; ++i) {
-        issue_t(i, sm.stages + s * sbytes, &sm.full[s]);
+        issue_t(i, sm.stages + s * sbytes, &sm.full[s], s);
         if (++s == nst) s = 0;
       }
     }
@@ -321,7 +343,7 @@ __device__ void w_producer(const GemmParams& p, WSmem& sm, const int* s_tile_off
       uint8_t* st = sm.stages + stage * sbytes;
       mbar_arrive_expect_tx(&sm.full[stage], stage_tx);
       issue_w(kb, st);
-      issue_t(kb, st, &sm.full[stage]);
+      issue_t(kb, st, &sm.full[stage], stage);
       trace_mark(p, 0, static_cast<int>(issued));
       ++issued;
       if (++stage == nst) { stage = 0; phase ^= 1; }
@@ -339,6 +361,7 @@ __device__ void w_producer(const GemmParams& p, WSmem& sm, const int* s_tile_off
 }
 
 // ------------------------------------------------------------------ MMA issuer (1 thread)
+template <bool MX>
 __device__ void w_mma(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
   int stage = 0, us = 0, acc = 0;
   uint32_t phase = 0, uphase = 0, aphase = 0;
@@ -349,6 +372,8 @@ __device__ void w_mma(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
   const uint64_t desc_b0 = sdesc_sw128(smem_u32(sm.stages));
   const uint64_t desc_a0 = desc_b0 + ((2 * W::W_TILE) >> 4);
   const uint64_t STAGE_D = static_cast<uint64_t>(p.w_stage_bytes) >> 4;
+  // accumulator slots: one in MX launches (the scale ring takes the other half of TMEM)
+  constexpr int nacc = MX ? 1 : W::NACC;
   while (ok) {
     if (!mbar_wait(&sm.ufull[us], uphase, sm.abort_flag, p.err, p.timeout)) break;
     const WUnit info = sm.ring[us];
@@ -364,8 +389,9 @@ __device__ void w_mma(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
     const int kb1 = T.kb_total;
     const bool dual = info.dual != 0;  // two token tiles share the weight operand
     // the slot after `acc` (the second tile of a dual unit) and its phase parity
-    const int acc2 = acc + 1 == W::NACC ? 0 : acc + 1;
-    const uint32_t aphase2 = acc + 1 == W::NACC ? aphase ^ 1 : aphase;
+    const int acc2 = acc + 1 == nacc ? 0 : acc + 1;
+    const uint32_t aphase2 = acc + 1 == nacc ? aphase ^ 1 : aphase;
+    const bool mxu = MX && T.a_sf != nullptr;  // block-scaled FP8 unit
     if (!promote) {
       if (!mbar_wait_spin(&sm.tempty[acc], aphase ^ 1, sm.abort_flag, p.err, p.timeout)) break;
       if (dual &&
@@ -391,8 +417,25 @@ __device__ void w_mma(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
       const uint64_t off = static_cast<uint64_t>(stage) * STAGE_D;
       const uint32_t accum = promote ? static_cast<uint32_t>(gpos > 0)
                                      : static_cast<uint32_t>(kb > 0);
-      if (fp8) mma4_fp8(d, desc_a0 + off, desc_b0 + off, idesc, accum);
-      else mma4_bf16(d, desc_a0 + off, desc_b0 + off, idesc, accum);
+      if (mxu) {
+        // this stage's scale tiles into its TMEM columns beside the accumulator (tokens:
+        // lane m column m/32; weights: lane n%32 column 4 + n/32), then the four K = 32
+        // MMAs of the k-block, each with the scale byte of its 32-wide chunk
+        const uint32_t sfc = tmem_base + W::TN + static_cast<uint32_t>(stage * W::SF_COLS);
+        const uint32_t sfs = smem_u32(sm.sf + stage * W::SF_STAGE);
+        tmem_cp_32x128b_x4(sfc, sfs);
+        tmem_cp_32x128b_x4(sfc + 4, sfs + 512);
+        tmem_cp_32x128b_x4(sfc + 8, sfs + 1024);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          mma_mx(d, desc_a0 + off + 2 * j, desc_b0 + off + 2 * j,
+                 idesc_mx(W::TM, W::TN, j, j), sfc, sfc + 4,
+                 static_cast<uint32_t>(kb > 0 || j > 0));
+      } else if (fp8) {
+        mma4_fp8(d, desc_a0 + off, desc_b0 + off, idesc, accum);
+      } else {
+        mma4_bf16(d, desc_a0 + off, desc_b0 + off, idesc, accum);
+      }
       if (dual) {  // second token tile, same weights, into the next slot
         const uint32_t d2 = tmem_base + static_cast<uint32_t>(acc2 * W::TN);
         const uint64_t da2 = desc_a0 + off + (W::T_TILE >> 4);
@@ -404,16 +447,16 @@ __device__ void w_mma(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
       if (promote && ++gpos == kpg) {
         gpos = 0;
         tc_commit(&sm.tfull[acc]);
-        if (++acc == W::NACC) { acc = 0; aphase ^= 1; }
+        if (++acc == nacc) { acc = 0; aphase ^= 1; }
       }
     }
     if (!ok) break;
     if (!promote) {
       tc_commit(&sm.tfull[acc]);
-      if (++acc == W::NACC) { acc = 0; aphase ^= 1; }
+      if (++acc == nacc) { acc = 0; aphase ^= 1; }
       if (dual) {
         tc_commit(&sm.tfull[acc]);
-        if (++acc == W::NACC) { acc = 0; aphase ^= 1; }
+        if (++acc == nacc) { acc = 0; aphase ^= 1; }
       }
     }
   }
@@ -527,7 +570,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <bool DET>
+template <bool DET, bool MX>
 __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ew = warp - W::FIRST_EPI_WARP;
@@ -539,6 +582,7 @@ __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
   uint32_t uphase = 0, aphase = 0;
   SigState sg;
   const int G_L = p.L / 128, G_I = p.I / 128;
+  constexpr int nacc = MX ? 1 : W::NACC;
 
   for (;;) {
     if (!mbar_wait(&sm.ufull[us], uphase, sm.abort_flag, p.err, p.timeout)) return;
@@ -627,7 +671,7 @@ __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.tempty[acc]);
-          if (++acc == W::NACC) { acc = 0; aphase ^= 1; }
+          if (++acc == nacc) { acc = 0; aphase ^= 1; }
   #pragma unroll
           for (int c = 0; c < 4; ++c)
   #pragma unroll
@@ -646,12 +690,53 @@ __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.tempty[acc]);
-        if (++acc == W::NACC) { acc = 0; aphase ^= 1; }
+        if (++acc == nacc) { acc = 0; aphase ^= 1; }
         if (ew == 0 && lane == 0) trace_mark(p, 2, steps++);
       }
 
       // ---- unit end (this thread: one token, 64 gate/up pairs or 128 features)
-      if (kind == TASK_ROUTED_L1) {
+      if (MX && kind == TASK_ROUTED_L1) {
+        // SwiGLU, then MX e4m3: one power-of-two scale per 32 outputs, 2^(floor(log2 amax)
+        // - 8); this thread's 64 outputs are two whole groups, so no other thread is
+        // involved.  The scale bytes go to the routed L2 units' token scale tile of this
+        // routed tile: k-block = this 128-output tile, chunk = 2 * half + group.
+  #pragma unroll
+        for (int i = 0; i < 64; ++i) a[i] = silu_fast(a[i]) * a[64 + i];
+        int ex[2];
+        float inv[2];
+  #pragma unroll
+        for (int gq = 0; gq < 2; ++gq) {
+          float m = 0.f;
+  #pragma unroll
+          for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(a[32 * gq + i]));
+          ex[gq] = mx_exponent(m);
+          inv[gq] = pow2_exact(-ex[gq]);
+        }
+        uint32_t sfw = 0x7F7Fu;  // rows past the tile's pairs: scale 1
+        if (valid) {
+          const size_t pp = static_cast<size_t>(row0 + tok);
+          const size_t col = static_cast<size_t>(info.ftile) * 128 + half * 64;
+          uint4* dq = reinterpret_cast<uint4*>(p.aq + pp * p.I + col);
+  #pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float iv = inv[c >> 1];  // 16 outputs per c: groups of 32 are c = 0,1 | 2,3
+            uint32_t w4[4];
+  #pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int i = c * 16 + q * 4;
+              w4[q] = f32x2_to_e4m3x2(a[i] * iv, a[i + 1] * iv) |
+                      (f32x2_to_e4m3x2(a[i + 2] * iv, a[i + 3] * iv) << 16);
+            }
+            dq[c] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
+          sfw = static_cast<uint32_t>(ex[0] + 127) | (static_cast<uint32_t>(ex[1] + 127) << 8);
+        }
+        uint8_t* tsf = p.asf_t +
+                       (static_cast<size_t>(dep_idx) * G_I + info.ftile) * 512 +
+                       (tok & 31) * 16 + 4 * (tok >> 5) + 2 * half;
+        *reinterpret_cast<uint16_t*>(tsf) = static_cast<uint16_t>(sfw);
+        if (p.l1_done != nullptr) w_signal(p, sm, sg, p.l1_done + dep_idx, ew, lane);
+      } else if (kind == TASK_ROUTED_L1) {
         // SwiGLU, then e4m3 with one scale per token per 128 outputs (both halves' amax)
         float m = 0.f;
   #pragma unroll
@@ -778,7 +863,7 @@ __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
   }
 }
 
-template <bool DET>
+template <bool DET, bool MX>
 __global__ void __launch_bounds__(W::THREADS, 1) wide_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   WSmem sm(smem_raw);
@@ -837,15 +922,15 @@ __global__ void __launch_bounds__(W::THREADS, 1) wide_kernel(const __grid_consta
         s_off[i] = p.off[i];
       }
       __syncwarp();
-      if (lane == 0) w_producer(p, sm, s_tile_off, s_off);
+      if (lane == 0) w_producer<MX>(p, sm, s_tile_off, s_off);
     } else if (warp == 1) {
-      if (lane == 0) w_mma(p, sm, tmem_base);
+      if (lane == 0) w_mma<MX>(p, sm, tmem_base);
     } else if (warp == W::SIGNAL_WARP) {
       if (lane == 0) w_signaller(p, sm);
     }
   } else {
     regs_inc<W::REGS_EPI>();
-    w_epilogue<DET>(p, sm, tmem_base);
+    w_epilogue<DET, MX>(p, sm, tmem_base);
   }
 
   tc_fence_before();
@@ -861,20 +946,32 @@ __global__ void __launch_bounds__(W::THREADS, 1) wide_kernel(const __grid_consta
 
 static_assert(WSmem::bytes() + 2 * (MAX_E + 1) * 4 <= 227 * 1024, "shared memory budget");
 
-int wide_kernel_regs() {  // both instantiations must launch with the planned registers
-  cudaFuncAttributes a, b;
-  if (cudaFuncGetAttributes(&a, wide_kernel<false>) != cudaSuccess) return -1;
-  if (cudaFuncGetAttributes(&b, wide_kernel<true>) != cudaSuccess) return -1;
-  return a.numRegs == b.numRegs ? a.numRegs : -1;
+int wide_kernel_regs() {  // every instantiation must launch with the planned registers
+  const void* k[] = {reinterpret_cast<const void*>(wide_kernel<false, false>),
+                     reinterpret_cast<const void*>(wide_kernel<true, false>),
+                     reinterpret_cast<const void*>(wide_kernel<false, true>),
+                     reinterpret_cast<const void*>(wide_kernel<true, true>)};
+  int regs = -1;
+  for (const void* f : k) {
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, f) != cudaSuccess) return -1;
+    if (regs >= 0 && a.numRegs != regs) return -1;
+    regs = a.numRegs;
+  }
+  return regs;
 }
 
 bool wide_regs_ok(int regs) { return regs == W::LAUNCH_REGS; }
 
 cudaError_t launch_wide(const GemmParams& p, int grid, cudaStream_t s, bool pdl) {
   const int smem = WSmem::bytes();
-  const bool det = p.yw != nullptr;  // deterministic combine: its own instantiation
-  cudaError_t e = cudaFuncSetAttribute(det ? wide_kernel<true> : wide_kernel<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // the deterministic combine and the MX launches are instantiations of their own
+  const bool det = p.yw != nullptr, mx = p.mx != 0;
+  const void* f = det ? (mx ? reinterpret_cast<const void*>(wide_kernel<true, true>)
+                            : reinterpret_cast<const void*>(wide_kernel<true, false>))
+                      : (mx ? reinterpret_cast<const void*>(wide_kernel<false, true>)
+                            : reinterpret_cast<const void*>(wide_kernel<false, false>));
+  cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -886,8 +983,10 @@ cudaError_t launch_wide(const GemmParams& p, int grid, cudaStream_t s, bool pdl)
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return det ? cudaLaunchKernelEx(&cfg, wide_kernel<true>, p)
-             : cudaLaunchKernelEx(&cfg, wide_kernel<false>, p);
+  if (det) return mx ? cudaLaunchKernelEx(&cfg, wide_kernel<true, true>, p)
+                     : cudaLaunchKernelEx(&cfg, wide_kernel<true, false>, p);
+  return mx ? cudaLaunchKernelEx(&cfg, wide_kernel<false, true>, p)
+            : cudaLaunchKernelEx(&cfg, wide_kernel<false, false>, p);
 }
 
 }  // namespace klt
