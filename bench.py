@@ -153,7 +153,8 @@ def algorithmic_bytes(cfg, cnt: np.ndarray, M: int):
     H, L, I, Is, k, E = cfg.H, cfg.L, cfg.I, cfg.Is, cfg.topk, cfg.E
     touched = int((cnt > 0).sum())
     Mk = M * k
-    wb = 1.0 if cfg.routed_fmt == "fp8" else 0.5 + 1.0 / 16
+    # routed weight bytes per element: codes plus scales
+    wb = {"fp8": 1.0, "mxfp8": 1.0 + 1.0 / 32, "nvfp4": 0.5 + 1.0 / 16}[cfg.routed_fmt]
     w13 = touched * 2 * I * L * wb
     w2 = touched * L * I * wb
     g1 = 2 * Is * H * 2 + M * H * 2 + w13 + Mk * L + Mk * I + M * Is * 2
@@ -180,6 +181,8 @@ HEADLINE = "decode_m16_e64_k8_fp8"
 def dtype_of(cfg) -> str:
     if cfg.routed_fmt == "fp8":
         return "fp8e4m3+bf16 (fp32 accumulate)"
+    if cfg.routed_fmt == "mxfp8":
+        return "mxfp8 (e4m3, power-of-two scales per 32, block-scaled MMA) + bf16 (fp32 accumulate)"
     return "nvfp4 weights (bf16-exact MMA) + fp8e4m3 activations + bf16 (fp32 accumulate)"
 
 
@@ -368,11 +371,12 @@ def measure(cfg, args, ws, rank, local, flush, with_cpu: bool, hidden: bool = Fa
             per[j] += evs[i][j].elapsed_time(evs[i][j + 1])
     per /= args.steps
     nt = nl - (1 if hidden else 0)  # launches of the tail itself
-    fused = nt <= 5
-    hist = nt in (5, 8)
+    mx = cfg.routed_fmt == "mxfp8"  # routed and dense GEMM launches
+    gemms = (["gemm_routed", "gemm_dense"] if mx else ["gemm_fused"]) if nt <= 5 + mx else \
+        ["gemm_l1", "gemm_l2", "norm", "gemm_out"]
+    hist = nt == 4 + len(gemms)
     names = ((["proj"] if hidden else []) + ["route"] + (["perm_hist"] if hist else []) +
-             ["perm_scatter", "perm_gather"] +
-             (["gemm_fused"] if fused else ["gemm_l1", "gemm_l2", "norm", "gemm_out"]))
+             ["perm_scatter", "perm_gather"] + gemms)
     per_launch_us = {n: round(float(v) * 1e3, 2) for n, v in zip(names, per)}
 
     # ---- end to end through the public API with host buffers
@@ -406,7 +410,11 @@ def measure(cfg, args, ws, rank, local, flush, with_cpu: bool, hidden: bool = Fa
     cnt_h = cnt.cpu().numpy()
     ab = algorithmic_bytes(cfg, cnt_h, M)
     hbm, bf16_tf, peak_src = _peaks()
-    if "gemm_fused" in per_launch_us:
+    if "gemm_routed" in per_launch_us:  # MX layers: the two GEMM launches together
+        dom = "gemm_routed+gemm_dense"
+        per_launch_us[dom] = round(per_launch_us["gemm_routed"] + per_launch_us["gemm_dense"], 2)
+        dom_bytes = ab["gemm_l1"] + ab["gemm_l2"] + ab["norm"] + ab["gemm_out"]
+    elif "gemm_fused" in per_launch_us:
         dom = "gemm_fused"
         dom_bytes = ab["gemm_l1"] + ab["gemm_l2"] + ab["norm"] + ab["gemm_out"]
     else:

@@ -372,7 +372,9 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
 int klt_launch_count(const klt_handle* h, int32_t M) {
   if (!h || M <= 0) return 0;
   const int nblocks = (M * h->d.topk + PERM_BLOCK - 1) / PERM_BLOCK;
-  const int gemm_launches = (h->flags & KLT_FLAG_PHASED) ? 4 : 1;  // phased: 3 GEMMs + norm
+  // phased: 3 GEMMs + norm; MX layers: routed and dense launches
+  const int gemm_launches = (h->flags & KLT_FLAG_PHASED) ? 4
+                            : (h->d.routed_fmt == KLT_FMT_MXFP8 ? 2 : 1);
   return 3 + gemm_launches + (nblocks > 1 ? 1 : 0);
 }
 
@@ -574,10 +576,7 @@ int forward_impl(klt_handle* h, const void* x, const void* z, const float* logit
     gw.ntasks = 5;
     // prefill-size batches: pairs of token tiles share each staged weight tile of the
     // BF16 tasks (3 stages of 64 KB); otherwise 4 stages of 48 KB
-    // MX launches keep one accumulator slot: the other half of TMEM holds the scale ring
-    // (so no dual units either)
-    const bool dual = !mx && ntiles >= kDualMinTiles;
-    gw.mx = mx ? 1 : 0;
+    const bool dual = ntiles >= kDualMinTiles;
     gw.asf_t = h->asf_t;
     gw.w_stages = dual ? 3 : 4;
     gw.w_stage_bytes = dual ? 64 * 1024 : 48 * 1024;
@@ -672,7 +671,34 @@ int forward_impl(klt_handle* h, const void* x, const void* z, const float* logit
     gw.gamma = h->gamma;
     gw.nrm = h->n;
     gw.eps = d.eps;
-    KLT_LAUNCH(launch_wide(gw, grid, s, pdl));
+    if (!mx) {
+      KLT_LAUNCH(launch_wide(gw, grid, s, pdl));
+    } else {
+      // MX layers: the block-scaled routed units keep one accumulator slot (their scale
+      // ring takes the other half of TMEM), so they run as a launch of their own; the BF16
+      // shared L1, norm and output GEMM follow in a second launch with two slots and dual
+      // token tiles.  The dependency counters carry over (zeroed once by routing).
+      GemmParams gr = gw, gd = gw;
+      gr.mx = 1;
+      gr.ntasks = 2;
+      gr.task[0] = gw.task[1];  // routed L1
+      gr.task[1] = gw.task[2];  // routed L2
+      gr.w_stages = 4;
+      gr.w_stage_bytes = 48 * 1024;
+      gr.pf_ptr = nullptr;
+      gr.pf_bytes = 0;
+      gd.mx = 0;
+      gd.ntasks = 3;
+      gd.task[0] = gw.task[0];  // shared L1
+      gd.task[1] = gw.task[3];  // norm
+      gd.task[2] = gw.task[4];  // output
+      gd.sched = h->sched + 4;
+      gd.pf_ptr = nullptr;
+      gd.pf_bytes = 0;
+      gd.trace = trace ? trace + trace_launch : nullptr;
+      KLT_LAUNCH(launch_wide(gr, grid, s, pdl));
+      KLT_LAUNCH(launch_wide(gd, grid, s, pdl));
+    }
   } else {
     GemmParams g1 = gp, g2 = gp, g3 = gp;
     // ---- GEMM 1: shared L1 (bf16, split-K) + routed L1 (fp8, SwiGLU + act quant)
