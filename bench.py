@@ -120,12 +120,16 @@ class Clocks:
 
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the dominant
-# kernel, from one ncu capture of `bench.py --steps 2 --warmup 3 --no-cpu-baseline` on the
-# workload, valid only while the kernel sources hash to the recorded digest.
+# kernel (MX layers: both GEMM launches), from one ncu launch-list capture of
+# `bench.py --workload W --steps 2 --warmup 3 --no-cpu-baseline` (the steady-state forward),
+# valid only while the kernel sources hash to the recorded digest.
 NCU_TRAFFIC = {
-    ("decode_m16_e64_k8_fp8", "gemm_fused"): (716931584, "2b0c9976ae05ea51"),
-    ("decode_m128_e64_k8_fp8_biased", "gemm_fused"): (817117440, "2b0c9976ae05ea51"),
-    ("prefill_m4096_e64_k8_fp8_zipf", "gemm_fused"): (1727170304, "2b0c9976ae05ea51"),
+    ("decode_m16_e64_k8_fp8", "gemm_fused"): (715912448, "6b7c111e8854dec9"),
+    ("tiny_m4_e16_k4", "gemm_fused"): (190675200, "6b7c111e8854dec9"),
+    ("decode_m128_e64_k8_fp8_biased", "gemm_fused"): (836889344, "6b7c111e8854dec9"),
+    ("prefill_m4096_e64_k8_fp8_zipf", "gemm_fused"): (1629829888, "6b7c111e8854dec9"),
+    ("prefill_m8192_e128_k8_nvfp4", "gemm_fused"): (6860687872, "6b7c111e8854dec9"),
+    ("prefill_m4096_e64_k8_mxfp8_zipf", "gemm_routed+gemm_dense"): (1673564672, "6b7c111e8854dec9"),
 }
 KERNEL_SOURCES = ("klt_gemm.cu", "klt_wide.cu", "klt_device.cuh", "klt_internal.h", "klt_api.cu",
                   "klt_route.cu")
