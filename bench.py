@@ -3,7 +3,8 @@
 One step = one klt_forward (routing, permutation, routed FP8/NVFP4 experts, combine,
 RMSNorm, up-projection + BF16 shared expert) over one batch of synthetic tokens.  Prints
 one JSON line.  By default every workload is measured in the same run (tiny M=4, decode
-M=16, decode M=128, prefill M=4096, prefill M=8192 NVFP4); the line's top-level figures
+M=16, decode M=128, prefill M=4096, prefill M=8192 NVFP4, plus decode M=16 from the hidden
+state alone and prefill M=4096 with MXFP8 routed weights); the line's top-level figures
 are the decode batch of 16 tokens (E=64, top-8, routed intermediate 1024 with FP8 128x128
 block scales, shared intermediate 2048, H=7168, L=3584) and `workloads` holds every
 workload's record (roofline, end to end, clocks, the oracle on the host cores).
@@ -508,8 +509,9 @@ def main():
 
     from latent_moe_layer_route_gb300 import configs
     # a workload name with "+hidden" runs that workload from the hidden state alone
-    if args.workload == "all":
-        names = [c.name for c in configs.ALL] + [HEADLINE + "+hidden"]
+    if args.workload == "all":  # the five workloads, the step before the tail, the MX variant
+        names = [c.name for c in configs.ALL] + [HEADLINE + "+hidden",
+                                                 configs.PREFILL_M4096_MX.name]
     else:  # one name, or several separated by commas (the first is the headline)
         names = args.workload.split(",")
     cfgs = [(configs.BY_NAME[n.split("+")[0]], n.endswith("+hidden")) for n in names]

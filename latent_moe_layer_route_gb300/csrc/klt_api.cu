@@ -278,9 +278,8 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
     KLT_ALLOC(h->asf_t, static_cast<int64_t>(h->sf_tiles) * (I / 128) * 512);
   }
   if (w->w_lat) {
-    // rows: W_lat (L), W_gate (E), zero rows up to a multiple of 256 (two 128-row tiles per
-    // projection unit)
-    h->proj_rows = static_cast<int>((L + E + 255) / 256 * 256);
+    // rows: W_lat (L), W_gate (E), zero rows up to a multiple of 128 (one output tile)
+    h->proj_rows = static_cast<int>((L + E + 127) / 128 * 128);
     KLT_ALLOC(h->w_proj, static_cast<int64_t>(h->proj_rows) * H * 2);
     KLT_ALLOC(h->zp, Mx * L * 2);
     KLT_ALLOC(h->lgp, Mx * E * 4);
@@ -462,10 +461,8 @@ int forward_impl(klt_handle* h, const void* x, const void* z, const float* logit
     gpj.lgp = h->lgp;
     GemmTask& P = gpj.task[0];
     P.kind = TASK_PROJ;
-    P.pair = 1;
-    P.a_rb_up = 1;
-    P.a_rb_step = 2;
-    P.ftiles = h->proj_rows / 256;
+    P.a_rb_step = 1;
+    P.ftiles = h->proj_rows / 128;
     P.kb_total = H / 64;
     P.kb_split0 = P.kb_total;
     P.a_kb[0] = P.a_kb[1] = H / 64;
@@ -473,7 +470,19 @@ int forward_impl(klt_handle* h, const void* x, const void* z, const float* logit
     if (!encode_2d(&P.tmB[0], x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, H, pbn))
       return KLT_ERR_CUDA;
     P.tmB[1] = P.tmB[0];
-    plan_split(P, (M + pbn - 1) / pbn, h->num_sms, pbn);
+    // split in K so that the units fill the SMs in one wave (a second wave doubles the
+    // launch's time at decode sizes); single 128-row tiles keep the partials that the last
+    // arriver of a tile sums small (a split of 5 at decode: 5 x 8 KB per tile)
+    {
+      const int pt = (M + pbn - 1) / pbn;
+      const int tiles = pt * P.ftiles;
+      int ks = std::max(1, std::min(P.kb_total / 4, h->num_sms / std::max(1, tiles)));
+      while (ks > 1 && tiles * ks > kMaxSplitUnits) --ks;
+      P.kb_per_split = (P.kb_total + ks - 1) / ks;
+      P.ksplit = (P.kb_total + P.kb_per_split - 1) / P.kb_per_split;
+      P.ntiles = pt;
+      P.units = tiles * P.ksplit;
+    }
     KLT_LAUNCH(launch_gemm(gpj, pbn, h->num_sms, s, pdl));
   }
 

@@ -314,7 +314,7 @@ __device__ bool wait_dependency(const GemmParams& p, int dep, int idx, const int
 // ------------------------------------------------------------------ producer (1 thread)
 template <int BN>
 __device__ void run_producer(const GemmParams& p, Smem<BN>& sm, const int* s_tile_off,
-                             const int* s_off) {
+                             const int* s_off, int u0) {
   using C = Cfg<BN>;
   const uint64_t pol_w = policy_evict_first();
   const uint64_t pol_t = policy_evict_last();
@@ -326,14 +326,12 @@ __device__ void run_producer(const GemmParams& p, Smem<BN>& sm, const int* s_til
   bool stalled = false;
   const bool streamk = p.task[0].streamk != 0;
   long long sk_x = 0, sk_end = 0;
-  int u = 0;
+  int u = u0;  // first unit, claimed by the caller
   if (streamk) {
     if (static_cast<int>(blockIdx.x) < p.task[0].sk_grid) {
       sk_x = sk_begin(p.task[0].sk_total, p.task[0].sk_grid, blockIdx.x);
       sk_end = sk_begin(p.task[0].sk_total, p.task[0].sk_grid, blockIdx.x + 1);
     }
-  } else {
-    u = atomicAdd(p.sched, 1);
   }
   for (;;) {
     UnitInfo info;
@@ -880,19 +878,56 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
       named_bar_sync(bar_grp, C::GROUP_THREADS);
       if (!sm.last_flag[grp]) continue;
       __threadfence();
-#pragma unroll
-      for (int j = 0; j < COLS; ++j) { g[j] = 0.f; u[j] = 0.f; }
-      for (int s = 0; s < info.ncontrib; ++s) {
+      // contributor s's partial: this thread's row of the part's first column
+      auto part = [&](int s) -> const float* {
         const size_t idx =
             T.streamk ? static_cast<size_t>(sk_slot(T.sk_total, T.sk_grid, T.kb_total,
                                                     info.cfirst + s,
                                                     info.tile_id - T.ws_tile_base))
                       : static_cast<size_t>(info.tile_id - T.ws_tile_base) * info.ncontrib + s;
-        const float* ps = p.ws + T.ws_off + idx * tile_floats;
+        return p.ws + T.ws_off + idx * tile_floats + static_cast<size_t>(c0) * 128 + row;
+      };
+#pragma unroll
+      for (int j = 0; j < COLS; ++j) { g[j] = 0.f; u[j] = 0.f; }
+      // The partials are added in contributor order 0, 1, ... whatever the batching.  With
+      // few columns per thread the loads of several contributors are issued before any of
+      // them is added, so their L2 round trips overlap instead of forming a chain (a tile
+      // split ten ways otherwise pays ten round trips at the end of the launch).
+      int s = 0;
+      if constexpr (COLS <= 16) {
+        // paired tiles: two contributors per batch (both parts); single tiles: four
+        const int nb = pair ? 2 : 4;
+        for (; s + nb <= info.ncontrib; s += nb) {
+          const float* pa = part(s);
+          const float* pb = part(s + 1);
+          const float* pc = pair ? pa + static_cast<size_t>(BN) * 128 : part(s + 2);
+          const float* pd = pair ? pb + static_cast<size_t>(BN) * 128 : part(s + 3);
+          float va[COLS], vb[COLS], vc[COLS], vd[COLS];
+#pragma unroll
+          for (int j = 0; j < COLS; ++j) {
+            va[j] = __ldcg(pa + static_cast<size_t>(j) * 128);
+            vb[j] = __ldcg(pb + static_cast<size_t>(j) * 128);
+            vc[j] = __ldcg(pc + static_cast<size_t>(j) * 128);
+            vd[j] = __ldcg(pd + static_cast<size_t>(j) * 128);
+          }
+          if (pair) {
+#pragma unroll
+            for (int j = 0; j < COLS; ++j) {
+              g[j] = (g[j] + va[j]) + vb[j];
+              u[j] = (u[j] + vc[j]) + vd[j];
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < COLS; ++j) g[j] = (((g[j] + va[j]) + vb[j]) + vc[j]) + vd[j];
+          }
+        }
+      }
+      for (; s < info.ncontrib; ++s) {
+        const float* ps = part(s);
 #pragma unroll
         for (int j = 0; j < COLS; ++j) {
-          g[j] += __ldcg(ps + static_cast<size_t>(c0 + j) * 128 + row);
-          if (pair) u[j] += __ldcg(ps + static_cast<size_t>(BN + c0 + j) * 128 + row);
+          g[j] += __ldcg(ps + static_cast<size_t>(j) * 128);
+          if (pair) u[j] += __ldcg(ps + static_cast<size_t>(BN + j) * 128);
         }
       }
     }
@@ -1048,17 +1083,36 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
   pdl_wait();
   pdl_trigger();
 
+  // Routing tile offsets for the producer's unit decode, read once per CTA by warp 0
+  // before the control warps give up registers.
+  __shared__ int s_tile_off[MAX_E + 1], s_off[MAX_E + 1];
+  int u0 = 0;
+  if (warp == 0) {
+    // the first unit claim and the offset loads are issued together (all independent),
+    // so the launch pays one round trip before its first copy instead of several
+    u0 = (lane == 0 && !p.task[0].streamk) ? atomicAdd(p.sched, 1) : 0;
+    constexpr int NL = (MAX_E + 1 + 31) / 32;
+    int to[NL], of[NL];
+#pragma unroll
+    for (int i = 0; i < NL; ++i) {
+      const int k = lane + 32 * i;
+      to[i] = k <= p.E ? p.tile_off[k] : 0;
+      of[i] = k <= p.E ? p.off[k] : 0;
+    }
+#pragma unroll
+    for (int i = 0; i < NL; ++i) {
+      const int k = lane + 32 * i;
+      if (k <= p.E) {
+        s_tile_off[k] = to[i];
+        s_off[k] = of[i];
+      }
+    }
+    __syncwarp();
+  }
   if (warp < C::FIRST_EPI_WARP) {
     regs_dec<C::REGS_CTRL>();
     if (warp == 0) {
-      // routing tile offsets for the producer's unit decode, read once per CTA
-      __shared__ int s_tile_off[MAX_E + 1], s_off[MAX_E + 1];
-      for (int i = lane; i <= p.E; i += 32) {
-        s_tile_off[i] = p.tile_off[i];
-        s_off[i] = p.off[i];
-      }
-      __syncwarp();
-      if (lane == 0) run_producer<BN>(p, sm, s_tile_off, s_off);
+      if (lane == 0) run_producer<BN>(p, sm, s_tile_off, s_off, u0);
     } else if (warp == 1) {
       if (lane == 0) run_mma<BN>(p, sm, tmem_base);
     } else if (warp - C::SIGNAL_WARP < C::NGROUPS && lane == 0) {

@@ -237,7 +237,7 @@ __device__ bool w_wait_dependency(const GemmParams& p, int dep, int idx, const i
 // other launches keep their code and registers unchanged).
 template <bool MX>
 __device__ void w_producer(const GemmParams& p, WSmem& sm, const int* s_tile_off,
-                           const int* s_off) {
+                           const int* s_off, int u0) {
   // weights are re-read by every token tile of their expert, tokens by every feature tile
   const uint64_t pol = policy_evict_normal();
   const uint64_t pol_w = policy_evict_last();
@@ -248,7 +248,7 @@ __device__ void w_producer(const GemmParams& p, WSmem& sm, const int* s_tile_off
   int published = 0;
   int dummy_abort = 0;
   bool stalled = false;
-  int u = atomicAdd(p.sched, 1);
+  int u = u0;  // first unit, claimed by the caller
   for (;;) {
     const WUnit info = w_decode(p, s_tile_off, s_off, u);
     // claim the next unit now so the counter round trip overlaps this unit's copies
@@ -912,17 +912,36 @@ __global__ void __launch_bounds__(W::THREADS, 1) wide_kernel(const __grid_consta
   pdl_wait();
   pdl_trigger();
 
+  // Routing tile offsets for the producer's unit decode, read once per CTA by warp 0
+  // before the control warps give up registers.
+  __shared__ int s_tile_off[MAX_E + 1], s_off[MAX_E + 1];
+  int u0 = 0;
+  if (warp == 0) {
+    // the first unit claim and the offset loads are issued together (all independent),
+    // so the launch pays one round trip before its first copy instead of several
+    u0 = lane == 0 ? atomicAdd(p.sched, 1) : 0;
+    constexpr int NL = (MAX_E + 1 + 31) / 32;
+    int to[NL], of[NL];
+#pragma unroll
+    for (int i = 0; i < NL; ++i) {
+      const int k = lane + 32 * i;
+      to[i] = k <= p.E ? p.tile_off[k] : 0;
+      of[i] = k <= p.E ? p.off[k] : 0;
+    }
+#pragma unroll
+    for (int i = 0; i < NL; ++i) {
+      const int k = lane + 32 * i;
+      if (k <= p.E) {
+        s_tile_off[k] = to[i];
+        s_off[k] = of[i];
+      }
+    }
+    __syncwarp();
+  }
   if (warp < W::FIRST_EPI_WARP) {
     regs_dec<W::REGS_CTRL>();
     if (warp == 0) {
-      // routing tile offsets for the producer's unit decode, read once per CTA
-      __shared__ int s_tile_off[MAX_E + 1], s_off[MAX_E + 1];
-      for (int i = lane; i <= p.E; i += 32) {
-        s_tile_off[i] = p.tile_off[i];
-        s_off[i] = p.off[i];
-      }
-      __syncwarp();
-      if (lane == 0) w_producer<MX>(p, sm, s_tile_off, s_off);
+      if (lane == 0) w_producer<MX>(p, sm, s_tile_off, s_off, u0);
     } else if (warp == 1) {
       if (lane == 0) w_mma<MX>(p, sm, tmem_base);
     } else if (warp == W::SIGNAL_WARP) {
