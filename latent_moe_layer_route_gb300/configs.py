@@ -13,6 +13,7 @@ from dataclasses import dataclass, replace
 FMT_FP8 = "fp8"      # e4m3 codes with one fp32 scale per 128x128 block
 FMT_NVFP4 = "nvfp4"  # e2m1 codes, e4m3 scale per 16 K-elements, fp32 per-matrix scale
 FMT_MXFP8 = "mxfp8"  # e4m3 codes, one power-of-two (UE8M0) scale per 32 K-elements
+FMT_W4A4 = "nvfp4_w4a4"  # NVFP4 weights and NVFP4 activations (e2m1, e4m3 scale per 16)
 
 
 @dataclass(frozen=True)
@@ -50,7 +51,12 @@ ALL = [TINY_M4, DECODE_M16, DECODE_M128, PREFILL_M4096, PREFILL_M8192_NVFP4]
 DECODE_M16_MX = DECODE_M16.with_(name="decode_m16_e64_k8_mxfp8", routed_fmt=FMT_MXFP8)
 PREFILL_M4096_MX = PREFILL_M4096.with_(name="prefill_m4096_e64_k8_mxfp8_zipf",
                                        routed_fmt=FMT_MXFP8)
-VARIANTS = [DECODE_M16_MX, PREFILL_M4096_MX]
+# The FP4 x FP4 variant of the NVFP4 prefill workload: the same weights, activations
+# quantised to NVFP4 too, so the routed GEMMs run block-scaled at the FP4 rate.
+DECODE_M16_W4A4 = DECODE_M16.with_(name="decode_m16_e64_k8_nvfp4_w4a4", routed_fmt=FMT_W4A4)
+PREFILL_M8192_W4A4 = PREFILL_M8192_NVFP4.with_(name="prefill_m8192_e128_k8_nvfp4_w4a4",
+                                               routed_fmt=FMT_W4A4)
+VARIANTS = [DECODE_M16_MX, PREFILL_M4096_MX, DECODE_M16_W4A4, PREFILL_M8192_W4A4]
 BY_NAME = {c.name: c for c in ALL + VARIANTS}
 
 # Small shapes (every width one or two 128-tiles) used by fast parity and oracle tests.

@@ -26,7 +26,7 @@ from typing import Dict, Optional
 import numpy as np
 import torch
 
-from .configs import FMT_FP8, FMT_MXFP8, FMT_NVFP4, TailConfig
+from .configs import FMT_FP8, FMT_MXFP8, FMT_NVFP4, FMT_W4A4, TailConfig
 
 __all__ = ["make_activations", "make_weights", "make_inputs", "make_projection_weights",
            "fp8_block_quantize", "mx_quantize", "nvfp4_quantize", "expert_load"]
@@ -157,7 +157,7 @@ def make_weights(cfg: TailConfig) -> Dict[str, torch.Tensor]:
         for e in range(E):
             w2_q[e], w2_sx[e] = mx_quantize(_normal(rng, (L, I), 1 / math.sqrt(I)))
         w.update(w13_q=w13_q, w13_sx=w13_sx, w2_q=w2_q, w2_sx=w2_sx)
-    elif cfg.routed_fmt == FMT_NVFP4:
+    elif cfg.routed_fmt in (FMT_NVFP4, FMT_W4A4):  # the same NVFP4 weights
         w13_q = torch.empty((E, 2 * I, L // 2), dtype=torch.uint8)
         w13_sb = torch.empty((E, 2 * I, L // 16), dtype=torch.uint8)
         w13_g = torch.empty(E, dtype=torch.float32)

@@ -80,3 +80,23 @@ def unpack_e2m1(packed) -> np.ndarray:
     out[..., 0::2] = p & 0xF
     out[..., 1::2] = p >> 4
     return out
+
+
+def e2m1_encode(v) -> np.ndarray:
+    """float values -> 4-bit e2m1 codes (one per array element): nearest of the eight
+    magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6, a tie going to the code with an even mantissa
+    bit, saturating at 6.  The sign bit is set only for a non-zero magnitude, so a value
+    that rounds to zero has the single code 0.  Magnitudes are located by searching the
+    sorted value table; a tie is detected as equal distance to the two neighbours."""
+    x = np.asarray(v, dtype=np.float64)
+    a = np.minimum(np.abs(x), 6.0)
+    mags = _E2M1_TABLE[:8]                          # codes 0..7, increasing magnitudes
+    hi = np.clip(np.searchsorted(mags, a, side="left"), 1, 7)
+    lo = hi - 1
+    d_lo = a - mags[lo]
+    d_hi = mags[hi] - a
+    take_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(take_hi, hi, lo).astype(np.int64)
+    sign = np.where((x < 0) & (code > 0), 8, 0)
+    return (code | sign).astype(np.uint8)
+

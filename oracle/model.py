@@ -24,6 +24,11 @@ PR 1062 "MNNVL CuTe-DSL finalize tail" (commit notes and Summary)):
 7. out = up-projection + shared output (the oracle rounds nothing here; the tail emits
    bf16).
 
+Format variants of steps 2 and 3 (DeepGEMM PR 416, Summary: the FP8/FP4 MegaMoE path):
+MXFP8 quantises activations per 32 with power-of-two scales (OCP Microscaling rule), and
+the FP4 x FP4 format quantises them to NVFP4 (e2m1, one e4m3 scale per 16) like its
+weights.
+
 Every product and sum runs in float64 on exactly dequantised weights.
 """
 from __future__ import annotations
@@ -32,11 +37,11 @@ from typing import Dict, Iterable, Optional
 
 import numpy as np
 
-from .codecs import e2m1_decode, e4m3_decode, e4m3_encode, unpack_e2m1
+from .codecs import e2m1_decode, e2m1_encode, e4m3_decode, e4m3_encode, unpack_e2m1
 
 __all__ = ["route", "permutation", "quant_per128", "silu", "dequant_fp8_blocks",
            "dequant_nvfp4", "rmsnorm", "swiglu_mlp", "tail", "to_f64", "latent_inputs",
-           "bf16_round", "quant_mx", "dequant_mx"]
+           "bf16_round", "quant_mx", "dequant_mx", "quant_nvfp4", "dequant_nvfp4_act"]
 
 
 def to_f64(t) -> np.ndarray:
@@ -154,6 +159,32 @@ def dequant_mx(q, sb) -> np.ndarray:
     return (e4m3_decode(q).reshape(n, C // 32, 32) * scale[..., None]).reshape(n, C)
 
 
+def quant_nvfp4(v32):
+    """NVFP4 activation quantisation (e2m1 elements, one e4m3 scale per 16, no tensor-wide
+    scale): per row, per 16 columns, s = e4m3(fp32(amax / 6)) (nearest even, saturating
+    at 448); elements q = e2m1(fp32(v / s)), nearest even, saturating at 6, no negative
+    zero.  A block whose scale is zero (amax below the smallest e4m3 step) has all codes 0.
+    Returns (codes uint8 [n,C], one 4-bit code per element; scale bytes uint8 [n,C/16])."""
+    v = np.asarray(v32, dtype=np.float32)
+    n, C = v.shape
+    g = v.reshape(n, C // 16, 16)
+    amax = np.abs(g).max(axis=-1)
+    sb = e4m3_encode((amax / np.float32(6.0)).astype(np.float32))
+    s = e4m3_decode(sb).astype(np.float32)
+    safe = np.where(s == 0, np.float32(1.0), s)
+    quot = (g / safe[..., None]).astype(np.float32)
+    q = np.where((s == 0)[..., None], np.uint8(0), e2m1_encode(quot))
+    return q.reshape(n, C).astype(np.uint8), sb
+
+
+def dequant_nvfp4_act(q, sb) -> np.ndarray:
+    """e2m1 codes [n,C] (one per element) with e4m3 scale bytes [n,C/16] -> float64."""
+    q = np.asarray(q)
+    n, C = q.shape
+    return (e2m1_decode(q).reshape(n, C // 16, 16)
+            * e4m3_decode(sb)[..., None]).reshape(n, C)
+
+
 def dequant_act(q, s) -> np.ndarray:
     q = np.asarray(q)
     n, C = q.shape
@@ -209,6 +240,7 @@ def _expert_weights(w: Dict, fmt: str, e: int):
     if fmt == "mxfp8":
         return (dequant_mx(_np(w["w13_q"][e]), _np(w["w13_sx"][e])),
                 dequant_mx(_np(w["w2_q"][e]), _np(w["w2_sx"][e])))
+    # "nvfp4" and "nvfp4_w4a4" share the NVFP4 weight format
     return (dequant_nvfp4(w["w13_q"][e], w["w13_sb"][e], float(w["w13_g"][e])),
             dequant_nvfp4(w["w2_q"][e], w["w2_sb"][e], float(w["w2_g"][e])))
 
@@ -225,9 +257,13 @@ def tail(act: Dict, w: Dict, cfg, tokens: Optional[Iterable[int]] = None) -> Dic
     tok = np.arange(M) if tokens is None else np.asarray(list(tokens), dtype=np.int64)
     n = len(tok)
 
-    # activation quantiser: fp32 amax/448 per 128 columns, or MX (power-of-two per 32)
+    # activation quantiser: fp32 amax/448 per 128 columns, MX (power-of-two per 32), or
+    # NVFP4 (e2m1 with an e4m3 scale per 16) for the FP4 x FP4 format
     mx = cfg.routed_fmt == "mxfp8"
-    quant, deq, G = (quant_mx, dequant_mx, 32) if mx else (quant_per128, dequant_act, 128)
+    a4 = cfg.routed_fmt == "nvfp4_w4a4"
+    quant, deq, G = ((quant_mx, dequant_mx, 32) if mx else
+                     (quant_nvfp4, dequant_nvfp4_act, 16) if a4 else
+                     (quant_per128, dequant_act, 128))
     z = _rows_f64(act["z"], tok)
     zq, zs = quant(z.astype(np.float32))
     zdq = deq(zq, zs)
@@ -235,7 +271,7 @@ def tail(act: Dict, w: Dict, cfg, tokens: Optional[Iterable[int]] = None) -> Dic
     # Routed experts, one expert at a time (bounded memory).
     r = np.zeros((n, cfg.L))
     aq = np.zeros((n, k, I), dtype=np.uint8)
-    as_ = np.zeros((n, k, I // G), dtype=np.uint8 if mx else np.float32)
+    as_ = np.zeros((n, k, I // G), dtype=np.uint8 if (mx or a4) else np.float32)
     sel_ids = ids[tok]
     for e in np.unique(sel_ids):
         rows, js = np.nonzero(sel_ids == e)

@@ -77,6 +77,32 @@ def quant_group_mx(vals):
     return [e4m3_round(f32(v / s)) for v in vals], s
 
 
+E2M1_POS = sorted((e2m1_value(c), c) for c in range(8))
+
+
+def e2m1_round(v: float) -> int:
+    """Nearest e2m1 code, ties to the code with an even mantissa bit, saturating at 6;
+    the sign bit only for a non-zero magnitude."""
+    a = abs(v)
+    best = None
+    for val, c in E2M1_POS:
+        key = (abs(val - a), c & 1)
+        if best is None or key < best[0]:
+            best = (key, c)
+    c = best[1]
+    return c | 8 if (v < 0 and c > 0) else c
+
+
+def quant_group_nvfp4(vals):
+    """One 16-wide group -> (codes, scale): scale = the e4m3 value nearest fp32(amax/6),
+    codes = e2m1 of fp32(v/scale); all codes 0 when the scale is 0."""
+    amax = max(abs(v) for v in vals)
+    s = e4m3_value(e4m3_round(f32(amax / 6.0)))
+    if s == 0.0:
+        return [0 for _ in vals], 0.0
+    return [e2m1_round(f32(v / s)) for v in vals], s
+
+
 def silu(v: float) -> float:
     return v / (1.0 + math.exp(-v))
 
@@ -85,10 +111,13 @@ def matvec(w, x):
     return [sum(wr[i] * x[i] for i in range(len(x))) for wr in w]
 
 
-def tail_token(logits, z, x, k, experts, gamma, eps, ws13, ws2, w_up, mx=False):
+def tail_token(logits, z, x, k, experts, gamma, eps, ws13, ws2, w_up, mx=False, a4=False):
     """Output vector of one token.  ``experts[e] = (w13 rows, w2 rows)`` dequantised.
-    ``mx``: activations quantised per 32 with power-of-two scales instead of per 128."""
-    G, qg = (32, quant_group_mx) if mx else (128, quant_group)
+    ``mx``: activations quantised per 32 with power-of-two scales instead of per 128;
+    ``a4``: activations quantised to NVFP4 (e2m1, e4m3 scale per 16)."""
+    G, qg = (32, quant_group_mx) if mx else (16, quant_group_nvfp4) if a4 else \
+        (128, quant_group)
+    val = e2m1_value if a4 else e4m3_value
     order = sorted(range(len(logits)), key=lambda e: (-logits[e], e))[:k]
     mx = logits[order[0]]
     ex = [math.exp(logits[e] - mx) for e in order]
@@ -97,7 +126,7 @@ def tail_token(logits, z, x, k, experts, gamma, eps, ws13, ws2, w_up, mx=False):
     zd = []
     for g0 in range(0, len(z), G):
         q, s = qg([f32(v) for v in z[g0:g0 + G]])
-        zd += [e4m3_value(c) * s for c in q]
+        zd += [val(c) * s for c in q]
     L = len(z)
     r = [0.0] * L
     for e, wj in zip(order, wts):
@@ -108,7 +137,7 @@ def tail_token(logits, z, x, k, experts, gamma, eps, ws13, ws2, w_up, mx=False):
         ad = []
         for g0 in range(0, inter, G):
             q, s = qg([f32(v) for v in a[g0:g0 + G]])
-            ad += [e4m3_value(c) * s for c in q]
+            ad += [val(c) * s for c in q]
         y = matvec(w2, ad)
         for c in range(L):
             r[c] += wj * y[c]

@@ -418,3 +418,103 @@ def test_tail_mx_matches_scalar_brute_force(kw):
                                            ws13, ws2, wup, mx=True)
         assert o["ids"][t].tolist() == order
         np.testing.assert_allclose(o["out"][t], ref, rtol=1e-9, atol=1e-9)
+
+
+# ---------------------------------------------------------------- NVFP4 activations (FP4 x FP4)
+
+def test_e2m1_encode_matches_nearest_value_search():
+    from oracle.codecs import e2m1_encode
+    grid = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    mids = [(a + b) / 2 for a, b in zip(grid, grid[1:])]
+    rng = np.random.default_rng(31)
+    vals = grid + mids + [6.5, 1e9, 1e-30] + list(rng.uniform(-7, 7, 400))
+    vals += [-v for v in vals]
+    got = e2m1_encode(np.array(vals)).tolist()
+    assert got == [brute.e2m1_round(v) for v in vals]
+    # ties go to the even code: 0.25->0, 0.75->1.0, 1.25->1.0, 1.75->2, 2.5->2, 3.5->4, 5->4
+    assert e2m1_encode(np.array(mids)).tolist() == [0, 2, 2, 4, 4, 6, 6]
+    # every code decodes and re-encodes to itself (negative zero excepted: it has code 0)
+    from oracle.codecs import e2m1_decode
+    codes = np.array([c for c in range(16) if c != 8])
+    assert e2m1_encode(e2m1_decode(codes)).tolist() == codes.tolist()
+
+
+def _nv_blocks(seed):
+    rng = np.random.default_rng(seed)
+    v = rng.standard_normal((6, 128)).astype(np.float32)
+    v[0] *= 1e-4                        # scales in the e4m3 subnormal range
+    v[1] *= 2e3                         # amax / 6 above 448: the scale saturates
+    v[2, :16] = 0.0                     # an all-zero block
+    v[2, 16:32] = np.float32(1e-5)      # amax / 6 rounds to a zero scale
+    v[3, 32:48] = np.float32(3.0)       # a constant block
+    v[4, 48:64] *= 2.0 ** 6
+    return v
+
+
+def test_quant_nvfp4_matches_scalar_rule():
+    v = _nv_blocks(32)
+    q, sb = T.quant_nvfp4(v)
+    for r in range(v.shape[0]):
+        for g in range(v.shape[1] // 16):
+            codes, s = brute.quant_group_nvfp4([float(a) for a in v[r, 16 * g:16 * g + 16]])
+            assert q[r, 16 * g:16 * g + 16].tolist() == codes, (r, g)
+            assert float(e4m3_decode(sb[r, g])) == s, (r, g)
+
+
+def test_quant_nvfp4_scale_and_range_properties():
+    v = _nv_blocks(33)
+    q, sb = T.quant_nvfp4(v)
+    d = T.dequant_nvfp4_act(q, sb)
+    s = e4m3_decode(sb)
+    assert sb[2, 0] == 0 and sb[2, 1] == 0 and not q[2, :32].any()
+    assert (sb[1] == 0x7E).all()        # saturated scales: 448
+    for r in (3, 4, 5):                 # normal-range blocks
+        for g in range(8):
+            blk = v[r, 16 * g:16 * g + 16].astype(np.float64)
+            amax = np.abs(blk).max()
+            # the scale is amax / 6 to within half an e4m3 step, so the block maximum
+            # lands on the top code 6 (code 7), saturating when the scale rounded down
+            assert abs(s[r, g] - amax / 6) <= s[r, g] * 2.0 ** -4
+            assert (q[r, 16 * g:16 * g + 16] & 7).max() == 7
+            # per element error: half the local e2m1 spacing (at most 1 in scaled units)
+            # plus the saturation at 6
+            err = np.abs(d[r, 16 * g:16 * g + 16] - blk)
+            assert (err <= s[r, g] * 1.0 + np.maximum(np.abs(blk) - 6 * s[r, g], 0) + 1e-12).all()
+    # scaling a row by a power of two moves each normal scale's exponent, codes unchanged
+    q2, sb2 = T.quant_nvfp4(v[5:6] * np.float32(2.0 ** 3))
+    np.testing.assert_array_equal(q2, q[5:6])
+    np.testing.assert_array_equal(sb2.astype(int), sb[5:6].astype(int) + (3 << 3))
+
+
+def test_dequant_nvfp4_act_matches_loops():
+    rng = np.random.default_rng(34)
+    q = rng.integers(0, 16, (3, 32)).astype(np.uint8)
+    sb = rng.integers(0, 0x7F, (3, 2)).astype(np.uint8)
+    d = T.dequant_nvfp4_act(q, sb)
+    for r in range(3):
+        for c in range(32):
+            assert d[r, c] == brute.e2m1_value(int(q[r, c])) * brute.e4m3_value(int(sb[r, c // 16]))
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(M=2, E=5, topk=3, seed=13)])
+def test_tail_w4a4_matches_scalar_brute_force(kw):
+    cfg, act, w = _small(routed_fmt="nvfp4_w4a4", **kw)
+    o = T.tail(act, w, cfg)
+    lg = act["logits"].numpy()
+    z = T.to_f64(act["z"])
+    x = T.to_f64(act["x"])
+    experts = {e: (T.dequant_nvfp4(w["w13_q"][e], w["w13_sb"][e], float(w["w13_g"][e])).tolist(),
+                   T.dequant_nvfp4(w["w2_q"][e], w["w2_sb"][e], float(w["w2_g"][e])).tolist())
+               for e in range(cfg.E)}
+    gamma = T.to_f64(w["gamma"]).tolist()
+    ws13, ws2, wup = (T.to_f64(w[k]).tolist() for k in ("ws13", "ws2", "w_up"))
+    for t in range(cfg.M):
+        ref, order, wts = brute.tail_token([float(v) for v in lg[t]], z[t].tolist(),
+                                           x[t].tolist(), cfg.topk, experts, gamma, cfg.eps,
+                                           ws13, ws2, wup, a4=True)
+        assert o["ids"][t].tolist() == order
+        np.testing.assert_allclose(o["out"][t], ref, rtol=1e-9, atol=1e-9)
+    # the latent codes are the quantiser's own (one e2m1 code per element)
+    q, sb = T.quant_nvfp4(z.astype(np.float32))
+    np.testing.assert_array_equal(o["zq"], q)
+    np.testing.assert_array_equal(o["zs"], sb)
