@@ -4,7 +4,8 @@ One step = one klt_forward (routing, permutation, routed FP8/NVFP4 experts, comb
 RMSNorm, up-projection + BF16 shared expert) over one batch of synthetic tokens.  Prints
 one JSON line.  By default every workload is measured in the same run (tiny M=4, decode
 M=16, decode M=128, prefill M=4096, prefill M=8192 NVFP4, plus decode M=16 from the hidden
-state alone and prefill M=4096 with MXFP8 routed weights); the line's top-level figures
+state alone, prefill M=4096 with MXFP8 routed weights and prefill M=8192 with NVFP4 weights
+and activations); the line's top-level figures
 are the decode batch of 16 tokens (E=64, top-8, routed intermediate 1024 with FP8 128x128
 block scales, shared intermediate 2048, H=7168, L=3584) and `workloads` holds every
 workload's record (roofline, end to end, clocks, the oracle on the host cores).
@@ -159,15 +160,18 @@ def algorithmic_bytes(cfg, cnt: np.ndarray, M: int):
     touched = int((cnt > 0).sum())
     Mk = M * k
     # routed weight bytes per element: codes plus scales
-    wb = {"fp8": 1.0, "mxfp8": 1.0 + 1.0 / 32, "nvfp4": 0.5 + 1.0 / 16}[cfg.routed_fmt]
+    wb = {"fp8": 1.0, "mxfp8": 1.0 + 1.0 / 32, "nvfp4": 0.5 + 1.0 / 16,
+          "nvfp4_w4a4": 0.5 + 1.0 / 16}[cfg.routed_fmt]
+    # quantised routed activation bytes per element (latent input, SwiGLU output)
+    qb = {"mxfp8": 1.0 + 1.0 / 32, "nvfp4_w4a4": 0.5 + 1.0 / 16}.get(cfg.routed_fmt, 1.0)
     w13 = touched * 2 * I * L * wb
     w2 = touched * L * I * wb
-    g1 = 2 * Is * H * 2 + M * H * 2 + w13 + Mk * L + Mk * I + M * Is * 2
-    g2 = w2 + Mk * I + M * L * 4
+    g1 = 2 * Is * H * 2 + M * H * 2 + w13 + Mk * L * qb + Mk * I * qb + M * Is * 2
+    g2 = w2 + Mk * I * qb + M * L * 4
     norm = M * L * 4 + M * L * 2
     g3 = H * L * 2 + H * Is * 2 + M * L * 2 + M * Is * 2 + M * H * 2
-    route = M * E * 4 + M * L * 2 + M * L + M * L * 4
-    perm = Mk * L * 2
+    route = M * E * 4 + M * L * 2 + M * L * qb + M * L * 4
+    perm = Mk * L * qb * 2
     total = g1 + g2 + norm + g3 + route + perm
     return {"gemm_l1": g1, "gemm_l2": g2, "norm": norm, "gemm_out": g3, "route": route,
             "perm": perm, "total": total, "touched_experts": touched}
@@ -188,6 +192,9 @@ def dtype_of(cfg) -> str:
         return "fp8e4m3+bf16 (fp32 accumulate)"
     if cfg.routed_fmt == "mxfp8":
         return "mxfp8 (e4m3, power-of-two scales per 32, block-scaled MMA) + bf16 (fp32 accumulate)"
+    if cfg.routed_fmt == "nvfp4_w4a4":
+        return ("nvfp4 weights and activations (e2m1, e4m3 scales per 16, block-scaled FP4 "
+                "MMA) + bf16 (fp32 accumulate)")
     return "nvfp4 weights (bf16-exact MMA) + fp8e4m3 activations + bf16 (fp32 accumulate)"
 
 
@@ -376,7 +383,7 @@ def measure(cfg, args, ws, rank, local, flush, with_cpu: bool, hidden: bool = Fa
             per[j] += evs[i][j].elapsed_time(evs[i][j + 1])
     per /= args.steps
     nt = nl - (1 if hidden else 0)  # launches of the tail itself
-    mx = cfg.routed_fmt == "mxfp8"  # routed and dense GEMM launches
+    mx = cfg.routed_fmt in ("mxfp8", "nvfp4_w4a4")  # routed and dense GEMM launches
     gemms = (["gemm_routed", "gemm_dense"] if mx else ["gemm_fused"]) if nt <= 5 + mx else \
         ["gemm_l1", "gemm_l2", "norm", "gemm_out"]
     hist = nt == 4 + len(gemms)
@@ -415,7 +422,7 @@ def measure(cfg, args, ws, rank, local, flush, with_cpu: bool, hidden: bool = Fa
     cnt_h = cnt.cpu().numpy()
     ab = algorithmic_bytes(cfg, cnt_h, M)
     hbm, bf16_tf, peak_src = _peaks()
-    if "gemm_routed" in per_launch_us:  # MX layers: the two GEMM launches together
+    if "gemm_routed" in per_launch_us:  # block-scaled layers: both GEMM launches together
         dom = "gemm_routed+gemm_dense"
         per_launch_us[dom] = round(per_launch_us["gemm_routed"] + per_launch_us["gemm_dense"], 2)
         dom_bytes = ab["gemm_l1"] + ab["gemm_l2"] + ab["norm"] + ab["gemm_out"]
@@ -429,9 +436,11 @@ def measure(cfg, args, ws, rank, local, flush, with_cpu: bool, hidden: bool = Fa
     if hidden:  # the projection: its weights, x again, z and logits written
         ab["total"] += (cfg.L + cfg.E) * cfg.H * 2 + M * cfg.H * 2 + M * (cfg.L * 2 + cfg.E * 4)
         dense_f += 2.0 * M * cfg.H * (cfg.L + cfg.E)
-    # fp8 routed contractions run at twice the bf16 rate (the nominal fp8:bf16 ratio applied
-    # to the measured bf16 peak); the fused launch's mixed peak follows from the flop mix
-    t_tensor = routed_f / (2 * bf16_tf * 1e12) + dense_f / (bf16_tf * 1e12)
+    # fp8 routed contractions run at twice the bf16 rate and fp4 x fp4 ones at six times
+    # (the nominal dense ratios 4.5 : 2.25 and 13.5 : 2.25 PFLOP/s applied to the measured
+    # bf16 peak); the fused launch's mixed peak follows from the flop mix
+    rr = 6.0 if cfg.routed_fmt == "nvfp4_w4a4" else 2.0
+    t_tensor = routed_f / (rr * bf16_tf * 1e12) + dense_f / (bf16_tf * 1e12)
     dom_s = per_launch_us[dom] * 1e-6
     traffic = recorded_traffic(cfg.name, dom)
     if t_tensor > dom_bytes / (hbm * 1e9):
@@ -440,7 +449,7 @@ def measure(cfg, args, ws, rank, local, flush, with_cpu: bool, hidden: bool = Fa
         roof = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1),
                 "peak": round(mixed_peak, 1), "unit": "TFLOP/s",
                 "frac": round(achieved / mixed_peak, 4),
-                "peak_source": f"{peak_src} bf16 burst, fp8 share at 2x",
+                "peak_source": f"{peak_src} bf16 burst, routed share at {rr:g}x",
                 "traffic": traffic, "algorithmic_flops": routed_f + dense_f,
                 "algorithmic_bytes": int(dom_bytes)}
     else:
@@ -509,9 +518,11 @@ def main():
 
     from latent_moe_layer_route_gb300 import configs
     # a workload name with "+hidden" runs that workload from the hidden state alone
-    if args.workload == "all":  # the five workloads, the step before the tail, the MX variant
+    if args.workload == "all":  # the five workloads, the step before the tail, the MX and
+        # FP4 x FP4 variants
         names = [c.name for c in configs.ALL] + [HEADLINE + "+hidden",
-                                                 configs.PREFILL_M4096_MX.name]
+                                                 configs.PREFILL_M4096_MX.name,
+                                                 configs.PREFILL_M8192_W4A4.name]
     else:  # one name, or several separated by commas (the first is the headline)
         names = args.workload.split(",")
     cfgs = [(configs.BY_NAME[n.split("+")[0]], n.endswith("+hidden")) for n in names]

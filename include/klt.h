@@ -53,12 +53,20 @@ enum klt_routed_format {
   KLT_FMT_FP8_B128 = 0,  /* e4m3 codes, one fp32 scale per 128 x 128 block            */
   KLT_FMT_NVFP4 = 1,     /* e2m1 codes (two per byte, even K in the low nibble), one
                             e4m3 scale per 16 K-elements, one fp32 scale per matrix    */
-  KLT_FMT_MXFP8 = 2      /* e4m3 codes, one power-of-two scale per 32 K-elements of a row
+  KLT_FMT_MXFP8 = 2,     /* e4m3 codes, one power-of-two scale per 32 K-elements of a row
                             (an UE8M0 byte b: scale 2^(b-127)); the routed activations are
                             quantised the same way (scale 2^(floor(log2 amax) - 8)) and the
                             tensor core applies the scales (block-scaled MMA, no epilogue
                             promotion).  Needs H and L multiples of 256; always runs the
                             token-major engine.                                         */
+  KLT_FMT_NVFP4_W4A4 = 3 /* NVFP4 weights as in KLT_FMT_NVFP4, kept packed in device
+                            memory (0.5625 bytes per weight), and NVFP4 routed
+                            activations: per 16 elements an e4m3 scale s = e4m3(amax / 6)
+                            and e2m1 codes of v / s (nearest even, saturating, no tensor
+                            scale).  The tensor core applies both operands' e4m3 scales
+                            (block-scaled FP4 MMA, scale vector of 4 per 64 K) and the
+                            epilogue the weights' fp32 per-matrix scale.  Needs H, L and I
+                            multiples of 256; always runs the token-major engine.      */
 };
 
 /* klt_create flags. */
@@ -98,7 +106,8 @@ typedef struct klt_dims {
  *   FP8 routed:   w13 e4m3 [E, 2I, L]; w13_scale f32 [E, 2I/128, L/128];
  *                 w2  e4m3 [E, L, I];  w2_scale  f32 [E, L/128, I/128];
  *                 w13_global, w2_global unused (may be NULL).
- *   NVFP4 routed: w13 packed e2m1 [E, 2I, L/2]; w13_scale e4m3 [E, 2I, L/16];
+ *   NVFP4 routed (KLT_FMT_NVFP4 and KLT_FMT_NVFP4_W4A4):
+ *                 w13 packed e2m1 [E, 2I, L/2]; w13_scale e4m3 [E, 2I, L/16];
  *                 w13_global f32 [E]; w2 packed [E, L, I/2]; w2_scale e4m3 [E, L, I/16];
  *                 w2_global f32 [E].
  *   MXFP8 routed: w13 e4m3 [E, 2I, L]; w13_scale uint8 UE8M0 [E, 2I, L/32];
@@ -144,9 +153,11 @@ typedef struct klt_routing {
 
 /* Optional stage outputs for testing and profiling (every pointer may be NULL; device
  * memory, caller owned; copied on `stream` after the stage that writes them).
- *   zq e4m3 [M, L], zs f32 [M, L/128]: quantised latent input (MXFP8 layers: zsx below);
+ *   zq e4m3 [M, L], zs f32 [M, L/128]: quantised latent input (MXFP8 layers: zsx below;
+ *     NVFP4_W4A4 layers: zq packed e2m1 [M, L/2], even column in the low nibble, and zsx);
  *   aq e4m3 [M * topk, I], as f32 [M * topk, I/128]: quantised routed SwiGLU output,
- *     rows in pair order p (MXFP8 layers: aq only);
+ *     rows in pair order p (MXFP8 layers: aq only; NVFP4_W4A4 layers: aq packed e2m1
+ *     [M * topk, I/2] only);
  *   r f32 [M, L]: routed combine (not formed with KLT_FLAG_DETERMINISTIC, whose norm sums
  *     the per-pair outputs directly); n bf16 [M, L]: RMSNorm output (gamma applied);
  *   a_s bf16 [M, Is]: shared-expert SwiGLU output;
@@ -185,7 +196,8 @@ typedef struct klt_debug {
    * it computed from the hidden state */
   void* z;
   float* logits;
-  /* MXFP8 layers: the latent input's UE8M0 scale bytes uint8 [M, L/32] (zs is not formed) */
+  /* MXFP8 layers: the latent input's UE8M0 scale bytes uint8 [M, L/32]; NVFP4_W4A4
+   * layers: its e4m3 scale bytes uint8 [M, L/16] (zs is not formed in either) */
   uint8_t* zsx;
 } klt_debug;
 

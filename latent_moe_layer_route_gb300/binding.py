@@ -24,6 +24,7 @@ KLT_NOALLOC_MAX_PAIRS = 65536
 KLT_FMT_FP8_B128 = 0
 KLT_FMT_NVFP4 = 1
 KLT_FMT_MXFP8 = 2
+KLT_FMT_NVFP4_W4A4 = 3
 KLT_FLAG_NO_PDL = 1
 KLT_FLAG_PHASED = 2
 KLT_FLAG_DETERMINISTIC = 4
@@ -116,8 +117,8 @@ def _ptr(t) -> Optional[int]:
 
 
 def dims_of(cfg, max_tokens: Optional[int] = None) -> KltDims:
-    fmt = {"nvfp4": KLT_FMT_NVFP4, "mxfp8": KLT_FMT_MXFP8}.get(cfg.routed_fmt,
-                                                             KLT_FMT_FP8_B128)
+    fmt = {"nvfp4": KLT_FMT_NVFP4, "mxfp8": KLT_FMT_MXFP8,
+           "nvfp4_w4a4": KLT_FMT_NVFP4_W4A4}.get(cfg.routed_fmt, KLT_FMT_FP8_B128)
     return KltDims(cfg.H, cfg.L, cfg.E, cfg.topk, cfg.I, cfg.Is, fmt, cfg.eps,
                    cfg.M if max_tokens is None else max_tokens)
 

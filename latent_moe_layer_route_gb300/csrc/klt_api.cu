@@ -85,10 +85,12 @@ struct klt_handle {
   __nv_bfloat16 *n, *a_s, *zqb_perm, *aqb;
   int *split_cnt, *sched, *err;
   int* dep_cnt;  // fused-launch dependency counters [routed tiles | l2 | norm tiles | shared]
-  // MXFP8 layers: weight scale tiles (512 bytes per 128-row block and k-block, the
-  // tcgen05.cp layout), the latent input's scale bytes, and the token scale tiles of the
-  // routed L1 and L2 units (one per routed tile of 128 pairs and k-block)
+  // Block-scaled layers (MXFP8, NVFP4_W4A4): weight scale tiles (512 bytes per 128-row
+  // block and 4 scale bytes of a row, the tcgen05.cp layout), the latent input's scale
+  // bytes, and the token scale tiles of the routed L1 and L2 units (per routed tile of 128
+  // pairs); NVFP4_W4A4 also the weights' fp32 per-matrix scales [E]
   uint8_t *w13_sf, *w2_sf, *zsx, *zsf_t, *asf_t;
+  float *w13_g, *w2_g;
   int sf_tiles;
   // the step before the tail (optional): [W_lat | W_gate | zero rows] bf16, tile-major,
   // proj_rows x H, and its outputs
@@ -100,13 +102,15 @@ struct klt_handle {
   bool wide_ok;  // token-major engine usable (dims and launch register count)
   // descriptors per BN variant (token-side maps depend on the box height)
   CUtensorMap tm_zqp[kNumBN], tm_aq[kNumBN], tm_n[kNumBN], tm_as[kNumBN];
-  void* allocs[48];
+  void* allocs[64];
   int nallocs;
 };
 
 namespace {
 
 cudaError_t halloc(klt_handle* h, void** p, size_t bytes) {
+  if (h->nallocs >= static_cast<int>(sizeof(h->allocs) / sizeof(h->allocs[0])))
+    return cudaErrorMemoryAllocation;
   cudaError_t e = cudaMalloc(p, bytes < 256 ? 256 : bytes);
   if (e != cudaSuccess) return e;
   h->allocs[h->nallocs++] = *p;
@@ -126,10 +130,13 @@ int check_dims(const klt_dims* d) {
   if (d->E > MAX_E || d->topk > d->E || d->topk > MAX_TOPK) return KLT_ERR_UNSUPPORTED;
   if (d->L > 128 * MAX_KB || d->I > 128 * MAX_KB) return KLT_ERR_UNSUPPORTED;
   if (d->routed_fmt != KLT_FMT_FP8_B128 && d->routed_fmt != KLT_FMT_NVFP4 &&
-      d->routed_fmt != KLT_FMT_MXFP8)
+      d->routed_fmt != KLT_FMT_MXFP8 && d->routed_fmt != KLT_FMT_NVFP4_W4A4)
     return KLT_ERR_UNSUPPORTED;
   // MXFP8 runs on the token-major engine only (256-wide units)
   if (d->routed_fmt == KLT_FMT_MXFP8 && (d->H % 256 || d->L % 256)) return KLT_ERR_UNSUPPORTED;
+  // so does NVFP4_W4A4, whose k-blocks are 256 e2m1 values (L and I are GEMM K extents)
+  if (d->routed_fmt == KLT_FMT_NVFP4_W4A4 && (d->H % 256 || d->L % 256 || d->I % 256))
+    return KLT_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(d->max_tokens) * d->topk > (1 << 20)) return KLT_ERR_UNSUPPORTED;
   return KLT_OK;
 }
@@ -186,9 +193,11 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
   if ((flags & KLT_FLAG_DETERMINISTIC) && (flags & KLT_FLAG_PHASED)) return KLT_ERR_UNSUPPORTED;
   const bool nvfp4 = d->routed_fmt == KLT_FMT_NVFP4;
   const bool mx = d->routed_fmt == KLT_FMT_MXFP8;
-  if (mx && (flags & KLT_FLAG_PHASED)) return KLT_ERR_UNSUPPORTED;
-  if (nvfp4 && (!w->w13_global || !w->w2_global)) return KLT_ERR_INVALID_ARG;
-  if (nvfp4 && (!aligned16(w->w13_global) || !aligned16(w->w2_global))) return KLT_ERR_ALIGN;
+  const bool nv4 = d->routed_fmt == KLT_FMT_NVFP4_W4A4;  // packed FP4 x FP4, block-scaled
+  if ((mx || nv4) && (flags & KLT_FLAG_PHASED)) return KLT_ERR_UNSUPPORTED;
+  if ((nvfp4 || nv4) && (!w->w13_global || !w->w2_global)) return KLT_ERR_INVALID_ARG;
+  if ((nvfp4 || nv4) && (!aligned16(w->w13_global) || !aligned16(w->w2_global)))
+    return KLT_ERR_ALIGN;
   if ((w->w_lat == nullptr) != (w->w_gate == nullptr)) return KLT_ERR_INVALID_ARG;
   if (w->w_lat && (!aligned16(w->w_lat) || !aligned16(w->w_gate))) return KLT_ERR_ALIGN;
   const void* ptrs[] = {w->w13, w->w13_scale, w->w2, w->w2_scale, w->ws13, w->ws2,
@@ -227,11 +236,13 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
       return KLT_ERR_OOM;                                                       \
     }                                                                           \
   } while (0)
-  // NVFP4 weights are held as their exact bf16 values (2 bytes per weight)
-  const int64_t wbytes = nvfp4 ? 2 : 1;
-  KLT_ALLOC(h->w13, E * 2 * I * L * wbytes);
+  // NVFP4 weights are held as their exact bf16 values (2 bytes per weight), except in the
+  // FP4 x FP4 format, which keeps them packed (two per byte)
+  const int64_t w13_bytes = nvfp4 ? E * 2 * I * L * 2 : (nv4 ? E * 2 * I * L / 2 : E * 2 * I * L);
+  const int64_t w2_bytes = nvfp4 ? E * L * I * 2 : (nv4 ? E * L * I / 2 : E * L * I);
+  KLT_ALLOC(h->w13, w13_bytes);
   KLT_ALLOC(h->w13_s, E * (2 * I / 128) * (L / 128) * 4);
-  KLT_ALLOC(h->w2, E * L * I * wbytes);
+  KLT_ALLOC(h->w2, w2_bytes);
   KLT_ALLOC(h->w2_s, E * (L / 128) * (I / 128) * 4);
   KLT_ALLOC(h->ws13, 2 * Is * H * 2);
   KLT_ALLOC(h->ws2, H * Is * 2);
@@ -269,13 +280,19 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
   h->dep_ntiles = static_cast<int>((Mx + 15) / 16);
   KLT_ALLOC(h->dep_cnt, (static_cast<int64_t>(h->dep_routed) + 1 + 2 * h->dep_ntiles) * 4);
   KLT_ALLOC(h->err, 256);
-  if (mx) {
+  if (mx || nv4) {
+    // one scale byte per sf_group K-elements of a row; 512-byte tiles of 4 bytes x 128 rows
+    const int64_t g = mx ? 32 : 16;
     h->sf_tiles = static_cast<int>(cap / 128 + E);
-    KLT_ALLOC(h->w13_sf, E * 2 * I * (L / 32));
-    KLT_ALLOC(h->w2_sf, E * L * (I / 32));
-    KLT_ALLOC(h->zsx, Mx * (L / 32));
-    KLT_ALLOC(h->zsf_t, static_cast<int64_t>(h->sf_tiles) * (L / 128) * 512);
-    KLT_ALLOC(h->asf_t, static_cast<int64_t>(h->sf_tiles) * (I / 128) * 512);
+    KLT_ALLOC(h->w13_sf, E * 2 * I * (L / g));
+    KLT_ALLOC(h->w2_sf, E * L * (I / g));
+    KLT_ALLOC(h->zsx, Mx * (L / g));
+    KLT_ALLOC(h->zsf_t, static_cast<int64_t>(h->sf_tiles) * (L / (4 * g)) * 512);
+    KLT_ALLOC(h->asf_t, static_cast<int64_t>(h->sf_tiles) * (I / (4 * g)) * 512);
+  }
+  if (nv4) {  // the weights' fp32 per-matrix scales, applied in the epilogue
+    KLT_ALLOC(h->w13_g, E * 4);
+    KLT_ALLOC(h->w2_g, E * 4);
   }
   if (w->w_lat) {
     // rows: W_lat (L), W_gate (E), zero rows up to a multiple of 128 (one output tile)
@@ -302,15 +319,20 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
                                    (2 * I / 128) * (L / 128), 0) == cudaSuccess;
     ok &= launch_fill_expert_scale(w->w2_global, h->w2_s, static_cast<int>(E),
                                    (L / 128) * (I / 128), 0) == cudaSuccess;
-  } else {
-    ok &= launch_tile_relayout(w->w13, h->w13, E * 2 * I, L, 0) == cudaSuccess;
-    ok &= launch_tile_relayout(w->w2, h->w2, E * L, I, 0) == cudaSuccess;
+  } else {  // e4m3 codes, or packed e2m1 (the same 128-byte k-blocks of a row)
+    ok &= launch_tile_relayout(w->w13, h->w13, E * 2 * I, nv4 ? L / 2 : L, 0) == cudaSuccess;
+    ok &= launch_tile_relayout(w->w2, h->w2, E * L, nv4 ? I / 2 : I, 0) == cudaSuccess;
   }
-  if (mx) {
-    ok &= launch_sf_relayout(static_cast<const uint8_t*>(w->w13_scale), h->w13_sf, E * 2 * I, L,
+  if (mx || nv4) {
+    const int64_t g = mx ? 32 : 16;
+    ok &= launch_sf_relayout(static_cast<const uint8_t*>(w->w13_scale), h->w13_sf, E * 2 * I,
+                             L / g, 0) == cudaSuccess;
+    ok &= launch_sf_relayout(static_cast<const uint8_t*>(w->w2_scale), h->w2_sf, E * L, I / g,
                              0) == cudaSuccess;
-    ok &= launch_sf_relayout(static_cast<const uint8_t*>(w->w2_scale), h->w2_sf, E * L, I, 0) ==
-          cudaSuccess;
+  }
+  if (nv4) {
+    ok &= cudaMemcpy(h->w13_g, w->w13_global, E * 4, cudaMemcpyDeviceToDevice) == cudaSuccess;
+    ok &= cudaMemcpy(h->w2_g, w->w2_global, E * 4, cudaMemcpyDeviceToDevice) == cudaSuccess;
   }
   ok &= launch_tile_relayout(w->ws13, h->ws13, 2 * Is, H * 2, 0) == cudaSuccess;
   ok &= launch_tile_relayout(w->ws2, h->ws2, H, Is * 2, 0) == cudaSuccess;
@@ -332,7 +354,7 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
     ok &= cudaDeviceSynchronize() == cudaSuccess;
     cudaFree(tmp);
   }
-  if (!nvfp4 && !mx) {
+  if (!nvfp4 && !mx && !nv4) {
     ok &= cudaMemcpy(h->w13_s, w->w13_scale, E * (2 * I / 128) * (L / 128) * 4,
                      cudaMemcpyDeviceToDevice) == cudaSuccess;
     ok &= cudaMemcpy(h->w2_s, w->w2_scale, E * (L / 128) * (I / 128) * 4,
@@ -346,9 +368,9 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
     if (nvfp4) {
       ok &= encode_2d(&h->tm_zqp[b], h->zqb_perm, BF, 2, cap, L, kBN[b]);
       ok &= encode_2d(&h->tm_aq[b], h->aqb, BF, 2, cap, I, kBN[b]);
-    } else {
-      ok &= encode_2d(&h->tm_zqp[b], h->zq_perm, U8, 1, cap, L, kBN[b]);
-      ok &= encode_2d(&h->tm_aq[b], h->aq, U8, 1, cap, I, kBN[b]);
+    } else {  // byte rows: e4m3 codes, or e2m1 codes two per byte
+      ok &= encode_2d(&h->tm_zqp[b], h->zq_perm, U8, 1, cap, nv4 ? L / 2 : L, kBN[b]);
+      ok &= encode_2d(&h->tm_aq[b], h->aq, U8, 1, cap, nv4 ? I / 2 : I, kBN[b]);
     }
     ok &= encode_2d(&h->tm_n[b], h->n, BF, 2, Mx, L, kBN[b]);
     ok &= encode_2d(&h->tm_as[b], h->a_s, BF, 2, Mx, Is, kBN[b]);
@@ -359,7 +381,7 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
     return KLT_ERR_CUDA;
   }
   h->wide_ok = L % 256 == 0 && H % 256 == 0 && wide_regs_ok(wide_kernel_regs());
-  if (mx && !h->wide_ok) {
+  if ((mx || nv4) && !h->wide_ok) {
     free_all(h);
     delete h;
     return KLT_ERR_UNSUPPORTED;
@@ -371,16 +393,17 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
 int klt_launch_count(const klt_handle* h, int32_t M) {
   if (!h || M <= 0) return 0;
   const int nblocks = (M * h->d.topk + PERM_BLOCK - 1) / PERM_BLOCK;
-  // phased: 3 GEMMs + norm; MX layers: routed and dense launches
-  const int gemm_launches = (h->flags & KLT_FLAG_PHASED) ? 4
-                            : (h->d.routed_fmt == KLT_FMT_MXFP8 ? 2 : 1);
+  // phased: 3 GEMMs + norm; block-scaled layers: routed and dense launches
+  const bool bs = h->d.routed_fmt == KLT_FMT_MXFP8 || h->d.routed_fmt == KLT_FMT_NVFP4_W4A4;
+  const int gemm_launches = (h->flags & KLT_FLAG_PHASED) ? 4 : (bs ? 2 : 1);
   return 3 + gemm_launches + (nblocks > 1 ? 1 : 0);
 }
 
 int klt_gemm_tile(const klt_handle* h, int32_t M, int32_t force_bn) {
   if (!h) return -KLT_ERR_INVALID_ARG;
   const bool phased = (h->flags & KLT_FLAG_PHASED) != 0;
-  if (h->d.routed_fmt == KLT_FMT_MXFP8)  // block-scaled units exist in the token-major engine
+  // block-scaled units exist in the token-major engine only
+  if (h->d.routed_fmt == KLT_FMT_MXFP8 || h->d.routed_fmt == KLT_FMT_NVFP4_W4A4)
     return (force_bn == 0 || force_bn == 256) && h->wide_ok && !phased ? 256
                                                                       : -KLT_ERR_UNSUPPORTED;
   if (force_bn == 256) return h->wide_ok && !phased ? 256 : -KLT_ERR_UNSUPPORTED;
@@ -418,7 +441,10 @@ int forward_impl(klt_handle* h, const void* x, const void* z, const float* logit
   const int bi = wide ? kNumBN - 1 : bn_index(M, tile);
   const int BN = kBN[bi];
   const bool nvfp4 = d.routed_fmt == KLT_FMT_NVFP4;
-  const int rkb = nvfp4 ? 64 : 128;  // routed K elements per k-block
+  const bool mx = d.routed_fmt == KLT_FMT_MXFP8;
+  const bool nv4 = d.routed_fmt == KLT_FMT_NVFP4_W4A4;
+  // routed K elements per 128-byte k-block: bf16 images, e4m3 codes, or e2m1 pairs
+  const int rkb = nvfp4 ? 64 : (nv4 ? 256 : 128);
   const int Mk = M * k;
   const int nblocks = (Mk + PERM_BLOCK - 1) / PERM_BLOCK;
   const long long timeout_cycles =
@@ -503,8 +529,7 @@ int forward_impl(klt_handle* h, const void* x, const void* z, const float* logit
   rp.E = E;
   rp.k = k;
   rp.L = L;
-  const bool mx = d.routed_fmt == KLT_FMT_MXFP8;
-  rp.mx = mx ? 1 : 0;
+  rp.bs = mx ? BS_MX8 : (nv4 ? BS_NV4 : BS_NONE);
   rp.zsx = h->zsx;
   KLT_LAUNCH(launch_route(rp, s, pdl));
 
@@ -533,8 +558,10 @@ int forward_impl(klt_handle* h, const void* x, const void* z, const float* logit
   pp.bn = BN;  // routed tile list in BN-token tiles (128 for the token-major engine)
   pp.nblocks = nblocks;
   pp.zsx = h->zsx;
-  pp.zsf_t = mx ? h->zsf_t : nullptr;
+  pp.zsf_t = (mx || nv4) ? h->zsf_t : nullptr;
   pp.sf_tiles = h->sf_tiles;
+  pp.sf_group = mx ? 32 : 16;
+  pp.zrow = nv4 ? L / 2 : L;
   if (nblocks > 1) KLT_LAUNCH(launch_perm_hist(pp, s, pdl));
   KLT_LAUNCH(launch_perm_scatter(pp, s, pdl));
   KLT_LAUNCH(launch_perm_gather(pp, s, pdl));
@@ -594,8 +621,8 @@ int forward_impl(klt_handle* h, const void* x, const void* z, const float* logit
     gw.trace = trace;
     GemmTask& R = gw.task[0];  // routed L1: gate and up row blocks of one 128-output tile
     R.kind = TASK_ROUTED_L1;
-    R.fp8 = !nvfp4;
-    R.kpg = mx ? 0 : (nvfp4 ? 2 : 1);  // MX: scales applied by the tensor core
+    R.fp8 = !nvfp4;  // byte operands (e4m3, or e2m1 pairs)
+    R.kpg = (mx || nv4) ? 0 : (nvfp4 ? 2 : 1);  // block-scaled: the tensor core scales
     R.routed = 1;
     R.ftiles = I / 128;
     R.kb_total = L / rkb;
@@ -607,8 +634,9 @@ int forward_impl(klt_handle* h, const void* x, const void* z, const float* logit
     R.a_kb[0] = R.a_kb[1] = L / rkb;
     R.a_ptr[0] = R.a_ptr[1] = h->w13;
     R.tmB[0] = R.tmB[1] = h->tm_zqp[bi];
-    R.a_sf = mx ? h->w13_sf : nullptr;
-    R.t_sf = mx ? h->zsf_t : nullptr;
+    R.a_sf = (mx || nv4) ? h->w13_sf : nullptr;
+    R.t_sf = (mx || nv4) ? h->zsf_t : nullptr;
+    R.a_g = nv4 ? h->w13_g : nullptr;
     GemmTask& S = gw.task[1];  // shared L1 (bf16)
     S.kind = TASK_SHARED_L1;
     S.ftiles = Is / 128;
@@ -628,9 +656,10 @@ int forward_impl(klt_handle* h, const void* x, const void* z, const float* logit
     GemmTask& R2 = gw.task[2];  // routed L2 + combine: two row blocks of W2 per unit
     R2.kind = TASK_ROUTED_L2;
     R2.fp8 = !nvfp4;
-    R2.kpg = mx ? 0 : (nvfp4 ? 2 : 1);
-    R2.a_sf = mx ? h->w2_sf : nullptr;
-    R2.t_sf = mx ? h->asf_t : nullptr;
+    R2.kpg = (mx || nv4) ? 0 : (nvfp4 ? 2 : 1);
+    R2.a_sf = (mx || nv4) ? h->w2_sf : nullptr;
+    R2.t_sf = (mx || nv4) ? h->asf_t : nullptr;
+    R2.a_g = nv4 ? h->w2_g : nullptr;
     R2.routed = 1;
     R2.ftiles = L / 256;
     R2.kb_total = I / rkb;
@@ -680,23 +709,24 @@ int forward_impl(klt_handle* h, const void* x, const void* z, const float* logit
     gw.gamma = h->gamma;
     gw.nrm = h->n;
     gw.eps = d.eps;
-    if (!mx) {
+    if (!mx && !nv4) {
       KLT_LAUNCH(launch_wide(gw, grid, s, pdl));
     } else {
-      // MX layers: the block-scaled routed units keep one accumulator slot (their scale
-      // ring takes the other half of TMEM), so they run as a launch of their own; the BF16
+      // Block-scaled layers: the routed units keep one accumulator slot (their scale ring
+      // takes the other half of TMEM), so they run as a launch of their own; the BF16
       // shared L1, norm and output GEMM follow in a second launch with two slots and dual
       // token tiles.  The dependency counters carry over (zeroed once by routing).
       GemmParams gr = gw, gd = gw;
-      gr.mx = 1;
+      gr.bs = mx ? BS_MX8 : BS_NV4;
       gr.ntasks = 2;
       gr.task[0] = gw.task[1];  // routed L1
       gr.task[1] = gw.task[2];  // routed L2
-      gr.w_stages = 4;
-      gr.w_stage_bytes = 48 * 1024;
+      // NVFP4: 3 stages that carry their 6 KB of scale tiles; MX: 4 of 48 KB
+      gr.w_stages = nv4 ? 3 : 4;
+      gr.w_stage_bytes = nv4 ? 48 * 1024 + 6 * 1024 : 48 * 1024;
       gr.pf_ptr = nullptr;
       gr.pf_bytes = 0;
-      gd.mx = 0;
+      gd.bs = BS_NONE;
       gd.ntasks = 3;
       gd.task[0] = gw.task[0];  // shared L1
       gd.task[1] = gw.task[3];  // norm
@@ -967,16 +997,17 @@ int forward_impl(klt_handle* h, const void* x, const void* z, const float* logit
   }
   if (dbg) {
     if (mx) ok &= cp(dbg->zsx, h->zsx, static_cast<size_t>(M) * (L / 32));
+    if (nv4) ok &= cp(dbg->zsx, h->zsx, static_cast<size_t>(M) * (L / 16));
     if (from_hidden) {
       ok &= cp(dbg->z, h->zp, static_cast<size_t>(M) * L * 2);
       ok &= cp(dbg->logits, h->lgp, static_cast<size_t>(M) * E * 4);
     }
-    ok &= cp(dbg->zq, h->zq, static_cast<size_t>(M) * L);
+    ok &= cp(dbg->zq, h->zq, static_cast<size_t>(M) * (nv4 ? L / 2 : L));
     ok &= cp(dbg->zs, h->zs, static_cast<size_t>(M) * (L / 128) * 4);
     ok &= cp(dbg->r, h->r, static_cast<size_t>(M) * L * 4);
     ok &= cp(dbg->n, h->n, static_cast<size_t>(M) * L * 2);
     ok &= cp(dbg->a_s, h->a_s, static_cast<size_t>(M) * Is * 2);
-    ok &= cp(dbg->aq, h->aq, static_cast<size_t>(Mk) * I);
+    ok &= cp(dbg->aq, h->aq, static_cast<size_t>(Mk) * (nv4 ? I / 2 : I));
     if (dbg->as) {  // stored transposed [I/128, cap] on the device
       const int G = I / 128;
       for (int g = 0; g < G; ++g)

@@ -235,6 +235,27 @@ KLT_DEV void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t id
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
 }
+// D (+)= A * B^T with e2m1 operands (two per byte) and one e4m3 scale per 16 K-elements
+// of each row (kind::mxf4nvf4, scale vector 4X): K = 64 per MMA (32 bytes of a row).  The
+// scales of A row m are the four bytes of TMEM lane m, column sfa_tmem + m / 32 (byte j
+// scales K-elements [16j, 16j + 16)); those of B row n are at lane n % 32, column
+// sfb_tmem + n / 32 -- the layout tcgen05.cp 32x128b.warpx4 makes of 512-byte tiles whose
+// byte (r % 32) * 16 + 4 * (r / 32) + j holds scale j of row r.
+KLT_DEV void mma_nv4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                     uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, "
+      "[%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+// Instruction descriptor of kind::mxf4nvf4 with e2m1 A and B (format 1), e4m3 scales
+// (scale format 0), fp32 accumulation, both operands K-major, shape M x N, K = 64.
+__host__ __device__ constexpr uint32_t idesc_nv4(int m, int n) {
+  return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
+}
 // Instruction descriptor of kind::mxf8f6f4 with e4m3 A and B, UE8M0 scales, fp32
 // accumulation, both operands K-major, shape M x N, scale ids for A and B.
 __host__ __device__ constexpr uint32_t idesc_mx(int m, int n, uint32_t a_sf_id,
@@ -459,6 +480,18 @@ KLT_DEV float e2m1_to_f32(uint32_t c) {
   const float mag = e == 0 ? 0.5f * static_cast<float>(m)
                            : __int_as_float(static_cast<int>((126u + e) << 23 | (m << 22)));
   return (c & 8u) ? -mag : mag;
+}
+
+// fp32 -> e2m1 code (4 bits): nearest of 0, 0.5, 1, 1.5, 2, 3, 4, 6, a tie going to the
+// even code (the midpoints 0.25, 1.25, 2.5 and 5 round down, 0.75, 1.75 and 3.5 up),
+// saturating at 6; the sign bit only for a non-zero magnitude.
+KLT_DEV uint32_t f32_to_e2m1(float v) {
+  const float a = fabsf(v);
+  const uint32_t c = static_cast<uint32_t>(a > 0.25f) + static_cast<uint32_t>(a >= 0.75f) +
+                     static_cast<uint32_t>(a > 1.25f) + static_cast<uint32_t>(a >= 1.75f) +
+                     static_cast<uint32_t>(a > 2.5f) + static_cast<uint32_t>(a >= 3.5f) +
+                     static_cast<uint32_t>(a > 5.0f);
+  return (v < 0.f && c != 0u) ? (c | 8u) : c;
 }
 
 // fp32 -> e4m3 code, round to nearest even, saturating to +-448.

@@ -10,6 +10,10 @@
 namespace klt {
 
 // ------------------------------------------------------------------ routing kernels
+// Block-scaled routed formats (the tensor core applies the scales): MXFP8 (e4m3 with an
+// UE8M0 scale per 32) and NVFP4 weights and activations (e2m1 with an e4m3 scale per 16).
+enum BlockScale : int { BS_NONE = 0, BS_MX8 = 1, BS_NV4 = 2 };
+
 struct RouteParams {
   const float* logits;     // [M, E]
   const __nv_bfloat16* z;  // [M, L]
@@ -23,8 +27,10 @@ struct RouteParams {
   int* zero_buf;           // dependency counters of the fused launch, zeroed here
   int zero_n;
   int M, E, k, L;
-  int mx;                  // MX quantisation: UE8M0 byte per 32 columns into zsx
-  uint8_t* zsx;            // [M, L/32]
+  int bs;                  // activation format: BS_NONE (fp32 scale per 128 into zs),
+                           // BS_MX8 (UE8M0 byte per 32 columns into zsx) or BS_NV4 (e2m1
+                           // codes packed two per byte into zq, e4m3 byte per 16 into zsx)
+  uint8_t* zsx;            // [M, L/32] or [M, L/16]
 };
 
 struct PermParams {
@@ -44,12 +50,16 @@ struct PermParams {
   const float* wts;    // [M*k] routing weights by pair i
   float* wperm;        // [cap] routing weight of pair p
   int M, E, k, L, cap, bn, nblocks;
-  // MX layers: the gathered token scale bytes as one 512-byte tile per (routed tile of bn
-  // = 128 pairs, 128-column k-block), laid out for tcgen05.cp: byte r%32*16 + 4*(r/32) + j
-  // = scale of tile row r, 32-column group j of the k-block (rows past the tile: scale 1)
-  const uint8_t* zsx;  // [M, L/32]
-  uint8_t* zsf_t;      // [tile capacity, L/128, 512]
+  // Block-scaled layers: the gathered token scale bytes as 512-byte tiles, one per
+  // (routed tile of bn = 128 pairs, 4 consecutive scale bytes of a row), laid out for
+  // tcgen05.cp: byte r%32*16 + 4*(r/32) + j = scale 4a + j of tile row r in tile a (rows
+  // past the tile: scale 1).  sf_group columns per scale byte: 32 (MX, a tile per
+  // 128-column k-block) or 16 (NVFP4 activations, a tile per 64 columns).
+  const uint8_t* zsx;  // [M, L/sf_group]
+  uint8_t* zsf_t;      // [tile capacity, L/(4 sf_group), 512]
   int sf_tiles;        // tile capacity (grid bound; tile_off[E] of the batch is <= it)
+  int sf_group;
+  int zrow;            // bytes per quantised latent row: L (e4m3) or L/2 (packed e2m1)
 };
 
 struct NormParams {
@@ -115,11 +125,13 @@ struct GemmTask {
                        // that share its weight tiles (units = ceil(ntiles / 2) * ftiles)
   int units;           // non-routed: ntiles * ftiles * ksplit
   int dep;             // DepKind of this task's units
-  // MX block-scaled units (token-major engine): scale tiles of 512 bytes in the tcgen05.cp
-  // layout, the weights' per (128-row block, k-block) like their data tiles, the tokens'
-  // per (routed tile, k-block); null for other tasks
+  // Block-scaled units (token-major engine): scale tiles of 512 bytes in the tcgen05.cp
+  // layout, the weights' per 128-row block like their data tiles, the tokens' per routed
+  // tile, in K order (MX: one tile per k-block; NVFP4: four, one per 64-wide MMA);
+  // null for other tasks
   const uint8_t* a_sf;
   const uint8_t* t_sf;
+  const float* a_g;    // NVFP4 units: the weights' fp32 per-matrix scale [E] (epilogue)
   int ws_tile_base;    // first arrival counter of this task (tile ids start here)
   long long ws_off;    // float offset of this task's partials in the workspace
   int streamk;         // 1: static stream-K partition of ntiles*ftiles*kb_total k-blocks
@@ -176,10 +188,12 @@ struct GemmParams {
   // preceding kernel (16-byte aligned, a multiple of 16 bytes; null/0: none)
   const uint8_t* pf_ptr;
   long long pf_bytes;
-  int mx;                      // token-major engine, MX layer: block-scaled routed units
-                               // (one accumulator slot; the scale ring takes the other half
-                               // of TMEM) and the routed L1 epilogue requantises per 32 with
-  uint8_t* asf_t;              //   power-of-two scales into these tiles [tiles, I/128, 512]
+  int bs;                      // token-major engine, block-scaled layer (BlockScale):
+                               // block-scaled routed units (one accumulator slot; the scale
+                               // ring takes the other half of TMEM) and the routed L1
+                               // epilogue requantises (MX: per 32 with power-of-two scales;
+                               // NVFP4: per 16 to e2m1 with e4m3 scales) into aq and the
+  uint8_t* asf_t;              //   token scale tiles of the L2 [tiles, I/(4 group), 512]
   __nv_bfloat16* zp;           // projection outputs: latent input [M, L]
   float* lgp;                  //   and router logits [M, E]
   long long* trace;            // optional timestamp trace (this launch's region)
@@ -206,10 +220,10 @@ cudaError_t launch_fill_expert_scale(const float* g, float* dst, int E, long lon
                                      cudaStream_t s);
 cudaError_t launch_tile_relayout(const void* src, void* dst, long long rows, long long row_bytes,
                                  cudaStream_t s);
-// UE8M0 scale bytes [rows, K/32] (rows % 128 == 0, K % 128 == 0) -> 512-byte tiles per
-// (128-row block rb, k-block kb) at (rb * K/128 + kb) * 512, byte (r%32)*16 + 4*((r%128)/32)
-// + j = scale of row r, 32-column group 4*kb + j (the tcgen05.cp 32x128b layout).
-cudaError_t launch_sf_relayout(const uint8_t* src, uint8_t* dst, long long rows, long long K,
+// Scale bytes [rows, nsc] (rows % 128 == 0, nsc % 4 == 0) -> 512-byte tiles per (128-row
+// block rb, group of 4 scale bytes a) at (rb * nsc/4 + a) * 512, byte (r%32)*16 +
+// 4*((r%128)/32) + j = scale 4a + j of row r (the tcgen05.cp 32x128b layout).
+cudaError_t launch_sf_relayout(const uint8_t* src, uint8_t* dst, long long rows, long long nsc,
                                cudaStream_t s);
 // bn in {16, 128}; grid = persistent CTAs.
 cudaError_t launch_gemm(const GemmParams& p, int bn, int grid, cudaStream_t s, bool pdl);

@@ -100,7 +100,26 @@ __global__ void __launch_bounds__(32 * ROUTE_WARPS)
   const float v2 = __low2float(b23), v3 = __high2float(b23);
   float amax = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
   uint32_t q;
-  if (p.mx) {
+  if (p.bs == BS_NV4) {
+    // NVFP4: per 16 columns (4 lanes) s = e4m3(amax / 6), codes e2m1(v / s) (a zero scale
+    // gives zero codes); quotients correctly rounded in fp32; two codes per byte, the even
+    // column in the low nibble
+#pragma unroll
+    for (int o = 2; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const uint8_t sc = f32_to_e4m3(amax / 6.0f);
+    const float s = e4m3_to_f32(sc);
+    uint32_t c = 0;
+    if (s != 0.f)
+      c = f32_to_e2m1(v0 / s) | (f32_to_e2m1(v1 / s) << 4) | (f32_to_e2m1(v2 / s) << 8) |
+          (f32_to_e2m1(v3 / s) << 12);
+    if ((lane & 3) == 0) p.zsx[static_cast<size_t>(t) * (p.L / 16) + g * 8 + (lane >> 2)] = sc;
+    *reinterpret_cast<uint16_t*>(p.zq + static_cast<size_t>(t) * (p.L / 2) + g * 64 +
+                                 lane * 2) = static_cast<uint16_t>(c);
+    reinterpret_cast<float4*>(p.r + static_cast<size_t>(t) * p.L + g * 128)[lane] =
+        make_float4(0.f, 0.f, 0.f, 0.f);
+    return;
+  }
+  if (p.bs == BS_MX8) {
     // MX: one power-of-two scale per 32 columns (8 lanes): 2^(floor(log2 amax) - 8); the
     // quotient by a power of two is exact, so the codes equal e4m3(v / scale)
 #pragma unroll
@@ -231,16 +250,16 @@ __global__ void __launch_bounds__(256) perm_gather_kernel(const PermParams p) {
   pdl_trigger();  // dependents may launch now; they wait for this grid before reading
   pdl_wait();
   const int G = p.L / 128;
-  const int row16 = p.L / 16;
+  const int row16 = p.zrow / 16;  // 16-byte chunks of a quantised latent row
   const long long Mk = static_cast<long long>(p.M) * p.k;
   const long long c = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
   if (c < Mk * row16) {
     const int pp = static_cast<int>(c / row16);
     const int ch = static_cast<int>(c - static_cast<long long>(pp) * row16);
     const int t = __ldg(p.gidx + pp);
-    const uint4 v = reinterpret_cast<const uint4*>(p.zq + static_cast<size_t>(t) * p.L)[ch];
+    const uint4 v = reinterpret_cast<const uint4*>(p.zq + static_cast<size_t>(t) * p.zrow)[ch];
     if (p.zqb_perm == nullptr) {
-      reinterpret_cast<uint4*>(p.zq_perm + static_cast<size_t>(pp) * p.L)[ch] = v;
+      reinterpret_cast<uint4*>(p.zq_perm + static_cast<size_t>(pp) * p.zrow)[ch] = v;
     } else {  // exact bf16 image of every e4m3 code (bf16-operand layers)
       const uint8_t* b = reinterpret_cast<const uint8_t*>(&v);
       uint32_t o[8];
@@ -262,11 +281,14 @@ __global__ void __launch_bounds__(256) perm_gather_kernel(const PermParams p) {
     p.zsT[static_cast<size_t>(g) * p.cap + pp] =
         p.zs[static_cast<size_t>(__ldg(p.gidx + pp)) * G + g];
   }
-  // MX layers: the token scale tiles of every routed tile (one 4-byte word per tile row and
-  // k-block); rows past the tile's pairs get scale 1 (their products are never stored)
-  if (p.zsf_t != nullptr && c < static_cast<long long>(p.sf_tiles) * 128 * G) {
-    const int tile = static_cast<int>(c / (128LL * G));
-    const int rem = static_cast<int>(c - static_cast<long long>(tile) * 128 * G);
+  // Block-scaled layers: the token scale tiles of every routed tile (one 4-byte word per
+  // tile row and tile a); rows past the tile's pairs get a unit scale (their products are
+  // never stored)
+  const int nsc = p.L / p.sf_group;  // scale bytes per row
+  const int NA = nsc / 4;            // scale tiles per routed tile
+  if (p.zsf_t != nullptr && c < static_cast<long long>(p.sf_tiles) * 128 * NA) {
+    const int tile = static_cast<int>(c / (128LL * NA));
+    const int rem = static_cast<int>(c - static_cast<long long>(tile) * 128 * NA);
     const int kb = rem / 128, r = rem - (rem / 128) * 128;
     if (tile < p.tile_off[p.E]) {
       int lo = 0, hi = p.E - 1;  // largest e with tile_off[e] <= tile
@@ -275,11 +297,12 @@ __global__ void __launch_bounds__(256) perm_gather_kernel(const PermParams p) {
         if (__ldg(p.tile_off + mid) <= tile) lo = mid; else hi = mid - 1;
       }
       const int pp = __ldg(p.off + lo) + (tile - __ldg(p.tile_off + lo)) * p.bn + r;
-      uint32_t word = 0x7F7F7F7Fu;
+      // unit scale: UE8M0 127 (MX) or e4m3 1.0 (NVFP4)
+      uint32_t word = p.sf_group == 32 ? 0x7F7F7F7Fu : 0x38383838u;
       if (pp < __ldg(p.off + lo + 1))
         word = *reinterpret_cast<const uint32_t*>(
-            p.zsx + static_cast<size_t>(__ldg(p.gidx + pp)) * (p.L / 32) + 4 * kb);
-      *reinterpret_cast<uint32_t*>(p.zsf_t + (static_cast<size_t>(tile) * G + kb) * 512 +
+            p.zsx + static_cast<size_t>(__ldg(p.gidx + pp)) * nsc + 4 * kb);
+      *reinterpret_cast<uint32_t*>(p.zsf_t + (static_cast<size_t>(tile) * NA + kb) * 512 +
                                    (r & 31) * 16 + 4 * (r >> 5)) = word;
     }
   }
@@ -359,14 +382,14 @@ __global__ void __launch_bounds__(256)
 }
 
 __global__ void __launch_bounds__(256)
-    sf_relayout_kernel(const uint8_t* src, uint8_t* dst, long long rows, long long K) {
-  const long long kbs = K / 128;
+    sf_relayout_kernel(const uint8_t* src, uint8_t* dst, long long rows, long long nsc) {
+  const long long na = nsc / 4;  // 512-byte tiles per 128-row block
   const long long q = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
-  if (q >= rows * kbs) return;
-  const long long row = q / kbs, kb = q - row * kbs;
-  const uint32_t word = *reinterpret_cast<const uint32_t*>(src + row * (K / 32) + 4 * kb);
+  if (q >= rows * na) return;
+  const long long row = q / na, a = q - row * na;
+  const uint32_t word = *reinterpret_cast<const uint32_t*>(src + row * nsc + 4 * a);
   const long long rb = row >> 7, r = row & 127;
-  *reinterpret_cast<uint32_t*>(dst + (rb * kbs + kb) * 512 + (r & 31) * 16 + 4 * (r >> 5)) = word;
+  *reinterpret_cast<uint32_t*>(dst + (rb * na + a) * 512 + (r & 31) * 16 + 4 * (r >> 5)) = word;
 }
 
 __global__ void __launch_bounds__(256)
@@ -405,11 +428,13 @@ cudaError_t launch_perm_scatter(const PermParams& p, cudaStream_t s, bool pdl) {
   return launch_simple(perm_scatter_kernel, dim3(p.nblocks), dim3(PERM_BLOCK), p, s, pdl);
 }
 cudaError_t launch_perm_gather(const PermParams& p, cudaStream_t s, bool pdl) {
-  long long chunks = static_cast<long long>(p.M) * p.k * (p.L / 16);
-  if (p.zsf_t != nullptr)
-    chunks = chunks > static_cast<long long>(p.sf_tiles) * 128 * (p.L / 128)
-                 ? chunks
-                 : static_cast<long long>(p.sf_tiles) * 128 * (p.L / 128);
+  long long chunks = static_cast<long long>(p.M) * p.k * (p.zrow / 16);
+  if (chunks < static_cast<long long>(p.M) * p.k * (p.L / 128))  // zsT transposition
+    chunks = static_cast<long long>(p.M) * p.k * (p.L / 128);
+  if (p.zsf_t != nullptr) {
+    const long long sf = static_cast<long long>(p.sf_tiles) * 128 * (p.L / p.sf_group / 4);
+    chunks = chunks > sf ? chunks : sf;
+  }
   return launch_simple(perm_gather_kernel, dim3(static_cast<unsigned>((chunks + 255) / 256)),
                        dim3(256), p, s, pdl);
 }
@@ -431,10 +456,11 @@ cudaError_t launch_fill_expert_scale(const float* g, float* dst, int E, long lon
                                                                                     per);
   return cudaGetLastError();
 }
-cudaError_t launch_sf_relayout(const uint8_t* src, uint8_t* dst, long long rows, long long K,
+cudaError_t launch_sf_relayout(const uint8_t* src, uint8_t* dst, long long rows, long long nsc,
                                cudaStream_t s) {
-  const long long n = rows * (K / 128);
-  sf_relayout_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(src, dst, rows, K);
+  const long long n = rows * (nsc / 4);
+  sf_relayout_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(src, dst, rows,
+                                                                              nsc);
   return cudaGetLastError();
 }
 cudaError_t launch_tile_relayout(const void* src, void* dst, long long rows, long long row_bytes,

@@ -51,6 +51,17 @@ struct W {
   static constexpr int SF_STAGE = 3 * 512;     // MX scale tiles per stage
   static constexpr int SF_COLS = 12;           // TMEM columns of one stage's scales
   static_assert(TN + STAGES * SF_COLS <= TMEM_COLS, "MX scale ring beside one slot");
+  // NVFP4 (e2m1 x e2m1) routed units: each stage also carries their scale tiles after the
+  // token tile (4 x 512 bytes for the 128 token rows and 8 x 512 for the 256 weight rows,
+  // one tile per 64-wide MMA), in a ring of 3 stages; a stage's tiles take 48 TMEM
+  // columns beside the single accumulator slot.
+  static constexpr int NV4_SF_BYTES = 12 * 512;
+  static constexpr int NV4_STAGE_BYTES = STAGE_BYTES + NV4_SF_BYTES;
+  static constexpr int NV4_STAGES = 3;
+  static constexpr int NV4_SF_COLS = 48;
+  static_assert(NV4_STAGES * NV4_STAGE_BYTES <= STAGES * STAGE_BYTES, "NVFP4 ring fits");
+  static_assert(NV4_STAGE_BYTES % 1024 == 0, "stage alignment of the swizzled tiles");
+  static_assert(TN + NV4_STAGES * NV4_SF_COLS <= TMEM_COLS, "NVFP4 scale ring beside one slot");
   static constexpr int US = 8;
   static constexpr int SIG = 8;             // completion-signal ring (epilogue -> signaller)
   static constexpr int SIGNAL_WARP = 2;     // control warp that publishes unit completions
@@ -233,9 +244,9 @@ __device__ bool w_wait_dependency(const GemmParams& p, int dep, int idx, const i
 }
 
 // ------------------------------------------------------------------ producer (1 thread)
-// MX: the launch carries block-scaled routed units (their own kernel instantiation, so the
-// other launches keep their code and registers unchanged).
-template <bool MX>
+// BS: the launch carries block-scaled routed units of that format (their own kernel
+// instantiation, so the other launches keep their code and registers unchanged).
+template <int BS>
 __device__ void w_producer(const GemmParams& p, WSmem& sm, const int* s_tile_off,
                            const int* s_off, int u0) {
   // weights are re-read by every token tile of their expert, tokens by every feature tile
@@ -262,7 +273,8 @@ __device__ void w_producer(const GemmParams& p, WSmem& sm, const int* s_tile_off
     }
     const GemmTask& T = p.task[info.task];
     const int elems_per_kb = T.fp8 ? 128 : 64;
-    const bool mxu = MX && T.a_sf != nullptr;  // block-scaled unit: scale tiles ride along
+    const bool mxu = BS == BS_MX8 && T.a_sf != nullptr;  // block-scaled: scale tiles ride along
+    const bool nvu = BS == BS_NV4 && T.a_sf != nullptr;
     auto issue_w = [&](int kb, uint8_t* st) {
       const int m = kb < T.kb_split0 ? 0 : 1;
       const int kk = m ? kb - T.kb_split0 : kb;
@@ -279,6 +291,13 @@ __device__ void w_producer(const GemmParams& p, WSmem& sm, const int* s_tile_off
         bulk_load(sf + 1024, T.a_sf + (static_cast<size_t>(info.rb1) * akb + kk) * 512, 512,
                   &sm.full[stage], pol_w);
       }
+      if (nvu) {  // the four 512-byte tiles of each weight row block for this k-block
+        uint8_t* sf = st + 2 * W::W_TILE + W::T_TILE;
+        bulk_load(sf + 2048, T.a_sf + (static_cast<size_t>(info.rb0) * akb + kk) * 2048, 2048,
+                  &sm.full[stage], pol_w);
+        bulk_load(sf + 4096, T.a_sf + (static_cast<size_t>(info.rb1) * akb + kk) * 2048, 2048,
+                  &sm.full[stage], pol_w);
+      }
     };
     auto issue_t = [&](int kb, uint8_t* st, uint64_t* bar, int stg_idx) {
       const int m = kb < T.kb_split0 ? 0 : 1;
@@ -291,10 +310,14 @@ __device__ void w_producer(const GemmParams& p, WSmem& sm, const int* s_tile_off
         bulk_load(sm.sf + stg_idx * W::SF_STAGE,
                   T.t_sf + (static_cast<size_t>(info.dep_idx) * T.kb_total + kk) * 512, 512, bar,
                   pol);
+      if (nvu)  // the routed tile's four token scale tiles of the k-block
+        bulk_load(st + 2 * W::W_TILE + W::T_TILE,
+                  T.t_sf + (static_cast<size_t>(info.dep_idx) * T.kb_total + kk) * 2048, 2048,
+                  bar, pol);
     };
     const uint32_t stage_tx = 2 * W::W_TILE +
                               (info.dual ? 2 : 1) * static_cast<uint32_t>(W::T_TILE) +
-                              (mxu ? W::SF_STAGE : 0);
+                              (mxu ? W::SF_STAGE : 0) + (nvu ? W::NV4_SF_BYTES : 0);
     const int kb_end = T.kb_total;
     int kb = 0;
     if (T.dep != DEP_NONE) {
@@ -361,7 +384,7 @@ __device__ void w_producer(const GemmParams& p, WSmem& sm, const int* s_tile_off
 }
 
 // ------------------------------------------------------------------ MMA issuer (1 thread)
-template <bool MX>
+template <int BS>
 __device__ void w_mma(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
   int stage = 0, us = 0, acc = 0;
   uint32_t phase = 0, uphase = 0, aphase = 0;
@@ -372,8 +395,10 @@ __device__ void w_mma(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
   const uint64_t desc_b0 = sdesc_sw128(smem_u32(sm.stages));
   const uint64_t desc_a0 = desc_b0 + ((2 * W::W_TILE) >> 4);
   const uint64_t STAGE_D = static_cast<uint64_t>(p.w_stage_bytes) >> 4;
-  // accumulator slots: one in MX launches (the scale ring takes the other half of TMEM)
-  constexpr int nacc = MX ? 1 : W::NACC;
+  // accumulator slots: one in block-scaled launches (the scale ring takes the other half of
+  // TMEM)
+  constexpr int nacc = BS != BS_NONE ? 1 : W::NACC;
+  constexpr uint32_t idesc_fp4 = idesc_nv4(W::TM, W::TN);
   while (ok) {
     if (!mbar_wait(&sm.ufull[us], uphase, sm.abort_flag, p.err, p.timeout)) break;
     const WUnit info = sm.ring[us];
@@ -391,7 +416,8 @@ __device__ void w_mma(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
     // the slot after `acc` (the second tile of a dual unit) and its phase parity
     const int acc2 = acc + 1 == nacc ? 0 : acc + 1;
     const uint32_t aphase2 = acc + 1 == nacc ? aphase ^ 1 : aphase;
-    const bool mxu = MX && T.a_sf != nullptr;  // block-scaled FP8 unit
+    const bool mxu = BS == BS_MX8 && T.a_sf != nullptr;  // block-scaled FP8 unit
+    const bool nvu = BS == BS_NV4 && T.a_sf != nullptr;  // block-scaled FP4 unit
     if (!promote) {
       if (!mbar_wait_spin(&sm.tempty[acc], aphase ^ 1, sm.abort_flag, p.err, p.timeout)) break;
       if (dual &&
@@ -417,7 +443,25 @@ __device__ void w_mma(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
       const uint64_t off = static_cast<uint64_t>(stage) * STAGE_D;
       const uint32_t accum = promote ? static_cast<uint32_t>(gpos > 0)
                                      : static_cast<uint32_t>(kb > 0);
-      if (mxu) {
+      if (nvu) {
+        // this stage's twelve scale tiles into its 48 TMEM columns beside the accumulator:
+        // MMA j (K = 64) reads the tokens' at +4j (lane m, column m/32) and the weights'
+        // at +16 + 8j (lane n%32, column n/32 over both row blocks), then the four MMAs
+        const uint32_t sfc = tmem_base + W::TN + static_cast<uint32_t>(stage * W::NV4_SF_COLS);
+        const uint32_t sfs =
+            smem_u32(sm.stages + static_cast<size_t>(stage) * p.w_stage_bytes + 2 * W::W_TILE +
+                     W::T_TILE);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          tmem_cp_32x128b_x4(sfc + 4 * j, sfs + 512 * j);
+          tmem_cp_32x128b_x4(sfc + 16 + 8 * j, sfs + 2048 + 512 * j);
+          tmem_cp_32x128b_x4(sfc + 20 + 8 * j, sfs + 4096 + 512 * j);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          mma_nv4(d, desc_a0 + off + 2 * j, desc_b0 + off + 2 * j, idesc_fp4, sfc + 4 * j,
+                  sfc + 16 + 8 * j, static_cast<uint32_t>(kb > 0 || j > 0));
+      } else if (mxu) {
         // this stage's scale tiles into its TMEM columns beside the accumulator (tokens:
         // lane m column m/32; weights: lane n%32 column 4 + n/32), then the four K = 32
         // MMAs of the k-block, each with the scale byte of its 32-wide chunk
@@ -570,7 +614,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <bool DET, bool MX>
+template <bool DET, int BS>
 __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ew = warp - W::FIRST_EPI_WARP;
@@ -582,7 +626,7 @@ __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
   uint32_t uphase = 0, aphase = 0;
   SigState sg;
   const int G_L = p.L / 128, G_I = p.I / 128;
-  constexpr int nacc = MX ? 1 : W::NACC;
+  constexpr int nacc = BS != BS_NONE ? 1 : W::NACC;
 
   for (;;) {
     if (!mbar_wait(&sm.ufull[us], uphase, sm.abort_flag, p.err, p.timeout)) return;
@@ -695,7 +739,53 @@ __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
       }
 
       // ---- unit end (this thread: one token, 64 gate/up pairs or 128 features)
-      if (MX && kind == TASK_ROUTED_L1) {
+      // NVFP4 units: the weights' fp32 per-matrix scale of this expert (the tensor core
+      // applied the per-16 scales); for the routed L2 it folds into the routing weight
+      if (BS == BS_NV4 && T.a_g != nullptr && kind == TASK_ROUTED_L2) wv *= __ldg(T.a_g + info.e);
+      if (BS == BS_NV4 && kind == TASK_ROUTED_L1) {
+        // scale by the expert's fp32 matrix scale, SwiGLU, then NVFP4: per 16 outputs an
+        // e4m3 scale s = e4m3(amax / 6) and e2m1 codes of a / s (a zero scale gives zero
+        // codes).  This thread's 64 outputs are one 64-wide MMA step of the routed L2, so
+        // its four scale bytes are one word of that step's token scale tile.
+        const float gw = __ldg(T.a_g + info.e);
+  #pragma unroll
+        for (int i = 0; i < 64; ++i) a[i] = silu_fast(gw * a[i]) * (gw * a[64 + i]);
+        uint32_t sfw = 0x38383838u;  // rows past the tile's pairs: scale 1
+        if (valid) {
+          uint32_t w8[8];  // 64 codes, two per byte
+          sfw = 0;
+  #pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            float m = 0.f;
+  #pragma unroll
+            for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(a[16 * b + i]));
+            const uint32_t sc = f32_to_e4m3(m / 6.0f);
+            const float s = e4m3_to_f32(static_cast<uint8_t>(sc));
+            const float inv = s != 0.f ? rcp_nr(s) : 0.f;
+  #pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              uint32_t w = 0;
+              if (s != 0.f) {
+  #pragma unroll
+                for (int i = 0; i < 8; ++i)
+                  w |= f32_to_e2m1(quot_rn(a[16 * b + 8 * q + i], s, inv)) << (4 * i);
+              }
+              w8[2 * b + q] = w;
+            }
+            sfw |= sc << (8 * b);
+          }
+          const size_t pp = static_cast<size_t>(row0 + tok);
+          uint4* dq = reinterpret_cast<uint4*>(p.aq + pp * (p.I / 2) +
+                                               (static_cast<size_t>(info.ftile) * 128 + half * 64) / 2);
+          dq[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+          dq[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+        }
+        *reinterpret_cast<uint32_t*>(p.asf_t +
+                                     (static_cast<size_t>(dep_idx) * (p.I / 64) +
+                                      2 * info.ftile + half) * 512 +
+                                     (tok & 31) * 16 + 4 * (tok >> 5)) = sfw;
+        if (p.l1_done != nullptr) w_signal(p, sm, sg, p.l1_done + dep_idx, ew, lane);
+      } else if (BS == BS_MX8 && kind == TASK_ROUTED_L1) {
         // SwiGLU, then MX e4m3: one power-of-two scale per 32 outputs, 2^(floor(log2 amax)
         // - 8); this thread's 64 outputs are two whole groups, so no other thread is
         // involved.  The scale bytes go to the routed L2 units' token scale tile of this
@@ -863,7 +953,7 @@ __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
   }
 }
 
-template <bool DET, bool MX>
+template <bool DET, int BS>
 __global__ void __launch_bounds__(W::THREADS, 1) wide_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   WSmem sm(smem_raw);
@@ -941,15 +1031,15 @@ __global__ void __launch_bounds__(W::THREADS, 1) wide_kernel(const __grid_consta
   if (warp < W::FIRST_EPI_WARP) {
     regs_dec<W::REGS_CTRL>();
     if (warp == 0) {
-      if (lane == 0) w_producer<MX>(p, sm, s_tile_off, s_off, u0);
+      if (lane == 0) w_producer<BS>(p, sm, s_tile_off, s_off, u0);
     } else if (warp == 1) {
-      if (lane == 0) w_mma<MX>(p, sm, tmem_base);
+      if (lane == 0) w_mma<BS>(p, sm, tmem_base);
     } else if (warp == W::SIGNAL_WARP) {
       if (lane == 0) w_signaller(p, sm);
     }
   } else {
     regs_inc<W::REGS_EPI>();
-    w_epilogue<DET, MX>(p, sm, tmem_base);
+    w_epilogue<DET, BS>(p, sm, tmem_base);
   }
 
   tc_fence_before();
@@ -965,11 +1055,20 @@ __global__ void __launch_bounds__(W::THREADS, 1) wide_kernel(const __grid_consta
 
 static_assert(WSmem::bytes() + 2 * (MAX_E + 1) * 4 <= 227 * 1024, "shared memory budget");
 
+// The six instantiations: deterministic combine or not x no block scale, MX, NVFP4.
+const void* wide_fn(bool det, int bs) {
+  if (det)
+    return bs == BS_MX8   ? reinterpret_cast<const void*>(wide_kernel<true, BS_MX8>)
+           : bs == BS_NV4 ? reinterpret_cast<const void*>(wide_kernel<true, BS_NV4>)
+                          : reinterpret_cast<const void*>(wide_kernel<true, BS_NONE>);
+  return bs == BS_MX8   ? reinterpret_cast<const void*>(wide_kernel<false, BS_MX8>)
+         : bs == BS_NV4 ? reinterpret_cast<const void*>(wide_kernel<false, BS_NV4>)
+                        : reinterpret_cast<const void*>(wide_kernel<false, BS_NONE>);
+}
+
 int wide_kernel_regs() {  // every instantiation must launch with the planned registers
-  const void* k[] = {reinterpret_cast<const void*>(wide_kernel<false, false>),
-                     reinterpret_cast<const void*>(wide_kernel<true, false>),
-                     reinterpret_cast<const void*>(wide_kernel<false, true>),
-                     reinterpret_cast<const void*>(wide_kernel<true, true>)};
+  const void* k[] = {wide_fn(false, BS_NONE), wide_fn(true, BS_NONE), wide_fn(false, BS_MX8),
+                     wide_fn(true, BS_MX8),   wide_fn(false, BS_NV4), wide_fn(true, BS_NV4)};
   int regs = -1;
   for (const void* f : k) {
     cudaFuncAttributes a;
@@ -984,12 +1083,8 @@ bool wide_regs_ok(int regs) { return regs == W::LAUNCH_REGS; }
 
 cudaError_t launch_wide(const GemmParams& p, int grid, cudaStream_t s, bool pdl) {
   const int smem = WSmem::bytes();
-  // the deterministic combine and the MX launches are instantiations of their own
-  const bool det = p.yw != nullptr, mx = p.mx != 0;
-  const void* f = det ? (mx ? reinterpret_cast<const void*>(wide_kernel<true, true>)
-                            : reinterpret_cast<const void*>(wide_kernel<true, false>))
-                      : (mx ? reinterpret_cast<const void*>(wide_kernel<false, true>)
-                            : reinterpret_cast<const void*>(wide_kernel<false, false>));
+  // the deterministic combine and the block-scaled launches are instantiations of their own
+  const void* f = wide_fn(p.yw != nullptr, p.bs);
   cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -1002,10 +1097,8 @@ cudaError_t launch_wide(const GemmParams& p, int grid, cudaStream_t s, bool pdl)
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  if (det) return mx ? cudaLaunchKernelEx(&cfg, wide_kernel<true, true>, p)
-                     : cudaLaunchKernelEx(&cfg, wide_kernel<true, false>, p);
-  return mx ? cudaLaunchKernelEx(&cfg, wide_kernel<false, true>, p)
-            : cudaLaunchKernelEx(&cfg, wide_kernel<false, false>, p);
+  void* args[] = {const_cast<GemmParams*>(&p)};
+  return cudaLaunchKernelExC(&cfg, f, args);
 }
 
 }  // namespace klt

@@ -10,7 +10,7 @@ import torch
 
 from latent_moe_layer_route_gb300 import binding as B
 from oracle import model as T
-from oracle.codecs import e4m3_decode
+from oracle.codecs import e4m3_decode, unpack_e2m1
 
 # Output bar of the tail (float): relative Frobenius error and per-element bound.
 REL_FRO = 5e-3
@@ -38,9 +38,10 @@ class Run:
         self.gidx = torch.full((M * k,), -7, **i32)
         self.slot = torch.full((M * k,), -7, **i32)
         self.pos = torch.full((M, k), -7, **i32)
-        self.zq = torch.zeros((M, L), dtype=torch.uint8, device=dev)
+        a4 = cfg.routed_fmt == "nvfp4_w4a4"  # codes packed two per byte
+        self.zq = torch.zeros((M, L // 2 if a4 else L), dtype=torch.uint8, device=dev)
         self.zs = torch.zeros((M, L // 128), dtype=torch.float32, device=dev)
-        self.aq = torch.zeros((M * k, I), dtype=torch.uint8, device=dev)
+        self.aq = torch.zeros((M * k, I // 2 if a4 else I), dtype=torch.uint8, device=dev)
         self.as_ = torch.zeros((M * k, I // 128), dtype=torch.float32, device=dev)
         self.r = torch.zeros((M, L), dtype=torch.float32, device=dev)
         self.n = torch.zeros((M, L), dtype=torch.bfloat16, device=dev)
@@ -55,8 +56,9 @@ class Run:
         dbg.stall_after_kblocks = stall_after
         dbg.timeout_ms = timeout_ms
         dbg.force_bn = force_bn
-        if cfg.routed_fmt == "mxfp8":  # power-of-two scale bytes of the latent input
-            self.zsx = torch.zeros((M, L // 32), dtype=torch.uint8, device=dev)
+        if cfg.routed_fmt in ("mxfp8", "nvfp4_w4a4"):  # scale bytes of the latent input
+            self.zsx = torch.zeros((M, L // (32 if cfg.routed_fmt == "mxfp8" else 16)),
+                                   dtype=torch.uint8, device=dev)
             dbg.zsx = self.zsx.data_ptr()
         if hidden:  # latent input and logits computed from x by the library
             self.z = torch.zeros((M, L), dtype=torch.bfloat16, device=dev)
@@ -106,12 +108,18 @@ def check_stages(run: Run, o: Dict, cfg, combine_buffer: bool = True):
     the forward ran the fixed-order combine, which keeps no fp32 combine row (its sum is
     checked through the normalised latent and the output)."""
     tok = o["tokens"]
+    a4 = cfg.routed_fmt == "nvfp4_w4a4"
     zq = run.host("zq").numpy()[tok]
+    if a4:  # e2m1 codes, two per byte (even column in the low nibble)
+        zq = unpack_e2m1(zq)
     np.testing.assert_array_equal(zq, o["zq"])
     pos = o["pos"][tok]
-    aq = run.host("aq").numpy()[pos.reshape(-1)].reshape(len(tok), cfg.topk, cfg.I)
-    if cfg.routed_fmt == "mxfp8":
-        # power-of-two scale bytes of the latent input, exact; the routed activations'
+    aq = run.host("aq").numpy()[pos.reshape(-1)]
+    if a4:
+        aq = unpack_e2m1(aq)
+    aq = aq.reshape(len(tok), cfg.topk, cfg.I)
+    if cfg.routed_fmt in ("mxfp8", "nvfp4_w4a4"):
+        # scale bytes of the latent input (UE8M0 or e4m3), exact; the routed activations'
         # scale bytes live in the tensor-core tiles only, so their codes are compared
         np.testing.assert_array_equal(run.host("zsx").numpy()[tok], o["zs"])
     else:
