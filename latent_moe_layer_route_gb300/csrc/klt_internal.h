@@ -243,6 +243,7 @@ bool wide_regs_ok(int regs);
 
 constexpr int PERM_BLOCK = 1024;  // pairs per permutation block
 constexpr int ROUTE_WARPS = 8;    // warps per routing block
+constexpr int ROUTE_QG = 4;       // 128-column latent groups quantised per routing warp
 constexpr int MAX_TOPK = 32;
 constexpr int MAX_E = 256;
 constexpr int MAX_KB = 32;       // routed K blocks of 128 per unit (L, I <= 4096)

@@ -23,77 +23,11 @@ __device__ __forceinline__ uint32_t ordered_key(float v) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Warp w handles token t = w / (G + 1): part 0 routes the token, part g + 1 quantises
-// its 128-column group g of z and zeroes the matching 128 floats of the combine buffer.
-__global__ void __launch_bounds__(32 * ROUTE_WARPS)
-    route_quant_kernel(const RouteParams p) {
-  pdl_trigger();  // dependents may launch now; they wait for this grid before reading
-  pdl_wait();
-  const int lane = lane_id();
-  if (blockIdx.x == 0 && threadIdx.x < p.nsched) p.sched[threadIdx.x] = 0;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-       i < p.zero_n; i += static_cast<long long>(gridDim.x) * blockDim.x)
-    p.zero_buf[i] = 0;
+// Quantisation of 128-column group g of token t's latent row (4 columns per lane, already
+// loaded into `raw`), and zeroing of the matching 128 floats of the combine buffer.
+__device__ __forceinline__ void quant_group(const RouteParams& p, int t, int g, uint2 raw,
+                                            int lane) {
   const int G = p.L / 128;
-  const long long w = static_cast<long long>(blockIdx.x) * ROUTE_WARPS + (threadIdx.x >> 5);
-  const int t = static_cast<int>(w / (G + 1));
-  const int part = static_cast<int>(w - static_cast<long long>(t) * (G + 1));
-  if (t >= p.M) return;
-
-  if (part == 0) {
-    // ---- top-k selection: key = (ordered logit, inverted index) so larger key wins and
-    // equal logits go to the lower expert index.
-    const float* lg = p.logits + static_cast<size_t>(t) * p.E;
-    constexpr int PER_LANE = MAX_E / 32;
-    uint32_t keys[PER_LANE];
-#pragma unroll
-    for (int i = 0; i < PER_LANE; ++i) {
-      const int e = lane + 32 * i;
-      keys[i] = e < p.E ? ordered_key(__ldg(lg + e)) : 0u;
-    }
-    uint32_t taken = 0;  // bit i: entry i of this lane already selected
-    int my_idx = 0;
-    float my_val = 0.f;
-    for (int j = 0; j < p.k; ++j) {
-      unsigned long long best = 0ull;
-#pragma unroll
-      for (int i = 0; i < PER_LANE; ++i) {
-        const int e = lane + 32 * i;
-        if (e < p.E && !(taken >> i & 1u)) {
-          const unsigned long long kk =
-              (static_cast<unsigned long long>(keys[i]) << 32) | (0xFFFFFFFFu - e);
-          best = kk > best ? kk : best;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-        best = other > best ? other : best;
-      }
-      const int e =
-          static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best & 0xFFFFFFFFull));
-      if ((e & 31) == lane) taken |= 1u << (e >> 5);
-      if (lane == j) {
-        my_idx = e;
-        my_val = __ldg(lg + e);
-      }
-    }
-    const float vmax = __shfl_sync(0xFFFFFFFFu, my_val, 0);
-    const float ex = lane < p.k ? expf(my_val - vmax) : 0.f;
-    float sum = ex;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-    if (lane < p.k) {
-      p.ids[static_cast<size_t>(t) * p.k + lane] = my_idx;
-      p.wts[static_cast<size_t>(t) * p.k + lane] = ex / sum;
-    }
-    return;
-  }
-
-  // ---- e4m3 quantisation of one 128-column group (4 columns per lane)
-  const int g = part - 1;
-  const __nv_bfloat16* zr = p.z + static_cast<size_t>(t) * p.L + g * 128;
-  const uint2 raw = *reinterpret_cast<const uint2*>(zr + lane * 4);
   const __nv_bfloat162 b01 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
   const __nv_bfloat162 b23 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
   const float v0 = __low2float(b01), v1 = __high2float(b01);
@@ -147,6 +81,89 @@ __global__ void __launch_bounds__(32 * ROUTE_WARPS)
   // ---- zero the matching 128 floats of the combine buffer
   reinterpret_cast<float4*>(p.r + static_cast<size_t>(t) * p.L + g * 128)[lane] =
       make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// Warp w handles token t = w / (P + 1), P = ceil(G / ROUTE_QG): part 0 routes the token,
+// part j + 1 quantises its 128-column groups [j * ROUTE_QG, (j + 1) * ROUTE_QG) of z and
+// zeroes the matching floats of the combine buffer.
+__global__ void __launch_bounds__(32 * ROUTE_WARPS)
+    route_quant_kernel(const RouteParams p) {
+  pdl_trigger();  // dependents may launch now; they wait for this grid before reading
+  pdl_wait();
+  const int lane = lane_id();
+  if (blockIdx.x == 0 && threadIdx.x < p.nsched) p.sched[threadIdx.x] = 0;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+       i < p.zero_n; i += static_cast<long long>(gridDim.x) * blockDim.x)
+    p.zero_buf[i] = 0;
+  const int G = p.L / 128;
+  const int P = (G + ROUTE_QG - 1) / ROUTE_QG;
+  const long long w = static_cast<long long>(blockIdx.x) * ROUTE_WARPS + (threadIdx.x >> 5);
+  const int t = static_cast<int>(w / (P + 1));
+  const int part = static_cast<int>(w - static_cast<long long>(t) * (P + 1));
+  if (t >= p.M) return;
+
+  if (part == 0) {
+    // ---- top-k selection: key = (ordered logit, inverted index) so larger key wins and
+    // equal logits go to the lower expert index.
+    const float* lg = p.logits + static_cast<size_t>(t) * p.E;
+    constexpr int PER_LANE = MAX_E / 32;
+    uint32_t keys[PER_LANE];
+#pragma unroll
+    for (int i = 0; i < PER_LANE; ++i) {
+      const int e = lane + 32 * i;
+      keys[i] = e < p.E ? ordered_key(__ldg(lg + e)) : 0u;
+    }
+    uint32_t taken = 0;  // bit i: entry i of this lane already selected
+    int my_idx = 0;
+    float my_val = 0.f;
+    for (int j = 0; j < p.k; ++j) {
+      unsigned long long best = 0ull;
+#pragma unroll
+      for (int i = 0; i < PER_LANE; ++i) {
+        const int e = lane + 32 * i;
+        if (e < p.E && !(taken >> i & 1u)) {
+          const unsigned long long kk =
+              (static_cast<unsigned long long>(keys[i]) << 32) | (0xFFFFFFFFu - e);
+          best = kk > best ? kk : best;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+        best = other > best ? other : best;
+      }
+      const int e =
+          static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best & 0xFFFFFFFFull));
+      if ((e & 31) == lane) taken |= 1u << (e >> 5);
+      if (lane == j) {
+        my_idx = e;
+        my_val = __ldg(lg + e);
+      }
+    }
+    const float vmax = __shfl_sync(0xFFFFFFFFu, my_val, 0);
+    const float ex = lane < p.k ? expf(my_val - vmax) : 0.f;
+    float sum = ex;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+    if (lane < p.k) {
+      p.ids[static_cast<size_t>(t) * p.k + lane] = my_idx;
+      p.wts[static_cast<size_t>(t) * p.k + lane] = ex / sum;
+    }
+    return;
+  }
+
+  // ---- quantisation of up to QG consecutive 128-column groups: their loads are issued
+  // together, so a warp has several DRAM round trips in flight
+  const int g0 = (part - 1) * ROUTE_QG;
+  uint2 raw[ROUTE_QG];
+#pragma unroll
+  for (int j = 0; j < ROUTE_QG; ++j)
+    if (g0 + j < G)
+      raw[j] = *reinterpret_cast<const uint2*>(p.z + static_cast<size_t>(t) * p.L +
+                                                (g0 + j) * 128 + lane * 4);
+#pragma unroll
+  for (int j = 0; j < ROUTE_QG; ++j)
+    if (g0 + j < G) quant_group(p, t, g0 + j, raw[j], lane);
 }
 
 __global__ void __launch_bounds__(PERM_BLOCK) perm_hist_kernel(const PermParams p) {
@@ -417,7 +434,8 @@ cudaError_t launch_simple(Kern k, dim3 grid, dim3 block, const Param& prm, cudaS
 }  // namespace
 
 cudaError_t launch_route(const RouteParams& p, cudaStream_t s, bool pdl) {
-  const long long warps = static_cast<long long>(p.M) * (p.L / 128 + 1);
+  const long long warps =
+      static_cast<long long>(p.M) * ((p.L / 128 + ROUTE_QG - 1) / ROUTE_QG + 1);
   const int blocks = static_cast<int>((warps + ROUTE_WARPS - 1) / ROUTE_WARPS);
   return launch_simple(route_quant_kernel, dim3(blocks), dim3(32 * ROUTE_WARPS), p, s, pdl);
 }
