@@ -159,7 +159,9 @@ typedef struct klt_routing {
  *     rows in pair order p (MXFP8 layers: aq only; NVFP4_W4A4 layers: aq packed e2m1
  *     [M * topk, I/2] only);
  *   r f32 [M, L]: routed combine (not formed with KLT_FLAG_DETERMINISTIC, whose norm sums
- *     the per-pair outputs directly); n bf16 [M, L]: RMSNorm output (gamma applied);
+ *     the per-pair outputs directly; the norm normally zeroes it for the next forward, so
+ *     asking for it makes the next forward clear the buffer first); n bf16 [M, L]:
+ *     RMSNorm output (gamma applied);
  *   a_s bf16 [M, Is]: shared-expert SwiGLU output;
  *   events: up to 8 cudaEvent_t handles, events[i] recorded after launch i (NULL skips);
  *   stall_after_kblocks: test hook, 0 = off; when > 0 the tile producer of the first

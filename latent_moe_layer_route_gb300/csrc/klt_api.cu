@@ -100,6 +100,10 @@ struct klt_handle {
   int dep_routed, dep_ntiles;
   int cap, max_hist_blocks;
   bool wide_ok;  // token-major engine usable (dims and launch register count)
+  // The combine buffer r must be all zero when a forward starts: each norm row zeroes its
+  // row of r after reading it.  A forward that copies r out (debug) leaves it in place,
+  // as may one that stopped early; the next forward then clears it whole first.
+  bool r_dirty;
   // descriptors per BN variant (token-side maps depend on the box height)
   CUtensorMap tm_zqp[kNumBN], tm_aq[kNumBN], tm_n[kNumBN], tm_as[kNumBN];
   void* allocs[64];
@@ -531,6 +535,15 @@ int forward_impl(klt_handle* h, const void* x, const void* z, const float* logit
   rp.L = L;
   rp.bs = mx ? BS_MX8 : (nv4 ? BS_NV4 : BS_NONE);
   rp.zsx = h->zsx;
+  // r is zeroed by the norm rows unless the caller copies the combine buffer out afterwards
+  const bool keep_r = dbg && dbg->r && !(h->flags & KLT_FLAG_DETERMINISTIC);
+  if (h->r_dirty) {
+    if (cudaMemsetAsync(h->r, 0, static_cast<size_t>(d.max_tokens) * L * 4, s) != cudaSuccess)
+      return KLT_ERR_CUDA;
+    h->r_dirty = false;
+  }
+  const bool r_left = keep_r;  // after this forward r holds the combine, or zeros
+  h->r_dirty = true;           // until every launch of this forward is issued
   KLT_LAUNCH(launch_route(rp, s, pdl));
 
   // ---- K1: permutation
@@ -587,6 +600,7 @@ int forward_impl(klt_handle* h, const void* x, const void* z, const float* logit
   gp.aqb = nvfp4 ? h->aqb : nullptr;
   gp.asT = h->asT;
   gp.r = h->r;
+  gp.zero_r = keep_r ? 0 : 1;
   gp.yw = (h->flags & KLT_FLAG_DETERMINISTIC) ? h->yw : nullptr;
   gp.pos = h->pos;
   gp.topk = k;
@@ -970,6 +984,7 @@ int forward_impl(klt_handle* h, const void* x, const void* z, const float* logit
       np.M = M;
       np.L = L;
       np.eps = d.eps;
+      np.zero_r = keep_r ? 0 : 1;
       KLT_LAUNCH(launch_norm(np, s, pdl));
       g3.ntasks = 1;
       g3.sched = h->sched + 2;
@@ -982,6 +997,7 @@ int forward_impl(klt_handle* h, const void* x, const void* z, const float* logit
 #undef KLT_LAUNCH
 
   // ---- optional copies of routing results and stage outputs
+  h->r_dirty = r_left;
   auto cp = [&](void* dst, const void* src, size_t bytes) -> bool {
     return !dst || cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s) == cudaSuccess;
   };
@@ -1039,6 +1055,7 @@ int klt_status(klt_handle* h) {
   int e = 0;
   if (cudaMemcpy(&e, h->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
     return KLT_ERR_CUDA;
+  if (e) h->r_dirty = true;  // a stopped forward may have left partial sums in r
   return e ? KLT_ERR_DEVICE_TIMEOUT : KLT_OK;
 }
 

@@ -494,6 +494,30 @@ KLT_DEV uint32_t f32_to_e2m1(float v) {
   return (v < 0.f && c != 0u) ? (c | 8u) : c;
 }
 
+// A code whose magnitude bits are zero loses its sign bit (eight 4-bit codes in a word):
+// bit 3 of ((m & 7) + 7) is set exactly when the magnitude m is non-zero.
+KLT_DEV uint32_t e2m1x8_drop_negative_zero(uint32_t x) {
+  const uint32_t nz = ((x & 0x77777777u) + 0x77777777u) & 0x88888888u;
+  return x & (nz | 0x77777777u);
+}
+// Eight fp32 values -> eight e2m1 codes in one word, v[0] in bits 0-3, v[1] in bits 4-7,
+// and so on (the even element in the low nibble of each byte): the tensor-core format
+// conversion (nearest even on the e2m1 grid, saturating at 6, as f32_to_e2m1), then the
+// sign dropped from zero magnitudes.
+KLT_DEV uint32_t f32x8_to_e2m1x8(float v0, float v1, float v2, float v3, float v4, float v5,
+                                 float v6, float v7) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(v0), "f"(v1), "f"(v2), "f"(v3), "f"(v4), "f"(v5), "f"(v6), "f"(v7));
+  return e2m1x8_drop_negative_zero(r);
+}
+
 // fp32 -> e4m3 code, round to nearest even, saturating to +-448.
 KLT_DEV uint8_t f32_to_e4m3(float v) {
   return static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));

@@ -770,6 +770,14 @@ __device__ void run_epilogue(const GemmParams& p, Smem<BN>& sm, uint32_t tmem_ba
       }
       for (int c = gtid + PER * C::GROUP_THREADS; c < n4; c += C::GROUP_THREADS)
         emit(c, row4(c), __ldg(gg + c));
+      if constexpr (!DET) {
+        // the row has been read (by this thread, the same elements): zero it for the next
+        // forward's combine
+        if (p.zero_r) {
+          float4* rw = reinterpret_cast<float4*>(p.r + t * p.L);
+          for (int c = gtid; c < n4; c += C::GROUP_THREADS) rw[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
       named_bar_sync(bar_grp, C::GROUP_THREADS);  // sm.red is reused by the next unit
       signal_done<BN>(p, sm, sg, p.norm_done + info.dep_idx, grp, gw, lane);
       continue;

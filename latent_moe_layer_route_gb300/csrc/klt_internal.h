@@ -21,7 +21,7 @@ struct RouteParams {
   float* wts;              // [M, k]
   uint8_t* zq;             // [M, L]
   float* zs;               // [M, L/128]
-  float* r;                // [M, L] zeroed here (the routed combine accumulates into it)
+  float* r;                // [M, L] fp32 combine buffer (zeroed by the previous norm)
   int* sched;              // per-launch tile counters, zeroed here
   int nsched;
   int* zero_buf;           // dependency counters of the fused launch, zeroed here
@@ -63,11 +63,12 @@ struct PermParams {
 };
 
 struct NormParams {
-  const float* r;              // [M, L]
+  float* r;                    // [M, L]
   const __nv_bfloat16* gamma;  // [L]
   __nv_bfloat16* n;            // [M, L]
   int M, L;
   float eps;
+  int zero_r;  // zero each row of r after normalising it (ready for the next forward)
 };
 
 // ------------------------------------------------------------------ tile GEMM engine
@@ -198,6 +199,8 @@ struct GemmParams {
   float* lgp;                  //   and router logits [M, E]
   long long* trace;            // optional timestamp trace (this launch's region)
   int trace_n;                 // entries per (CTA, role)
+  int zero_r;                  // norm units zero each row of r once it is normalised, so
+                               // the next forward's routed L2 units add into zeros
 };
 
 // Launchers (return cudaError_t of the launch).

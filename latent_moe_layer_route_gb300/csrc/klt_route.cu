@@ -24,7 +24,7 @@ __device__ __forceinline__ uint32_t ordered_key(float v) {
 }
 
 // Quantisation of 128-column group g of token t's latent row (4 columns per lane, already
-// loaded into `raw`), and zeroing of the matching 128 floats of the combine buffer.
+// loaded into `raw`).
 __device__ __forceinline__ void quant_group(const RouteParams& p, int t, int g, uint2 raw,
                                             int lane) {
   const int G = p.L / 128;
@@ -40,17 +40,19 @@ __device__ __forceinline__ void quant_group(const RouteParams& p, int t, int g, 
     // column in the low nibble
 #pragma unroll
     for (int o = 2; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-    const uint8_t sc = f32_to_e4m3(amax / 6.0f);
+    // correctly rounded quotients from correctly rounded reciprocals (Markstein's
+    // correction, as in the GEMM epilogues): fp32(amax / 6) and fp32(v / s)
+    const uint8_t sc = f32_to_e4m3(quot_rn(amax, 6.0f, 1.0f / 6.0f));
     const float s = e4m3_to_f32(sc);
     uint32_t c = 0;
-    if (s != 0.f)
-      c = f32_to_e2m1(v0 / s) | (f32_to_e2m1(v1 / s) << 4) | (f32_to_e2m1(v2 / s) << 8) |
-          (f32_to_e2m1(v3 / s) << 12);
+    if (s != 0.f) {
+      const float inv = 1.0f / s;
+      c = f32x8_to_e2m1x8(quot_rn(v0, s, inv), quot_rn(v1, s, inv), quot_rn(v2, s, inv),
+                          quot_rn(v3, s, inv), 0.f, 0.f, 0.f, 0.f);
+    }
     if ((lane & 3) == 0) p.zsx[static_cast<size_t>(t) * (p.L / 16) + g * 8 + (lane >> 2)] = sc;
     *reinterpret_cast<uint16_t*>(p.zq + static_cast<size_t>(t) * (p.L / 2) + g * 64 +
                                  lane * 2) = static_cast<uint16_t>(c);
-    reinterpret_cast<float4*>(p.r + static_cast<size_t>(t) * p.L + g * 128)[lane] =
-        make_float4(0.f, 0.f, 0.f, 0.f);
     return;
   }
   if (p.bs == BS_MX8) {
@@ -70,22 +72,19 @@ __device__ __forceinline__ void quant_group(const RouteParams& p, int t, int g, 
   } else {
 #pragma unroll
     for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    // fp32(v / s) from the correctly rounded reciprocal (Markstein's correction)
     const float s = amax == 0.f ? 1.0f : amax / 448.0f;
-    q = static_cast<uint32_t>(f32_to_e4m3(v0 / s)) |
-        (static_cast<uint32_t>(f32_to_e4m3(v1 / s)) << 8) |
-        (static_cast<uint32_t>(f32_to_e4m3(v2 / s)) << 16) |
-        (static_cast<uint32_t>(f32_to_e4m3(v3 / s)) << 24);
+    const float inv = 1.0f / s;
+    q = f32x2_to_e4m3x2(quot_rn(v0, s, inv), quot_rn(v1, s, inv)) |
+        (f32x2_to_e4m3x2(quot_rn(v2, s, inv), quot_rn(v3, s, inv)) << 16);
     if (lane == 0) p.zs[static_cast<size_t>(t) * G + g] = s;
   }
   *reinterpret_cast<uint32_t*>(p.zq + static_cast<size_t>(t) * p.L + g * 128 + lane * 4) = q;
-  // ---- zero the matching 128 floats of the combine buffer
-  reinterpret_cast<float4*>(p.r + static_cast<size_t>(t) * p.L + g * 128)[lane] =
-      make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // Warp w handles token t = w / (P + 1), P = ceil(G / ROUTE_QG): part 0 routes the token,
-// part j + 1 quantises its 128-column groups [j * ROUTE_QG, (j + 1) * ROUTE_QG) of z and
-// zeroes the matching floats of the combine buffer.
+// part j + 1 quantises its 128-column groups [j * ROUTE_QG, (j + 1) * ROUTE_QG) of z.  The
+// combine buffer r the routed L2 units add into was zeroed by the previous forward's norm.
 __global__ void __launch_bounds__(32 * ROUTE_WARPS)
     route_quant_kernel(const RouteParams p) {
   pdl_trigger();  // dependents may launch now; they wait for this grid before reading
@@ -344,8 +343,10 @@ __global__ void __launch_bounds__(128) norm_kernel(const NormParams p) {
   const float inv = rsqrtf(tot / static_cast<float>(p.L) + p.eps);
   const uint2* gg = reinterpret_cast<const uint2*>(p.gamma);
   uint2* nn = reinterpret_cast<uint2*>(p.n + static_cast<size_t>(t) * p.L);
+  float4* rz = reinterpret_cast<float4*>(p.r) + static_cast<size_t>(t) * (p.L / 4);
   for (int c = threadIdx.x; c < p.L / 4; c += 128) {
     const float4 v = rr[c];
+    if (p.zero_r) rz[c] = make_float4(0.f, 0.f, 0.f, 0.f);  // ready for the next forward
     const uint2 graw = gg[c];
     const __nv_bfloat162 g01 = *reinterpret_cast<const __nv_bfloat162*>(&graw.x);
     const __nv_bfloat162 g23 = *reinterpret_cast<const __nv_bfloat162*>(&graw.y);

@@ -582,6 +582,17 @@ __device__ void w_norm_rows(const GemmParams& p, WSmem& sm, SigState& sg, int ro
 #pragma unroll
     for (int i = 0; i < PER; ++i)
       ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+    if constexpr (!DET) {
+      // the row is in registers: zero it for the next forward's combine
+      if (p.zero_r) {
+        float4* rw = reinterpret_cast<float4*>(p.r + t * p.L);
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+          const int c = lane + i * 32;
+          if (c < n4) rw[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+    }
 #pragma unroll
     for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
     const float inv = rsqrtf(ss / static_cast<float>(p.L) + p.eps);
@@ -759,18 +770,18 @@ __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
             float m = 0.f;
   #pragma unroll
             for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(a[16 * b + i]));
-            const uint32_t sc = f32_to_e4m3(m / 6.0f);
+            const uint32_t sc = f32_to_e4m3(quot_rn(m, 6.0f, 1.0f / 6.0f));
             const float s = e4m3_to_f32(static_cast<uint8_t>(sc));
             const float inv = s != 0.f ? rcp_nr(s) : 0.f;
   #pragma unroll
             for (int q = 0; q < 2; ++q) {
-              uint32_t w = 0;
-              if (s != 0.f) {
-  #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                  w |= f32_to_e2m1(quot_rn(a[16 * b + 8 * q + i], s, inv)) << (4 * i);
-              }
-              w8[2 * b + q] = w;
+              const float* x = a + 16 * b + 8 * q;
+              w8[2 * b + q] =
+                  s != 0.f ? f32x8_to_e2m1x8(quot_rn(x[0], s, inv), quot_rn(x[1], s, inv),
+                                             quot_rn(x[2], s, inv), quot_rn(x[3], s, inv),
+                                             quot_rn(x[4], s, inv), quot_rn(x[5], s, inv),
+                                             quot_rn(x[6], s, inv), quot_rn(x[7], s, inv))
+                           : 0u;
             }
             sfw |= sc << (8 * b);
           }

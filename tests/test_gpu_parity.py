@@ -364,3 +364,35 @@ def test_prefill_m8192_nvfp4_sampled_tokens():
     tok = np.sort(rng.choice(cfg.M, 32, replace=False))
     tok[0], tok[-1] = 0, cfg.M - 1
     run_case(cfg, tokens=tok, expect_tile=256)
+
+
+# ------------------------------------------------------------------ combine buffer reuse
+
+@pytest.mark.parametrize("M1,M2,flags,fmt", [(12, 16, 0, "fp8"), (40, 70, 0, "fp8"),
+                                             (12, 16, B.KLT_FLAG_PHASED, "fp8"),
+                                             (40, 70, 0, "mxfp8")])
+def test_combine_buffer_reuse_across_forwards(M1, M2, flags, fmt):
+    """The fp32 combine buffer is zeroed by the norm rows for the next forward (not by the
+    routing kernel); a forward that copies it out leaves it, and the next one clears it.
+    Forwards of growing and shrinking M on one handle, with and without that copy, must
+    each match the oracle."""
+    cfg = configs.SMALL.with_(routed_fmt=fmt, E=8, topk=3, seed=91)
+    w_cpu, w_gpu = weights_for(cfg)
+    tail = B.LatentMoETail(cfg, w_gpu, max_tokens=max(M1, M2), flags=flags)
+    try:
+        plan = [(M1, False), (M2, False), (M1, True), (M2, False), (M1, False)]
+        for i, (M, debug) in enumerate(plan):
+            act = inputs.make_activations(cfg.with_(seed=100 + i), M)
+            o = T.tail(act, w_cpu, cfg)
+            if debug:  # copies r out: the next forward clears it first
+                run = PU.Run(tail, PU.to_cuda(act), cfg)
+                assert tail.status() == B.KLT_OK
+                PU.check_stages(run, o, cfg)
+            else:
+                a = PU.to_cuda(act)
+                out = tail.forward(a["x"], a["z"], a["logits"])
+                torch.cuda.synchronize()
+                assert tail.status() == B.KLT_OK
+                PU.assert_output_close(out.float().cpu().numpy().astype(np.float64), o["out"])
+    finally:
+        tail.close()
