@@ -122,16 +122,20 @@ class Clocks:
 
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the dominant
-# kernel (MX layers: both GEMM launches), from one ncu launch-list capture of
+# kernel (block-scaled layers: both GEMM launches), from one ncu launch-list capture of
 # `bench.py --workload W --steps 2 --warmup 3 --no-cpu-baseline` (the steady-state forward),
 # valid only while the kernel sources hash to the recorded digest.
 NCU_TRAFFIC = {
-    ("decode_m16_e64_k8_fp8", "gemm_fused"): (715912448, "6b7c111e8854dec9"),
-    ("tiny_m4_e16_k4", "gemm_fused"): (190675200, "6b7c111e8854dec9"),
-    ("decode_m128_e64_k8_fp8_biased", "gemm_fused"): (836889344, "6b7c111e8854dec9"),
-    ("prefill_m4096_e64_k8_fp8_zipf", "gemm_fused"): (1629829888, "6b7c111e8854dec9"),
-    ("prefill_m8192_e128_k8_nvfp4", "gemm_fused"): (6860687872, "6b7c111e8854dec9"),
-    ("prefill_m4096_e64_k8_mxfp8_zipf", "gemm_routed+gemm_dense"): (1673564672, "6b7c111e8854dec9"),
+    ("decode_m16_e64_k8_fp8", "gemm_fused"): (715676928, "f6ac211fad7ae4e7"),
+    ("tiny_m4_e16_k4", "gemm_fused"): (190601472, "f6ac211fad7ae4e7"),
+    ("decode_m128_e64_k8_fp8_biased", "gemm_fused"): (839727360, "f6ac211fad7ae4e7"),
+    ("prefill_m4096_e64_k8_fp8_zipf", "gemm_fused"): (1683489024, "f6ac211fad7ae4e7"),
+    ("prefill_m8192_e128_k8_nvfp4", "gemm_fused"): (7013585920, "f6ac211fad7ae4e7"),
+    ("prefill_m4096_e64_k8_mxfp8_zipf", "gemm_routed+gemm_dense"): (1729753856,
+                                                                     "f6ac211fad7ae4e7"),
+    ("prefill_m8192_e128_k8_nvfp4_w4a4", "gemm_routed+gemm_dense"): (3548310016,
+                                                                      "f6ac211fad7ae4e7"),
+    ("decode_m16_e64_k8_fp8+hidden", "gemm_fused"): (781839872, "f6ac211fad7ae4e7"),
 }
 KERNEL_SOURCES = ("klt_gemm.cu", "klt_wide.cu", "klt_device.cuh", "klt_internal.h", "klt_api.cu",
                   "klt_route.cu")
@@ -442,7 +446,7 @@ def measure(cfg, args, ws, rank, local, flush, with_cpu: bool, hidden: bool = Fa
     rr = 6.0 if cfg.routed_fmt == "nvfp4_w4a4" else 2.0
     t_tensor = routed_f / (rr * bf16_tf * 1e12) + dense_f / (bf16_tf * 1e12)
     dom_s = per_launch_us[dom] * 1e-6
-    traffic = recorded_traffic(cfg.name, dom)
+    traffic = recorded_traffic(cfg.name + ("+hidden" if hidden else ""), dom)
     if t_tensor > dom_bytes / (hbm * 1e9):
         mixed_peak = (routed_f + dense_f) / t_tensor / 1e12
         achieved = (routed_f + dense_f) / dom_s / 1e12
