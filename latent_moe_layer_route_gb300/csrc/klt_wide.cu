@@ -66,10 +66,11 @@ struct W {
   static constexpr int SIG = 8;             // completion-signal ring (epilogue -> signaller)
   static constexpr int SIGNAL_WARP = 2;     // control warp that publishes unit completions
   // Registers: 384 threads launch with 168 each (3 warps share a scheduler); the control
-  // warpgroup drops to 56 and the two epilogue warpgroups rise to 216, within the
-  // registers released.
+  // warpgroup drops to 72 and the two epilogue warpgroups rise to 216, exactly the
+  // registers released (72 keeps the producer's scale-tile paths and the MMA issuer's
+  // block-scaled loop free of spills).
   static constexpr int LAUNCH_REGS = 168;
-  static constexpr int REGS_CTRL = 56;
+  static constexpr int REGS_CTRL = 72;
   static constexpr int REGS_EPI = 216;
   static_assert(4 * (LAUNCH_REGS - REGS_CTRL) >= 8 * (REGS_EPI - LAUNCH_REGS),
                 "register hand-over must balance");
