@@ -92,8 +92,17 @@ def test_hidden_small(M, bn, fmt):
     _check(cfg, w, act, run)
 
 
+@pytest.mark.parametrize("fmt,M", [("mxfp8", 12), ("nvfp4_w4a4", 12), ("nvfp4_w4a4", 150)])
+def test_hidden_block_scaled_formats(fmt, M):
+    # the projection feeds the block-scaled routed formats the same way (their latent
+    # quantisation happens in the routing kernel on the projected z)
+    cfg = configs.SMALL.with_(E=8, topk=2, I=256, routed_fmt=fmt, seed=63)
+    w, act, run = _run(cfg, M, expect_tile=256)
+    _check(cfg, w, act, run)
+
+
 def test_hidden_wider_shapes_and_gate_padding():
-    # E = 40 gate rows padded with zero rows to a multiple of 256 after L = 384 latent rows
+    # E = 40 gate rows padded with zero rows to a multiple of 128 after L = 384 latent rows
     cfg = configs.SMALL.with_(H=512, L=384, I=256, Is=256, E=40, topk=5, seed=62)
     w, act, run = _run(cfg, 23)
     _check(cfg, w, act, run)
