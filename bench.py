@@ -181,6 +181,18 @@ def algorithmic_bytes(cfg, cnt: np.ndarray, M: int):
             "perm": perm, "total": total, "touched_experts": touched}
 
 
+def launch_names(cfg, nt: int, phased: bool, hidden: bool):
+    """Names of a forward's launches, in order, from the tail's launch count `nt`: the
+    routing launches (one fused launch for a small batch; else routing, the expert
+    histogram above one permutation block, scatter, gather), then the GEMM launches."""
+    bs = cfg.routed_fmt in ("mxfp8", "nvfp4_w4a4")  # routed and dense GEMM launches
+    gemms = (["gemm_l1", "gemm_l2", "norm", "gemm_out"] if phased else
+             ["gemm_routed", "gemm_dense"] if bs else ["gemm_fused"])
+    routing = {1: ["route_perm"], 3: ["route", "perm_scatter", "perm_gather"],
+               4: ["route", "perm_hist", "perm_scatter", "perm_gather"]}[nt - len(gemms)]
+    return (["proj"] if hidden else []) + routing + gemms
+
+
 def flops(cfg, M: int):
     H, L, I, Is, k = cfg.H, cfg.L, cfg.I, cfg.Is, cfg.topk
     routed = 2.0 * M * k * (2 * I * L + L * I)
@@ -386,13 +398,7 @@ def measure(cfg, args, ws, rank, local, flush, with_cpu: bool, hidden: bool = Fa
         for j in range(nl):
             per[j] += evs[i][j].elapsed_time(evs[i][j + 1])
     per /= args.steps
-    nt = nl - (1 if hidden else 0)  # launches of the tail itself
-    mx = cfg.routed_fmt in ("mxfp8", "nvfp4_w4a4")  # routed and dense GEMM launches
-    gemms = (["gemm_routed", "gemm_dense"] if mx else ["gemm_fused"]) if nt <= 5 + mx else \
-        ["gemm_l1", "gemm_l2", "norm", "gemm_out"]
-    hist = nt == 4 + len(gemms)
-    names = ((["proj"] if hidden else []) + ["route"] + (["perm_hist"] if hist else []) +
-             ["perm_scatter", "perm_gather"] + gemms)
+    names = launch_names(cfg, nl - (1 if hidden else 0), args.phased, hidden)
     per_launch_us = {n: round(float(v) * 1e3, 2) for n, v in zip(names, per)}
 
     # ---- end to end through the public API with host buffers

@@ -261,7 +261,11 @@ int klt_destroy(klt_handle* h);
 /* Static description of a status code. */
 const char* klt_strerror(int code);
 
-/* Number of kernels one klt_forward launches for the given M and handle (0 for M == 0). */
+/* Number of kernels one klt_forward launches for the given M and handle at the automatic
+ * GEMM configuration (0 for M == 0): the routing launches (one for a feature-major batch of
+ * at most 256 (token, choice) pairs with e4m3 activations; otherwise routing, an expert
+ * histogram above 1024 pairs, scatter and gather) and then the GEMM launches (one; two for
+ * the block-scaled formats; four with KLT_FLAG_PHASED). */
 int klt_launch_count(const klt_handle* h, int32_t M);
 
 /* GEMM configuration klt_forward uses for M tokens when klt_debug.force_bn = force_bn

@@ -145,6 +145,13 @@ int check_dims(const klt_dims* d) {
   return KLT_OK;
 }
 
+// Routing of a small batch in one launch (route_small_kernel): the feature-major engine,
+// one permutation block of at most SMALL_PAIRS pairs, e4m3 activations with fp32 scales.
+bool small_routing(const klt_handle* h, int M, bool wide) {
+  const bool bs = h->d.routed_fmt == KLT_FMT_MXFP8 || h->d.routed_fmt == KLT_FMT_NVFP4_W4A4;
+  return !wide && !bs && static_cast<long long>(M) * h->d.topk <= SMALL_PAIRS;
+}
+
 // Token-tile width: the smallest tile that holds a decode batch, 64 beyond that (the
 // 128-wide tile is kept for explicit selection).
 int bn_index(int M, int force_bn) {
@@ -400,7 +407,10 @@ int klt_launch_count(const klt_handle* h, int32_t M) {
   // phased: 3 GEMMs + norm; block-scaled layers: routed and dense launches
   const bool bs = h->d.routed_fmt == KLT_FMT_MXFP8 || h->d.routed_fmt == KLT_FMT_NVFP4_W4A4;
   const int gemm_launches = (h->flags & KLT_FLAG_PHASED) ? 4 : (bs ? 2 : 1);
-  return 3 + gemm_launches + (nblocks > 1 ? 1 : 0);
+  const int routing = small_routing(h, M, klt_gemm_tile(h, M, 0) == 256)
+                          ? 1
+                          : 3 + (nblocks > 1 ? 1 : 0);
+  return routing + gemm_launches;
 }
 
 int klt_gemm_tile(const klt_handle* h, int32_t M, int32_t force_bn) {
@@ -544,7 +554,6 @@ int forward_impl(klt_handle* h, const void* x, const void* z, const float* logit
   }
   const bool r_left = keep_r;  // after this forward r holds the combine, or zeros
   h->r_dirty = true;           // until every launch of this forward is issued
-  KLT_LAUNCH(launch_route(rp, s, pdl));
 
   // ---- K1: permutation
   PermParams pp;
@@ -575,9 +584,14 @@ int forward_impl(klt_handle* h, const void* x, const void* z, const float* logit
   pp.sf_tiles = h->sf_tiles;
   pp.sf_group = mx ? 32 : 16;
   pp.zrow = nv4 ? L / 2 : L;
-  if (nblocks > 1) KLT_LAUNCH(launch_perm_hist(pp, s, pdl));
-  KLT_LAUNCH(launch_perm_scatter(pp, s, pdl));
-  KLT_LAUNCH(launch_perm_gather(pp, s, pdl));
+  if (small_routing(h, M, wide)) {
+    KLT_LAUNCH(launch_route_small(rp, pp, s, pdl));
+  } else {
+    KLT_LAUNCH(launch_route(rp, s, pdl));
+    if (nblocks > 1) KLT_LAUNCH(launch_perm_hist(pp, s, pdl));
+    KLT_LAUNCH(launch_perm_scatter(pp, s, pdl));
+    KLT_LAUNCH(launch_perm_gather(pp, s, pdl));
+  }
 
   // ---- common GEMM parameters
   GemmParams gp;

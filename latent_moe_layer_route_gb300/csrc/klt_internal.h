@@ -208,6 +208,9 @@ cudaError_t launch_route(const RouteParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_perm_hist(const PermParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_perm_scatter(const PermParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_perm_gather(const PermParams& p, cudaStream_t s, bool pdl);
+// route + scatter + gather in one launch; needs M·k <= SMALL_PAIRS and e4m3 activations
+cudaError_t launch_route_small(const RouteParams& rp, const PermParams& p, cudaStream_t s,
+                               bool pdl);
 cudaError_t launch_norm(const NormParams& p, cudaStream_t s, bool pdl);
 // Row-major [rows, row_bytes] -> 128-row x 128-byte tiles, tile (rb, kb) at
 // ((rb * row_bytes/128) + kb) * 16384 bytes (rows % 128 == 0, row_bytes % 128 == 0), each
@@ -247,6 +250,8 @@ bool wide_regs_ok(int regs);
 constexpr int PERM_BLOCK = 1024;  // pairs per permutation block
 constexpr int ROUTE_WARPS = 8;    // warps per routing block
 constexpr int ROUTE_QG = 4;       // 128-column latent groups quantised per routing warp
+constexpr int SMALL_PAIRS = 256;  // most pairs the one-launch routing takes
+constexpr int SMALL_THREADS = 512;  // threads per block of the one-launch routing
 constexpr int MAX_TOPK = 32;
 constexpr int MAX_E = 256;
 constexpr int MAX_KB = 32;       // routed K blocks of 128 per unit (L, I <= 4096)

@@ -7,6 +7,8 @@
 //  perm_scatter_kernel stable counting-sort scatter: cnt/off/tile_off, gidx/slot/pos.
 //  perm_gather_kernel  gather of each pair's quantised latent row into expert order (the
 //                      routed L1 GEMM reads it with plain TMA tiles).
+//  route_small_kernel  the three above in one launch for a small batch (one permutation
+//                      block, e4m3 activations).
 //  norm_kernel         RMSNorm of the routed combine with fp32 statistics on the fp32
 //                      sum (tokenspeed PR 1062 commit notes: fp32-internal norm), gamma
 //                      applied, rounded once to bf16 as the up-projection operand.
@@ -21,6 +23,70 @@ __device__ __forceinline__ uint32_t ordered_key(float v) {
   uint32_t u = __float_as_uint(v);
   if ((u & 0x7FFFFFFFu) == 0) u = 0;  // -0 and +0 compare equal
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// e4m3 codes of one 128-column group held 4 columns per lane: s = amax / 448 (1 for an
+// all-zero group), codes e4m3(v / s) with fp32(v / s) from the correctly rounded reciprocal
+// (Markstein's correction).  Returns this lane's 4 codes, the first column in the low byte.
+__device__ __forceinline__ uint32_t quant128_e4m3(float v0, float v1, float v2, float v3,
+                                                  float& s_out) {
+  float amax = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
+#pragma unroll
+  for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+  const float s = amax == 0.f ? 1.0f : amax / 448.0f;
+  const float inv = 1.0f / s;
+  s_out = s;
+  return f32x2_to_e4m3x2(quot_rn(v0, s, inv), quot_rn(v1, s, inv)) |
+         (f32x2_to_e4m3x2(quot_rn(v2, s, inv), quot_rn(v3, s, inv)) << 16);
+}
+
+// Top-k of token t's logits with softmax over the selected ones, by one warp: the key is
+// (ordered logit, inverted index), so the larger key wins and equal logits go to the lower
+// expert index.  Lane j < k returns choice j's expert and weight.
+__device__ __forceinline__ void route_token(const float* logits, int E, int k, int t, int lane,
+                                            int& idx_out, float& wt_out) {
+  const float* lg = logits + static_cast<size_t>(t) * E;
+  constexpr int PER_LANE = MAX_E / 32;
+  uint32_t keys[PER_LANE];
+#pragma unroll
+  for (int i = 0; i < PER_LANE; ++i) {
+    const int e = lane + 32 * i;
+    keys[i] = e < E ? ordered_key(__ldg(lg + e)) : 0u;
+  }
+  uint32_t taken = 0;  // bit i: entry i of this lane already selected
+  int my_idx = 0;
+  float my_val = 0.f;
+  for (int j = 0; j < k; ++j) {
+    unsigned long long best = 0ull;
+#pragma unroll
+    for (int i = 0; i < PER_LANE; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !(taken >> i & 1u)) {
+        const unsigned long long kk =
+            (static_cast<unsigned long long>(keys[i]) << 32) | (0xFFFFFFFFu - e);
+        best = kk > best ? kk : best;
+      }
+    }
+    // the warp's largest 64-bit key: the largest high word, then the largest low word
+    // among the lanes holding it
+    const uint32_t hi = static_cast<uint32_t>(best >> 32);
+    const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, hi);
+    const uint32_t lo =
+        __reduce_max_sync(0xFFFFFFFFu, hi == top ? static_cast<uint32_t>(best) : 0u);
+    const int e = static_cast<int>(0xFFFFFFFFu - lo);
+    if ((e & 31) == lane) taken |= 1u << (e >> 5);
+    if (lane == j) {
+      my_idx = e;
+      my_val = __ldg(lg + e);
+    }
+  }
+  const float vmax = __shfl_sync(0xFFFFFFFFu, my_val, 0);
+  const float ex = lane < k ? expf(my_val - vmax) : 0.f;
+  float sum = ex;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+  idx_out = my_idx;
+  wt_out = ex / sum;
 }
 
 // Quantisation of 128-column group g of token t's latent row (4 columns per lane, already
@@ -70,13 +136,8 @@ __device__ __forceinline__ void quant_group(const RouteParams& p, int t, int g, 
       p.zsx[static_cast<size_t>(t) * (p.L / 32) + g * 4 + (lane >> 3)] =
           static_cast<uint8_t>(e + 127);
   } else {
-#pragma unroll
-    for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-    // fp32(v / s) from the correctly rounded reciprocal (Markstein's correction)
-    const float s = amax == 0.f ? 1.0f : amax / 448.0f;
-    const float inv = 1.0f / s;
-    q = f32x2_to_e4m3x2(quot_rn(v0, s, inv), quot_rn(v1, s, inv)) |
-        (f32x2_to_e4m3x2(quot_rn(v2, s, inv), quot_rn(v3, s, inv)) << 16);
+    float s;
+    q = quant128_e4m3(v0, v1, v2, v3, s);
     if (lane == 0) p.zs[static_cast<size_t>(t) * G + g] = s;
   }
   *reinterpret_cast<uint32_t*>(p.zq + static_cast<size_t>(t) * p.L + g * 128 + lane * 4) = q;
@@ -102,51 +163,12 @@ __global__ void __launch_bounds__(32 * ROUTE_WARPS)
   if (t >= p.M) return;
 
   if (part == 0) {
-    // ---- top-k selection: key = (ordered logit, inverted index) so larger key wins and
-    // equal logits go to the lower expert index.
-    const float* lg = p.logits + static_cast<size_t>(t) * p.E;
-    constexpr int PER_LANE = MAX_E / 32;
-    uint32_t keys[PER_LANE];
-#pragma unroll
-    for (int i = 0; i < PER_LANE; ++i) {
-      const int e = lane + 32 * i;
-      keys[i] = e < p.E ? ordered_key(__ldg(lg + e)) : 0u;
-    }
-    uint32_t taken = 0;  // bit i: entry i of this lane already selected
-    int my_idx = 0;
-    float my_val = 0.f;
-    for (int j = 0; j < p.k; ++j) {
-      unsigned long long best = 0ull;
-#pragma unroll
-      for (int i = 0; i < PER_LANE; ++i) {
-        const int e = lane + 32 * i;
-        if (e < p.E && !(taken >> i & 1u)) {
-          const unsigned long long kk =
-              (static_cast<unsigned long long>(keys[i]) << 32) | (0xFFFFFFFFu - e);
-          best = kk > best ? kk : best;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-        best = other > best ? other : best;
-      }
-      const int e =
-          static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best & 0xFFFFFFFFull));
-      if ((e & 31) == lane) taken |= 1u << (e >> 5);
-      if (lane == j) {
-        my_idx = e;
-        my_val = __ldg(lg + e);
-      }
-    }
-    const float vmax = __shfl_sync(0xFFFFFFFFu, my_val, 0);
-    const float ex = lane < p.k ? expf(my_val - vmax) : 0.f;
-    float sum = ex;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+    int idx;
+    float wt;
+    route_token(p.logits, p.E, p.k, t, lane, idx, wt);
     if (lane < p.k) {
-      p.ids[static_cast<size_t>(t) * p.k + lane] = my_idx;
-      p.wts[static_cast<size_t>(t) * p.k + lane] = ex / sum;
+      p.ids[static_cast<size_t>(t) * p.k + lane] = idx;
+      p.wts[static_cast<size_t>(t) * p.k + lane] = wt;
     }
     return;
   }
@@ -324,6 +346,158 @@ __global__ void __launch_bounds__(256) perm_gather_kernel(const PermParams p) {
   }
 }
 
+// Routing, quantisation and permutation of a small batch (M·k <= SMALL_PAIRS pairs, one
+// permutation block) in one launch instead of three.  Every block routes all M tokens and
+// counting-sorts the pairs in shared memory, with the arithmetic and the stable order of
+// route_quant_kernel and perm_scatter_kernel; block 0 publishes the routing arrays.  Then
+// warp w of the grid quantises QG consecutive 128-column groups of one pair's latent row
+// (item w = pair * P + part, P = ceil(G / QG)) straight into expert order (zq_perm or its
+// bf16 image, zsT); the pair that is its token's choice 0 also writes the token-order zq
+// and zs.  Only e4m3 activations (per-128 fp32 scales) take this path.
+__global__ void __launch_bounds__(SMALL_THREADS)
+    route_small_kernel(const RouteParams rp, const PermParams p) {
+  constexpr int NW = SMALL_THREADS / 32;  // warps per block
+  constexpr int PW = SMALL_PAIRS / 32;    // warps holding a pair
+  __shared__ int s_ids[SMALL_PAIRS];
+  __shared__ float s_wts[SMALL_PAIRS];
+  __shared__ int s_gidx[SMALL_PAIRS];
+  __shared__ int s_slot[SMALL_PAIRS];
+  __shared__ int warp_cnt[PW][MAX_E];
+  __shared__ int total[MAX_E];
+  pdl_trigger();  // dependents may launch now; they wait for this grid before reading
+  pdl_wait();
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int E = rp.E, k = rp.k, Mk = rp.M * rp.k;
+  const bool pub = blockIdx.x == 0;
+  if (pub && tid < rp.nsched) rp.sched[tid] = 0;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + tid; i < rp.zero_n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x)
+    rp.zero_buf[i] = 0;
+  for (int c = tid; c < PW * MAX_E; c += SMALL_THREADS) (&warp_cnt[0][0])[c] = 0;
+  if (tid < E) total[tid] = 0;
+
+  // ---- top-k of every token (warp w: tokens w, w + NW, ...)
+  for (int t = w; t < rp.M; t += NW) {
+    int idx;
+    float wt;
+    route_token(rp.logits, E, k, t, lane, idx, wt);
+    if (lane < k) {
+      s_ids[t * k + lane] = idx;
+      s_wts[t * k + lane] = wt;
+      if (pub) {
+        rp.ids[static_cast<size_t>(t) * k + lane] = idx;
+        rp.wts[static_cast<size_t>(t) * k + lane] = wt;
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- stable counting sort of the pairs by expert
+  if (tid < Mk) atomicAdd(&total[s_ids[tid]], 1);
+  __syncthreads();
+  if (w == 0) {  // exclusive scans over experts, 32 at a time
+    int acc = 0, tacc = 0;
+    for (int b = 0; b < E; b += 32) {
+      const int e = b + lane;
+      const int c = e < E ? total[e] : 0, tc = (c + p.bn - 1) / p.bn;
+      int ic = c, it = tc;  // inclusive scans across the lanes
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xFFFFFFFFu, ic, o);
+        const int y = __shfl_up_sync(0xFFFFFFFFu, it, o);
+        if (lane >= o) {
+          ic += x;
+          it += y;
+        }
+      }
+      if (e < E) {
+        total[e] = acc + ic - c;  // now the expert offset
+        if (pub) {
+          p.cnt[e] = c;
+          p.off[e] = acc + ic - c;
+          p.tile_off[e] = tacc + it - tc;
+        }
+      }
+      acc += __shfl_sync(0xFFFFFFFFu, ic, 31);
+      tacc += __shfl_sync(0xFFFFFFFFu, it, 31);
+    }
+    if (pub && lane == 0) {
+      p.off[E] = acc;
+      p.tile_off[E] = tacc;
+    }
+  }
+  // rank inside the warp among pairs of the same expert (lower lane = lower pair index)
+  const int e = tid < Mk ? s_ids[tid] : -1 - lane;  // inactive lanes get unique keys
+  const unsigned same = __match_any_sync(0xFFFFFFFFu, e);
+  const int rank = __popc(same & ((1u << lane) - 1u));
+  if (e >= 0 && rank == 0) warp_cnt[w][e] = __popc(same);  // e >= 0 only in warps < PW
+  __syncthreads();
+  if (tid < E) {  // exclusive scan over warps, per expert
+    int acc = 0;
+    for (int ww = 0; ww < PW; ++ww) {
+      const int c = warp_cnt[ww][tid];
+      warp_cnt[ww][tid] = acc;
+      acc += c;
+    }
+  }
+  __syncthreads();
+  if (e >= 0) {
+    const int pp = total[e] + warp_cnt[w][e] + rank;
+    s_gidx[pp] = tid / k;
+    s_slot[pp] = tid;
+    if (pub) {
+      p.gidx[pp] = tid / k;
+      p.slot[pp] = tid;
+      p.pos[tid] = pp;
+      p.wperm[pp] = s_wts[tid];
+    }
+  }
+  __syncthreads();
+
+  // ---- quantisation into expert order
+  const int G = rp.L / 128;
+  const int P = (G + ROUTE_QG - 1) / ROUTE_QG;
+  const long long item = static_cast<long long>(blockIdx.x) * NW + w;
+  if (item >= static_cast<long long>(Mk) * P) return;
+  const int pp = static_cast<int>(item / P);
+  const int g0 = static_cast<int>(item - static_cast<long long>(pp) * P) * ROUTE_QG;
+  const int t = s_gidx[pp];
+  const bool first = s_slot[pp] % k == 0;  // the token's choice 0 writes token order
+  uint2 raw[ROUTE_QG];
+#pragma unroll
+  for (int j = 0; j < ROUTE_QG; ++j)
+    if (g0 + j < G)
+      raw[j] = *reinterpret_cast<const uint2*>(rp.z + static_cast<size_t>(t) * rp.L +
+                                                (g0 + j) * 128 + lane * 4);
+#pragma unroll
+  for (int j = 0; j < ROUTE_QG; ++j) {
+    const int g = g0 + j;
+    if (g >= G) break;
+    const __nv_bfloat162 b01 = *reinterpret_cast<const __nv_bfloat162*>(&raw[j].x);
+    const __nv_bfloat162 b23 = *reinterpret_cast<const __nv_bfloat162*>(&raw[j].y);
+    float sc;
+    const uint32_t q = quant128_e4m3(__low2float(b01), __high2float(b01), __low2float(b23),
+                                     __high2float(b23), sc);
+    const size_t col = static_cast<size_t>(g) * 128 + lane * 4;
+    if (p.zqb_perm == nullptr) {
+      *reinterpret_cast<uint32_t*>(p.zq_perm + static_cast<size_t>(pp) * rp.L + col) = q;
+    } else {  // exact bf16 image of every e4m3 code (bf16-operand layers)
+      const __nv_bfloat162 h01 = __floats2bfloat162_rn(e4m3_to_f32(q & 0xFF),
+                                                       e4m3_to_f32((q >> 8) & 0xFF));
+      const __nv_bfloat162 h23 = __floats2bfloat162_rn(e4m3_to_f32((q >> 16) & 0xFF),
+                                                       e4m3_to_f32(q >> 24));
+      *reinterpret_cast<uint2*>(p.zqb_perm + static_cast<size_t>(pp) * rp.L + col) =
+          make_uint2(*reinterpret_cast<const uint32_t*>(&h01),
+                     *reinterpret_cast<const uint32_t*>(&h23));
+    }
+    if (lane == 0) p.zsT[static_cast<size_t>(g) * p.cap + pp] = sc;
+    if (first) {
+      *reinterpret_cast<uint32_t*>(rp.zq + static_cast<size_t>(t) * rp.L + col) = q;
+      if (lane == 0) rp.zs[static_cast<size_t>(t) * G + g] = sc;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(128) norm_kernel(const NormParams p) {
   __shared__ float red[4];
   pdl_trigger();  // dependents may launch now; they wait for this grid before reading
@@ -456,6 +630,23 @@ cudaError_t launch_perm_gather(const PermParams& p, cudaStream_t s, bool pdl) {
   }
   return launch_simple(perm_gather_kernel, dim3(static_cast<unsigned>((chunks + 255) / 256)),
                        dim3(256), p, s, pdl);
+}
+cudaError_t launch_route_small(const RouteParams& rp, const PermParams& p, cudaStream_t s,
+                               bool pdl) {
+  const long long items =
+      static_cast<long long>(rp.M) * rp.k * ((rp.L / 128 + ROUTE_QG - 1) / ROUTE_QG);
+  constexpr int NW = SMALL_THREADS / 32;
+  const int blocks = static_cast<int>((items + NW - 1) / NW);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(SMALL_THREADS);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, route_small_kernel, rp, p);
 }
 cudaError_t launch_norm(const NormParams& p, cudaStream_t s, bool pdl) {
   return launch_simple(norm_kernel, dim3(p.M), dim3(128), p, s, pdl);

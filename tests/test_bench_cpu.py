@@ -63,3 +63,19 @@ def test_recorded_traffic_only_for_the_recorded_sources():
 def test_job_throughput_counts_every_replica():
     assert bench.job_throughput(1, 16, 10, 1.0) == pytest.approx(160000.0)
     assert bench.job_throughput(4, 16, 10, 1.0) == pytest.approx(640000.0)
+
+
+def test_launch_names_follow_the_launch_structure():
+    d16, mx = configs.DECODE_M16, configs.PREFILL_M4096.with_(routed_fmt="mxfp8")
+    assert bench.launch_names(d16, 2, False, False) == ["route_perm", "gemm_fused"]
+    assert bench.launch_names(d16, 2, False, True) == ["proj", "route_perm", "gemm_fused"]
+    assert bench.launch_names(d16, 5, True, False) == \
+        ["route_perm", "gemm_l1", "gemm_l2", "norm", "gemm_out"]
+    assert bench.launch_names(configs.DECODE_M128, 4, False, False) == \
+        ["route", "perm_scatter", "perm_gather", "gemm_fused"]
+    assert bench.launch_names(configs.PREFILL_M4096, 5, False, False) == \
+        ["route", "perm_hist", "perm_scatter", "perm_gather", "gemm_fused"]
+    assert bench.launch_names(mx, 6, False, False) == \
+        ["route", "perm_hist", "perm_scatter", "perm_gather", "gemm_routed", "gemm_dense"]
+    assert bench.launch_names(configs.PREFILL_M4096, 8, True, False)[-4:] == \
+        ["gemm_l1", "gemm_l2", "norm", "gemm_out"]

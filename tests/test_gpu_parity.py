@@ -84,6 +84,26 @@ def test_routed_l1_k_split(fmt, M):
     run_case(cfg, M=M, force_bn=16)
 
 
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+@pytest.mark.parametrize("M,topk,L,launches", [
+    (16, 16, 256, 2),  # 256 pairs: the most the one-launch routing takes
+    (5, 3, 640, 2),    # five 128-column groups: a partial group batch per warp
+    (17, 16, 640, 4),  # 272 pairs: routing, scatter and gather launches
+])
+def test_one_launch_routing_at_its_pair_limit(fmt, M, topk, L, launches):
+    # a feature-major batch of at most 256 (token, choice) pairs is routed, sorted and
+    # quantised into expert order by one launch; one pair more takes the three-launch chain
+    cfg = configs.SMALL.with_(routed_fmt=fmt, E=64, topk=topk, L=L, seed=39)
+    w_cpu, w_gpu = weights_for(cfg)
+    tail = B.LatentMoETail(cfg, w_gpu, max_tokens=M)
+    try:
+        assert tail.gemm_tile(M, 0) != 256
+        assert tail.launch_count(M) == launches
+        run_case(cfg, M=M, tail=tail)
+    finally:
+        tail.close()
+
+
 @pytest.mark.parametrize("bn", [16, 32, 64, 128, 256])
 @pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
 def test_every_token_tile_width(bn, fmt):
@@ -306,7 +326,8 @@ def test_m_zero_is_a_noop_and_bad_m_is_rejected():
                                out.data_ptr(), None, None, s) == B.KLT_ERR_ALIGN
         assert lib.klt_forward(tail.handle, None, z.data_ptr(), lg.data_ptr(), 4,
                                out.data_ptr(), None, None, s) == B.KLT_ERR_INVALID_ARG
-        assert tail.launch_count(4) == 4 and tail.launch_count(0) == 0
+        # one routing launch (a small batch) and the fused GEMM launch
+        assert tail.launch_count(4) == 2 and tail.launch_count(0) == 0
     finally:
         tail.close()
 
