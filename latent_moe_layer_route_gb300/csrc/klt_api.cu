@@ -84,6 +84,8 @@ struct klt_handle {
   uint8_t *zq, *zq_perm, *aq;
   __nv_bfloat16 *n, *a_s, *zqb_perm, *aqb;
   int *split_cnt, *sched, *err;
+  float* out_acc;  // token-major k-split output tiles (fp32, zero between forwards)
+  int* out_cnt;    //   and their arrival counters
   int* dep_cnt;  // fused-launch dependency counters [routed tiles | l2 | norm tiles | shared]
   // Block-scaled layers (MXFP8, NVFP4_W4A4): weight scale tiles (512 bytes per 128-row
   // block and 4 scale bytes of a row, the tcgen05.cp layout), the latent input's scale
@@ -286,6 +288,8 @@ int klt_create(const klt_dims* d, const klt_weights* w, uint32_t flags, klt_hand
   // split-K partials: [shared L1 | output GEMM], one half each
   KLT_ALLOC(h->ws, 2LL * kMaxSplitUnits * 2 * 128 * 128 * 4);
   KLT_ALLOC(h->split_cnt, 2LL * kMaxCounters * 4);
+  KLT_ALLOC(h->out_acc, static_cast<int64_t>(kWideSplitMaxTiles) * 128 * H * 4);
+  KLT_ALLOC(h->out_cnt, static_cast<int64_t>(kWideSplitMaxTiles) * (H / 128) * 4);
   KLT_ALLOC(h->sched, 64 * 4);
   h->dep_routed = static_cast<int>((cap + 15) / 16 + E);
   h->dep_ntiles = static_cast<int>((Mx + 15) / 16);
@@ -720,6 +724,21 @@ int forward_impl(klt_handle* h, const void* x, const void* z, const float* logit
     O.dual = dual;
     O.units = (O.dual ? (ntiles + 1) / 2 : ntiles) * O.ftiles;
     O.dep = DEP_OUT_TILE;
+    // A batch of one or two token tiles has few output units, and they run after the norm
+    // on few SMs: split them in K (at least 8 k-blocks each) so that one wave of units
+    // covers the GPU.  The splits add into out_acc and the last of a tile rounds it (not
+    // with the fixed-order combine, whose output stays bitwise reproducible).
+    if (!dual && ntiles <= kWideSplitMaxTiles && !(h->flags & KLT_FLAG_DETERMINISTIC)) {
+      const int tiles = ntiles * O.ftiles;
+      const int ks = std::min(grid / tiles, O.kb_total / 8);
+      if (ks > 1) {
+        O.kb_per_split = (O.kb_total + ks - 1) / ks;
+        O.ksplit = (O.kb_total + O.kb_per_split - 1) / O.kb_per_split;
+        O.units = tiles * O.ksplit;
+      }
+    }
+    gw.out_acc = h->out_acc;
+    gw.out_cnt = h->out_cnt;
     O.a_ptr[0] = reinterpret_cast<const uint8_t*>(h->w_up);
     O.a_ptr[1] = reinterpret_cast<const uint8_t*>(h->ws2);
     O.tmB[0] = h->tm_n[bi];

@@ -201,6 +201,10 @@ struct GemmParams {
   int trace_n;                 // entries per (CTA, role)
   int zero_r;                  // norm units zero each row of r once it is normalised, so
                                // the next forward's routed L2 units add into zeros
+  // token-major output GEMM split in K (few token tiles): the splits add into out_acc and
+  // the last of a tile rounds it into out, then zeroes its rows and its counter
+  float* out_acc;              // [kWideSplitMaxTiles * 128, H] fp32, zero between uses
+  int* out_cnt;                // [kWideSplitMaxTiles * H / 256] arrivals, zero between uses
 };
 
 // Launchers (return cudaError_t of the launch).
@@ -243,6 +247,8 @@ bool gemm_regs_ok();
 // was built for: wide_regs_ok(wide_kernel_regs()) must hold before launch_wide is used.
 // Token-major engine: RMSNorm rows per norm unit (one per epilogue warp).
 constexpr int kWideNormRows = 8;
+// Token-major output GEMM: split in K for batches of at most this many 128-token tiles.
+constexpr int kWideSplitMaxTiles = 2;
 cudaError_t launch_wide(const GemmParams& p, int grid, cudaStream_t s, bool pdl);
 int wide_kernel_regs();
 bool wide_regs_ok(int regs);

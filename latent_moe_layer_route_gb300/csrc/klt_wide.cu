@@ -86,6 +86,7 @@ struct WUnit {
   int rb0, rb1;  // weight row blocks staged as B rows [0, 128) and [128, 256)
   int dep_idx;  // routed token tile (routed kinds) or token tile (others)
   int dual;     // 1: a second token tile follows (rows from row0 + TM, token tile dep_idx + 1)
+  int kb0, kb1;  // k-blocks [kb0, kb1) of the unit (a k-split output unit: one split)
 };
 
 // Combine staging: per warp 32 tokens x 16 features (fp32), each row's four 16-byte quads
@@ -101,6 +102,7 @@ struct WSmem {
   WUnit* ring;
   uint32_t* tmem_holder;
   int* abort_flag;
+  int* split_last;  // k-split output units: set when this CTA's split was a tile's last
   float* amax;  // [2 unit parities][2 column halves][TM]
   float* stg;   // [EPI_WARPS][32 tokens][STG_LD] per-warp transpose staging of the combine
                 // (16-byte aligned)
@@ -132,6 +134,7 @@ struct WSmem {
     ring = reinterpret_cast<WUnit*>(sptr + W::SIG);
     tmem_holder = reinterpret_cast<uint32_t*>(ring + W::US);
     abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
+    split_last = reinterpret_cast<int*>(tmem_holder + 2);
     amax = reinterpret_cast<float*>(tmem_holder + 16);
     stg = reinterpret_cast<float*>(
         (reinterpret_cast<uintptr_t>(amax + 4 * W::TM) + 15) & ~static_cast<uintptr_t>(15));
@@ -176,6 +179,8 @@ __device__ WUnit w_decode(const GemmParams& p, const int* s_tile_off, const int*
         info.rb1 = pair ? info.rb0 + T.a_rb_up : info.rb0 + 1;
         info.dep_idx = t;
         info.dual = 0;
+        info.kb0 = 0;
+        info.kb1 = T.kb_total;
         return info;
       }
       u -= units;
@@ -184,6 +189,8 @@ __device__ WUnit w_decode(const GemmParams& p, const int* s_tile_off, const int*
         info.task = ti;
         info.e = 0;
         info.dual = 0;
+        info.kb0 = 0;
+        info.kb1 = T.kb_total;
         if (T.kind == TASK_NORM) {  // NORM_ROWS token rows, all in one token tile
           info.row0 = u * W::NORM_ROWS;
           info.rows = min(W::NORM_ROWS, p.M - info.row0);
@@ -192,10 +199,17 @@ __device__ WUnit w_decode(const GemmParams& p, const int* s_tile_off, const int*
           info.dep_idx = info.row0 / W::TM;
         } else {
           // feature-tile major: every token tile of a weight tile runs close together in
-          // time, so each weight tile is read from DRAM once and stays hot in L2
-          const int per_ft = T.dual ? (T.ntiles + 1) / 2 : T.ntiles;
+          // time, so each weight tile is read from DRAM once and stays hot in L2; a k-split
+          // task (single token tiles) has its splits innermost
+          const int ks = T.ksplit;
+          const int per_ft = (T.dual ? (T.ntiles + 1) / 2 : T.ntiles) * ks;
           const int ft = u / per_ft;
-          const int j = u - ft * per_ft;
+          const int js = u - ft * per_ft;
+          const int j = js / ks;
+          if (ks > 1) {
+            info.kb0 = (js - j * ks) * T.kb_per_split;
+            info.kb1 = min(T.kb_total, info.kb0 + T.kb_per_split);
+          }
           const int nt = T.dual ? 2 * j : j;
           info.row0 = nt * W::TM;
           info.rows = min(W::TM, p.M - info.row0);
@@ -319,12 +333,14 @@ __device__ void w_producer(const GemmParams& p, WSmem& sm, const int* s_tile_off
     const uint32_t stage_tx = 2 * W::W_TILE +
                               (info.dual ? 2 : 1) * static_cast<uint32_t>(W::T_TILE) +
                               (mxu ? W::SF_STAGE : 0) + (nvu ? W::NV4_SF_BYTES : 0);
-    const int kb_end = T.kb_total;
-    int kb = 0;
+    // (block-scaled launches run routed units only, which are never split in K)
+    const int kb_end = BS != BS_NONE ? T.kb_total : info.kb1;
+    const int kb_first = BS != BS_NONE ? 0 : info.kb0;
+    int kb = kb_first;
     if (T.dep != DEP_NONE) {
       // Stream the unit's weight tiles into the stages that are free now, then wait for
       // the token operand's producers, then copy the token tiles of those stages.
-      // the early stages are consecutive ring slots holding k-blocks 0, 1, ...
+      // the early stages are consecutive ring slots holding k-blocks kb0, kb0 + 1, ...
       const int st0 = stage;
       int npre = 0;
       while (kb < kb_end && npre < nst) {
@@ -344,7 +360,7 @@ __device__ void w_producer(const GemmParams& p, WSmem& sm, const int* s_tile_off
           !w_wait_dependency(p, T.dep, info.dep_idx + 1, s_tile_off, sm.abort_flag))
         break;
       for (int i = 0, s = st0; i < npre; ++i) {
-        issue_t(i, sm.stages + s * sbytes, &sm.full[s], s);
+        issue_t(kb_first + i, sm.stages + s * sbytes, &sm.full[s], s);
         if (++s == nst) s = 0;
       }
     }
@@ -412,7 +428,9 @@ __device__ void w_mma(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
     const bool promote = kpg > 0;
     const bool fp8 = T.fp8 != 0;
     const uint32_t idesc = fp8 ? idesc_fp8 : idesc_bf16;
-    const int kb1 = T.kb_total;
+    // (block-scaled launches run routed units only, which are never split in K)
+    const int kb0 = BS != BS_NONE ? 0 : info.kb0;
+    const int kb1 = BS != BS_NONE ? T.kb_total : info.kb1;
     const bool dual = info.dual != 0;  // two token tiles share the weight operand
     // the slot after `acc` (the second tile of a dual unit) and its phase parity
     const int acc2 = acc + 1 == nacc ? 0 : acc + 1;
@@ -427,7 +445,7 @@ __device__ void w_mma(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
       tc_fence_after();
     }
     int gpos = 0;  // position of the next k-block in its promotion group
-    for (int kb = 0; kb < kb1; ++kb) {
+    for (int kb = kb0; kb < kb1; ++kb) {
       if (!mbar_wait_spin(&sm.full[stage], phase, sm.abort_flag, p.err, p.timeout)) {
         ok = false;
         break;
@@ -443,8 +461,8 @@ __device__ void w_mma(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
       const uint32_t d = tmem_base + static_cast<uint32_t>(acc * W::TN);
       const uint64_t off = static_cast<uint64_t>(stage) * STAGE_D;
       const uint32_t accum = promote ? static_cast<uint32_t>(gpos > 0)
-                                     : static_cast<uint32_t>(kb > 0);
-      if (nvu) {
+                                     : static_cast<uint32_t>(kb > kb0);
+      if (nvu) {  // (block-scaled units are routed: never split in K, kb0 = 0)
         // this stage's twelve scale tiles into its 48 TMEM columns beside the accumulator:
         // MMA j (K = 64) reads the tokens' at +4j (lane m, column m/32) and the weights'
         // at +16 + 8j (lane n%32, column n/32 over both row blocks), then the four MMAs
@@ -543,6 +561,71 @@ __device__ void w_signaller(const GemmParams& p, WSmem& sm) {
   }
 }
 
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// One k-split of an output tile (token tile of `rows` tokens x 256 features): this thread's
+// 128 fp32 sums (token (ew % 4) * 32 + lane, features [128 half, 128 half + 128) of the tile)
+// are added into the tile's fp32 rows of out_acc, 16 features of the warp's 32 tokens at a
+// time through the per-warp transpose (8 tokens x 64 contiguous bytes per vector
+// reduction).  After a fence, the tile's arrival counter tells the last split, whose
+// epilogue warps round the tile to bf16 into out (row by row, coalesced), zero its rows of
+// out_acc and its counter for the next forward.
+__device__ __forceinline__ void w_out_split(const GemmParams& p, WSmem& sm, const GemmTask& T,
+                                         const WUnit& info, int row0, int rows,
+                                         const float* a, int ew, int lane) {
+  const int half = ew / 4;
+  float* st = sm.stg + ew * 32 * STG_LD;
+  const int qd = lane & 3;
+  // lane: quad qd of warp-local tokens lane / 4 + 8 it (tile rows (ew % 4) * 32 + those)
+  float* base = p.out_acc + static_cast<size_t>(row0 + (ew & 3) * 32 + (lane >> 2)) * p.H +
+                static_cast<size_t>(info.ftile) * 256 + half * 128 + 4 * qd;
+  const int tk0 = (ew & 3) * 32 + (lane >> 2);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      *reinterpret_cast<float4*>(st + stg_quad(lane, j)) =
+          make_float4(a[16 * c + 4 * j], a[16 * c + 4 * j + 1], a[16 * c + 4 * j + 2],
+                      a[16 * c + 4 * j + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      const float4 v =
+          *reinterpret_cast<const float4*>(st + stg_quad(it * 8 + (lane >> 2), qd));
+      if (tk0 + 8 * it < rows)
+        red_add_v4(base + static_cast<size_t>(8 * it) * p.H + 16 * c, v.x, v.y, v.z, v.w);
+    }
+    __syncwarp();
+  }
+  __threadfence();  // this thread's additions before the arrival below
+  named_bar_sync(2, W::EPI_THREADS);
+  if (ew == 0 && lane == 0) {
+    const int tile = info.dep_idx * T.ftiles + info.ftile;
+    const int last = atomicAdd(p.out_cnt + tile, 1) == T.ksplit - 1;
+    if (last) p.out_cnt[tile] = 0;  // every split has arrived: ready for the next forward
+    *reinterpret_cast<volatile int*>(sm.split_last) = last;
+  }
+  named_bar_sync(2, W::EPI_THREADS);
+  if (!*reinterpret_cast<volatile int*>(sm.split_last)) return;
+  __threadfence();  // the other splits' additions before the reads below
+  // warp ew: tile rows ew, ew + 8, ...; lane: features [8 lane, 8 lane + 8)
+  for (int r = ew; r < rows; r += W::EPI_WARPS) {
+    float4* acc = reinterpret_cast<float4*>(p.out_acc + static_cast<size_t>(row0 + r) * p.H +
+                                            static_cast<size_t>(info.ftile) * 256) +
+                  2 * lane;
+    const float4 v0 = __ldcg(acc), v1 = __ldcg(acc + 1);
+    __stcg(acc, make_float4(0.f, 0.f, 0.f, 0.f));
+    __stcg(acc + 1, make_float4(0.f, 0.f, 0.f, 0.f));
+    *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(row0 + r) * p.H +
+                              static_cast<size_t>(info.ftile) * 256 + 8 * lane) =
+        make_uint4(pack_bf16x2(v0.x, v0.y), pack_bf16x2(v0.z, v0.w), pack_bf16x2(v1.x, v1.y),
+                   pack_bf16x2(v1.z, v1.w));
+  }
+}
+
 // RMSNorm of up to NORM_ROWS token rows of the fp32 combine, one row per epilogue warp:
 // fp32 statistic (lane partials, then a shuffle tree), gamma applied, one bf16 rounding (the
 // output GEMM's token operand).  No barrier between the warps.
@@ -619,11 +702,6 @@ __device__ void w_norm_rows(const GemmParams& p, WSmem& sm, SigState& sg, int ro
     }
   }
   w_signal(p, sm, sg, p.norm_done + row0 / W::TM, ew, lane);
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 template <bool DET, int BS>
@@ -949,6 +1027,8 @@ __device__ void w_epilogue(const GemmParams& p, WSmem& sm, uint32_t tmem_base) {
         }
         }
         if (p.l2_done != nullptr) w_signal(p, sm, sg, p.l2_done, ew, lane);
+      } else if (!DET && BS == BS_NONE && T.ksplit > 1) {  // TASK_OUT, one k-split of a tile
+        w_out_split(p, sm, T, info, row0, rows, a, ew, lane);
       } else {  // TASK_OUT
         if (valid) {
           uint4* dst = reinterpret_cast<uint4*>(

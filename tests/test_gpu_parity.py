@@ -126,6 +126,22 @@ def test_token_major_engine_on_several_feature_tiles(fmt):
         tail.close()
 
 
+@pytest.mark.parametrize("M", [17, 200])
+def test_token_major_output_split_in_k(M):
+    # one or two token tiles (the second ragged): the output GEMM runs as k-splits that add
+    # into fp32 tiles, the last split of each tile rounding it; a second forward on the
+    # same handle finds the tiles and their counters reset
+    cfg = configs.SMALL.with_(H=1024, L=1024, I=256, Is=512, E=8, topk=2, seed=40)
+    w_cpu, w_gpu = weights_for(cfg)
+    tail = B.LatentMoETail(cfg, w_gpu, max_tokens=M)
+    try:
+        assert tail.gemm_tile(M, 256) == 256
+        for _ in range(2):
+            run_case(cfg, M=M, tail=tail, force_bn=256)
+    finally:
+        tail.close()
+
+
 def test_token_major_engine_with_long_k():
     # a small batch with long K: the output GEMM's k loop crosses from the up-projection
     # into the shared down projection far from the first k-block
